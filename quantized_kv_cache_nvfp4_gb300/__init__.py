@@ -1,0 +1,289 @@
+"""GB300-native KV-cache quantisation codec: Python binding of libkvq.so.
+
+The functions here carry the names of the C entry points in include/kvq.h and only
+marshal arguments: torch tensors become pointers and pitches, the current CUDA
+stream becomes the launch stream, and a non-OK status becomes ``KvqError``.  Every
+step of the codec runs in the library's sm_103a kernels; there is no CPU path, and
+a missing library raises.
+
+Allocation helpers (``Nvfp4Pool``, ``Packed``) use torch for device memory only.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT_INT4, FMT_NVFP4,
+                   KIND_KEY, KIND_VALUE)
+
+__all__ = [
+    "KvqError", "Nvfp4Pool", "Packed", "kvq_quant_scatter", "kvq_restore", "kvq_pack",
+    "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_storage_bytes",
+    "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "KIND_KEY",
+    "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN",
+]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{_abi.STATUS_NAMES.get(status, status)}: {detail}")
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def _lib():
+    return _abi.load()
+
+
+def _check(status: int) -> None:
+    if status != _abi.KVQ_OK:
+        raise KvqError(status, _lib().kvq_last_error().decode())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _view3(t: torch.Tensor, name: str):
+    """(ptr, row_pitch, head_pitch) of a bf16 [rows, heads, dim] tensor, inner stride 1."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 3 or (t.size(2) > 1 and t.stride(2) != 1):
+        raise ValueError(f"{name} must be [rows, heads, dim] with inner stride 1")
+    return t.data_ptr(), t.stride(0), t.stride(1)
+
+
+def _bf16_in(t: torch.Tensor, name: str):
+    p, r, h = _view3(t, name)
+    return _abi.Bf16In(p, r, h)
+
+
+def _bf16_out(t: torch.Tensor, name: str):
+    p, r, h = _view3(t, name)
+    return _abi.Bf16Out(p, r, h)
+
+
+# ---------------------------------------------------------------------------
+# device memory holders
+# ---------------------------------------------------------------------------
+@dataclass
+class Nvfp4Pool:
+    """Paged NVFP4 planes for K and V: codes [slots, H, D/2] u8, bscale [slots, H, D/16]
+    u8 (E4M3), rscale [slots, H] f32.  Slot = block * block_size + offset."""
+
+    k_codes: torch.Tensor
+    k_bscale: torch.Tensor
+    k_rscale: torch.Tensor
+    v_codes: torch.Tensor
+    v_bscale: torch.Tensor
+    v_rscale: torch.Tensor
+    block_size: int
+
+    @classmethod
+    def empty(cls, num_slots: int, num_heads: int, head_dim: int, block_size: int = 16,
+              device="cuda", fill: Optional[int] = None) -> "Nvfp4Pool":
+        def u8(*shape):
+            t = torch.empty(shape, dtype=torch.uint8, device=device)
+            return t.fill_(fill) if fill is not None else t
+
+        def f32(*shape):
+            t = torch.empty(shape, dtype=torch.float32, device=device)
+            if fill is not None:
+                t.view(torch.uint8).fill_(fill)
+            return t
+
+        return cls(u8(num_slots, num_heads, head_dim // 2), u8(num_slots, num_heads, head_dim // 16),
+                   f32(num_slots, num_heads), u8(num_slots, num_heads, head_dim // 2),
+                   u8(num_slots, num_heads, head_dim // 16), f32(num_slots, num_heads), block_size)
+
+    @property
+    def num_slots(self) -> int:
+        return self.k_codes.size(0)
+
+    @property
+    def num_heads(self) -> int:
+        return self.k_codes.size(1)
+
+    @property
+    def head_dim(self) -> int:
+        return self.k_codes.size(2) * 2
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale, self.v_rscale))
+
+    def _struct(self) -> _abi.Nvfp4Pool:
+        for t in (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale, self.v_rscale):
+            if not t.is_contiguous():
+                raise ValueError("pool planes must be contiguous")
+        return _abi.Nvfp4Pool(
+            _abi.Nvfp4Plane(self.k_codes.data_ptr(), self.k_bscale.data_ptr(), self.k_rscale.data_ptr()),
+            _abi.Nvfp4Plane(self.v_codes.data_ptr(), self.v_bscale.data_ptr(), self.v_rscale.data_ptr()),
+            self.num_slots, self.block_size, self.num_heads, self.head_dim)
+
+
+@dataclass
+class Packed:
+    """A logical packed tensor [rows, heads, dim] (see kvq_packed in include/kvq.h)."""
+
+    fmt: int
+    kind: int
+    group_size: int
+    rows: int
+    heads: int
+    dim: int
+    codes: torch.Tensor
+    meta0: torch.Tensor
+    meta1: Optional[torch.Tensor] = None
+    rscale: Optional[torch.Tensor] = None
+
+    @classmethod
+    def empty(cls, fmt: int, kind: int, rows: int, heads: int, dim: int, group_size: int = 64,
+              device="cuda") -> "Packed":
+        codes = torch.empty((rows, heads, dim // 2), dtype=torch.uint8, device=device)
+        if fmt == FMT_NVFP4:
+            return cls(fmt, kind, 16, rows, heads, dim, codes,
+                       torch.empty((rows, heads, dim // 16), dtype=torch.uint8, device=device),
+                       None, torch.empty((rows, heads), dtype=torch.float32, device=device))
+        if kind == KIND_KEY:
+            ms = (math.ceil(rows / group_size), heads, dim)
+        else:
+            ms = (rows, heads, math.ceil(dim / group_size))
+        return cls(fmt, kind, group_size, rows, heads, dim, codes,
+                   torch.empty(ms, dtype=torch.float16, device=device),
+                   torch.empty(ms, dtype=torch.float16, device=device), None)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.codes, self.meta0, self.meta1, self.rscale)
+                   if t is not None)
+
+    def _struct(self) -> _abi.Packed:
+        for t in (self.codes, self.meta0, self.meta1, self.rscale):
+            if t is not None and not t.is_contiguous():
+                raise ValueError("packed buffers must be contiguous")
+        return _abi.Packed(self.fmt, self.kind, self.group_size, self.rows, self.heads, self.dim,
+                           self.codes.data_ptr(), self.meta0.data_ptr(),
+                           None if self.meta1 is None else self.meta1.data_ptr(),
+                           None if self.rscale is None else self.rscale.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+def kvq_quant_scatter(k: Optional[torch.Tensor], v: Optional[torch.Tensor], slot_ids: torch.Tensor,
+                      pool: Nvfp4Pool, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """NVFP4 quantise + scatter of K/V [T, H, D] bf16 into pool slots slot_ids[T] (int64)."""
+    src = k if k is not None else v
+    if src is None:
+        raise ValueError("k and v are both None")
+    if slot_ids.dtype != torch.int64:
+        raise TypeError("slot_ids must be int64")
+    T = src.size(0)
+    kin = _bf16_in(k, "k") if k is not None else None
+    vin = _bf16_in(v, "v") if v is not None else None
+    ps = pool._struct()
+    _check(_lib().kvq_quant_scatter(
+        ctypes.byref(kin) if kin is not None else None, ctypes.byref(vin) if vin is not None else None,
+        T, _ptr(slot_ids), ctypes.byref(ps), _ptr(dev_status), _stream(stream)))
+
+
+def _seq_view(t: torch.Tensor, S: int, Tmax: int, name: str):
+    """[S, Tmax, H, D] (or [S*Tmax, H, D]) bf16 -> Bf16Out over S*Tmax rows."""
+    if t.dim() == 4:
+        if t.size(0) != S or t.size(1) != Tmax or (S > 1 and t.stride(0) != Tmax * t.stride(1)):
+            raise ValueError(f"{name} must be [S, Tmax, H, D] with sequence stride Tmax*token stride")
+        t = t.flatten(0, 1)
+    return _bf16_out(t, name)
+
+
+def kvq_restore(pool: Nvfp4Pool, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                k_out: Optional[torch.Tensor], v_out: Optional[torch.Tensor],
+                dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Paged NVFP4 restore into k_out / v_out [S, max_seq_len, H, D] bf16."""
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [S, max_blocks]")
+    S, max_blocks = block_table.shape
+    ko = _seq_view(k_out, S, max_seq_len, "k_out") if k_out is not None else None
+    vo = _seq_view(v_out, S, max_seq_len, "v_out") if v_out is not None else None
+    ps = pool._struct()
+    _check(_lib().kvq_restore(
+        ctypes.byref(ps), _ptr(block_table), S, max_blocks, _ptr(seq_lens), max_seq_len,
+        ctypes.byref(ko) if ko is not None else None, ctypes.byref(vo) if vo is not None else None,
+        _ptr(dev_status), _stream(stream)))
+
+
+def kvq_pack(x: torch.Tensor, out: Packed, stream=None) -> Packed:
+    xin = _bf16_in(x, "x")
+    ps = out._struct()
+    _check(_lib().kvq_pack(ctypes.byref(xin), ctypes.byref(ps), _stream(stream)))
+    return out
+
+
+def kvq_unpack(packed: Packed, y: torch.Tensor, stream=None) -> torch.Tensor:
+    yo = _bf16_out(y, "y")
+    ps = packed._struct()
+    _check(_lib().kvq_unpack(ctypes.byref(ps), ctypes.byref(yo), _stream(stream)))
+    return y
+
+
+def kvq_encode_residual(cur: torch.Tensor, prev: torch.Tensor, pos: Optional[torch.Tensor],
+                        payload: Packed, pos_out: Optional[torch.Tensor] = None,
+                        dev_status: Optional[torch.Tensor] = None, stream=None) -> Packed:
+    if pos is not None and pos.dtype != torch.int32:
+        raise TypeError("pos must be int32")
+    ci, pi = _bf16_in(cur, "cur"), _bf16_in(prev, "prev")
+    n = cur.size(0) if pos is None else pos.numel()
+    ps = payload._struct()
+    pos_ptr = _ptr(pos)
+    if pos is not None and pos.numel() == 0:
+        pos_ptr = ctypes.c_void_p(prev.data_ptr())  # non-NULL marks "sparse, nothing kept"
+    _check(_lib().kvq_encode_residual(
+        ctypes.byref(ci), ctypes.byref(pi), cur.size(0), pos_ptr, n, ctypes.byref(ps),
+        _ptr(pos_out), _ptr(dev_status), _stream(stream)))
+    return payload
+
+
+def kvq_decode_residual(payload: Packed, pos: Optional[torch.Tensor], prev: torch.Tensor,
+                        out: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    if pos is not None and pos.dtype != torch.int32:
+        raise TypeError("pos must be int32")
+    pi, oo = _bf16_in(prev, "prev"), _bf16_out(out, "out")
+    n = prev.size(0) if pos is None else pos.numel()
+    ps = payload._struct()
+    pos_ptr = _ptr(pos)
+    if pos is not None and pos.numel() == 0:
+        pos_ptr = ctypes.c_void_p(prev.data_ptr())  # non-NULL marks "sparse, nothing kept"
+    _check(_lib().kvq_decode_residual(
+        ctypes.byref(ps), pos_ptr, n, ctypes.byref(pi), prev.size(0), ctypes.byref(oo),
+        _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def kvq_storage_bytes(fmt: int, kind: int, group_size: int, rows: int, heads: int, dim: int) -> int:
+    return int(_lib().kvq_storage_bytes(fmt, kind, group_size, rows, heads, dim))
+
+
+def kvq_status_string(status: int) -> str:
+    return _lib().kvq_status_string(status).decode()
+
+
+def kvq_last_error() -> str:
+    return _lib().kvq_last_error().decode()

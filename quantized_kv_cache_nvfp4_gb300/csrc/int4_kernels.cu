@@ -1,0 +1,272 @@
+// int4_kernels.cu -- INT4 affine codec encode kernels (plain pack and residual).
+//
+// Format ("vllm-rlt PR #166: INT4 KV packing/unpacking and cross-loop residual
+// reconstruction", Purpose, and the review by 0z5a): groups of G values share an
+// FP16 minimum and an FP16 scale; codes are computed in FP32 BEFORE the metadata is
+// rounded to FP16; K groups run over G token rows per (head, channel), V groups over
+// G channels per (token, head); the last group may be partial.  Per group, in order
+// (binary32, nearest even):
+//   mn = min x;  mx = max x;  sc = (mx - mn) / 15
+//   code = 0 if sc == 0, else clamp(rint((x - mn) / sc), 0, 15)   (rint: ties even)
+//   stored: fp16(mn), fp16(sc); two codes per byte, low nibble = even channel.
+// Residual encode feeds the same codec with r = bf16(cur - prev) of the kept rows
+// (same page, Purpose: residuals subtract the reconstructed predecessor in the
+// input dtype; K groups follow the compact row order).
+#include "kvq_device.cuh"
+#include "kvq_params.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// Code of x in a group with FP32 minimum mn and scale sc (sc > 0).
+__device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc) {
+  float q = rintf(__fdiv_rn(__fsub_rn(x, mn), sc));
+  q = fminf(fmaxf(q, 0.0f), 15.0f);
+  return static_cast<uint32_t>(q);
+}
+
+// The 8 bf16 values of one 16-byte chunk of a compact row (residual: bf16(cur-prev)).
+// Returns false for a residual row whose position is out of range (values zero).
+template <bool kResidual>
+__device__ __forceinline__ bool load_chunk8(const Int4EncodeParams& p, int32_t row, int32_t h,
+                                            int32_t col, uint32_t (&w)[4]) {
+  int64_t src = row;
+  if constexpr (kResidual) {
+    if (p.pos != nullptr) src = p.pos[row];
+    if (src < 0 || src >= p.src_rows) {
+      w[0] = w[1] = w[2] = w[3] = 0u;
+      return false;
+    }
+  }
+  const uint16_t* a = p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col;
+  asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+      : "l"(a));
+  if constexpr (kResidual) {
+    uint32_t q[4];
+    const uint16_t* b =
+        p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col;
+    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+        : "l"(b));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = pack_bf16x2(__fsub_rn(bf16lo(w[i]), bf16lo(q[i])),
+                         __fsub_rn(bf16hi(w[i]), bf16hi(q[i])));
+  }
+  return true;
+}
+
+template <bool kResidual>
+__device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row) {
+  if constexpr (kResidual) {
+    if (p.pos == nullptr) return;
+    const int32_t ps = p.pos[row];
+    bool bad = ps < 0 || ps >= p.src_rows;
+    if (row > 0 && p.pos[row - 1] >= ps) bad = true;
+    if (bad) set_status(p.status, 4u);
+    if (p.pos_out != nullptr) p.pos_out[row] = ps;
+  }
+}
+
+// KEY kind: one lane per (group, head, 8-channel chunk) column task; the lane walks
+// the group's rows twice (min/max, then codes).  Consecutive lanes take consecutive
+// chunks of the same head and row, so every row read is one coalesced span.
+template <bool kResidual>
+__global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
+  const int32_t nchunk = p.D / 8;
+  const int32_t ngroups = (p.rows + p.G - 1) / p.G;
+  const int64_t tasks = static_cast<int64_t>(ngroups) * p.H * nchunk;
+  for (int64_t task = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; task < tasks;
+       task += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int32_t chunk = static_cast<int32_t>(task % nchunk);
+    const int32_t h = static_cast<int32_t>((task / nchunk) % p.H);
+    const int32_t g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * p.H));
+    const int32_t r0 = g * p.G;
+    const int32_t r1 = min(p.rows, r0 + p.G);
+    const int32_t col = chunk * 8;
+
+    float mn[8], mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mn[i] = __int_as_float(0x7F800000);   // +inf
+      mx[i] = __int_as_float(0xFF800000);   // -inf
+    }
+#pragma unroll 4
+    for (int32_t r = r0; r < r1; ++r) {
+      uint32_t w[4];
+      load_chunk8<kResidual>(p, r, h, col, w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mn[2 * i] = fminf(mn[2 * i], bf16lo(w[i]));
+        mx[2 * i] = fmaxf(mx[2 * i], bf16lo(w[i]));
+        mn[2 * i + 1] = fminf(mn[2 * i + 1], bf16hi(w[i]));
+        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16hi(w[i]));
+      }
+    }
+    float sc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i] = __fdiv_rn(__fsub_rn(mx[i], mn[i]), 15.0f);
+
+#pragma unroll 4
+    for (int32_t r = r0; r < r1; ++r) {
+      uint32_t w[4];
+      load_chunk8<kResidual>(p, r, h, col, w);
+      if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
+      uint32_t packed = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t cl = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i]) : 0u;
+        const uint32_t ch =
+            sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1]) : 0u;
+        packed |= (cl | (ch << 4)) << (8 * i);
+      }
+      *reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
+                                   col / 2) = packed;
+    }
+    uint32_t m16[4], s16[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m16[i] = static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i])) |
+               (static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i + 1])) << 16);
+      s16[i] = static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i])) |
+               (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
+    }
+    const int64_t m = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p.dst.mn + m), "r"(m16[0]),
+                 "r"(m16[1]), "r"(m16[2]), "r"(m16[3])
+                 : "memory");
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p.dst.sc + m), "r"(s16[0]),
+                 "r"(s16[1]), "r"(s16[2]), "r"(s16[3])
+                 : "memory");
+  }
+}
+
+// VALUE kind: one lane per 16-channel block of a row; a group spans W = min(G/16, L)
+// aligned lanes, reduced with a xor butterfly of uniform width.
+template <int L, bool kResidual>
+__global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodeParams p) {
+  constexpr int kRowsPerWarp = 32 / L;
+  const int lane = threadIdx.x & 31;
+  const int b = lane % L;
+  const int sub = lane / L;
+  const int nb = p.D / 16;
+  const int W = min(p.G / 16, L);
+  const int ngv = (p.D + p.G - 1) / p.G;
+  const uint32_t total = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H);
+  const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
+  const bool has = b < nb;
+
+  for (uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
+       row - sub < total; row += stride) {
+    const bool valid = row < total && has;
+    const int32_t r = static_cast<int32_t>((valid ? row : 0u) / static_cast<uint32_t>(p.H));
+    const int32_t h = static_cast<int32_t>((valid ? row : 0u) % static_cast<uint32_t>(p.H));
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
+    if (valid) {
+      uint32_t a[4], c[4];
+      load_chunk8<kResidual>(p, r, h, 16 * b, a);
+      load_chunk8<kResidual>(p, r, h, 16 * b + 8, c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[i] = a[i];
+        w[4 + i] = c[i];
+      }
+      if (b == 0 && h == 0) check_pos<kResidual>(p, r);
+    }
+    float lmn = __int_as_float(0x7F800000), lmx = __int_as_float(0xFF800000);
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lmn = fminf(lmn, fminf(bf16lo(w[i]), bf16hi(w[i])));
+        lmx = fmaxf(lmx, fmaxf(bf16lo(w[i]), bf16hi(w[i])));
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float omn = __shfl_xor_sync(0xFFFFFFFFu, lmn, o);
+      const float omx = __shfl_xor_sync(0xFFFFFFFFu, lmx, o);
+      if (o < W) {
+        lmn = fminf(lmn, omn);
+        lmx = fmaxf(lmx, omx);
+      }
+    }
+    if (!valid) continue;
+    const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
+    uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t cl = sc != 0.0f ? int4_code(bf16lo(w[i]), lmn, sc) : 0u;
+      const uint32_t ch = sc != 0.0f ? int4_code(bf16hi(w[i]), lmn, sc) : 0u;
+      if (i < 4)
+        c0 |= (cl | (ch << 4)) << (8 * i);
+      else
+        c1 |= (cl | (ch << 4)) << (8 * (i - 4));
+    }
+    const int64_t drow = static_cast<int64_t>(r) * p.H + h;
+    store8B(p.dst.codes + drow * (p.D / 2) + 8 * b, c0, c1);
+    if ((16 * b) % p.G == 0) {
+      const int64_t m = drow * ngv + (16 * b) / p.G;
+      p.dst.mn[m] = f32_to_f16_bits(lmn);
+      p.dst.sc[m] = f32_to_f16_bits(sc);
+    }
+  }
+}
+
+template <typename K>
+int grid_cap(K kernel, int64_t work_items, int items_per_cta) {
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+  if (occ < 1) occ = 1;
+  int64_t need = (work_items + items_per_cta - 1) / items_per_cta;
+  int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+  if (need < 1) need = 1;
+  return static_cast<int>(need < cap ? need : cap);
+}
+
+template <int L, bool kRes>
+cudaError_t value_launch(const Int4EncodeParams& p, cudaStream_t s) {
+  auto k = int4_value_kernel<L, kRes>;
+  int grid = grid_cap(k, static_cast<int64_t>(p.rows) * p.H, (kThreads / 32) * (32 / L));
+  k<<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool kRes>
+cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
+  int nb = p.D / 16, L = 1;
+  while (L < nb) L <<= 1;
+  switch (L) {
+    case 1: return value_launch<1, kRes>(p, s);
+    case 2: return value_launch<2, kRes>(p, s);
+    case 4: return value_launch<4, kRes>(p, s);
+    case 8: return value_launch<8, kRes>(p, s);
+    case 16: return value_launch<16, kRes>(p, s);
+    case 32: return value_launch<32, kRes>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s) {
+  if (p.kind == 0) {
+    const int64_t tasks = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
+    if (p.residual) {
+      auto k = int4_key_kernel<true>;
+      k<<<grid_cap(k, tasks, kThreads), kThreads, 0, s>>>(p);
+    } else {
+      auto k = int4_key_kernel<false>;
+      k<<<grid_cap(k, tasks, kThreads), kThreads, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+  }
+  return p.residual ? value_dispatch<true>(p, s) : value_dispatch<false>(p, s);
+}
+
+}  // namespace kvq

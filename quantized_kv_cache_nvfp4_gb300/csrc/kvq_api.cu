@@ -1,0 +1,499 @@
+// kvq_api.cu -- the C ABI declared in include/kvq.h: argument checks on the host,
+// then one kernel launch on the caller's stream.  Nothing here allocates, frees or
+// synchronises, so every entry point can be captured in a CUDA graph.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kvq.h"
+#include "kvq_params.h"
+
+namespace kvq {
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+
+// Device memory of the current device, else an error status.
+kvq_status check_dev(const void* p, const char* what) {
+  if (p == nullptr) return fail(KVQ_ERR_INVALID_ARG, "%s is NULL", what);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // do not leave the error behind for the launch check
+    return fail(KVQ_ERR_NOT_DEVICE_PTR, "%s: cudaPointerGetAttributes failed (%s)", what,
+                cudaGetErrorString(e));
+  }
+  if (a.type != cudaMemoryTypeDevice)
+    return fail(KVQ_ERR_NOT_DEVICE_PTR, "%s is not device memory (type %d)", what,
+                static_cast<int>(a.type));
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (a.device != dev)
+    return fail(KVQ_ERR_NOT_DEVICE_PTR, "%s lives on device %d, current device is %d", what,
+                a.device, dev);
+  return KVQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A bf16 view: device, 16-byte base, pitches multiple of 8 elements (16 bytes).
+// v8 reports whether every 16-element block starts on a 32-byte boundary.
+kvq_status check_view(const void* ptr, int64_t row_pitch, int64_t head_pitch, const char* what,
+                      bool& v8) {
+  kvq_status st = check_dev(ptr, what);
+  if (st != KVQ_OK) return st;
+  if (row_pitch < 0 || head_pitch < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "%s: negative pitch", what);
+  if (!aligned(ptr, 16) || row_pitch % 8 != 0 || head_pitch % 8 != 0)
+    return fail(KVQ_ERR_MISALIGNED,
+                "%s: base must be 16-byte aligned and pitches multiples of 8 elements", what);
+  v8 = v8 && aligned(ptr, 32) && row_pitch % 16 == 0 && head_pitch % 16 == 0;
+  return KVQ_OK;
+}
+
+kvq_status check_plane(const void* p, const char* what) {
+  kvq_status st = check_dev(p, what);
+  if (st != KVQ_OK) return st;
+  if (!aligned(p, 16)) return fail(KVQ_ERR_MISALIGNED, "%s must be 16-byte aligned", what);
+  return KVQ_OK;
+}
+
+kvq_status check_head_dim(int32_t H, int32_t D) {
+  if (H <= 0) return fail(KVQ_ERR_INVALID_ARG, "heads must be positive (got %d)", H);
+  if (D <= 0 || D % 16 != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "head_dim must be a positive multiple of 16 (got %d)", D);
+  if (D > 512) return fail(KVQ_ERR_UNSUPPORTED, "head_dim above 512 is not supported (got %d)", D);
+  return KVQ_OK;
+}
+
+int lanes_for(int32_t D) {
+  int nb = D / 16, L = 1;
+  while (L < nb) L <<= 1;
+  return L;
+}
+
+kvq_status launched(cudaError_t e) {
+  if (e != cudaSuccess)
+    return fail(KVQ_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+bool fits_u31(int64_t v) { return v >= 0 && v < (int64_t{1} << 31); }
+
+kvq_status check_packed(const kvq_packed* pk, const char* what) {
+  if (pk == nullptr) return fail(KVQ_ERR_INVALID_ARG, "%s is NULL", what);
+  kvq_status st = check_head_dim(pk->heads, pk->dim);
+  if (st != KVQ_OK) return st;
+  if (pk->rows < 0) return fail(KVQ_ERR_INVALID_ARG, "%s: negative rows", what);
+  if (pk->fmt == KVQ_FMT_NVFP4) {
+    if (pk->group_size != 16 && pk->group_size != 0)
+      return fail(KVQ_ERR_INVALID_ARG, "%s: NVFP4 groups are 16 values", what);
+    if (pk->rows == 0) return KVQ_OK;
+    if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->meta0, "meta0 (block scales)")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->rscale, "rscale")) != KVQ_OK) return st;
+  } else if (pk->fmt == KVQ_FMT_INT4) {
+    const int G = pk->group_size;
+    if (!(G == 16 || G == 32 || G == 64 || G == 128 || G == 256 || G == 512))
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: INT4 group size must be 16..512, a power of two (got %d)",
+                  what, G);
+    if (pk->kind != KVQ_KIND_KEY && pk->kind != KVQ_KIND_VALUE)
+      return fail(KVQ_ERR_INVALID_ARG, "%s: kind must be KEY or VALUE", what);
+    if (pk->rows == 0) return KVQ_OK;
+    if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->meta0, "meta0 (fp16 minimum)")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->meta1, "meta1 (fp16 scale)")) != KVQ_OK) return st;
+  } else {
+    return fail(KVQ_ERR_INVALID_ARG, "%s: unknown format %d", what, pk->fmt);
+  }
+  if (!fits_u31(static_cast<int64_t>(pk->rows) * pk->heads * 2))
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: rows x heads too large", what);
+  return KVQ_OK;
+}
+
+PayloadRef payload_ref(const kvq_packed* pk) {
+  PayloadRef r;
+  r.fmt = pk->fmt;
+  r.kind = pk->kind;
+  r.G = pk->group_size;
+  r.codes = pk->codes;
+  r.meta0 = pk->meta0;
+  r.meta1 = pk->meta1;
+  r.rscale = pk->rscale;
+  r.rows = pk->rows;
+  return r;
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 148;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
+                                     int32_t num_tokens, const int64_t* slot_ids,
+                                     const kvq_nvfp4_pool* pool, uint32_t* dev_status,
+                                     kvq_stream_t stream) {
+  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (k == nullptr && v == nullptr) return fail(KVQ_ERR_INVALID_ARG, "both k and v are NULL");
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_tokens");
+  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
+  if (st != KVQ_OK) return st;
+  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
+  if (num_tokens == 0) return KVQ_OK;
+  const int ntensors = (k != nullptr) + (v != nullptr);
+  if (!fits_u31(static_cast<int64_t>(num_tokens) * pool->num_heads * ntensors))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_tokens x heads too large");
+  if ((st = check_dev(slot_ids, "slot_ids")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+
+  EncodeParams p{};
+  bool v8 = true;
+  int i = 0;
+  const kvq_bf16_in* src[2] = {k, v};
+  const kvq_nvfp4_plane* dst[2] = {&pool->k, &pool->v};
+  const char* names[2] = {"k", "v"};
+  for (int j = 0; j < 2; ++j) {
+    if (src[j] == nullptr) continue;
+    if ((st = check_view(src[j]->ptr, src[j]->row_pitch, src[j]->head_pitch, names[j], v8)) != KVQ_OK)
+      return st;
+    if ((st = check_plane(dst[j]->codes, "pool codes")) != KVQ_OK) return st;
+    if ((st = check_plane(dst[j]->bscale, "pool bscale")) != KVQ_OK) return st;
+    if ((st = check_plane(dst[j]->rscale, "pool rscale")) != KVQ_OK) return st;
+    EncodeTensor& t = p.ten[i++];
+    t.x = static_cast<const uint16_t*>(src[j]->ptr);
+    t.row_pitch = src[j]->row_pitch;
+    t.head_pitch = src[j]->head_pitch;
+    t.dst = Nvfp4Planes{dst[j]->codes, dst[j]->bscale, dst[j]->rscale};
+  }
+  p.ntensors = ntensors;
+  p.rows_per_tensor = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(pool->num_heads);
+  p.div_h = FastDiv(static_cast<uint32_t>(pool->num_heads));
+  p.H = pool->num_heads;
+  p.nb = pool->head_dim / 16;
+  p.slot_ids = slot_ids;
+  p.num_slots = pool->num_slots;
+  p.status = dev_status;
+  return launched(launch_nvfp4_encode(p, kEncScatter, lanes_for(pool->head_dim), v8,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_table,
+                               int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
+                               int32_t max_seq_len, const kvq_bf16_out* k_out,
+                               const kvq_bf16_out* v_out, uint32_t* dev_status,
+                               kvq_stream_t stream) {
+  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (k_out == nullptr && v_out == nullptr)
+    return fail(KVQ_ERR_INVALID_ARG, "both k_out and v_out are NULL");
+  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
+  if (st != KVQ_OK) return st;
+  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
+  if (num_seqs < 0 || max_blocks < 0 || max_seq_len < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "negative num_seqs, max_blocks or max_seq_len");
+  if (num_seqs == 0 || max_seq_len == 0) return KVQ_OK;
+  const int ntensors = (k_out != nullptr) + (v_out != nullptr);
+  if (!fits_u31(static_cast<int64_t>(num_seqs) * max_seq_len * pool->num_heads * ntensors))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_seqs x max_seq_len x heads too large");
+  if ((st = check_dev(block_table, "block_table")) != KVQ_OK) return st;
+  if ((st = check_dev(seq_lens, "seq_lens")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+
+  DecodeParams p{};
+  bool v8 = true;
+  int i = 0;
+  const kvq_bf16_out* out[2] = {k_out, v_out};
+  const kvq_nvfp4_plane* src[2] = {&pool->k, &pool->v};
+  const char* names[2] = {"k_out", "v_out"};
+  for (int j = 0; j < 2; ++j) {
+    if (out[j] == nullptr) continue;
+    if ((st = check_view(out[j]->ptr, out[j]->row_pitch, out[j]->head_pitch, names[j], v8)) != KVQ_OK)
+      return st;
+    if ((st = check_plane(src[j]->codes, "pool codes")) != KVQ_OK) return st;
+    if ((st = check_plane(src[j]->bscale, "pool bscale")) != KVQ_OK) return st;
+    if ((st = check_plane(src[j]->rscale, "pool rscale")) != KVQ_OK) return st;
+    DecodeTensor& t = p.ten[i++];
+    t.codes = src[j]->codes;
+    t.bscale = src[j]->bscale;
+    t.rscale = src[j]->rscale;
+    t.y = static_cast<uint16_t*>(out[j]->ptr);
+    t.row_pitch = out[j]->row_pitch;
+    t.head_pitch = out[j]->head_pitch;
+  }
+  p.ntensors = ntensors;
+  p.rows_per_tensor = static_cast<uint32_t>(num_seqs) * static_cast<uint32_t>(max_seq_len) *
+                      static_cast<uint32_t>(pool->num_heads);
+  p.div_h = FastDiv(static_cast<uint32_t>(pool->num_heads));
+  p.div_tmax = FastDiv(static_cast<uint32_t>(max_seq_len));
+  p.div_bs = FastDiv(static_cast<uint32_t>(pool->block_size));
+  p.H = pool->num_heads;
+  p.nb = pool->head_dim / 16;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks;
+  p.tmax = max_seq_len;
+  const int64_t cap = static_cast<int64_t>(max_blocks) * pool->block_size;
+  p.seq_cap = static_cast<int32_t>(cap < max_seq_len ? cap : max_seq_len);
+  p.num_blocks = pool->num_slots / pool->block_size;
+  p.block_size = pool->block_size;
+  p.status = dev_status;
+  return launched(launch_nvfp4_decode(p, kDecRestore, lanes_for(pool->head_dim), v8,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_stream_t stream) {
+  kvq_status st = check_packed(out, "out");
+  if (st != KVQ_OK) return st;
+  if (x == nullptr) return fail(KVQ_ERR_INVALID_ARG, "x is NULL");
+  if (out->rows == 0) return KVQ_OK;
+  bool v8 = true;
+  if ((st = check_view(x->ptr, x->row_pitch, x->head_pitch, "x", v8)) != KVQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (out->fmt == KVQ_FMT_NVFP4) {
+    EncodeParams p{};
+    p.ten[0].x = static_cast<const uint16_t*>(x->ptr);
+    p.ten[0].row_pitch = x->row_pitch;
+    p.ten[0].head_pitch = x->head_pitch;
+    p.ten[0].dst = Nvfp4Planes{out->codes, static_cast<uint8_t*>(out->meta0), out->rscale};
+    p.ntensors = 1;
+    p.rows_per_tensor = static_cast<uint32_t>(out->rows) * static_cast<uint32_t>(out->heads);
+    p.div_h = FastDiv(static_cast<uint32_t>(out->heads));
+    p.H = out->heads;
+    p.nb = out->dim / 16;
+    return launched(launch_nvfp4_encode(p, kEncPack, lanes_for(out->dim), v8, s));
+  }
+  Int4EncodeParams p{};
+  p.x = static_cast<const uint16_t*>(x->ptr);
+  p.row_pitch = x->row_pitch;
+  p.head_pitch = x->head_pitch;
+  p.dst = Int4Payload{out->codes, static_cast<uint16_t*>(out->meta0),
+                      static_cast<uint16_t*>(out->meta1)};
+  p.rows = out->rows;
+  p.H = out->heads;
+  p.D = out->dim;
+  p.G = out->group_size;
+  p.kind = out->kind;
+  p.residual = 0;
+  p.src_rows = out->rows;
+  return launched(launch_int4_encode(p, s));
+}
+
+KVQ_API kvq_status kvq_unpack(const kvq_packed* in, const kvq_bf16_out* y, kvq_stream_t stream) {
+  kvq_status st = check_packed(in, "in");
+  if (st != KVQ_OK) return st;
+  if (y == nullptr) return fail(KVQ_ERR_INVALID_ARG, "y is NULL");
+  if (in->rows == 0) return KVQ_OK;
+  bool v8 = true;
+  if ((st = check_view(y->ptr, y->row_pitch, y->head_pitch, "y", v8)) != KVQ_OK) return st;
+  UnpackParams u{};
+  u.pay = payload_ref(in);
+  u.H = in->heads;
+  u.D = in->dim;
+  u.nb = in->dim / 16;
+  u.div_h = FastDiv(static_cast<uint32_t>(in->heads));
+  u.total_rows = static_cast<uint32_t>(in->rows) * static_cast<uint32_t>(in->heads);
+  u.y = static_cast<uint16_t*>(y->ptr);
+  u.y_row_pitch = y->row_pitch;
+  u.y_head_pitch = y->head_pitch;
+  u.mode = 0;
+  return launched(launch_payload_decode(u, lanes_for(in->dim), v8,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in* prev,
+                                       int32_t num_rows, const int32_t* pos, int32_t num_pos,
+                                       const kvq_packed* payload, int32_t* pos_out,
+                                       uint32_t* dev_status, kvq_stream_t stream) {
+  kvq_status st = check_packed(payload, "payload");
+  if (st != KVQ_OK) return st;
+  if (cur == nullptr || prev == nullptr) return fail(KVQ_ERR_INVALID_ARG, "cur or prev is NULL");
+  if (num_rows < 0 || num_pos < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_rows or num_pos");
+  if (pos == nullptr && num_pos != num_rows)
+    return fail(KVQ_ERR_INVALID_ARG, "dense residual (pos NULL) needs num_pos == num_rows");
+  if (payload->rows != num_pos)
+    return fail(KVQ_ERR_INVALID_ARG, "payload rows (%d) must equal num_pos (%d)", payload->rows,
+                num_pos);
+  if (num_pos == 0) return KVQ_OK;
+  bool v8 = true;
+  if ((st = check_view(cur->ptr, cur->row_pitch, cur->head_pitch, "cur", v8)) != KVQ_OK) return st;
+  if ((st = check_view(prev->ptr, prev->row_pitch, prev->head_pitch, "prev", v8)) != KVQ_OK)
+    return st;
+  if (pos != nullptr && (st = check_dev(pos, "pos")) != KVQ_OK) return st;
+  if (pos_out != nullptr && (st = check_dev(pos_out, "pos_out")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (payload->fmt == KVQ_FMT_NVFP4) {
+    EncodeParams p{};
+    EncodeTensor& t = p.ten[0];
+    t.x = static_cast<const uint16_t*>(cur->ptr);
+    t.row_pitch = cur->row_pitch;
+    t.head_pitch = cur->head_pitch;
+    t.prev = static_cast<const uint16_t*>(prev->ptr);
+    t.prev_row_pitch = prev->row_pitch;
+    t.prev_head_pitch = prev->head_pitch;
+    t.dst = Nvfp4Planes{payload->codes, static_cast<uint8_t*>(payload->meta0), payload->rscale};
+    p.ntensors = 1;
+    p.rows_per_tensor = static_cast<uint32_t>(num_pos) * static_cast<uint32_t>(payload->heads);
+    p.div_h = FastDiv(static_cast<uint32_t>(payload->heads));
+    p.H = payload->heads;
+    p.nb = payload->dim / 16;
+    p.pos = pos;
+    p.pos_out = pos_out;
+    p.src_rows = num_rows;
+    p.status = dev_status;
+    return launched(launch_nvfp4_encode(p, kEncResidual, lanes_for(payload->dim), v8, s));
+  }
+  Int4EncodeParams p{};
+  p.x = static_cast<const uint16_t*>(cur->ptr);
+  p.row_pitch = cur->row_pitch;
+  p.head_pitch = cur->head_pitch;
+  p.prev = static_cast<const uint16_t*>(prev->ptr);
+  p.prev_row_pitch = prev->row_pitch;
+  p.prev_head_pitch = prev->head_pitch;
+  p.dst = Int4Payload{payload->codes, static_cast<uint16_t*>(payload->meta0),
+                      static_cast<uint16_t*>(payload->meta1)};
+  p.rows = num_pos;
+  p.H = payload->heads;
+  p.D = payload->dim;
+  p.G = payload->group_size;
+  p.kind = payload->kind;
+  p.residual = 1;
+  p.pos = pos;
+  p.pos_out = pos_out;
+  p.src_rows = num_rows;
+  p.status = dev_status;
+  return launched(launch_int4_encode(p, s));
+}
+
+KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t* pos,
+                                       int32_t num_pos, const kvq_bf16_in* prev,
+                                       int32_t num_rows, const kvq_bf16_out* out,
+                                       uint32_t* dev_status, kvq_stream_t stream) {
+  kvq_status st = check_packed(payload, "payload");
+  if (st != KVQ_OK) return st;
+  if (prev == nullptr || out == nullptr) return fail(KVQ_ERR_INVALID_ARG, "prev or out is NULL");
+  if (num_rows < 0 || num_pos < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_rows or num_pos");
+  if (pos == nullptr && num_pos != num_rows)
+    return fail(KVQ_ERR_INVALID_ARG, "dense residual (pos NULL) needs num_pos == num_rows");
+  if (payload->rows != num_pos)
+    return fail(KVQ_ERR_INVALID_ARG, "payload rows (%d) must equal num_pos (%d)", payload->rows,
+                num_pos);
+  if (!fits_u31(static_cast<int64_t>(num_rows) * payload->heads))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_rows x heads too large");
+  const bool in_place = out->ptr == prev->ptr && out->row_pitch == prev->row_pitch &&
+                        out->head_pitch == prev->head_pitch;
+  if (num_rows == 0 || (in_place && num_pos == 0)) return KVQ_OK;
+  bool v8 = true;
+  if ((st = check_view(prev->ptr, prev->row_pitch, prev->head_pitch, "prev", v8)) != KVQ_OK)
+    return st;
+  if ((st = check_view(out->ptr, out->row_pitch, out->head_pitch, "out", v8)) != KVQ_OK) return st;
+  if (!in_place) {
+    // the two views must not share memory
+    const int64_t span = 2 * ((static_cast<int64_t>(num_rows) - 1) * prev->row_pitch +
+                              (static_cast<int64_t>(payload->heads) - 1) * prev->head_pitch +
+                              payload->dim);
+    const int64_t ospan = 2 * ((static_cast<int64_t>(num_rows) - 1) * out->row_pitch +
+                               (static_cast<int64_t>(payload->heads) - 1) * out->head_pitch +
+                               payload->dim);
+    const char* a = static_cast<const char*>(prev->ptr);
+    const char* b = static_cast<const char*>(out->ptr);
+    if (a < b + ospan && b < a + span)
+      return fail(KVQ_ERR_INVALID_ARG, "out overlaps prev without being the same view");
+  }
+  if (pos != nullptr && num_pos > 0 && (st = check_dev(pos, "pos")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+  UnpackParams u{};
+  u.pay = payload_ref(payload);
+  u.H = payload->heads;
+  u.D = payload->dim;
+  u.nb = payload->dim / 16;
+  u.div_h = FastDiv(static_cast<uint32_t>(payload->heads));
+  u.y = static_cast<uint16_t*>(out->ptr);
+  u.y_row_pitch = out->row_pitch;
+  u.y_head_pitch = out->head_pitch;
+  u.prev = static_cast<const uint16_t*>(prev->ptr);
+  u.prev_row_pitch = prev->row_pitch;
+  u.prev_head_pitch = prev->head_pitch;
+  u.pos = pos;  // non-NULL with num_pos == 0: every row is absent (never dereferenced)
+  u.num_pos = num_pos;
+  u.src_rows = num_rows;
+  u.status = dev_status;
+  if (in_place) {
+    u.mode = 1;
+    u.total_rows = static_cast<uint32_t>(num_pos) * static_cast<uint32_t>(payload->heads);
+  } else {
+    u.mode = 2;
+    u.total_rows = static_cast<uint32_t>(num_rows) * static_cast<uint32_t>(payload->heads);
+  }
+  return launched(launch_payload_decode(u, lanes_for(payload->dim), v8,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_size, int64_t rows,
+                                 int32_t heads, int32_t dim) {
+  if (rows < 0 || heads <= 0 || dim <= 0) return 0;
+  const int64_t rh = rows * heads;
+  if (fmt == KVQ_FMT_NVFP4) {
+    if (dim % 16 != 0) return 0;
+    return static_cast<size_t>(rh * (dim / 2 + dim / 16 + 4));
+  }
+  if (fmt == KVQ_FMT_INT4) {
+    if (dim % 2 != 0 || group_size <= 0) return 0;
+    const int64_t codes = rh * (dim / 2);
+    int64_t groups;
+    if (kind == KVQ_KIND_KEY)
+      groups = ((rows + group_size - 1) / group_size) * heads * dim;
+    else if (kind == KVQ_KIND_VALUE)
+      groups = rh * ((dim + group_size - 1) / group_size);
+    else
+      return 0;
+    return static_cast<size_t>(codes + groups * 4);
+  }
+  return 0;
+}
+
+KVQ_API const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_MISALIGNED: return "KVQ_ERR_MISALIGNED";
+    case KVQ_ERR_NOT_DEVICE_PTR: return "KVQ_ERR_NOT_DEVICE_PTR";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+  }
+  return "KVQ_ERR_UNKNOWN";
+}
+
+KVQ_API const char* kvq_last_error(void) { return g_last_error; }
+
+}  // extern "C"

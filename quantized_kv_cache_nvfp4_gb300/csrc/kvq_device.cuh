@@ -1,0 +1,194 @@
+// kvq_device.cuh -- device helpers shared by the codec kernels (sm_103a).
+//
+// Rounding contract: every floating-point step below is a single IEEE binary32
+// operation with round-to-nearest-even, written with the __f*_rn intrinsics so
+// that nvcc can neither contract a mul and an add into an FMA nor reorder them.
+// Denormals are kept (no -ftz, no fast math).  The FP4/FP8 conversions are the
+// hardware cvt instructions (.rn = nearest even, .satfinite = clamp to the
+// largest finite value); the tests check them code by code against the oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+constexpr float kE2M1Max = 6.0f;    // largest E2M1 magnitude
+constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 value
+
+// ---------------------------------------------------------------------------
+// memory
+// ---------------------------------------------------------------------------
+// 32 bytes = 16 bf16 = one NVFP4 block, read with one 256-bit load when the
+// address is 32-byte aligned (kV8) and with two 128-bit loads otherwise.
+// kNC selects the read-only path; it is off where a kernel may write the same
+// rows it reads (in-place residual decode).
+template <bool kV8, bool kNC>
+__device__ __forceinline__ void load32B(const void* p, uint32_t (&w)[8]) {
+  if constexpr (kV8 && kNC) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+          "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+  } else if constexpr (kV8) {
+    asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p)
+                 : "memory");
+  } else if constexpr (kNC) {
+    const char* c = static_cast<const char*>(p);
+    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "l"(c));
+    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(c + 16));
+  } else {
+    const char* c = static_cast<const char*>(p);
+    asm volatile("ld.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "l"(c)
+                 : "memory");
+    asm volatile("ld.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(c + 16)
+                 : "memory");
+  }
+}
+
+template <bool kV8>
+__device__ __forceinline__ void store32B(void* p, const uint32_t (&w)[8]) {
+  if constexpr (kV8) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    char* c = static_cast<char*>(p);
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(c), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3])
+                 : "memory");
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(c + 16), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7])
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void store8B(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void load8B(const void* p, uint32_t& a, uint32_t& b) {
+  asm("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
+}
+
+// ---------------------------------------------------------------------------
+// bf16 / fp16 / fp32
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2 (lo in bits 0..15), each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+  uint16_t h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+
+// Largest |x| of the 16 bf16 in w (returned as fp32).  Comparisons only: exact.
+__device__ __forceinline__ float absmax16(const uint32_t (&w)[8]) {
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    uint32_t a = w[i] & 0x7FFF7FFFu;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(a));
+  }
+  return fmaxf(bf16lo(m), bf16hi(m));
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 and E2M1
+// ---------------------------------------------------------------------------
+// Non-negative fp32 -> E4M3 byte, nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_from_f32(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+// E4M3 byte -> fp16x2 bits (the value in the low half; every E4M3 value is an
+// fp16 value, so this is exact).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  uint16_t in = static_cast<uint16_t>(byte & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+  return r;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  return f16_bits_to_f32(static_cast<uint16_t>(e4m3_to_f16x2(byte) & 0xFFFFu));
+}
+
+// Two fp32 -> one byte of E2M1 codes: `lo` in bits 0..3, `hi` in bits 4..7.
+// Nearest even, saturating at +-6, sign kept (including -0 and negatives that
+// round to zero).
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One byte of E2M1 codes -> fp16x2 (low nibble -> low half).  Exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+
+// fp16x2 * fp16x2, each half rounded to nearest even (exact for E2M1 x E4M3).
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) {
+  lo = f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
+  hi = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+  if (status != nullptr) atomicOr(status, bit);
+}
+
+// Width-limited butterfly reductions inside aligned groups of `kWidth` lanes.
+template <int kWidth>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = kWidth / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+template <int kWidth>
+__device__ __forceinline__ float group_min(float v) {
+#pragma unroll
+  for (int o = kWidth / 2; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+}  // namespace kvq

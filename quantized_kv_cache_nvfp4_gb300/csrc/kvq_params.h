@@ -1,0 +1,173 @@
+// kvq_params.h -- launch parameter blocks passed by value from the C ABI layer to
+// the kernels, and the host-side launch functions each kernel file defines.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// Exact unsigned division of n < 2^31 by a fixed divisor d >= 1 with one
+// multiply-high, an add and a shift (Granlund & Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, the round-up method):
+//   l = ceil(log2 d),  m = floor(2^32 * (2^l - d) / d) + 1,
+//   n / d = (mulhi(m, n) + n) >> l.
+// For n < 2^31 the sum cannot overflow 32 bits.
+struct FastDiv {
+  uint32_t d = 1, m = 0, l = 0;
+  FastDiv() = default;
+  explicit FastDiv(uint32_t div) : d(div) {
+    l = 0;
+    while ((1ull << l) < div) ++l;
+    uint64_t two_l = 1ull << l;
+    m = static_cast<uint32_t>(((two_l - div) << 32) / div + 1);
+  }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    uint32_t hi = __umulhi(m, n);
+#else
+    uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(m) * n) >> 32);
+#endif
+    return (hi + n) >> l;
+  }
+  __host__ __device__ __forceinline__ void divmod(uint32_t n, uint32_t& q, uint32_t& r) const {
+    q = div(n);
+    r = n - q * d;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// NVFP4 encode: quant-scatter, logical pack and residual encode share one kernel.
+// ---------------------------------------------------------------------------
+enum EncodeMode : int { kEncScatter = 0, kEncPack = 1, kEncResidual = 2 };
+
+struct Nvfp4Planes {
+  uint8_t* codes;   // [rows][D/2]  (rows = slot*H + h, or p*H + h)
+  uint8_t* bscale;  // [rows][D/16]
+  float* rscale;    // [rows]
+};
+
+struct EncodeTensor {
+  const uint16_t* x;     // bf16 source (residual: current)
+  int64_t row_pitch;     // elements
+  int64_t head_pitch;
+  const uint16_t* prev;  // residual: reconstructed predecessor
+  int64_t prev_row_pitch;
+  int64_t prev_head_pitch;
+  Nvfp4Planes dst;
+};
+
+struct EncodeParams {
+  EncodeTensor ten[2];
+  int32_t ntensors;         // 1 or 2
+  uint32_t rows_per_tensor; // tokens * H (residual: num_pos * H)
+  FastDiv div_h;            // by H
+  int32_t H;
+  int32_t nb;               // D / 16
+  const int64_t* slot_ids;  // scatter
+  int64_t num_slots;
+  const int32_t* pos;       // residual; nullptr = dense
+  int32_t* pos_out;
+  int32_t src_rows;         // residual: rows of cur/prev (positions must be below)
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// NVFP4 decode: paged restore and logical unpack.
+// ---------------------------------------------------------------------------
+enum DecodeMode : int { kDecRestore = 0, kDecUnpack = 1 };
+
+struct DecodeTensor {
+  const uint8_t* codes;
+  const uint8_t* bscale;
+  const float* rscale;
+  uint16_t* y;
+  int64_t row_pitch;
+  int64_t head_pitch;
+};
+
+struct DecodeParams {
+  DecodeTensor ten[2];
+  int32_t ntensors;
+  uint32_t rows_per_tensor;  // restore: S * Tmax * H; unpack: rows * H
+  FastDiv div_h;             // by H
+  FastDiv div_tmax;          // by Tmax (restore)
+  FastDiv div_bs;            // by block_size (restore)
+  int32_t H;
+  int32_t nb;
+  const int32_t* block_table;  // [S][max_blocks]
+  const int32_t* seq_lens;     // [S]
+  int32_t max_blocks;
+  int32_t tmax;
+  int32_t seq_cap;             // min(Tmax, max_blocks * block_size)
+  int64_t num_blocks;
+  int32_t block_size;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// INT4 affine codec and residual decode.
+// ---------------------------------------------------------------------------
+struct Int4Payload {
+  uint8_t* codes;   // [rows][H][D/2]
+  uint16_t* mn;     // fp16 bits
+  uint16_t* sc;     // fp16 bits
+};
+
+struct Int4EncodeParams {
+  const uint16_t* x;  // residual: current
+  int64_t row_pitch, head_pitch;
+  const uint16_t* prev;
+  int64_t prev_row_pitch, prev_head_pitch;
+  Int4Payload dst;
+  int32_t rows;       // compact rows (T, or num_pos)
+  int32_t H, D, G;
+  int32_t kind;       // 0 key, 1 value
+  int32_t residual;   // 0/1
+  const int32_t* pos;
+  int32_t* pos_out;
+  int32_t src_rows;
+  uint32_t* status;
+};
+
+// Decoder of a packed payload row into bf16, plus an optional residual add.
+struct PayloadRef {
+  int32_t fmt;         // 1 nvfp4, 2 int4
+  int32_t kind;
+  int32_t G;
+  const uint8_t* codes;
+  const void* meta0;   // nvfp4: bscale; int4: min
+  const void* meta1;   // int4: scale
+  const float* rscale; // nvfp4
+  int32_t rows;
+};
+
+struct UnpackParams {
+  PayloadRef pay;
+  int32_t H, D, nb;
+  FastDiv div_h;
+  uint32_t total_rows;  // rows * H of the iteration space
+  // plain unpack: y = decode(payload)
+  uint16_t* y;
+  int64_t y_row_pitch, y_head_pitch;
+  // residual decode: out = prev (+ decode at kept rows)
+  const uint16_t* prev;
+  int64_t prev_row_pitch, prev_head_pitch;
+  const int32_t* pos;   // nullptr = dense
+  int32_t num_pos;
+  int32_t src_rows;     // rows of prev/out
+  int32_t mode;         // 0 unpack, 1 residual in place (iterate kept rows), 2 residual out of place
+  uint32_t* status;
+};
+
+// Launchers (return the cudaGetLastError() of the launch).
+cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int lanes, bool v8,
+                                cudaStream_t s);
+cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int lanes, bool v8,
+                                cudaStream_t s);
+cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s);
+cudaError_t launch_payload_decode(const UnpackParams& p, int lanes, bool v8, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace kvq

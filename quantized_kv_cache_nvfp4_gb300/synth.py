@@ -96,12 +96,13 @@ def decode_step_case(seed: int = 2, T: int = 256, H: int = 8, D: int = 128,
 
 
 def residual_loops(T: int = 4096, H: int = 8, D: int = 128, loops: int = 4, seed: int = 4,
-                   step: float = 0.1):
-    """loop 0 ~ N(0,1); loop i = bf16(loop i-1 + step * N(0,1))."""
+                   step: float = 0.1, stream: int = STREAM_K):
+    """loop 0 ~ N(0,1); loop i = bf16(loop i-1 + step * N(0,1)).  One chain per
+    stream (K and V draw from different generators)."""
     out = []
-    prev = normal_bf16((T, H, D), seed, STREAM_K)
+    prev = normal_bf16((T, H, D), seed, stream)
     out.append(prev)
-    g = gen(seed, STREAM_STEP)
+    g = gen(seed, STREAM_STEP + 10 * stream)
     for _ in range(1, loops):
         noise = torch.randn((T, H, D), generator=g, dtype=torch.float32)
         prev = (prev.float() + step * noise).to(torch.bfloat16)

@@ -1,0 +1,85 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/kvq.h
+declares, and its host-only calls (storage accounting, status names, argument
+checks that fail before any CUDA call) behave as documented."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_six_codec_calls():
+    names = declared_symbols()
+    for n in ["kvq_pack", "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual",
+              "kvq_quant_scatter", "kvq_restore", "kvq_storage_bytes", "kvq_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvq_lib_path):
+    lib = ctypes.CDLL(kvq_lib_path)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq_lib_path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", out))
+    assert set(declared_symbols()) <= exported
+    # nothing but the ABI is exported from our own code
+    ours = {s for s in exported if s.startswith("kvq") or "kvq" in s}
+    assert ours == set(declared_symbols())
+
+
+def test_storage_bytes_agrees_with_the_oracle(kvq_lib_path):
+    import quantized_kv_cache_nvfp4_gb300 as kvq
+
+    for fmt in (1, 2):
+        for kind in (0, 1):
+            for G in (16, 64):
+                for (T, H, D) in [(1, 1, 128), (256, 8, 128), (4100, 8, 96), (1048576, 4, 256), (0, 2, 32)]:
+                    g = 16 if fmt == 1 else G
+                    assert kvq.kvq_storage_bytes(fmt, kind, g, T, H, D) == O.storage_bytes(fmt, kind, g, T, H, D)
+    assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 128) == 76
+    assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 100) == 0
+    assert kvq.kvq_storage_bytes(9, 0, 16, 1, 1, 128) == 0
+
+
+def test_status_strings(kvq_lib_path):
+    import quantized_kv_cache_nvfp4_gb300 as kvq
+
+    assert [kvq.kvq_status_string(i) for i in range(6)] == [
+        "KVQ_OK", "KVQ_ERR_INVALID_ARG", "KVQ_ERR_UNSUPPORTED", "KVQ_ERR_MISALIGNED",
+        "KVQ_ERR_NOT_DEVICE_PTR", "KVQ_ERR_CUDA"]
+
+
+def test_host_checks_fail_before_any_cuda_call(kvq_lib_path):
+    from quantized_kv_cache_nvfp4_gb300 import _abi
+
+    lib = _abi.load()
+    pool = _abi.Nvfp4Pool(_abi.Nvfp4Plane(), _abi.Nvfp4Plane(), 64, 16, 2, 100)
+    x = _abi.Bf16In(None, 256, 128)
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
+    assert b"multiple of 16" in lib.kvq_last_error()
+    pool.head_dim = 1024
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 2
+    pool.head_dim = 128
+    pool.num_slots = 65
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
+    assert lib.kvq_quant_scatter(None, None, 4, None, ctypes.byref(pool), None, None) == 1
+    pk = _abi.Packed(2, 0, 48, 4, 2, 128, None, None, None, None)
+    assert lib.kvq_pack(ctypes.byref(x), ctypes.byref(pk), None) == 2
+    pk = _abi.Packed(7, 0, 64, 4, 2, 128, None, None, None, None)
+    assert lib.kvq_unpack(ctypes.byref(pk), None, None) == 1
+    # zero-sized work is a no-op that needs no pointers
+    pool.num_slots = 64
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 0, None, ctypes.byref(pool), None, None) == 0
+    pk = _abi.Packed(2, 0, 64, 0, 2, 128, None, None, None, None)
+    assert lib.kvq_pack(ctypes.byref(x), ctypes.byref(pk), None) == 0

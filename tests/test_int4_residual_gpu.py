@@ -1,0 +1,200 @@
+"""INT4 affine codec and residual encode/decode on the GPU through the C ABI,
+compared bit for bit with the CPU oracle (codes, FP16 metadata, position maps and
+reconstructed bf16)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import quantized_kv_cache_nvfp4_gb300 as kvq
+from quantized_kv_cache_nvfp4_gb300 import synth
+from kvq_testutil import POISON, bits, f16bits, f32bits, poison_bf16, status_word, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def gpu_int4_pack(x, kind, G=64):
+    T, H, D = x.shape
+    pk = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G)
+    kvq.kvq_pack(x, pk)
+    y = poison_bf16((T, H, D))
+    kvq.kvq_unpack(pk, y)
+    torch.cuda.synchronize()
+    return pk, y
+
+
+def check_int4(pk, codes, mn, sc):
+    np.testing.assert_array_equal(u8(pk.codes), codes, err_msg="codes")
+    np.testing.assert_array_equal(f16bits(pk.meta0), mn, err_msg="fp16 minimum")
+    np.testing.assert_array_equal(f16bits(pk.meta1), sc, err_msg="fp16 scale")
+
+
+def check_payload(pay, opay):
+    np.testing.assert_array_equal(u8(pay.codes), opay["codes"], err_msg="payload codes")
+    if pay.fmt == kvq.FMT_INT4:
+        np.testing.assert_array_equal(f16bits(pay.meta0), opay["meta_a"], err_msg="payload min")
+        np.testing.assert_array_equal(f16bits(pay.meta1), opay["meta_b"], err_msg="payload scale")
+    else:
+        np.testing.assert_array_equal(u8(pay.meta0), opay["meta_a"], err_msg="payload block scales")
+        np.testing.assert_array_equal(f32bits(pay.rscale), f32bits(opay["rscale"]), err_msg="row scales")
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+@pytest.mark.parametrize("T,H,D,G", [(256, 8, 128, 64), (4100, 2, 128, 64), (130, 3, 96, 64),
+                                     (64, 2, 32, 64), (200, 2, 128, 16), (77, 1, 512, 512)])
+def test_int4_pack_unpack_matches_oracle(kind, T, H, D, G):
+    x = synth.normal_bf16((T, H, D), seed=50 + T, stream=1, outlier_frac=0.01, outlier_scale=20.0)
+    pk, y = gpu_int4_pack(x.to(DEV), kind, G)
+    codes, mn, sc = O.int4_pack(bits(x), kind, G)
+    check_int4(pk, codes, mn, sc)
+    np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, G))
+
+
+def test_int4_constant_and_exact_groups():
+    x = torch.full((64, 2, 32), 0.3, dtype=torch.bfloat16)
+    x[:, 1] = torch.arange(32, dtype=torch.float32).remainder(16).to(torch.bfloat16)  # exact grid
+    for kind in (kvq.KIND_KEY, kvq.KIND_VALUE):
+        pk, y = gpu_int4_pack(x.to(DEV), kind)
+        codes, mn, sc = O.int4_pack(bits(x), kind, 64)
+        check_int4(pk, codes, mn, sc)
+        np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
+
+
+def _chain(kind, fmt_res, T=4096, H=8, D=128, P=1024, loops=4, seed=4, inplace_check=True):
+    """Base INT4 pack of loop 0, then loops 1.. residual-encoded against the
+    reconstructed predecessor with P kept rows; every step checked against the oracle."""
+    stream = synth.STREAM_K if kind == kvq.KIND_KEY else synth.STREAM_V
+    L = synth.residual_loops(T, H, D, loops, seed, stream=stream)
+    pk, recon = gpu_int4_pack(L[0].to(DEV), kind)
+    codes, mn, sc = O.int4_pack(bits(L[0]), kind, 64)
+    check_int4(pk, codes, mn, sc)
+    recon_o = O.int4_unpack(codes, mn, sc, kind, 64)
+    np.testing.assert_array_equal(bits(recon), recon_o)
+    st = status_word()
+    for i in range(1, loops):
+        pos = synth.sorted_positions(T, P, seed, stream=synth.STREAM_POS + i) if P is not None else None
+        n = T if pos is None else P
+        pay = kvq.Packed.empty(fmt_res, kind, n, H, D, 64)
+        pos_out = torch.full((max(n, 1),), -7, dtype=torch.int32, device=DEV)[:n]
+        posd = pos.to(DEV) if pos is not None else None
+        kvq.kvq_encode_residual(L[i].to(DEV), recon, posd, pay, pos_out if pos is not None else None, st)
+        nxt = poison_bf16((T, H, D))
+        kvq.kvq_decode_residual(pay, posd, recon, nxt, st)
+        if inplace_check:
+            ip = recon.clone()
+            kvq.kvq_decode_residual(pay, posd, ip, ip, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        opay, ost = O.residual_encode(bits(L[i]), recon_o, None if pos is None else pos.numpy(), fmt_res, kind, 64)
+        assert ost == 0
+        check_payload(pay, opay)
+        if pos is not None:
+            np.testing.assert_array_equal(pos_out.cpu().numpy(), pos.numpy())
+        recon_o, _ = O.residual_decode(opay, recon_o)
+        np.testing.assert_array_equal(bits(nxt), recon_o, err_msg=f"loop {i} reconstruction")
+        if inplace_check:
+            assert torch.equal(ip.view(torch.int16), nxt.view(torch.int16))
+        recon = nxt
+    return recon
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_g64_residual_chain_sparse_quarter_rows(kind):
+    """4 loops of [4096, 8, 128]; loops 1-3 keep 25% of rows (int32 position map)."""
+    _chain(kind, kvq.FMT_INT4)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_dense_residual_chain(kind):
+    _chain(kind, kvq.FMT_INT4, T=1000, H=2, D=64, P=None)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_base_nvfp4_residual_chain(kind):
+    """A mixed chain: INT4 base, NVFP4 residual rows."""
+    _chain(kind, kvq.FMT_NVFP4, T=600, H=3, D=96, P=150)
+
+
+def test_ragged_compact_groups_and_odd_sizes():
+    _chain(kvq.KIND_KEY, kvq.FMT_INT4, T=777, H=1, D=48, P=333, loops=3)
+
+
+def test_empty_and_full_position_maps_and_bad_maps():
+    T, H, D = 128, 2, 32
+    cur = synth.normal_bf16((T, H, D), 60, 1).to(DEV)
+    prev = synth.normal_bf16((T, H, D), 60, 2).to(DEV)
+    st = status_word()
+    # empty map: nothing kept, out == prev (copy and in place)
+    empty = torch.zeros(0, dtype=torch.int32, device=DEV)
+    pay = kvq.Packed.empty(kvq.FMT_INT4, kvq.KIND_KEY, 0, H, D, 64)
+    kvq.kvq_encode_residual(cur, prev, empty, pay, None, st)
+    out = poison_bf16((T, H, D))
+    kvq.kvq_decode_residual(pay, empty, prev, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out.view(torch.int16), prev.view(torch.int16))
+    # every row kept == dense, bitwise
+    allpos = torch.arange(T, dtype=torch.int32, device=DEV)
+    for fmt, kind in ((kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_INT4, kvq.KIND_VALUE), (kvq.FMT_NVFP4, 0)):
+        a = kvq.Packed.empty(fmt, kind, T, H, D, 64)
+        b = kvq.Packed.empty(fmt, kind, T, H, D, 64)
+        kvq.kvq_encode_residual(cur, prev, allpos, a, None, st)
+        kvq.kvq_encode_residual(cur, prev, None, b, None, st)
+        oa, ob = poison_bf16((T, H, D)), poison_bf16((T, H, D))
+        kvq.kvq_decode_residual(a, allpos, prev, oa, st)
+        kvq.kvq_decode_residual(b, None, prev, ob, st)
+        torch.cuda.synchronize()
+        assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+        assert torch.equal(a.codes, b.codes)
+    assert int(st.item()) == 0
+    # unsorted / out-of-range maps are flagged, and nothing faults
+    for bad in ([5, 3, 9], [1, 1, 2], [-1, 4, 6], [2, 4, T]):
+        st.zero_()
+        pos = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        for fmt, kind in ((kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_INT4, kvq.KIND_VALUE), (kvq.FMT_NVFP4, 0)):
+            pay = kvq.Packed.empty(fmt, kind, 3, H, D, 64)
+            kvq.kvq_encode_residual(cur, prev, pos, pay, None, st)
+            o = prev.clone()
+            kvq.kvq_decode_residual(pay, pos, o, o, st)
+            o2 = poison_bf16((T, H, D))
+            kvq.kvq_decode_residual(pay, pos, prev, o2, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & kvq.DEV_BAD_POS, bad
+    # the context is still healthy
+    torch.cuda.synchronize()
+
+
+def test_zero_residual_reproduces_prev_bitwise():
+    T, H, D = 300, 2, 64
+    prev = synth.normal_bf16((T, H, D), 61, 1).to(DEV)
+    pos = synth.sorted_positions(T, 100, 61).to(DEV)
+    for fmt, kind in ((kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_INT4, kvq.KIND_VALUE), (kvq.FMT_NVFP4, 0)):
+        pay = kvq.Packed.empty(fmt, kind, 100, H, D, 64)
+        kvq.kvq_encode_residual(prev, prev, pos, pay)
+        out = poison_bf16((T, H, D))
+        kvq.kvq_decode_residual(pay, pos, prev, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), prev.view(torch.int16))
+
+
+def test_residual_with_strided_views():
+    """cur a strided view (row pitch 3*H*D), prev contiguous, out a strided view."""
+    T, H, D = 200, 2, 64
+    big = synth.normal_bf16((T, 3 * H * D), 62, 1).to(DEV)
+    cur = big[:, H * D:2 * H * D].unflatten(1, (H, D))
+    prev = synth.normal_bf16((T, H, D), 62, 2).to(DEV)
+    pos = synth.sorted_positions(T, 64, 62).to(DEV)
+    for fmt, kind in ((kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_NVFP4, 0)):
+        pay = kvq.Packed.empty(fmt, kind, 64, H, D, 64)
+        kvq.kvq_encode_residual(cur, prev, pos, pay)
+        outbig = poison_bf16((T, 2 * H * D))
+        out = outbig[:, H * D:].unflatten(1, (H, D))
+        kvq.kvq_decode_residual(pay, pos, prev, out)
+        torch.cuda.synchronize()
+        opay, _ = O.residual_encode(bits(cur), bits(prev), pos.cpu().numpy(), fmt, kind, 64)
+        check_payload(pay, opay)
+        want, _ = O.residual_decode(opay, bits(prev))
+        np.testing.assert_array_equal(bits(out), want)
+        assert (bits(outbig[:, :H * D]) == 0xA5A5).all()

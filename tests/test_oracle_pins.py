@@ -614,11 +614,11 @@ def test_scatter_reads_each_tensor_with_its_own_pitch():
     """FreeToken PR #408, the V-pitch fix: K a view of a fused qkv (row pitch 1152,
     column offset 384) and V contiguous (pitch 384), 8 tokens x 3 heads x 128."""
     T, H, D = 8, 3, 128
-    qkv = synth.bf16_bits(synth.normal_bf16((T, 1152 + 384), 23, 1))
+    qkv = synth.bf16_bits(synth.normal_bf16((T, 1152), 23, 1))
     v = synth.bf16_bits(synth.normal_bf16((T, H * D), 23, 2))
     poolk, poolv = O.new_pool(16, H, D), O.new_pool(16, H, D)
     slots = np.arange(T, dtype=np.int64)[::-1].copy()
-    assert O.nvfp4_scatter(qkv.ravel()[384:], 1152 + 384, D, T, H, D, slots, poolk) == 0
+    assert O.nvfp4_scatter(qkv.ravel()[384:], 1152, D, T, H, D, slots, poolk) == 0
     assert O.nvfp4_scatter(v, H * D, D, T, H, D, slots, poolv) == 0
     kc = np.ascontiguousarray(qkv[:, 384:384 + H * D]).reshape(T, H, D)
     ck, bk, rk = O.nvfp4_encode_rows(kc)
