@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -21,7 +22,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD_DIR = os.path.join(ROOT, "_build")
+BUILD_DIR = os.path.join(ROOT, "_build", platform.machine())
 LIB = os.path.join(PKG, "libkvq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
