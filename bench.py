@@ -225,9 +225,9 @@ def run_ours(args):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     dist = init_dist(world, "nccl")
-    T, H, D, bs = T_TOKENS, HEADS, HEAD_DIM, BLOCK
+    T, H, D, bs = args.tokens, HEADS, HEAD_DIM, BLOCK
     nblocks = T // bs
-    k, v, slots, table, lens = make_workload(device, seed=SEED + 1000 * rank)
+    k, v, slots, table, lens = make_workload(device, seed=SEED + 1000 * rank, T=T)
     pool = kvq.Nvfp4Pool.empty(T, H, D, bs, device=device)
     ko = torch.empty((1, T, H, D), dtype=torch.bfloat16, device=device)
     vo = torch.empty_like(ko)
@@ -276,7 +276,7 @@ def run_ours(args):
     rmse = float((vo[0].float() - v.float()).pow(2).mean().sqrt().item())
     st_final = int(status.item())
 
-    e2e = run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist) if not args.no_e2e else None
+    e2e = run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist, T) if not args.no_e2e else None
 
     if rank != 0:
         if dist is not None:
@@ -304,7 +304,7 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded N(0,1) bf16 with 0.5% x50 outliers, generated on the GPU)",
         "config": {
-            "workload": WORKLOAD, "tokens": T, "kv_heads": H, "head_dim": D, "block_size": BLOCK,
+            "workload": WORKLOAD if T == T_TOKENS else WORKLOAD.replace("1,048,576", f"{T:,}"), "tokens": T, "kv_heads": H, "head_dim": D, "block_size": BLOCK,
             "pool_slots": T, "parallelism": f"replicas x{world}", "l2": "inputs and outputs larger than L2 (no flush)",
             "bytes_per_step": step_bytes,
         },
@@ -334,10 +334,10 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist):
+def run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist, T):
     """Same metric through the public API with host buffers: every step copies the
     step's inputs host->device (pinned) and the restored K/V device->host."""
-    T, H, D = T_TOKENS, HEADS, HEAD_DIM
+    H, D = HEADS, HEAD_DIM
     hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
     hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
     hs = torch.empty(slots.shape, dtype=slots.dtype, pin_memory=True)
@@ -475,6 +475,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=16384)
+    ap.add_argument("--tokens", type=int, default=T_TOKENS,
+                    help="tokens of the workload (default: the 1,048,576-token case); smaller "
+                         "values give the same kernels on a smaller case for profiling")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

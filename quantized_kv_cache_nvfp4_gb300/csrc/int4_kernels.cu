@@ -42,14 +42,14 @@ __device__ __forceinline__ bool load_chunk8(const Int4EncodeParams& p, int32_t r
     }
   }
   const uint16_t* a = p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col;
-  asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
       : "l"(a));
   if constexpr (kResidual) {
     uint32_t q[4];
     const uint16_t* b =
         p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col;
-    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
         : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
         : "l"(b));
 #pragma unroll

@@ -26,7 +26,7 @@ constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 value
 template <bool kV8, bool kNC>
 __device__ __forceinline__ void load32B(const void* p, uint32_t (&w)[8]) {
   if constexpr (kV8 && kNC) {
-    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
           "=r"(w[6]), "=r"(w[7])
         : "l"(p));
@@ -38,10 +38,10 @@ __device__ __forceinline__ void load32B(const void* p, uint32_t (&w)[8]) {
                  : "memory");
   } else if constexpr (kNC) {
     const char* c = static_cast<const char*>(p);
-    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
         : "l"(c));
-    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
         : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
         : "l"(c + 16));
   } else {
@@ -79,7 +79,7 @@ __device__ __forceinline__ void store8B(void* p, uint32_t a, uint32_t b) {
 }
 
 __device__ __forceinline__ void load8B(const void* p, uint32_t& a, uint32_t& b) {
-  asm("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
+  asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
 }
 
 // ---------------------------------------------------------------------------
