@@ -51,11 +51,12 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, verbose: bool, checked: bool = False) -> str:
+    bdir = BUILD_DIR + ("-checked" if checked else "")
+    obj = os.path.join(bdir, os.path.basename(src) + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) > max(os.path.getmtime(src), _headers_mtime()):
         return obj
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *NVCC_FLAGS, *(["-DKVQ_CHECKED"] if checked else []), "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -66,22 +67,28 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Compile and link libkvq.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link libkvq.so; returns its path.
+
+    checked=True builds libkvq_checked.so instead: a debugging variant in which
+    every global access of every kernel is tested against the buffer ranges of its
+    launch, recorded and skipped when out of range, and each launch is followed by
+    a synchronisation and a one-line report on stderr."""
+    os.makedirs(BUILD_DIR + ("-checked" if checked else ""), exist_ok=True)
+    out = LIB.replace("libkvq.so", "libkvq_checked.so") if checked else LIB
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) > max(os.path.getmtime(o) for o in objs):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, checked), srcs))
+    if os.path.exists(out) and os.path.getmtime(out) > max(os.path.getmtime(o) for o in objs):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libkvq.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -35,23 +35,16 @@ __device__ __forceinline__ bool load_chunk8(const Int4EncodeParams& p, int32_t r
                                             int32_t col, uint32_t (&w)[4]) {
   int64_t src = row;
   if constexpr (kResidual) {
-    if (p.pos != nullptr) src = p.pos[row];
+    if (p.pos != nullptr) src = LDX(p.pos + row);
     if (src < 0 || src >= p.src_rows) {
       w[0] = w[1] = w[2] = w[3] = 0u;
       return false;
     }
   }
-  const uint16_t* a = p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col;
-  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-      : "l"(a));
+  load16B(p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col, w);
   if constexpr (kResidual) {
     uint32_t q[4];
-    const uint16_t* b =
-        p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col;
-    asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
-        : "l"(b));
+    load16B(p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col, q);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       w[i] = pack_bf16x2(__fsub_rn(bf16lo(w[i]), bf16lo(q[i])),
@@ -64,11 +57,11 @@ template <bool kResidual>
 __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row) {
   if constexpr (kResidual) {
     if (p.pos == nullptr) return;
-    const int32_t ps = p.pos[row];
+    const int32_t ps = LDX(p.pos + row);
     bool bad = ps < 0 || ps >= p.src_rows;
-    if (row > 0 && p.pos[row - 1] >= ps) bad = true;
+    if (row > 0 && LDX(p.pos + row - 1) >= ps) bad = true;
     if (bad) set_status(p.status, 4u);
-    if (p.pos_out != nullptr) p.pos_out[row] = ps;
+    if (p.pos_out != nullptr) STX(p.pos_out + row, ps);
   }
 }
 
@@ -124,8 +117,9 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
             sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1]) : 0u;
         packed |= (cl | (ch << 4)) << (8 * i);
       }
-      *reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
-                                   col / 2) = packed;
+      STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
+                                      col / 2),
+          packed);
     }
     uint32_t m16[4], s16[4];
 #pragma unroll
@@ -136,12 +130,8 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
                (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
     }
     const int64_t m = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
-    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p.dst.mn + m), "r"(m16[0]),
-                 "r"(m16[1]), "r"(m16[2]), "r"(m16[3])
-                 : "memory");
-    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p.dst.sc + m), "r"(s16[0]),
-                 "r"(s16[1]), "r"(s16[2]), "r"(s16[3])
-                 : "memory");
+    store16B(p.dst.mn + m, m16);
+    store16B(p.dst.sc + m, s16);
   }
 }
 
@@ -212,8 +202,8 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     store8B(p.dst.codes + drow * (p.D / 2) + 8 * b, c0, c1);
     if ((16 * b) % p.G == 0) {
       const int64_t m = drow * ngv + (16 * b) / p.G;
-      p.dst.mn[m] = f32_to_f16_bits(lmn);
-      p.dst.sc[m] = f32_to_f16_bits(sc);
+      STX(p.dst.mn + m, f32_to_f16_bits(lmn));
+      STX(p.dst.sc + m, f32_to_f16_bits(sc));
     }
   }
 }
@@ -233,8 +223,9 @@ template <int L, bool kRes>
 cudaError_t value_launch(const Int4EncodeParams& p, cudaStream_t s) {
   auto k = int4_value_kernel<L, kRes>;
   int grid = grid_cap(k, static_cast<int64_t>(p.rows) * p.H, (kThreads / 32) * (32 / L));
-  k<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("int4_value_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
+  return e;
 }
 
 template <bool kRes>
@@ -257,14 +248,17 @@ cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s) {
   if (p.kind == 0) {
     const int64_t tasks = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
+    cudaError_t e = cudaSuccess;
     if (p.residual) {
       auto k = int4_key_kernel<true>;
-      k<<<grid_cap(k, tasks, kThreads), kThreads, 0, s>>>(p);
+      const int grid = grid_cap(k, tasks, kThreads);
+      KVQ_LAUNCH("int4_key_kernel<res>", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
     } else {
       auto k = int4_key_kernel<false>;
-      k<<<grid_cap(k, tasks, kThreads), kThreads, 0, s>>>(p);
+      const int grid = grid_cap(k, tasks, kThreads);
+      KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
     }
-    return cudaGetLastError();
+    return e;
   }
   return p.residual ? value_dispatch<true>(p, s) : value_dispatch<false>(p, s);
 }

@@ -5,6 +5,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "kvq.h"
@@ -22,6 +23,37 @@ kvq_status fail(kvq_status st, const char* fmt, ...) {
   vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
   va_end(ap);
   return st;
+}
+
+// Checked build: the byte ranges of the next launch (see kvq_device.cuh).
+thread_local dbg::HostRange g_ranges[32];
+thread_local int g_nranges = 0;
+
+void dbg_clear() { g_nranges = 0; }
+void dbg_add(const void* p, int64_t bytes, const char* name) {
+  if (p == nullptr || bytes <= 0 || g_nranges >= 32) return;
+  const unsigned long long lo = reinterpret_cast<unsigned long long>(p);
+  g_ranges[g_nranges++] = dbg::HostRange{lo, lo + static_cast<unsigned long long>(bytes), name};
+}
+// Bytes spanned by a bf16 view of `rows` rows.
+int64_t view_bytes(int64_t rows, int64_t row_pitch, int64_t heads, int64_t head_pitch, int64_t dim) {
+  if (rows <= 0) return 0;
+  return 2 * ((rows - 1) * row_pitch + (heads - 1) * head_pitch + dim);
+}
+void dbg_packed(const kvq_packed* pk) {
+  const int64_t rh = static_cast<int64_t>(pk->rows) * pk->heads;
+  dbg_add(pk->codes, rh * (pk->dim / 2), "codes");
+  if (pk->fmt == KVQ_FMT_NVFP4) {
+    dbg_add(pk->meta0, rh * (pk->dim / 16), "bscale");
+    dbg_add(pk->rscale, rh * 4, "rscale");
+  } else {
+    const int G = pk->group_size;
+    const int64_t n = pk->kind == KVQ_KIND_KEY
+                          ? static_cast<int64_t>((pk->rows + G - 1) / G) * pk->heads * pk->dim
+                          : rh * ((pk->dim + G - 1) / G);
+    dbg_add(pk->meta0, 2 * n, "min16");
+    dbg_add(pk->meta1, 2 * n, "scale16");
+  }
 }
 
 constexpr int kMaxDevices = 64;
@@ -62,6 +94,9 @@ kvq_status check_view(const void* ptr, int64_t row_pitch, int64_t head_pitch, co
     return fail(KVQ_ERR_MISALIGNED,
                 "%s: base must be 16-byte aligned and pitches multiples of 8 elements", what);
   v8 = v8 && aligned(ptr, 32) && row_pitch % 16 == 0 && head_pitch % 16 == 0;
+#ifdef KVQ_CHECKED
+  if (getenv("KVQ_FORCE_V4") != nullptr) v8 = false;
+#endif
   return KVQ_OK;
 }
 
@@ -140,6 +175,11 @@ PayloadRef payload_ref(const kvq_packed* pk) {
 
 }  // namespace
 
+dbg::HostRange* dbg::pending(int* n) {
+  *n = g_nranges;
+  return g_ranges;
+}
+
 int num_sms() {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -203,6 +243,17 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
   p.slot_ids = slot_ids;
   p.num_slots = pool->num_slots;
   p.status = dev_status;
+  dbg_clear();
+  for (int j = 0; j < 2; ++j) {
+    if (src[j] == nullptr) continue;
+    dbg_add(src[j]->ptr, view_bytes(num_tokens, src[j]->row_pitch, pool->num_heads, src[j]->head_pitch, pool->head_dim), names[j]);
+    const int64_t rh = pool->num_slots * pool->num_heads;
+    dbg_add(dst[j]->codes, rh * (pool->head_dim / 2), "pool codes");
+    dbg_add(dst[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(dst[j]->rscale, rh * 4, "pool rscale");
+  }
+  dbg_add(slot_ids, 8ll * num_tokens, "slot_ids");
+  dbg_add(dev_status, 4, "status");
   return launched(launch_nvfp4_encode(p, kEncScatter, lanes_for(pool->head_dim), v8,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -267,6 +318,18 @@ KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_
   p.num_blocks = pool->num_slots / pool->block_size;
   p.block_size = pool->block_size;
   p.status = dev_status;
+  dbg_clear();
+  for (int j = 0; j < 2; ++j) {
+    if (out[j] == nullptr) continue;
+    dbg_add(out[j]->ptr, view_bytes(static_cast<int64_t>(num_seqs) * max_seq_len, out[j]->row_pitch, pool->num_heads, out[j]->head_pitch, pool->head_dim), names[j]);
+    const int64_t rh = pool->num_slots * pool->num_heads;
+    dbg_add(src[j]->codes, rh * (pool->head_dim / 2), "pool codes");
+    dbg_add(src[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(src[j]->rscale, rh * 4, "pool rscale");
+  }
+  dbg_add(block_table, 4ll * num_seqs * max_blocks, "block_table");
+  dbg_add(seq_lens, 4ll * num_seqs, "seq_lens");
+  dbg_add(dev_status, 4, "status");
   return launched(launch_nvfp4_decode(p, kDecRestore, lanes_for(pool->head_dim), v8,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -279,6 +342,9 @@ KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_str
   bool v8 = true;
   if ((st = check_view(x->ptr, x->row_pitch, x->head_pitch, "x", v8)) != KVQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dbg_clear();
+  dbg_add(x->ptr, view_bytes(out->rows, x->row_pitch, out->heads, x->head_pitch, out->dim), "x");
+  dbg_packed(out);
   if (out->fmt == KVQ_FMT_NVFP4) {
     EncodeParams p{};
     p.ten[0].x = static_cast<const uint16_t*>(x->ptr);
@@ -326,6 +392,9 @@ KVQ_API kvq_status kvq_unpack(const kvq_packed* in, const kvq_bf16_out* y, kvq_s
   u.y_row_pitch = y->row_pitch;
   u.y_head_pitch = y->head_pitch;
   u.mode = 0;
+  dbg_clear();
+  dbg_add(y->ptr, view_bytes(in->rows, y->row_pitch, in->heads, y->head_pitch, in->dim), "y");
+  dbg_packed(in);
   return launched(launch_payload_decode(u, lanes_for(in->dim), v8,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -352,6 +421,13 @@ KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in
   if (pos_out != nullptr && (st = check_dev(pos_out, "pos_out")) != KVQ_OK) return st;
   if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dbg_clear();
+  dbg_add(cur->ptr, view_bytes(num_rows, cur->row_pitch, payload->heads, cur->head_pitch, payload->dim), "cur");
+  dbg_add(prev->ptr, view_bytes(num_rows, prev->row_pitch, payload->heads, prev->head_pitch, payload->dim), "prev");
+  dbg_packed(payload);
+  dbg_add(pos, 4ll * num_pos, "pos");
+  dbg_add(pos_out, 4ll * num_pos, "pos_out");
+  dbg_add(dev_status, 4, "status");
   if (payload->fmt == KVQ_FMT_NVFP4) {
     EncodeParams p{};
     EncodeTensor& t = p.ten[0];
@@ -448,6 +524,13 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
   u.num_pos = num_pos;
   u.src_rows = num_rows;
   u.status = dev_status;
+  dbg_clear();
+  dbg_add(prev->ptr, view_bytes(num_rows, prev->row_pitch, payload->heads, prev->head_pitch, payload->dim), "prev");
+  if (!in_place)
+    dbg_add(out->ptr, view_bytes(num_rows, out->row_pitch, payload->heads, out->head_pitch, payload->dim), "out");
+  dbg_packed(payload);
+  if (num_pos > 0) dbg_add(pos, 4ll * num_pos, "pos");
+  dbg_add(dev_status, 4, "status");
   if (in_place) {
     u.mode = 1;
     u.total_rows = static_cast<uint32_t>(num_pos) * static_cast<uint32_t>(payload->heads);

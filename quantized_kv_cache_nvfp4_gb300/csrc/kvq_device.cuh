@@ -13,6 +13,112 @@
 
 namespace kvq {
 
+// ---------------------------------------------------------------------------
+// checked build (-DKVQ_CHECKED, a debugging aid, never the product library):
+// every global access is tested against the byte ranges the host registered for
+// the launch and against its alignment; a bad access is counted, the first one
+// recorded, and the access skipped.  Each translation unit has its own copy of
+// these symbols, set by that unit's launchers.
+// ---------------------------------------------------------------------------
+#ifdef KVQ_CHECKED
+namespace dbg {
+struct Range {
+  unsigned long long lo, hi;
+};
+static __device__ Range g_ranges[32];
+static __device__ int g_nranges;
+static __device__ unsigned long long g_bad[4];  // count, first address, bytes, line
+
+__device__ __forceinline__ bool ok(const void* p, unsigned bytes, unsigned align, unsigned line) {
+  const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+  bool good = (a % align) == 0;
+  if (good) {
+    good = false;
+    for (int i = 0; i < g_nranges; ++i)
+      if (a >= g_ranges[i].lo && a + bytes <= g_ranges[i].hi) {
+        good = true;
+        break;
+      }
+  }
+  if (!good && atomicAdd(&g_bad[0], 1ull) == 0ull) {
+    g_bad[1] = a;
+    g_bad[2] = bytes;
+    g_bad[3] = line;
+  }
+  return good;
+}
+}  // namespace dbg
+#define KVQ_OK(p, n, a) ::kvq::dbg::ok((p), (n), (a), __LINE__)
+}  // namespace kvq
+#include <cstdio>
+#include "kvq_params.h"
+namespace kvq {
+namespace dbg {
+// Host side, per translation unit: copy the registered ranges before a launch,
+// synchronise after it and print what the kernel recorded.
+static inline void before() {
+  int n = 0;
+  HostRange* r = pending(&n);
+  Range dr[32];
+  for (int i = 0; i < n; ++i) dr[i] = Range{r[i].lo, r[i].hi};
+  cudaMemcpyToSymbol(g_ranges, dr, sizeof(Range) * 32);
+  cudaMemcpyToSymbol(g_nranges, &n, sizeof(int));
+  unsigned long long z[4] = {0, 0, 0, 0};
+  cudaMemcpyToSymbol(g_bad, z, sizeof(z));
+}
+static inline void after(const char* kernel, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  unsigned long long bad[4] = {0, 0, 0, 0};
+  if (e == cudaSuccess) cudaMemcpyFromSymbol(bad, g_bad, sizeof(bad));
+  int n = 0;
+  HostRange* r = pending(&n);
+  std::fprintf(stderr, "[kvq checked] %s: sync=%s bad=%llu", kernel, cudaGetErrorString(e), bad[0]);
+  if (bad[0]) {
+    std::fprintf(stderr, " first=0x%llx bytes=%llu line=%llu", bad[1], bad[2], bad[3]);
+    for (int i = 0; i < n; ++i)
+      std::fprintf(stderr, " | %s [0x%llx,0x%llx) off=%lld", r[i].name, r[i].lo, r[i].hi,
+                   static_cast<long long>(bad[1] - r[i].lo));
+  }
+  std::fprintf(stderr, "\n");
+}
+}  // namespace dbg
+#else
+#define KVQ_OK(p, n, a) true
+#endif
+
+#ifdef KVQ_CHECKED
+#define KVQ_LAUNCH(name, stream, ...) \
+  do {                                \
+    ::kvq::dbg::before();             \
+    __VA_ARGS__;                      \
+    ::kvq::dbg::after(name, stream);  \
+  } while (0)
+#else
+#define KVQ_LAUNCH(name, stream, ...) \
+  do {                                \
+    __VA_ARGS__;                      \
+  } while (0)
+#endif
+
+template <typename T>
+__device__ __forceinline__ T ldx(const T* p, unsigned line) {
+#ifdef KVQ_CHECKED
+  if (!dbg::ok(p, sizeof(T), alignof(T), line)) return T{};
+#endif
+  (void)line;
+  return *p;
+}
+template <typename T>
+__device__ __forceinline__ void stx(T* p, T v, unsigned line) {
+#ifdef KVQ_CHECKED
+  if (!dbg::ok(p, sizeof(T), alignof(T), line)) return;
+#endif
+  (void)line;
+  *p = v;
+}
+#define LDX(p) ::kvq::ldx((p), __LINE__)
+#define STX(p, v) ::kvq::stx((p), (v), __LINE__)
+
 constexpr float kE2M1Max = 6.0f;    // largest E2M1 magnitude
 constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 value
 
@@ -25,6 +131,11 @@ constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 value
 // rows it reads (in-place residual decode).
 template <bool kV8, bool kNC>
 __device__ __forceinline__ void load32B(const void* p, uint32_t (&w)[8]) {
+  if (!KVQ_OK(p, 32, kV8 ? 32 : 16)) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
+    return;
+  }
   if constexpr (kV8 && kNC) {
     asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
@@ -59,6 +170,7 @@ __device__ __forceinline__ void load32B(const void* p, uint32_t (&w)[8]) {
 
 template <bool kV8>
 __device__ __forceinline__ void store32B(void* p, const uint32_t (&w)[8]) {
+  if (!KVQ_OK(p, 32, kV8 ? 32 : 16)) return;
   if constexpr (kV8) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -75,10 +187,15 @@ __device__ __forceinline__ void store32B(void* p, const uint32_t (&w)[8]) {
 }
 
 __device__ __forceinline__ void store8B(void* p, uint32_t a, uint32_t b) {
+  if (!KVQ_OK(p, 8, 8)) return;
   asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void load8B(const void* p, uint32_t& a, uint32_t& b) {
+  if (!KVQ_OK(p, 8, 8)) {
+    a = b = 0u;
+    return;
+  }
   asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
 }
 
@@ -174,7 +291,25 @@ __device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) 
 }
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
-  if (status != nullptr) atomicOr(status, bit);
+  if (status != nullptr && KVQ_OK(status, 4, 4)) atomicOr(status, bit);
+}
+
+// 16-byte load (four words), read-only path.
+__device__ __forceinline__ void load16B(const void* p, uint32_t (&w)[4]) {
+  if (!KVQ_OK(p, 16, 16)) {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    return;
+  }
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void store16B(void* p, const uint32_t (&w)[4]) {
+  if (!KVQ_OK(p, 16, 16)) return;
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3])
+               : "memory");
 }
 
 // Width-limited butterfly reductions inside aligned groups of `kWidth` lanes.

@@ -160,6 +160,16 @@ struct UnpackParams {
   uint32_t* status;
 };
 
+// Checked build only: the byte ranges a launch may touch, registered by the C ABI
+// layer before each launch and copied to the device by the launcher.
+namespace dbg {
+struct HostRange {
+  unsigned long long lo, hi;
+  const char* name;
+};
+HostRange* pending(int* n);  // the list for the next launch (at most 32 entries)
+}  // namespace dbg
+
 // Launchers (return the cudaGetLastError() of the launch).
 cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int lanes, bool v8,
                                 cudaStream_t s);

@@ -52,7 +52,7 @@ __device__ __forceinline__ bool load_source(const EncodeParams& p, const RowLoc&
   const EncodeTensor& T = p.ten[loc.tensor];
   if constexpr (kMode == kEncResidual) {
     int64_t src = loc.tok;
-    if (p.pos != nullptr) src = p.pos[loc.tok];
+    if (p.pos != nullptr) src = LDX(p.pos + loc.tok);
     if (src < 0 || src >= p.src_rows) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = 0u;  // a zero residual row
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodePara
     bool skip = !valid;
     if constexpr (kMode == kEncScatter) {
       if (valid) {
-        int64_t slot = p.slot_ids[loc.tok];
+        int64_t slot = LDX(p.slot_ids + loc.tok);
         if (slot < 0) {
           skip = true;
         } else if (slot >= p.num_slots) {
@@ -129,11 +129,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodePara
     }
     if constexpr (kMode == kEncResidual) {
       if (valid && loc.h == 0 && b == 0 && loc.tensor == 0 && p.pos != nullptr) {
-        int32_t ps = p.pos[loc.tok];
+        int32_t ps = LDX(p.pos + loc.tok);
         bool bad = ps < 0 || ps >= p.src_rows;
-        if (loc.tok > 0 && p.pos[loc.tok - 1] >= ps) bad = true;
+        if (loc.tok > 0 && LDX(p.pos + loc.tok - 1) >= ps) bad = true;
         if (bad) set_status(p.status, 4u);
-        if (p.pos_out != nullptr) p.pos_out[loc.tok] = ps;
+        if (p.pos_out != nullptr) STX(p.pos_out + loc.tok, ps);
       }
     }
 
@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodePara
     if (!skip && lane_has_block) {
       const Nvfp4Planes& d = p.ten[loc.tensor].dst;
       store8B(d.codes + drow * (8 * p.nb) + 8 * b, c0, c1);
-      d.bscale[drow * p.nb + b] = static_cast<uint8_t>(bsb);
-      if (b == 0) d.rscale[drow] = rs;
+      STX(d.bscale + drow * p.nb + b, static_cast<uint8_t>(bsb));
+      if (b == 0) STX(d.rscale + drow, rs);
     }
 
 #pragma unroll
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
     if constexpr (kMode == kDecRestore) {
       uint32_t s, t;
       p.div_tmax.divmod(orow, s, t);
-      const int32_t len = p.seq_lens[s];
+      const int32_t len = LDX(p.seq_lens + s);
       if (len < 0 || len > p.seq_cap) {
         if (t == 0 && h == 0 && b == 0 && tensor == 0) set_status(p.status, 8u);
         continue;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
       if (static_cast<int32_t>(t) >= len) continue;
       uint32_t blk_i, off;
       p.div_bs.divmod(t, blk_i, off);
-      const int32_t blk = p.block_table[static_cast<int64_t>(s) * p.max_blocks + blk_i];
+      const int32_t blk = LDX(p.block_table + static_cast<int64_t>(s) * p.max_blocks + blk_i);
       if (blk < 0 || blk >= p.num_blocks) {
         if (h == 0 && b == 0 && tensor == 0) set_status(p.status, 2u);
         continue;
@@ -223,8 +223,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
     const DecodeTensor& T = p.ten[tensor];
     uint32_t cw0, cw1;
     load8B(T.codes + srow * (8 * p.nb) + 8 * b, cw0, cw1);
-    const uint32_t bsb = T.bscale[srow * p.nb + b];
-    const float rs = T.rscale[srow];
+    const uint32_t bsb = LDX(T.bscale + srow * p.nb + b);
+    const float rs = LDX(T.rscale + srow);
     const uint32_t bs2 = e4m3_to_f16x2(bsb) & 0xFFFFu;
     const uint32_t bsx2 = bs2 | (bs2 << 16);
 
@@ -261,8 +261,9 @@ cudaError_t enc_launch(const EncodeParams& p, cudaStream_t s) {
   auto k = nvfp4_encode_kernel<L, kV8, kMode>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L));
-  k<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("nvfp4_encode_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
+  return e;
 }
 
 template <int L, bool kV8, int kMode>
@@ -270,8 +271,9 @@ cudaError_t dec_launch(const DecodeParams& p, cudaStream_t s) {
   auto k = nvfp4_decode_kernel<L, kV8, kMode>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L));
-  k<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("nvfp4_decode_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
+  return e;
 }
 
 template <int kMode>

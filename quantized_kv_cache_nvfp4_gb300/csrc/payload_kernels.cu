@@ -32,8 +32,8 @@ __device__ __forceinline__ void decode_block(const UnpackParams& u, int64_t p, i
   uint32_t cw0, cw1;
   load8B(P.codes + prow * (u.D / 2) + 8 * b, cw0, cw1);
   if constexpr (kFmt == 1) {
-    const uint32_t bsb = static_cast<const uint8_t*>(P.meta0)[prow * u.nb + b];
-    const float rs = P.rscale[prow];
+    const uint32_t bsb = LDX(static_cast<const uint8_t*>(P.meta0) + prow * u.nb + b);
+    const float rs = LDX(P.rscale + prow);
     const uint32_t bs2 = e4m3_to_f16x2(bsb) & 0xFFFFu;
     const uint32_t bsx2 = bs2 | (bs2 << 16);
 #pragma unroll
@@ -62,8 +62,8 @@ __device__ __forceinline__ void decode_block(const UnpackParams& u, int64_t p, i
     } else {  // VALUE: one group covers the whole 16-channel block
       const int ngv = (u.D + P.G - 1) / P.G;
       const int64_t m = prow * ngv + (16 * b) / P.G;
-      const float mv = f16_bits_to_f32(mnp[m]);
-      const float sv = f16_bits_to_f32(scp[m]);
+      const float mv = f16_bits_to_f32(LDX(mnp + m));
+      const float sv = f16_bits_to_f32(LDX(scp + m));
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         mn[i] = mv;
@@ -85,12 +85,12 @@ __device__ __forceinline__ int32_t find_pos(const int32_t* pos, int32_t n, int32
   int32_t lo = 0, hi = n;  // first index with pos[i] >= t
   while (lo < hi) {
     const int32_t mid = (lo + hi) >> 1;
-    if (pos[mid] < t)
+    if (LDX(pos + mid) < t)
       lo = mid + 1;
     else
       hi = mid;
   }
-  return (lo < n && pos[lo] == t) ? lo : -1;
+  return (lo < n && LDX(pos + lo) == t) ? lo : -1;
 }
 
 template <int L, bool kV8, int kFmt, int kMode>
@@ -105,8 +105,8 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
     if (u.pos != nullptr) {
       for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < u.num_pos;
            i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int32_t ps = u.pos[i];
-        if (ps < 0 || ps >= u.src_rows || (i > 0 && u.pos[i - 1] >= ps)) set_status(u.status, 4u);
+        const int32_t ps = LDX(u.pos + i);
+        if (ps < 0 || ps >= u.src_rows || (i > 0 && LDX(u.pos + i - 1) >= ps)) set_status(u.status, 4u);
       }
     }
   }
@@ -128,9 +128,9 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
         p = r;
         t = r;
         if (u.pos != nullptr) {
-          t = u.pos[r];
+          t = LDX(u.pos + r);
           bool bad = t < 0 || t >= u.src_rows;
-          if (h == 0 && b == 0 && r > 0 && u.pos[r - 1] >= t) set_status(u.status, 4u);
+          if (h == 0 && b == 0 && r > 0 && LDX(u.pos + r - 1) >= t) set_status(u.status, 4u);
           if (bad) {
             if (h == 0 && b == 0) set_status(u.status, 4u);
             continue;
@@ -166,8 +166,10 @@ cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   int64_t need = (static_cast<int64_t>(u.total_rows) + rows_per_cta - 1) / rows_per_cta;
   int64_t cap = static_cast<int64_t>(num_sms()) * occ;
   if (need < 1) need = 1;
-  k<<<static_cast<int>(need < cap ? need : cap), kThreads, 0, s>>>(u);
-  return cudaGetLastError();
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("payload_kernel", s, k<<<grid, kThreads, 0, s>>>(u); e = cudaGetLastError());
+  return e;
 }
 
 template <int L, bool kV8>
