@@ -138,7 +138,10 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
         }
       } else {  // copy: row r is the output row t
         t = r;
-        p = (u.pos != nullptr) ? find_pos(u.pos, u.num_pos, static_cast<int32_t>(r)) : r;
+        // both arms signed: a -1 from find_pos must stay negative (with an unsigned
+        // arm the conditional would convert it to 0xFFFFFFFF)
+        p = (u.pos != nullptr) ? static_cast<int64_t>(find_pos(u.pos, u.num_pos, static_cast<int32_t>(r)))
+                               : static_cast<int64_t>(r);
       }
       uint32_t q[8];
       load32B<kV8, kMode == 2>(u.prev + t * u.prev_row_pitch +
