@@ -182,6 +182,17 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def sources_hash(paths) -> str:
+    """sha256 (16 hex digits) of the concatenated kernel sources a capture measured."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source changed since the capture."""
@@ -192,9 +203,7 @@ def ncu_traffic(kernel: str):
         with open(path) as f:
             d = json.load(f)
         rec = d[kernel]
-        src = os.path.join(ROOT, rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != rec["source_sha256_16"]:
+        if sources_hash(rec["sources"]) != rec["sources_sha256_16"]:
             return None
         return int(rec["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -441,7 +450,7 @@ def run_reference(args):
     t0 = time.perf_counter()
     oracle_step(O, k, v, slots, table)
     per_tok = (time.perf_counter() - t0) / 256
-    budget = 150.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     tokens = int(max(BLOCK, min(65536, budget / per_tok)) // BLOCK * BLOCK)
     k, v, slots, table = oracle_sample(tokens)
     for _ in range(args.warmup):
@@ -475,6 +484,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=16384)
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="reference arm: CPU seconds the whole --steps/--warmup run may take")
     ap.add_argument("--tokens", type=int, default=T_TOKENS,
                     help="tokens of the workload (default: the 1,048,576-token case); smaller "
                          "values give the same kernels on a smaller case for profiling")

@@ -80,9 +80,8 @@ def test_reference_arm_prints_from_rank_zero_only():
 @pytest.mark.parametrize("steps", [1])
 def test_reference_arm_json_line(steps):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", str(steps), "--warmup", "0"],
-                       capture_output=True, text=True, timeout=600,
-                       env=dict(os.environ, KVQ_REFERENCE_BUDGET_S="2"))
+                        "--steps", str(steps), "--warmup", "0", "--ref-seconds", "2"],
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
