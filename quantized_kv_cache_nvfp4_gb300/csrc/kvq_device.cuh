@@ -225,14 +225,39 @@ __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
 }
 
 // Largest |x| of the 16 bf16 in w (returned as fp32).  Comparisons only: exact.
+// max.xorsign.abs compares magnitudes; only the sign of its result is
+// meaningless, and it is cleared at the end.
 __device__ __forceinline__ float absmax16(const uint32_t (&w)[8]) {
-  uint32_t m = w[0] & 0x7FFF7FFFu;
+  uint32_t m = w[0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    uint32_t a = w[i] & 0x7FFF7FFFu;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(a));
-  }
+  for (int i = 1; i < 8; ++i) asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(w[i]));
+  m &= 0x7FFF7FFFu;
   return fmaxf(bf16lo(m), bf16hi(m));
+}
+
+// Two fp32 packed in one 64-bit register (lo = element 0).
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo_bits, uint32_t hi_bits) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, uint32_t& lo_bits, uint32_t& hi_bits) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo_bits), "=r"(hi_bits) : "l"(v));
+}
+// Element-wise binary32 product of two pairs, each rounded to nearest even.
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Byte merge: the low byte of each of a, b, c, d into one word (a lowest).
+__device__ __forceinline__ uint32_t bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  uint32_t ab, cd, r;
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(ab) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(cd) : "r"(c), "r"(d));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(ab), "r"(cd));
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -256,6 +281,45 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2(uint32_t byte) {
 
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   return f16_bits_to_f32(static_cast<uint16_t>(e4m3_to_f16x2(byte) & 0xFFFFu));
+}
+
+// Two non-negative fp32 -> two E4M3 bytes (lo in bits 0..7, hi in 8..15), nearest
+// even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The E4M3 code of the block scale t = min((vb / 6) / rs, 448) (0 when rs == 0),
+// exactly as the two divisions define it, usually without dividing.
+//
+// te = (vb * RN(1/6)) * RN(1/rs) carries four roundings and the defined t two, so
+// when every intermediate is a normal binary32 (rs, vb >= 2^-120 ensures it for
+// any t near a code boundary) |t / te - 1| <= 6.001 * 2^-24.  The bracket
+// [te * (1 - 2^-20), te * (1 + 2^-20)] therefore holds t even after its own
+// rounding, and E4M3 rounding is monotone: when both ends of the bracket round to
+// the same code, t rounds to it too.  Otherwise (a bracket across a rounding
+// boundary, or tiny operands) t is computed by the two divisions.
+__device__ __forceinline__ uint32_t block_scale_code(float vb, float rs, float rinv) {
+  if (rs >= 0x1p-120f && vb >= 0x1p-120f) {
+    const float te = __fmul_rn(__fmul_rn(vb, 0x1.555556p-3f), rinv);
+    const float lo = fminf(__fmul_rn(te, 0x1.ffffep-1f), kE4M3Max);
+    const float hi = fminf(__fmul_rn(te, 0x1.00001p+0f), kE4M3Max);
+    const uint32_t two = e4m3x2_from_f32(lo, hi);
+    if ((two & 0xFFu) == (two >> 8)) return two & 0xFFu;
+  }
+  float t = 0.0f;
+  if (rs != 0.0f) t = __fdiv_rn(__fdiv_rn(vb, kE2M1Max), rs);
+  return e4m3_from_f32(fminf(t, kE4M3Max));
+}
+
+// Mixed-precision exact product: fp32(a_f16) * fp32(b_f16) + (-0), one rounding
+// (none here: an E2M1 value times an E4M3 value has at most 6 significant bits).
+__device__ __forceinline__ float mul_f16_to_f32(uint16_t a, uint16_t b) {
+  float r;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(r) : "h"(a), "h"(b), "f"(-0.0f));
+  return r;
 }
 
 // Two fp32 -> one byte of E2M1 codes: `lo` in bits 0..3, `hi` in bits 4..7.

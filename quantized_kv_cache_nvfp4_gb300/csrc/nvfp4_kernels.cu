@@ -15,12 +15,13 @@
 // The tiny-scale direct division follows "vllm-rlt PR #166: INT4 KV packing ...",
 // Purpose ("a direct-division fallback when their reciprocal overflows").
 //
-// Work mapping: one lane owns one 16-element block (32 bytes of bf16, one 256-bit
-// load when aligned); the D/16 lanes of a row form an aligned sub-warp of L lanes
-// (L = next power of two), so the row amax is a log2(L)-step xor butterfly.  A
-// warp therefore handles 32/L rows per iteration; a grid-stride loop with the next
-// row's load issued before the current row's arithmetic keeps two loads in flight
-// per lane.  No tensor cores: nothing here is a contraction.
+// Work mapping: a lane owns BPL consecutive 16-element blocks of a row (BPL = 2 when
+// the row has an even number of blocks: two 256-bit loads, 64 contiguous bytes per
+// lane).  The L lanes of a row (L = next power of two of D/16/BPL) form an aligned
+// sub-warp, so the row amax is a log2(L)-step xor butterfly.  A warp handles 32/L
+// rows per iteration (at D256, H4: exactly the four heads of one token); a grid-stride
+// loop issues the next row's loads before the current row's arithmetic.  No tensor
+// cores: nothing here is a contraction.
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 
@@ -44,58 +45,91 @@ __device__ __forceinline__ RowLoc locate(uint32_t row, uint32_t rows_per_tensor,
   return r;
 }
 
-// Source block of 16 bf16 for (row, block b).  Residual mode builds
-// bf16(cur - prev) for the row at position pos[p].
-template <int kMode, bool kV8>
-__device__ __forceinline__ bool load_source(const EncodeParams& p, const RowLoc& loc, int b,
-                                            uint32_t (&w)[8]) {
+// The BPL source blocks of this lane for one row (zeros past the row's end).
+// Residual mode builds bf16(cur - prev) for the row at position pos[p].
+template <int kMode, bool kV8, int BPL>
+__device__ __forceinline__ void load_source(const EncodeParams& p, const RowLoc& loc, int b0,
+                                            uint32_t (&w)[BPL][8]) {
   const EncodeTensor& T = p.ten[loc.tensor];
+  int64_t src = loc.tok;
   if constexpr (kMode == kEncResidual) {
-    int64_t src = loc.tok;
     if (p.pos != nullptr) src = LDX(p.pos + loc.tok);
-    if (src < 0 || src >= p.src_rows) {
+    if (src < 0 || src >= p.src_rows) {  // a zero residual row
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = 0u;  // a zero residual row
-      return false;
-    }
-    uint32_t c[8], q[8];
-    load32B<kV8, true>(T.x + src * T.row_pitch + loc.h * T.head_pitch + 16 * b, c);
-    load32B<kV8, true>(T.prev + src * T.prev_row_pitch + loc.h * T.prev_head_pitch + 16 * b, q);
+      for (int j = 0; j < BPL; ++j)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float lo = __fsub_rn(bf16lo(c[i]), bf16lo(q[i]));
-      float hi = __fsub_rn(bf16hi(c[i]), bf16hi(q[i]));
-      w[i] = pack_bf16x2(lo, hi);
+        for (int i = 0; i < 8; ++i) w[j][i] = 0u;
+      return;
     }
-    return true;
-  } else {
-    load32B<kV8, true>(T.x + static_cast<int64_t>(loc.tok) * T.row_pitch +
-                           static_cast<int64_t>(loc.h) * T.head_pitch + 16 * b,
-                       w);
-    return true;
+  }
+  const uint16_t* x = T.x + src * T.row_pitch + static_cast<int64_t>(loc.h) * T.head_pitch;
+#pragma unroll
+  for (int j = 0; j < BPL; ++j) {
+    if (b0 + j < p.nb) {
+      load32B<kV8, true>(x + 16 * (b0 + j), w[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[j][i] = 0u;
+    }
+  }
+  if constexpr (kMode == kEncResidual) {
+    const uint16_t* q = T.prev + src * T.prev_row_pitch + static_cast<int64_t>(loc.h) * T.prev_head_pitch;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      if (b0 + j >= p.nb) continue;
+      uint32_t pw[8];
+      load32B<kV8, true>(q + 16 * (b0 + j), pw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[j][i] = pack_bf16x2(__fsub_rn(bf16lo(w[j][i]), bf16lo(pw[i])),
+                              __fsub_rn(bf16hi(w[j][i]), bf16hi(pw[i])));
+    }
   }
 }
 
-template <int L, bool kV8, int kMode>
-__global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodeParams p) {
+// Codes of one 16-element block against s = bs * rs; returns the 8 code bytes as
+// two words (low nibble of each byte = the even element).
+__device__ __forceinline__ void quantize_block(const uint32_t (&w)[8], float s, uint32_t& c0,
+                                               uint32_t& c1) {
+  const float inv = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
+  uint32_t byte[8];
+  if (!isinf(inv)) {
+    const uint64_t inv2 = pack_f32x2(__float_as_uint(inv), __float_as_uint(inv));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t ql, qh;
+      unpack_f32x2(mul_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), inv2), ql, qh);
+      byte[i] = e2m1x2_from_f32(__uint_as_float(ql), __uint_as_float(qh));
+    }
+  } else {  // tiny scale: the reciprocal overflowed, divide directly
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      byte[i] = e2m1x2_from_f32(__fdiv_rn(bf16lo(w[i]), s), __fdiv_rn(bf16hi(w[i]), s));
+  }
+  c0 = bytes4(byte[0], byte[1], byte[2], byte[3]);
+  c1 = bytes4(byte[4], byte[5], byte[6], byte[7]);
+}
+
+template <int L, int BPL, bool kV8, int kMode>
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_encode_kernel(const EncodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
-  const int b = lane % L;
+  const int li = lane % L;
   const int sub = lane / L;
+  const int b0 = li * BPL;
   const uint32_t total = p.rows_per_tensor * static_cast<uint32_t>(p.ntensors);
   const uint32_t nwarps = gridDim.x * (kThreads / 32);
   const uint32_t stride = nwarps * kRowsPerWarp;
   uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
-  const bool lane_has_block = b < p.nb;
+  const bool lane_active = b0 < p.nb;
 
-  // prefetch the first row
-  uint32_t w[8];
-  {
-    bool act = lane_has_block && row < total;
+  uint32_t w[BPL][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0u;
-    if (act) load_source<kMode, kV8>(p, locate(row, p.rows_per_tensor, p.div_h), b, w);
-  }
+  for (int j = 0; j < BPL; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[j][i] = 0u;
+  if (lane_active && row < total)
+    load_source<kMode, kV8, BPL>(p, locate(row, p.rows_per_tensor, p.div_h), b0, w);
 
   // The loop bound is uniform across the warp (row - sub is), so every lane runs
   // every shuffle of every iteration.
@@ -103,33 +137,35 @@ __global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodePara
     const bool valid = row < total;
     const RowLoc loc = locate(valid ? row : 0u, p.rows_per_tensor, p.div_h);
 
-    // issue the next row's load before this row's arithmetic
-    uint32_t nw[8];
+    // issue the next row's loads before this row's arithmetic
+    uint32_t nw[BPL][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) nw[i] = 0u;
+    for (int j = 0; j < BPL; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nw[j][i] = 0u;
     const uint32_t nrow = row + stride;
-    if (lane_has_block && nrow < total)
-      load_source<kMode, kV8>(p, locate(nrow, p.rows_per_tensor, p.div_h), b, nw);
+    if (lane_active && nrow < total)
+      load_source<kMode, kV8, BPL>(p, locate(nrow, p.rows_per_tensor, p.div_h), b0, nw);
 
     // destination row and skip decision
     int64_t drow = static_cast<int64_t>(loc.tok) * p.H + loc.h;
     bool skip = !valid;
     if constexpr (kMode == kEncScatter) {
       if (valid) {
-        int64_t slot = LDX(p.slot_ids + loc.tok);
+        const int64_t slot = LDX(p.slot_ids + loc.tok);
         if (slot < 0) {
           skip = true;
         } else if (slot >= p.num_slots) {
           skip = true;
-          if (loc.h == 0 && b == 0 && loc.tensor == 0) set_status(p.status, 1u);
+          if (loc.h == 0 && li == 0 && loc.tensor == 0) set_status(p.status, 1u);
         } else {
           drow = slot * p.H + loc.h;
         }
       }
     }
     if constexpr (kMode == kEncResidual) {
-      if (valid && loc.h == 0 && b == 0 && loc.tensor == 0 && p.pos != nullptr) {
-        int32_t ps = LDX(p.pos + loc.tok);
+      if (valid && loc.h == 0 && li == 0 && loc.tensor == 0 && p.pos != nullptr) {
+        const int32_t ps = LDX(p.pos + loc.tok);
         bool bad = ps < 0 || ps >= p.src_rows;
         if (loc.tok > 0 && LDX(p.pos + loc.tok - 1) >= ps) bad = true;
         if (bad) set_status(p.status, 4u);
@@ -137,61 +173,76 @@ __global__ void __launch_bounds__(kThreads) nvfp4_encode_kernel(const EncodePara
       }
     }
 
-    // row and block scales
-    const float vb = lane_has_block ? absmax16(w) : 0.0f;
-    const float amax = group_max<L>(vb);
+    // row scale
+    float vb[BPL];
+    float lmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      vb[j] = absmax16(w[j]);  // zero for blocks past the row's end
+      lmax = fmaxf(lmax, vb[j]);
+    }
+    const float amax = group_max<L>(lmax);
     const float rs = __fdiv_rn(amax, kE2M1Max * kE4M3Max);
-    float t = 0.0f;
-    if (rs != 0.0f) t = __fdiv_rn(__fdiv_rn(vb, kE2M1Max), rs);
-    t = fminf(t, kE4M3Max);
-    const uint32_t bsb = e4m3_from_f32(t);
-    const float bs = e4m3_to_f32(bsb);
-    const float s = __fmul_rn(bs, rs);
-    const float inv = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
-    const bool use_div = isinf(inv);
+    const float rinv = (rs != 0.0f) ? __frcp_rn(rs) : 0.0f;
 
-    // element codes, two per byte, low nibble first
-    uint32_t c0 = 0u, c1 = 0u;
+    uint32_t c[BPL][2];
+    uint32_t bsb[BPL];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float xl = bf16lo(w[i]);
-      const float xh = bf16hi(w[i]);
-      float ql, qh;
-      if (use_div) {
-        ql = __fdiv_rn(xl, s);
-        qh = __fdiv_rn(xh, s);
-      } else {
-        ql = __fmul_rn(xl, inv);
-        qh = __fmul_rn(xh, inv);
-      }
-      const uint32_t byte = e2m1x2_from_f32(ql, qh);
-      if (i < 4)
-        c0 |= byte << (8 * i);
-      else
-        c1 |= byte << (8 * (i - 4));
+    for (int j = 0; j < BPL; ++j) {
+      bsb[j] = block_scale_code(vb[j], rs, rinv);
+      const float s = __fmul_rn(e4m3_to_f32(bsb[j]), rs);
+      quantize_block(w[j], s, c[j][0], c[j][1]);
     }
 
-    if (!skip && lane_has_block) {
+    if (!skip && lane_active) {
       const Nvfp4Planes& d = p.ten[loc.tensor].dst;
-      store8B(d.codes + drow * (8 * p.nb) + 8 * b, c0, c1);
-      STX(d.bscale + drow * p.nb + b, static_cast<uint8_t>(bsb));
-      if (b == 0) STX(d.rscale + drow, rs);
+      uint8_t* cp = d.codes + drow * (8 * p.nb) + 8 * b0;
+      uint8_t* bp = d.bscale + drow * p.nb + b0;
+      if constexpr (BPL == 2) {
+        const uint32_t cw[4] = {c[0][0], c[0][1], c[1][0], c[1][1]};
+        store16B(cp, cw);
+        STX(reinterpret_cast<uint16_t*>(bp), static_cast<uint16_t>(bsb[0] | (bsb[1] << 8)));
+      } else {
+        store8B(cp, c[0][0], c[0][1]);
+        STX(bp, static_cast<uint8_t>(bsb[0]));
+      }
+      if (li == 0) STX(d.rscale + drow, rs);
     }
 
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = nw[i];
+    for (int j = 0; j < BPL; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[j][i] = nw[j][i];
   }
 }
 
-template <int L, bool kV8, int kMode>
+// y = bf16((e2m1 * bs) * rs) for the 16 codes of one block (8 code bytes).
+__device__ __forceinline__ void decode_block(uint32_t cw0, uint32_t cw1, uint32_t bsb, float rs,
+                                             uint32_t (&out)[8]) {
+  const uint16_t bs16 = static_cast<uint16_t>(e4m3_to_f16x2(bsb) & 0xFFFFu);
+  const uint64_t rs2 = pack_f32x2(__float_as_uint(rs), __float_as_uint(rs));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
+    const uint32_t h2 = e2m1x2_to_f16x2(byte);
+    const float lo = mul_f16_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu), bs16);  // exact
+    const float hi = mul_f16_to_f32(static_cast<uint16_t>(h2 >> 16), bs16);
+    uint32_t yl, yh;
+    unpack_f32x2(mul_f32x2(pack_f32x2(__float_as_uint(lo), __float_as_uint(hi)), rs2), yl, yh);
+    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+  }
+}
+
+template <int L, int BPL, bool kV8, int kMode>
 __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
-  const int b = lane % L;
+  const int li = lane % L;
   const int sub = lane / L;
+  const int b0 = li * BPL;
   const uint32_t total = p.rows_per_tensor * static_cast<uint32_t>(p.ntensors);
   const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
-  if (b >= p.nb) return;  // no shuffles below: idle lanes may leave
+  if (b0 >= p.nb) return;  // no shuffles below: idle lanes may leave
 
   for (uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
        row < total; row += stride) {
@@ -205,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
       p.div_tmax.divmod(orow, s, t);
       const int32_t len = LDX(p.seq_lens + s);
       if (len < 0 || len > p.seq_cap) {
-        if (t == 0 && h == 0 && b == 0 && tensor == 0) set_status(p.status, 8u);
+        if (t == 0 && h == 0 && li == 0 && tensor == 0) set_status(p.status, 8u);
         continue;
       }
       if (static_cast<int32_t>(t) >= len) continue;
@@ -213,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
       p.div_bs.divmod(t, blk_i, off);
       const int32_t blk = LDX(p.block_table + static_cast<int64_t>(s) * p.max_blocks + blk_i);
       if (blk < 0 || blk >= p.num_blocks) {
-        if (h == 0 && b == 0 && tensor == 0) set_status(p.status, 2u);
+        if (h == 0 && li == 0 && tensor == 0) set_status(p.status, 2u);
         continue;
       }
       srow = (static_cast<int64_t>(blk) * p.block_size + off) * p.H + h;
@@ -221,32 +272,30 @@ __global__ void __launch_bounds__(kThreads) nvfp4_decode_kernel(const DecodePara
       srow = rr;
     }
     const DecodeTensor& T = p.ten[tensor];
-    uint32_t cw0, cw1;
-    load8B(T.codes + srow * (8 * p.nb) + 8 * b, cw0, cw1);
-    const uint32_t bsb = LDX(T.bscale + srow * p.nb + b);
     const float rs = LDX(T.rscale + srow);
-    const uint32_t bs2 = e4m3_to_f16x2(bsb) & 0xFFFFu;
-    const uint32_t bsx2 = bs2 | (bs2 << 16);
-
-    uint32_t out[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
-      const uint32_t v2 = hmul2_bits(e2m1x2_to_f16x2(byte), bsx2);  // exact
-      float lo, hi;
-      f16x2_to_f32(v2, lo, hi);
-      out[i] = pack_bf16x2(__fmul_rn(lo, rs), __fmul_rn(hi, rs));
+    uint16_t* y = T.y + static_cast<int64_t>(orow) * T.row_pitch + static_cast<int64_t>(h) * T.head_pitch;
+    if constexpr (BPL == 2) {
+      uint32_t cw[4];
+      load16B(T.codes + srow * (8 * p.nb) + 8 * b0, cw);
+      const uint32_t bs2 = LDX(reinterpret_cast<const uint16_t*>(T.bscale + srow * p.nb + b0));
+      uint32_t out[8];
+      decode_block(cw[0], cw[1], bs2 & 0xFFu, rs, out);
+      store32B<kV8>(y + 16 * b0, out);
+      decode_block(cw[2], cw[3], bs2 >> 8, rs, out);
+      store32B<kV8>(y + 16 * (b0 + 1), out);
+    } else {
+      uint32_t cw0, cw1;
+      load8B(T.codes + srow * (8 * p.nb) + 8 * b0, cw0, cw1);
+      const uint32_t bsb = LDX(T.bscale + srow * p.nb + b0);
+      uint32_t out[8];
+      decode_block(cw0, cw1, bsb, rs, out);
+      store32B<kV8>(y + 16 * b0, out);
     }
-    store32B<kV8>(T.y + static_cast<int64_t>(orow) * T.row_pitch +
-                      static_cast<int64_t>(h) * T.head_pitch + 16 * b,
-                  out);
   }
 }
 
 template <typename K>
 int grid_for(K kernel, uint32_t rows, int rows_per_cta) {
-  static int per_sm[64] = {0};
-  (void)per_sm;
   int occ = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
   if (occ < 1) occ = 1;
@@ -256,9 +305,9 @@ int grid_for(K kernel, uint32_t rows, int rows_per_cta) {
   return static_cast<int>(need < cap ? need : cap);
 }
 
-template <int L, bool kV8, int kMode>
+template <int L, int BPL, bool kV8, int kMode>
 cudaError_t enc_launch(const EncodeParams& p, cudaStream_t s) {
-  auto k = nvfp4_encode_kernel<L, kV8, kMode>;
+  auto k = nvfp4_encode_kernel<L, BPL, kV8, kMode>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L));
   cudaError_t e = cudaSuccess;
@@ -266,9 +315,9 @@ cudaError_t enc_launch(const EncodeParams& p, cudaStream_t s) {
   return e;
 }
 
-template <int L, bool kV8, int kMode>
+template <int L, int BPL, bool kV8, int kMode>
 cudaError_t dec_launch(const DecodeParams& p, cudaStream_t s) {
-  auto k = nvfp4_decode_kernel<L, kV8, kMode>;
+  auto k = nvfp4_decode_kernel<L, BPL, kV8, kMode>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L));
   cudaError_t e = cudaSuccess;
@@ -276,63 +325,59 @@ cudaError_t dec_launch(const DecodeParams& p, cudaStream_t s) {
   return e;
 }
 
+// Lanes per row and blocks per lane for nb = D / 16 blocks.
+void row_shape(int nb, int& lanes, int& bpl) {
+  bpl = (nb % 2 == 0) ? 2 : 1;
+  const int per = nb / bpl;
+  lanes = 1;
+  while (lanes < per) lanes <<= 1;
+}
+
+#define KVQ_SHAPES(X) X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) \
+                      X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2)
+
 template <int kMode>
-cudaError_t enc_dispatch(const EncodeParams& p, int lanes, bool v8, cudaStream_t s) {
-#define KVQ_ENC(LN)                                                   \
-  case LN:                                                            \
-    return v8 ? enc_launch<LN, true, kMode>(p, s) : enc_launch<LN, false, kMode>(p, s);
-  switch (lanes) {
-    KVQ_ENC(1)
-    KVQ_ENC(2)
-    KVQ_ENC(4)
-    KVQ_ENC(8)
-    KVQ_ENC(16)
-    KVQ_ENC(32)
-  }
+cudaError_t enc_dispatch(const EncodeParams& p, bool v8, cudaStream_t s) {
+  int lanes, bpl;
+  row_shape(p.nb, lanes, bpl);
+#define KVQ_ENC(LN, B)                                                                    \
+  if (lanes == LN && bpl == B)                                                            \
+    return v8 ? enc_launch<LN, B, true, kMode>(p, s) : enc_launch<LN, B, false, kMode>(p, s);
+  KVQ_SHAPES(KVQ_ENC)
 #undef KVQ_ENC
   return cudaErrorInvalidValue;
 }
 
 template <int kMode>
-cudaError_t dec_dispatch(const DecodeParams& p, int lanes, bool v8, cudaStream_t s) {
-#define KVQ_DEC(LN)                                                   \
-  case LN:                                                            \
-    return v8 ? dec_launch<LN, true, kMode>(p, s) : dec_launch<LN, false, kMode>(p, s);
-  switch (lanes) {
-    KVQ_DEC(1)
-    KVQ_DEC(2)
-    KVQ_DEC(4)
-    KVQ_DEC(8)
-    KVQ_DEC(16)
-    KVQ_DEC(32)
-  }
+cudaError_t dec_dispatch(const DecodeParams& p, bool v8, cudaStream_t s) {
+  int lanes, bpl;
+  row_shape(p.nb, lanes, bpl);
+#define KVQ_DEC(LN, B)                                                                    \
+  if (lanes == LN && bpl == B)                                                            \
+    return v8 ? dec_launch<LN, B, true, kMode>(p, s) : dec_launch<LN, B, false, kMode>(p, s);
+  KVQ_SHAPES(KVQ_DEC)
 #undef KVQ_DEC
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int lanes, bool v8,
+cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int /*lanes*/, bool v8,
                                 cudaStream_t s) {
   switch (mode) {
     case kEncScatter:
-      return enc_dispatch<kEncScatter>(p, lanes, v8, s);
+      return enc_dispatch<kEncScatter>(p, v8, s);
     case kEncPack:
-      return enc_dispatch<kEncPack>(p, lanes, v8, s);
+      return enc_dispatch<kEncPack>(p, v8, s);
     case kEncResidual:
-      return enc_dispatch<kEncResidual>(p, lanes, v8, s);
+      return enc_dispatch<kEncResidual>(p, v8, s);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int lanes, bool v8,
+cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int /*lanes*/, bool v8,
                                 cudaStream_t s) {
-  switch (mode) {
-    case kDecRestore:
-      return dec_dispatch<kDecRestore>(p, lanes, v8, s);
-    case kDecUnpack:
-      return dec_dispatch<kDecUnpack>(p, lanes, v8, s);
-  }
+  if (mode == kDecRestore) return dec_dispatch<kDecRestore>(p, v8, s);
   return cudaErrorInvalidValue;
 }
 
