@@ -286,6 +286,10 @@ def run_ours(args):
     st_final = int(status.item())
 
     e2e = run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist, T) if not args.no_e2e else None
+    rows_other = None
+    if not args.no_other_rows and rank == 0:
+        rows_other = other_rows(kvq, device, peak=measured_peaks()[0])
+        rows_other["latency_us_one_residual_loop"] = residual_loop_latency(kvq, device)
 
     if rank != 0:
         if dist is not None:
@@ -336,6 +340,7 @@ def run_ours(args):
         "device_status": st_final,
         "clocks": clocks,
         "e2e": e2e,
+        "other_rows": rows_other,
         "cpu_baseline": cpu,
     }
     print(json.dumps(out), flush=True)
@@ -344,52 +349,168 @@ def run_ours(args):
 
 
 def run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist, T):
-    """Same metric through the public API with host buffers: every step copies the
-    step's inputs host->device (pinned) and the restored K/V device->host."""
+    """Same metric through the public API with host buffers.
+
+    Every step copies the step's inputs host->device from pinned memory (K, V, slot
+    ids, block table, lengths) and the restored K/V device->host.  The step is cut
+    into chunks of tokens on three streams, so that the copy-in of chunk c+1, the
+    scatter + restore of chunk c and the copy-out of chunk c-1 overlap (the two copy
+    directions run concurrently on the host link).  Chunk c's restore reads the
+    block-table slice of its own tokens, so the chunks together do exactly the work
+    of one scatter and one restore of the whole workload."""
     H, D = HEADS, HEAD_DIM
+    nch = max(1, args.e2e_chunks)
+    while T % (nch * BLOCK) != 0:
+        nch -= 1
+    C = T // nch
     hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
     hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
     hs = torch.empty(slots.shape, dtype=slots.dtype, pin_memory=True)
     ht = torch.empty(table.shape, dtype=table.dtype, pin_memory=True)
-    hl = torch.empty(lens.shape, dtype=lens.dtype, pin_memory=True)
+    hl = torch.full((nch,), C, dtype=torch.int32).pin_memory()
     hk.copy_(k)
     hv.copy_(v)
     hs.copy_(slots)
     ht.copy_(table)
-    hl.copy_(lens)
-    ok = torch.empty((1, T, H, D), dtype=torch.bfloat16, pin_memory=True)
+    ok = torch.empty((T, H, D), dtype=torch.bfloat16, pin_memory=True)
     ov = torch.empty_like(ok)
-    dk, dv, ds, dt, dl = (torch.empty_like(x) for x in (k, v, slots, table, lens))
-    yk = torch.empty((1, T, H, D), dtype=torch.bfloat16, device=device)
+    dk, dv, ds, dt = (torch.empty_like(x) for x in (k, v, slots, table))
+    dl = torch.empty((nch,), dtype=torch.int32, device=device)
+    yk = torch.empty((T, H, D), dtype=torch.bfloat16, device=device)
     yv = torch.empty_like(yk)
-    stream = torch.cuda.current_stream(device)
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    consumed = [ev() for _ in range(nch)]  # the scatter of chunk c read its inputs
+    restored = [ev() for _ in range(nch)]  # the restore of chunk c wrote its output
+    shipped = [ev() for _ in range(nch)]   # the copy-out of chunk c finished
+    arrived = [ev() for _ in range(nch)]   # the copy-in of chunk c finished
+    bpc = C // BLOCK
+    first = [True]
 
     def step():
-        for dst, src in ((dk, hk), (dv, hv), (ds, hs), (dt, ht), (dl, hl)):
-            dst.copy_(src, non_blocking=True)
-        kvq.kvq_quant_scatter(dk, dv, ds, pool)
-        kvq.kvq_restore(pool, dt, dl, T, yk, yv)
-        ok.copy_(yk, non_blocking=True)
-        ov.copy_(yv, non_blocking=True)
+        for c in range(nch):
+            sl = slice(c * C, (c + 1) * C)
+            with torch.cuda.stream(s_in):
+                if not first[0]:
+                    s_in.wait_event(consumed[c])
+                dk[sl].copy_(hk[sl], non_blocking=True)
+                dv[sl].copy_(hv[sl], non_blocking=True)
+                ds[sl].copy_(hs[sl], non_blocking=True)
+                dt[:, c * bpc:(c + 1) * bpc].copy_(ht[:, c * bpc:(c + 1) * bpc], non_blocking=True)
+                dl[c:c + 1].copy_(hl[c:c + 1], non_blocking=True)
+                arrived[c].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(arrived[c])
+                if not first[0]:
+                    s_cmp.wait_event(shipped[c])
+                kvq.kvq_quant_scatter(dk[sl], dv[sl], ds[sl], pool, stream=s_cmp)
+                consumed[c].record(s_cmp)
+                kvq.kvq_restore(pool, dt[:, c * bpc:(c + 1) * bpc], dl[c:c + 1], C,
+                                yk[sl].unsqueeze(0), yv[sl].unsqueeze(0), stream=s_cmp)
+                restored[c].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(restored[c])
+                ok[sl].copy_(yk[sl], non_blocking=True)
+                ov[sl].copy_(yv[sl], non_blocking=True)
+                shipped[c].record(s_out)
+        first[0] = False
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
-    torch.cuda.synchronize()
+    torch.cuda.synchronize(device)
     K = max(1, min(args.steps, args.e2e_steps))
     barrier(dist, device)
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(device)
+    t0.record(cur)
+    for st in (s_in, s_cmp, s_out):
+        st.wait_event(t0)
     for _ in range(K):
         step()
-    s1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(dist, s0.elapsed_time(s1) / K, device)
+    for e in shipped:
+        cur.wait_event(e)
+    t1.record(cur)
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(dist, t0.elapsed_time(t1) / K, device)
+    # the host copy of the restored V equals what the device restored
+    same = bool(torch.equal(ov[: 4096].to(device).view(torch.int16), yv[:4096].view(torch.int16)))
     world = dist.get_world_size() if dist is not None else 1
     step_bytes = scatter_bytes(T, H, D) + restore_bytes(T, H, D, T // BLOCK)
-    bi = sum(x.numel() * x.element_size() for x in (hk, hv, hs, ht, hl))
+    bi = sum(x.numel() * x.element_size() for x in (hk, hv, hs, ht)) + 4 * nch
     bo = ok.numel() * ok.element_size() * 2
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "ms_per_step": round(ms, 3), "steps": K, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "ms_per_step": round(ms, 3), "steps": K, "chunks": nch, "streams": 3,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "h2d_plus_d2h_GBps": round((bi + bo) / (ms * 1e-3) / 1e9, 1), "output_matches": same}
+
+
+# ---------------------------------------------------------------------------
+# the other rows of the hot path: INT4 and NVFP4 logical codecs, residuals
+# ---------------------------------------------------------------------------
+def int4_meta_bytes(kind: int, rows: int, H: int, D: int, G: int) -> int:
+    groups = (-(-rows // G)) * H * D if kind == 0 else rows * H * (-(-D // G))
+    return 4 * groups
+
+
+def other_rows(kvq, device, T=262144, H=8, D=128, G=64, P=None, iters=20, peak=6795.5):
+    """GB/s of every other entry point on a [T, H, D] bf16 case (inputs far larger
+    than L2), each timed alone with CUDA events over `iters` back-to-back calls."""
+    from quantized_kv_cache_nvfp4_gb300 import synth
+
+    P = P if P is not None else T // 4
+    cur, prev = synth.layer_kv(T, H, D, seed=4, device=str(device))
+    pos = synth.sorted_positions(T, P, 4).to(device)
+    y = torch.empty_like(cur)
+    out = {}
+
+    def timed(name, fn, nbytes):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize(device)
+        ms = a.elapsed_time(b) / iters
+        out[name] = {"ms": round(ms, 4), "bytes": nbytes, "GB/s": round(nbytes / ms / 1e6, 1),
+                     "frac": round(nbytes / ms / 1e6 / peak, 4)}
+
+    rows_b = T * H * 2 * D  # bf16 bytes of the whole tensor
+    nv = kvq.Packed.empty(kvq.FMT_NVFP4, 0, T, H, D, device=device)
+    nvb = T * H * (D // 2 + D // 16 + 4)
+    timed("kvq_pack nvfp4", lambda: kvq.kvq_pack(cur, nv), rows_b + nvb)
+    timed("kvq_unpack nvfp4", lambda: kvq.kvq_unpack(nv, y), nvb + rows_b)
+    for kind, kname in ((0, "key"), (1, "value")):
+        pk = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G, device=device)
+        ib = T * H * (D // 2) + int4_meta_bytes(kind, T, H, D, G)
+        timed(f"kvq_pack int4 {kname} G{G}", lambda: kvq.kvq_pack(cur, pk), rows_b + ib)
+        timed(f"kvq_unpack int4 {kname} G{G}", lambda: kvq.kvq_unpack(pk, y), ib + rows_b)
+        pay = kvq.Packed.empty(kvq.FMT_INT4, kind, P, H, D, G, device=device)
+        pb = P * H * (D // 2) + int4_meta_bytes(kind, P, H, D, G)
+        kept_b = P * H * 2 * D
+        timed(f"kvq_encode_residual int4 {kname} 25%", lambda: kvq.kvq_encode_residual(cur, prev, pos, pay),
+              2 * kept_b + 4 * P + pb)
+        timed(f"kvq_decode_residual int4 {kname} 25% copy", lambda: kvq.kvq_decode_residual(pay, pos, prev, y),
+              rows_b + pb + 4 * P + rows_b)
+        ip = prev.clone()
+        timed(f"kvq_decode_residual int4 {kname} 25% in place",
+              lambda: kvq.kvq_decode_residual(pay, pos, ip, ip), kept_b + pb + 4 * P + kept_b)
+    pay = kvq.Packed.empty(kvq.FMT_NVFP4, 0, P, H, D, device=device)
+    pb = P * H * (D // 2 + D // 16 + 4)
+    timed("kvq_encode_residual nvfp4 25%", lambda: kvq.kvq_encode_residual(cur, prev, pos, pay),
+          2 * P * H * 2 * D + 4 * P + pb)
+    timed("kvq_decode_residual nvfp4 25% copy", lambda: kvq.kvq_decode_residual(pay, pos, prev, y),
+          rows_b + pb + 4 * P + rows_b)
+    return {"workload": f"[{T} tokens, {H} KV heads, D{D}] bf16, INT4 G{G}, residual rows kept {P}/{T}",
+            "kernels": out}
+
+
+def residual_loop_latency(kvq, device, iters=50):
+    """Microseconds per call on one residual loop of the INT4 + residual case:
+    [4096, 8, 128], 1024 kept rows (the sizes of the pages' loop study)."""
+    r = other_rows(kvq, device, T=4096, H=8, D=128, G=64, P=1024, iters=iters)
+    return {k: round(v["ms"] * 1000, 2) for k, v in r["kernels"].items()}
 
 
 # ---------------------------------------------------------------------------
@@ -483,6 +604,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=16)
     ap.add_argument("--cpu-tokens", type=int, default=16384)
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="reference arm: CPU seconds the whole --steps/--warmup run may take")
@@ -490,6 +612,7 @@ def main():
                     help="tokens of the workload (default: the 1,048,576-token case); smaller "
                          "values give the same kernels on a smaller case for profiling")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-rows", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
