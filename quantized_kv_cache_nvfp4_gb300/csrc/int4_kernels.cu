@@ -21,12 +21,27 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Code of x in a group with FP32 minimum mn and scale sc (sc > 0).
-__device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc) {
-  float q = rintf(__fdiv_rn(__fsub_rn(x, mn), sc));
-  q = fminf(fmaxf(q, 0.0f), 15.0f);
-  return static_cast<uint32_t>(q);
+// Code of x in a group with FP32 minimum mn and scale sc > 0, rsc = RN(1 / sc):
+// clamp(rint(RN(RN(x - mn) / sc)), 0, 15), usually without dividing.
+//
+// With d = RN(x - mn) >= 0, the estimate qe = RN(d * rsc) and the defined quotient
+// q = RN(d / sc) both lie within 2 * 2^-24 (relative) of d / sc, and d / sc <= 15 *
+// (1 + 2^-23) because x <= max; so after clamping to 15, |qe - q| < 2.9e-6 < 2^-17.
+// When qe is more than 2^-17 away from the half-integers around it, q rounds to the
+// same integer as qe (rint is ties-to-even, and no tie is possible there).
+// Otherwise, and whenever sc is not a normal binary32 (rsc could overflow), the
+// quotient is formed by the division itself.
+__device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float rsc) {
+  const float d = __fsub_rn(x, mn);
+  if (sc >= 0x1p-126f) {
+    const float qe = fminf(__fmul_rn(d, rsc), 15.0f);
+    const float r = rintf(qe);
+    if (fabsf(__fsub_rn(qe, r)) < 0.49999237f) return static_cast<uint32_t>(r);  // 0.5 - 2^-17
+  }
+  return static_cast<uint32_t>(rintf(fminf(__fdiv_rn(d, sc), 15.0f)));
 }
+
+__device__ __forceinline__ float int4_rcp(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }
 
 // The 8 bf16 values of one 16-byte chunk of a compact row (residual: bf16(cur-prev)).
 // Returns false for a residual row whose position is out of range (values zero).
@@ -65,31 +80,42 @@ __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row
   }
 }
 
-// KEY kind: one lane per (group, head, 8-channel chunk) column task; the lane walks
-// the group's rows twice (min/max, then codes).  Consecutive lanes take consecutive
-// chunks of the same head and row, so every row read is one coalesced span.
-template <bool kResidual>
+// KEY kind: a column task is (group of G rows, head, 8-channel chunk).  RS lanes
+// share a task, each walking every RS-th row of the group twice (min/max, then
+// codes); the RS partial minima/maxima meet in a xor butterfly.  A warp holds 32/RS
+// consecutive tasks (consecutive chunks of one row), so each row read is one
+// coalesced span per row split.
+template <bool kResidual, int RS>
 __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
+  constexpr int CW = 32 / RS;
+  const int lane = threadIdx.x & 31;
+  const int rs = lane / CW;
+  const int cl = lane % CW;
   const int32_t nchunk = p.D / 8;
   const int32_t ngroups = (p.rows + p.G - 1) / p.G;
-  const int64_t tasks = static_cast<int64_t>(ngroups) * p.H * nchunk;
-  for (int64_t task = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; task < tasks;
-       task += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int32_t chunk = static_cast<int32_t>(task % nchunk);
-    const int32_t h = static_cast<int32_t>((task / nchunk) % p.H);
-    const int32_t g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * p.H));
+  const int64_t ntask = static_cast<int64_t>(ngroups) * p.H * nchunk;
+  const int64_t nwtask = (ntask + CW - 1) / CW;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
+       wt += nwarps) {
+    const int64_t task = wt * CW + cl;
+    const bool valid = task < ntask;
+    const int64_t tk = valid ? task : 0;
+    const int32_t chunk = static_cast<int32_t>(tk % nchunk);
+    const int32_t h = static_cast<int32_t>((tk / nchunk) % p.H);
+    const int32_t g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
     const int32_t r0 = g * p.G;
-    const int32_t r1 = min(p.rows, r0 + p.G);
+    const int32_t r1 = valid ? min(p.rows, r0 + p.G) : r0;
     const int32_t col = chunk * 8;
 
     float mn[8], mx[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      mn[i] = __int_as_float(0x7F800000);   // +inf
-      mx[i] = __int_as_float(0xFF800000);   // -inf
+      mn[i] = __int_as_float(0x7F800000);  // +inf
+      mx[i] = __int_as_float(0xFF800000);  // -inf
     }
 #pragma unroll 4
-    for (int32_t r = r0; r < r1; ++r) {
+    for (int32_t r = r0 + rs; r < r1; r += RS) {
       uint32_t w[4];
       load_chunk8<kResidual>(p, r, h, col, w);
 #pragma unroll
@@ -100,38 +126,52 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16hi(w[i]));
       }
     }
-    float sc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i] = __fdiv_rn(__fsub_rn(mx[i], mn[i]), 15.0f);
+    for (int o = CW; o < 32; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mn[i] = fminf(mn[i], __shfl_xor_sync(0xFFFFFFFFu, mn[i], o));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xFFFFFFFFu, mx[i], o));
+      }
+    }
+    if (!valid) continue;
+    float sc[8], rsc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sc[i] = __fdiv_rn(__fsub_rn(mx[i], mn[i]), 15.0f);
+      rsc[i] = int4_rcp(sc[i]);
+    }
 
 #pragma unroll 4
-    for (int32_t r = r0; r < r1; ++r) {
+    for (int32_t r = r0 + rs; r < r1; r += RS) {
       uint32_t w[4];
       load_chunk8<kResidual>(p, r, h, col, w);
       if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
       uint32_t packed = 0u;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t cl = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i]) : 0u;
-        const uint32_t ch =
-            sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1]) : 0u;
-        packed |= (cl | (ch << 4)) << (8 * i);
+        const uint32_t cl0 = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i], rsc[2 * i]) : 0u;
+        const uint32_t ch0 =
+            sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1], rsc[2 * i + 1]) : 0u;
+        packed |= (cl0 | (ch0 << 4)) << (8 * i);
       }
       STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
                                       col / 2),
           packed);
     }
-    uint32_t m16[4], s16[4];
+    if (rs == 0) {
+      uint32_t m16[4], s16[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      m16[i] = static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i])) |
-               (static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i + 1])) << 16);
-      s16[i] = static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i])) |
-               (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
+      for (int i = 0; i < 4; ++i) {
+        m16[i] = static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i])) |
+                 (static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i + 1])) << 16);
+        s16[i] = static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i])) |
+                 (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
+      }
+      const int64_t m = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
+      store16B(p.dst.mn + m, m16);
+      store16B(p.dst.sc + m, s16);
     }
-    const int64_t m = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
-    store16B(p.dst.mn + m, m16);
-    store16B(p.dst.sc + m, s16);
   }
 }
 
@@ -188,11 +228,12 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     }
     if (!valid) continue;
     const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
+    const float rsc = int4_rcp(sc);
     uint32_t c0 = 0u, c1 = 0u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t cl = sc != 0.0f ? int4_code(bf16lo(w[i]), lmn, sc) : 0u;
-      const uint32_t ch = sc != 0.0f ? int4_code(bf16hi(w[i]), lmn, sc) : 0u;
+      const uint32_t cl = sc != 0.0f ? int4_code(bf16lo(w[i]), lmn, sc, rsc) : 0u;
+      const uint32_t ch = sc != 0.0f ? int4_code(bf16hi(w[i]), lmn, sc, rsc) : 0u;
       if (i < 4)
         c0 |= (cl | (ch << 4)) << (8 * i);
       else
@@ -243,22 +284,26 @@ cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+template <bool kRes, int RS>
+cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s) {
+  auto k = int4_key_kernel<kRes, RS>;
+  const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
+  const int grid = grid_cap(k, warps, kThreads / 32);
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s) {
   if (p.kind == 0) {
-    const int64_t tasks = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
-    cudaError_t e = cudaSuccess;
-    if (p.residual) {
-      auto k = int4_key_kernel<true>;
-      const int grid = grid_cap(k, tasks, kThreads);
-      KVQ_LAUNCH("int4_key_kernel<res>", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
-    } else {
-      auto k = int4_key_kernel<false>;
-      const int grid = grid_cap(k, tasks, kThreads);
-      KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
-    }
-    return e;
+    // column tasks; with few of them (short tensors) each gets 8 row splits so the
+    // launch still fills the GPU, otherwise 4
+    const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
+    const bool small = ntask * 4 < static_cast<int64_t>(num_sms()) * 2048;
+    if (p.residual) return small ? key_launch<true, 8>(p, ntask, s) : key_launch<true, 4>(p, ntask, s);
+    return small ? key_launch<false, 8>(p, ntask, s) : key_launch<false, 4>(p, ntask, s);
   }
   return p.residual ? value_dispatch<true>(p, s) : value_dispatch<false>(p, s);
 }

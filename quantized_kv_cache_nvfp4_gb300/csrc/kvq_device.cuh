@@ -354,6 +354,50 @@ __device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) 
   hi = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
 }
 
+// NVFP4 decode of one 16-element block: y = bf16((e2m1 * bs) * rs).  e2m1 * bs is
+// exact (fma.rn.f32.f16 of two fp16 values, at most 6 significant bits), then one
+// binary32 rounding by the row scale, then bf16.
+__device__ __forceinline__ void nvfp4_decode16(uint32_t cw0, uint32_t cw1, uint32_t bsb, float rs,
+                                               uint32_t (&out)[8]) {
+  const uint16_t bs16 = static_cast<uint16_t>(e4m3_to_f16x2(bsb) & 0xFFFFu);
+  const uint64_t rs2 = pack_f32x2(__float_as_uint(rs), __float_as_uint(rs));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
+    const uint32_t h2 = e2m1x2_to_f16x2(byte);
+    const float lo = mul_f16_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu), bs16);
+    const float hi = mul_f16_to_f32(static_cast<uint16_t>(h2 >> 16), bs16);
+    uint32_t yl, yh;
+    unpack_f32x2(mul_f32x2(pack_f32x2(__float_as_uint(lo), __float_as_uint(hi)), rs2), yl, yh);
+    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+  }
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// INT4 decode of 16 codes (8 bytes) with per-element fp32 minimum and scale:
+// y = bf16(code * sc + mn), a multiply then an add, each rounded (no FMA).
+__device__ __forceinline__ void int4_decode16(uint32_t cw0, uint32_t cw1, const float (&mn)[16],
+                                              const float (&sc)[16], uint32_t (&out)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
+    // 2^23 + c is exact for c < 16, so subtracting 2^23 gives float(c) exactly
+    uint64_t c2 = pack_f32x2(0x4B000000u | (byte & 15u), 0x4B000000u | (byte >> 4));
+    uint64_t neg = pack_f32x2(0xCB000000u, 0xCB000000u);  // -2^23
+    c2 = add_f32x2(c2, neg);
+    uint64_t v = mul_f32x2(c2, pack_f32x2(__float_as_uint(sc[2 * i]), __float_as_uint(sc[2 * i + 1])));
+    v = add_f32x2(v, pack_f32x2(__float_as_uint(mn[2 * i]), __float_as_uint(mn[2 * i + 1])));
+    uint32_t yl, yh;
+    unpack_f32x2(v, yl, yh);
+    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+  }
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
   if (status != nullptr && KVQ_OK(status, 4, 4)) atomicOr(status, bit);
 }

@@ -216,23 +216,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(cons
   }
 }
 
-// y = bf16((e2m1 * bs) * rs) for the 16 codes of one block (8 code bytes).
-__device__ __forceinline__ void decode_block(uint32_t cw0, uint32_t cw1, uint32_t bsb, float rs,
-                                             uint32_t (&out)[8]) {
-  const uint16_t bs16 = static_cast<uint16_t>(e4m3_to_f16x2(bsb) & 0xFFFFu);
-  const uint64_t rs2 = pack_f32x2(__float_as_uint(rs), __float_as_uint(rs));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
-    const uint32_t h2 = e2m1x2_to_f16x2(byte);
-    const float lo = mul_f16_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu), bs16);  // exact
-    const float hi = mul_f16_to_f32(static_cast<uint16_t>(h2 >> 16), bs16);
-    uint32_t yl, yh;
-    unpack_f32x2(mul_f32x2(pack_f32x2(__float_as_uint(lo), __float_as_uint(hi)), rs2), yl, yh);
-    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
-  }
-}
-
 // Restore one row (or skip it): resolve the slot through the block table.
 struct RestoreRow {
   int64_t srow;  // pool row (slot * H + h), or -1 to skip
@@ -320,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_decode_kernel(cons
       uint32_t out[8];
 #pragma unroll
       for (int j = 0; j < BPL; ++j) {
-        decode_block(cw[r][2 * j], cw[r][2 * j + 1], (bsb[r] >> (8 * j)) & 0xFFu, rs[r], out);
+        nvfp4_decode16(cw[r][2 * j], cw[r][2 * j + 1], (bsb[r] >> (8 * j)) & 0xFFu, rs[r], out);
         store32B<kV8>(rr[r].y + 16 * (b0 + j), out);
       }
     }

@@ -9,11 +9,13 @@
 //   INT4   y = bf16(code * fp32(sc16) + fp32(mn16))   (a mul, then an add)
 //   residual out[pos[p]] = bf16(prev[pos[p]] + y[p]); other rows keep prev.
 //
-// Iteration spaces:
-//   unpack            every (row, head) of the payload
+// Work mapping: a lane owns BPL consecutive 16-element blocks of a row (as in the
+// NVFP4 kernels).  Iteration spaces:
+//   unpack            every (row, head) of the payload, grid-stride
 //   residual in place every kept row: t = pos[p] (the other rows are already prev)
-//   residual copy     every row t of out; t is looked up in the sorted pos map by
-//                     binary search (kept: add, absent: copy prev)
+//   residual copy     every row t of out, in contiguous runs of kRun tokens per warp:
+//                     one binary search of the sorted position map at the start of a
+//                     run, then a cursor that only moves forward
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 
@@ -22,66 +24,93 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRun = 64;  // tokens per warp run in the residual copy mode
 
-// 16 decoded bf16 (packed in w) of payload row p, head h, block b.
-template <int kFmt>
-__device__ __forceinline__ void decode_block(const UnpackParams& u, int64_t p, int32_t h, int b,
-                                             uint32_t (&w)[8]) {
+// BPL decoded blocks (16 bf16 each, packed in w) of payload row p, head h, from
+// block b0 on.
+template <int kFmt, int BPL>
+__device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, int32_t h, int b0,
+                                              uint32_t (&w)[BPL][8]) {
   const PayloadRef& P = u.pay;
   const int64_t prow = p * u.H + h;
-  uint32_t cw0, cw1;
-  load8B(P.codes + prow * (u.D / 2) + 8 * b, cw0, cw1);
-  if constexpr (kFmt == 1) {
-    const uint32_t bsb = LDX(static_cast<const uint8_t*>(P.meta0) + prow * u.nb + b);
-    const float rs = LDX(P.rscale + prow);
-    const uint32_t bs2 = e4m3_to_f16x2(bsb) & 0xFFFFu;
-    const uint32_t bsx2 = bs2 | (bs2 << 16);
+  uint32_t cw[2 * BPL];
+  if constexpr (BPL == 2) {
+    uint32_t c4[4];
+    load16B(P.codes + prow * (u.D / 2) + 8 * b0, c4);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
-      float lo, hi;
-      f16x2_to_f32(hmul2_bits(e2m1x2_to_f16x2(byte), bsx2), lo, hi);
-      w[i] = pack_bf16x2(__fmul_rn(lo, rs), __fmul_rn(hi, rs));
-    }
+    for (int i = 0; i < 4; ++i) cw[i] = c4[i];
+  } else {
+    load8B(P.codes + prow * (u.D / 2) + 8 * b0, cw[0], cw[1]);
+  }
+  if constexpr (kFmt == 1) {
+    const uint8_t* bsp = static_cast<const uint8_t*>(P.meta0) + prow * u.nb + b0;
+    uint32_t bsb;
+    if constexpr (BPL == 2)
+      bsb = LDX(reinterpret_cast<const uint16_t*>(bsp));
+    else
+      bsb = LDX(bsp);
+    const float rs = LDX(P.rscale + prow);
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) nvfp4_decode16(cw[2 * j], cw[2 * j + 1], (bsb >> (8 * j)) & 0xFFu, rs, w[j]);
   } else {
     const uint16_t* mnp = static_cast<const uint16_t*>(P.meta0);
     const uint16_t* scp = static_cast<const uint16_t*>(P.meta1);
-    float mn[16], sc[16];
-    if (P.kind == 0) {  // KEY: per-channel metadata of group p / G
-      const int64_t m = ((p / P.G) * u.H + h) * u.D + 16 * b;
-      uint32_t a[8], c[8];
-      load32B<false, true>(mnp + m, a);
-      load32B<false, true>(scp + m, c);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mn[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(a[i] & 0xFFFFu));
-        mn[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(a[i] >> 16));
-        sc[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(c[i] & 0xFFFFu));
-        sc[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(c[i] >> 16));
+    for (int j = 0; j < BPL; ++j) {
+      const int b = b0 + j;
+      float mn[16], sc[16];
+      if (P.kind == 0) {  // KEY: per-channel metadata of group p / G
+        const int64_t m = ((p / P.G) * u.H + h) * u.D + 16 * b;
+        uint32_t a[8], c[8];
+        load32B<false, true>(mnp + m, a);
+        load32B<false, true>(scp + m, c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mn[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(a[i] & 0xFFFFu));
+          mn[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(a[i] >> 16));
+          sc[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(c[i] & 0xFFFFu));
+          sc[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(c[i] >> 16));
+        }
+      } else {  // VALUE: one group covers the whole 16-channel block
+        const int ngv = (u.D + P.G - 1) / P.G;
+        const int64_t m = prow * ngv + (16 * b) / P.G;
+        const float mv = f16_bits_to_f32(LDX(mnp + m));
+        const float sv = f16_bits_to_f32(LDX(scp + m));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          mn[i] = mv;
+          sc[i] = sv;
+        }
       }
-    } else {  // VALUE: one group covers the whole 16-channel block
-      const int ngv = (u.D + P.G - 1) / P.G;
-      const int64_t m = prow * ngv + (16 * b) / P.G;
-      const float mv = f16_bits_to_f32(LDX(mnp + m));
-      const float sv = f16_bits_to_f32(LDX(scp + m));
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        mn[i] = mv;
-        sc[i] = sv;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = ((i < 4 ? cw0 : cw1) >> (8 * (i & 3))) & 0xFFu;
-      const float lo = __fadd_rn(__fmul_rn(static_cast<float>(byte & 15u), sc[2 * i]), mn[2 * i]);
-      const float hi =
-          __fadd_rn(__fmul_rn(static_cast<float>(byte >> 4), sc[2 * i + 1]), mn[2 * i + 1]);
-      w[i] = pack_bf16x2(lo, hi);
+      int4_decode16(cw[2 * j], cw[2 * j + 1], mn, sc, w[j]);
     }
   }
 }
 
-__device__ __forceinline__ int32_t find_pos(const int32_t* pos, int32_t n, int32_t t) {
+// out row = bf16(prev + y) for the BPL blocks of this lane, or a copy of prev when
+// `add` is false (kNC: prev is read-only in this launch, i.e. it is not the output).
+template <bool kV8, bool kNC, int BPL>
+__device__ __forceinline__ void add_store(const uint16_t* prev, uint16_t* out, int b0,
+                                          const uint32_t (&w)[BPL][8], bool add) {
+#pragma unroll
+  for (int j = 0; j < BPL; ++j) {
+    uint32_t q[8];
+    load32B<kV8, kNC>(prev + 16 * (b0 + j), q);
+    if (add) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t lo, hi;
+        unpack_f32x2(add_f32x2(pack_f32x2(q[i] << 16, q[i] & 0xFFFF0000u),
+                               pack_f32x2(w[j][i] << 16, w[j][i] & 0xFFFF0000u)),
+                     lo, hi);
+        q[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+      }
+    }
+    store32B<kV8>(out + 16 * (b0 + j), q);
+  }
+}
+
+__device__ __forceinline__ int32_t lower_bound(const int32_t* pos, int32_t n, int32_t t) {
   int32_t lo = 0, hi = n;  // first index with pos[i] >= t
   while (lo < hi) {
     const int32_t mid = (lo + hi) >> 1;
@@ -90,16 +119,18 @@ __device__ __forceinline__ int32_t find_pos(const int32_t* pos, int32_t n, int32
     else
       hi = mid;
   }
-  return (lo < n && LDX(pos + lo) == t) ? lo : -1;
+  return lo;
 }
 
-template <int L, bool kV8, int kFmt, int kMode>
+template <int L, int BPL, bool kV8, int kFmt, int kMode>
 __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
-  const int b = lane % L;
+  const int li = lane % L;
   const int sub = lane / L;
-  const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
+  const int b0 = li * BPL;
+  const uint32_t gwarp = blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+  const uint32_t nwarps = gridDim.x * (kThreads / 32);
 
   if constexpr (kMode == 2) {  // the copy mode does not visit kept rows by p: check the map here
     if (u.pos != nullptr) {
@@ -110,64 +141,78 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
       }
     }
   }
-  if (b >= u.nb) return;
+  if (b0 >= u.nb) return;  // no shuffles below: idle lanes may leave
 
-  for (uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
-       row < u.total_rows; row += stride) {
+  if constexpr (kMode == 2) {
+    // residual decode into a separate output: every row t of out, runs of kRun tokens
+    const uint32_t nruns = (static_cast<uint32_t>(u.src_rows) + kRun - 1) / kRun;
+    for (uint32_t run = gwarp; run < nruns; run += nwarps) {
+      const int32_t t0 = static_cast<int32_t>(run * kRun);
+      const int32_t t1 = min(u.src_rows, t0 + kRun);
+      int32_t cur = (u.pos != nullptr) ? lower_bound(u.pos, u.num_pos, t0) : 0;
+      for (uint32_t row = static_cast<uint32_t>(t0) * u.H + sub; row < static_cast<uint32_t>(t1) * u.H;
+           row += kRowsPerWarp) {
+        uint32_t t, h;
+        u.div_h.divmod(row, t, h);
+        int64_t p = t;
+        if (u.pos != nullptr) {
+          while (cur < u.num_pos && LDX(u.pos + cur) < static_cast<int32_t>(t)) ++cur;
+          // both arms signed: -1 must stay negative
+          p = (cur < u.num_pos && LDX(u.pos + cur) == static_cast<int32_t>(t)) ? static_cast<int64_t>(cur)
+                                                                              : static_cast<int64_t>(-1);
+        }
+        uint32_t w[BPL][8];
+        if (p >= 0) decode_blocks<kFmt, BPL>(u, p, static_cast<int32_t>(h), b0, w);
+        add_store<kV8, true, BPL>(u.prev + static_cast<int64_t>(t) * u.prev_row_pitch +
+                                      static_cast<int64_t>(h) * u.prev_head_pitch,
+                                  u.y + static_cast<int64_t>(t) * u.y_row_pitch +
+                                      static_cast<int64_t>(h) * u.y_head_pitch,
+                                  b0, w, p >= 0);
+      }
+    }
+    return;
+  }
+
+  const uint32_t stride = nwarps * kRowsPerWarp;
+  for (uint32_t row = gwarp * kRowsPerWarp + sub; row < u.total_rows; row += stride) {
     uint32_t r, h;
     u.div_h.divmod(row, r, h);
-    uint32_t w[8];
-    if constexpr (kMode == 0) {
-      decode_block<kFmt>(u, r, h, b, w);
-      store32B<kV8>(u.y + static_cast<int64_t>(r) * u.y_row_pitch +
-                        static_cast<int64_t>(h) * u.y_head_pitch + 16 * b,
-                    w);
-    } else {
-      int64_t t, p;
-      if constexpr (kMode == 1) {  // in place: row r is the compact index p
-        p = r;
-        t = r;
-        if (u.pos != nullptr) {
-          t = LDX(u.pos + r);
-          bool bad = t < 0 || t >= u.src_rows;
-          if (h == 0 && b == 0 && r > 0 && LDX(u.pos + r - 1) >= t) set_status(u.status, 4u);
-          if (bad) {
-            if (h == 0 && b == 0) set_status(u.status, 4u);
-            continue;
-          }
-        }
-      } else {  // copy: row r is the output row t
-        t = r;
-        // both arms signed: a -1 from find_pos must stay negative (with an unsigned
-        // arm the conditional would convert it to 0xFFFFFFFF)
-        p = (u.pos != nullptr) ? static_cast<int64_t>(find_pos(u.pos, u.num_pos, static_cast<int32_t>(r)))
-                               : static_cast<int64_t>(r);
-      }
-      uint32_t q[8];
-      load32B<kV8, kMode == 2>(u.prev + t * u.prev_row_pitch +
-                                   static_cast<int64_t>(h) * u.prev_head_pitch + 16 * b,
-                               q);
-      if (p >= 0) {
-        decode_block<kFmt>(u, p, h, b, w);
+    uint32_t w[BPL][8];
+    if constexpr (kMode == 0) {  // unpack
+      decode_blocks<kFmt, BPL>(u, r, static_cast<int32_t>(h), b0, w);
+      uint16_t* y = u.y + static_cast<int64_t>(r) * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          q[i] = pack_bf16x2(__fadd_rn(bf16lo(q[i]), bf16lo(w[i])),
-                             __fadd_rn(bf16hi(q[i]), bf16hi(w[i])));
+      for (int j = 0; j < BPL; ++j) store32B<kV8>(y + 16 * (b0 + j), w[j]);
+    } else {  // residual in place: row r is the compact index p
+      int64_t t = r;
+      if (u.pos != nullptr) {
+        t = LDX(u.pos + r);
+        if (h == 0 && li == 0 && r > 0 && LDX(u.pos + r - 1) >= t) set_status(u.status, 4u);
+        if (t < 0 || t >= u.src_rows) {
+          if (h == 0 && li == 0) set_status(u.status, 4u);
+          continue;
+        }
       }
-      store32B<kV8>(u.y + t * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + 16 * b, q);
+      decode_blocks<kFmt, BPL>(u, r, static_cast<int32_t>(h), b0, w);
+      add_store<kV8, false, BPL>(u.prev + t * u.prev_row_pitch + static_cast<int64_t>(h) * u.prev_head_pitch,
+                                 u.y + t * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch, b0, w,
+                                 true);
     }
   }
 }
 
-template <int L, bool kV8, int kFmt, int kMode>
+template <int L, int BPL, bool kV8, int kFmt, int kMode>
 cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
-  auto k = payload_kernel<L, kV8, kFmt, kMode>;
+  auto k = payload_kernel<L, BPL, kV8, kFmt, kMode>;
   int occ = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
   if (occ < 1) occ = 1;
-  const int rows_per_cta = (kThreads / 32) * (32 / L);
-  int64_t need = (static_cast<int64_t>(u.total_rows) + rows_per_cta - 1) / rows_per_cta;
-  int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+  int64_t need;
+  if (kMode == 2)  // one warp per run of kRun tokens
+    need = ((static_cast<int64_t>(u.src_rows) + kRun - 1) / kRun + kThreads / 32 - 1) / (kThreads / 32);
+  else
+    need = (static_cast<int64_t>(u.total_rows) + (kThreads / 32) * (32 / L) - 1) / ((kThreads / 32) * (32 / L));
+  const int64_t cap = static_cast<int64_t>(num_sms()) * occ * 2;
   if (need < 1) need = 1;
   const int grid = static_cast<int>(need < cap ? need : cap);
   cudaError_t e = cudaSuccess;
@@ -175,34 +220,31 @@ cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   return e;
 }
 
-template <int L, bool kV8>
+template <int L, int BPL, bool kV8>
 cudaError_t pl_dispatch_fm(const UnpackParams& u, cudaStream_t s) {
   const int f = u.pay.fmt == 1 ? 1 : 2;
   switch (u.mode * 2 + (f - 1)) {
-    case 0: return pl_launch<L, kV8, 1, 0>(u, s);
-    case 1: return pl_launch<L, kV8, 2, 0>(u, s);
-    case 2: return pl_launch<L, kV8, 1, 1>(u, s);
-    case 3: return pl_launch<L, kV8, 2, 1>(u, s);
-    case 4: return pl_launch<L, kV8, 1, 2>(u, s);
-    case 5: return pl_launch<L, kV8, 2, 2>(u, s);
+    case 0: return pl_launch<L, BPL, kV8, 1, 0>(u, s);
+    case 1: return pl_launch<L, BPL, kV8, 2, 0>(u, s);
+    case 2: return pl_launch<L, BPL, kV8, 1, 1>(u, s);
+    case 3: return pl_launch<L, BPL, kV8, 2, 1>(u, s);
+    case 4: return pl_launch<L, BPL, kV8, 1, 2>(u, s);
+    case 5: return pl_launch<L, BPL, kV8, 2, 2>(u, s);
   }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_payload_decode(const UnpackParams& u, int lanes, bool v8, cudaStream_t s) {
-#define KVQ_PL(LN) \
-  case LN:         \
-    return v8 ? pl_dispatch_fm<LN, true>(u, s) : pl_dispatch_fm<LN, false>(u, s);
-  switch (lanes) {
-    KVQ_PL(1)
-    KVQ_PL(2)
-    KVQ_PL(4)
-    KVQ_PL(8)
-    KVQ_PL(16)
-    KVQ_PL(32)
-  }
+cudaError_t launch_payload_decode(const UnpackParams& u, int /*lanes*/, bool v8, cudaStream_t s) {
+  const int bpl = (u.nb % 2 == 0) ? 2 : 1;
+  int lanes = 1;
+  while (lanes < u.nb / bpl) lanes <<= 1;
+#define KVQ_PL(LN, B)                                                                          \
+  if (lanes == LN && bpl == B)                                                                 \
+    return v8 ? pl_dispatch_fm<LN, B, true>(u, s) : pl_dispatch_fm<LN, B, false>(u, s);
+  KVQ_PL(1, 1) KVQ_PL(2, 1) KVQ_PL(4, 1) KVQ_PL(8, 1) KVQ_PL(16, 1) KVQ_PL(32, 1)
+  KVQ_PL(1, 2) KVQ_PL(2, 2) KVQ_PL(4, 2) KVQ_PL(8, 2) KVQ_PL(16, 2)
 #undef KVQ_PL
   return cudaErrorInvalidValue;
 }
