@@ -198,3 +198,36 @@ def test_residual_with_strided_views():
         want, _ = O.residual_decode(opay, bits(prev))
         np.testing.assert_array_equal(bits(out), want)
         assert (bits(outbig[:, :H * D]) == 0xA5A5).all()
+
+
+def _tie_rows(scale, n_rows=64):
+    """Channel groups (V kind, G = 64 channels) with min 0 and max 15 * scale, so the
+    scale is `scale` up to rounding and (x - min) / scale hits every k + 1/2 (a tie,
+    where rint must go to even), its bf16 neighbours, and the integers."""
+    import numpy as np
+
+    vals = []
+    for k in range(15):
+        m = (k + 0.5) * scale
+        vals += [m, np.nextafter(np.float32(m), np.float32(0)), np.nextafter(np.float32(m), np.float32(99)),
+                 k * scale, (k + 0.49) * scale, (k + 0.51) * scale]
+    vals = np.array(vals, np.float64)
+    rows = []
+    for r in range(n_rows):
+        body = np.roll(vals, r)[:62]
+        rows.append(np.concatenate([[0.0, 15.0 * scale], body]))
+    return np.array(rows)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.25, 0.3, 1.7, 3e-3, 1e-30])
+def test_int4_half_integer_quotients_round_to_even(scale):
+    import numpy as np
+
+    rows = _tie_rows(scale)
+    xb = O.f32_to_bf16(rows.astype(np.float32)).reshape(-1, 1, 64)
+    x = synth.from_bits(xb).to(DEV)
+    for kind in (kvq.KIND_VALUE, kvq.KIND_KEY):
+        pk, y = gpu_int4_pack(x, kind)
+        codes, mn, sc = O.int4_pack(xb, kind, 64)
+        check_int4(pk, codes, mn, sc)
+        np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
