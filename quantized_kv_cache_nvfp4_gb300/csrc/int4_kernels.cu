@@ -31,14 +31,21 @@ constexpr int kThreads = 256;
 // same integer as qe (rint is ties-to-even, and no tie is possible there).
 // Otherwise, and whenever sc is not a normal binary32 (rsc could overflow), the
 // quotient is formed by the division itself.
+//
+// Rounding to an integer: for 0 <= v <= 15, RN(v + 1.5 * 2^23) has unit spacing, so
+// it is v rounded to nearest with ties to even, and its low four mantissa bits are
+// that integer.
+constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+
 __device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float rsc) {
   const float d = __fsub_rn(x, mn);
   if (sc >= 0x1p-126f) {
     const float qe = fminf(__fmul_rn(d, rsc), 15.0f);
-    const float r = rintf(qe);
-    if (fabsf(__fsub_rn(qe, r)) < 0.49999237f) return static_cast<uint32_t>(r);  // 0.5 - 2^-17
+    const float t = __fadd_rn(qe, kRound);
+    if (fabsf(__fsub_rn(qe, __fsub_rn(t, kRound))) < 0.49999237f)  // 0.5 - 2^-17
+      return __float_as_uint(t) & 15u;
   }
-  return static_cast<uint32_t>(rintf(fminf(__fdiv_rn(d, sc), 15.0f)));
+  return __float_as_uint(__fadd_rn(fminf(__fdiv_rn(d, sc), 15.0f), kRound)) & 15u;
 }
 
 __device__ __forceinline__ float int4_rcp(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }

@@ -379,6 +379,24 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
+// INT4 decode of 8 codes (one word, low nibble first) with per-element minimum and
+// scale: y = bf16(code * sc + mn), a multiply then an add, each rounded (no FMA).
+__device__ __forceinline__ void int4_decode8(uint32_t cw, const float (&mn)[8], const float (&sc)[8],
+                                             uint32_t (&out)[4]) {
+  const uint64_t neg = pack_f32x2(0xCB000000u, 0xCB000000u);  // -2^23
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t byte = (cw >> (8 * i)) & 0xFFu;
+    // 2^23 + c is exact for c < 16, so adding -2^23 gives float(c) exactly
+    const uint64_t c2 = add_f32x2(pack_f32x2(0x4B000000u | (byte & 15u), 0x4B000000u | (byte >> 4)), neg);
+    uint64_t v = mul_f32x2(c2, pack_f32x2(__float_as_uint(sc[2 * i]), __float_as_uint(sc[2 * i + 1])));
+    v = add_f32x2(v, pack_f32x2(__float_as_uint(mn[2 * i]), __float_as_uint(mn[2 * i + 1])));
+    uint32_t yl, yh;
+    unpack_f32x2(v, yl, yh);
+    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+  }
+}
+
 // INT4 decode of 16 codes (8 bytes) with per-element fp32 minimum and scale:
 // y = bf16(code * sc + mn), a multiply then an add, each rounded (no FMA).
 __device__ __forceinline__ void int4_decode16(uint32_t cw0, uint32_t cw1, const float (&mn)[16],
@@ -411,6 +429,18 @@ __device__ __forceinline__ void load16B(const void* p, uint32_t (&w)[4]) {
   asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                : "l"(p));
+}
+
+// 16-byte load through the coherent path (for rows this launch also writes).
+__device__ __forceinline__ void load16B_rw(const void* p, uint32_t (&w)[4]) {
+  if (!KVQ_OK(p, 16, 16)) {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    return;
+  }
+  asm volatile("ld.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "l"(p)
+               : "memory");
 }
 
 __device__ __forceinline__ void store16B(void* p, const uint32_t (&w)[4]) {

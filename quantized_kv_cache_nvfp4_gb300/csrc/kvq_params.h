@@ -157,6 +157,7 @@ struct UnpackParams {
   int32_t num_pos;
   int32_t src_rows;     // rows of prev/out
   int32_t mode;         // 0 unpack, 1 residual in place (iterate kept rows), 2 residual out of place
+  int32_t run;          // residual copy: tokens per warp run (set by the launcher)
   uint32_t* status;
 };
 

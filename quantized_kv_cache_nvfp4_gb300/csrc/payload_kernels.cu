@@ -13,9 +13,12 @@
 // NVFP4 kernels).  Iteration spaces:
 //   unpack            every (row, head) of the payload, grid-stride
 //   residual in place every kept row: t = pos[p] (the other rows are already prev)
-//   residual copy     every row t of out, in contiguous runs of kRun tokens per warp:
-//                     one binary search of the sorted position map at the start of a
-//                     run, then a cursor that only moves forward
+//   residual copy     every row t of out, in contiguous runs of tokens per warp (4
+//                     to 64, so that short tensors still spread over the GPU): one
+//                     binary search of the sorted position map at the start of a run,
+//                     then a cursor that only moves forward
+// INT4 K payloads (groups over token rows) decode column-wise instead: see
+// int4_key_decode_kernel.
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 
@@ -24,7 +27,6 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRun = 64;  // tokens per warp run in the residual copy mode
 
 // BPL decoded blocks (16 bf16 each, packed in w) of payload row p, head h, from
 // block b0 on.
@@ -144,11 +146,11 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
   if (b0 >= u.nb) return;  // no shuffles below: idle lanes may leave
 
   if constexpr (kMode == 2) {
-    // residual decode into a separate output: every row t of out, runs of kRun tokens
-    const uint32_t nruns = (static_cast<uint32_t>(u.src_rows) + kRun - 1) / kRun;
+    // residual decode into a separate output: every row t of out, runs of u.run tokens
+    const uint32_t nruns = (static_cast<uint32_t>(u.src_rows) + u.run - 1) / u.run;
     for (uint32_t run = gwarp; run < nruns; run += nwarps) {
-      const int32_t t0 = static_cast<int32_t>(run * kRun);
-      const int32_t t1 = min(u.src_rows, t0 + kRun);
+      const int32_t t0 = static_cast<int32_t>(run * u.run);
+      const int32_t t1 = min(u.src_rows, t0 + u.run);
       int32_t cur = (u.pos != nullptr) ? lower_bound(u.pos, u.num_pos, t0) : 0;
       for (uint32_t row = static_cast<uint32_t>(t0) * u.H + sub; row < static_cast<uint32_t>(t1) * u.H;
            row += kRowsPerWarp) {
@@ -201,6 +203,95 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
   }
 }
 
+// INT4 K payloads, unpack (kInPlace = false) or residual decode in place: a column
+// task is (group of G compact rows, head, 8-channel chunk); its FP16 minimum and
+// scale are read once, then RS lanes walk every RS-th row of the group: 4 bytes of
+// codes in, 16 bytes of bf16 out (plus 16 bytes of prev in place).  A warp holds
+// 32/RS consecutive chunks of a row, so every row access is one coalesced span.
+template <bool kInPlace, int RS>
+__global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackParams u) {
+  constexpr int CW = 32 / RS;
+  const int lane = threadIdx.x & 31;
+  const int rs = lane / CW;
+  const int cl = lane % CW;
+  const PayloadRef& P = u.pay;
+  const int32_t nchunk = u.D / 8;
+  const int32_t ngroups = (P.rows + P.G - 1) / P.G;
+  const int64_t ntask = static_cast<int64_t>(ngroups) * u.H * nchunk;
+  const int64_t nwtask = (ntask + CW - 1) / CW;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
+       wt += nwarps) {
+    const int64_t task = wt * CW + cl;
+    if (task >= ntask) continue;  // no shuffles in this kernel
+    const int32_t chunk = static_cast<int32_t>(task % nchunk);
+    const int32_t h = static_cast<int32_t>((task / nchunk) % u.H);
+    const int32_t g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * u.H));
+    const int32_t r0 = g * P.G;
+    const int32_t r1 = min(P.rows, r0 + P.G);
+    const int32_t col = chunk * 8;
+    const int64_t m = (static_cast<int64_t>(g) * u.H + h) * u.D + col;
+    uint32_t a[4], c[4];
+    load16B(static_cast<const uint16_t*>(P.meta0) + m, a);
+    load16B(static_cast<const uint16_t*>(P.meta1) + m, c);
+    float mn[8], sc[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mn[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(a[i] & 0xFFFFu));
+      mn[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(a[i] >> 16));
+      sc[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(c[i] & 0xFFFFu));
+      sc[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(c[i] >> 16));
+    }
+#pragma unroll 4
+    for (int32_t r = r0 + rs; r < r1; r += RS) {
+      const uint32_t cw = LDX(reinterpret_cast<const uint32_t*>(P.codes + (static_cast<int64_t>(r) * u.H + h) * (u.D / 2) + col / 2));
+      uint32_t y[4];
+      int4_decode8(cw, mn, sc, y);
+      if constexpr (!kInPlace) {
+        store16B(u.y + static_cast<int64_t>(r) * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col, y);
+      } else {
+        int64_t t = r;
+        if (u.pos != nullptr) {
+          t = LDX(u.pos + r);
+          if (chunk == 0 && h == 0 && r > 0 && LDX(u.pos + r - 1) >= t) set_status(u.status, 4u);
+          if (t < 0 || t >= u.src_rows) {
+            if (chunk == 0 && h == 0) set_status(u.status, 4u);
+            continue;
+          }
+        }
+        uint16_t* o = u.y + t * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col;
+        uint32_t q[4];
+        load16B_rw(o, q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t lo, hi;
+          unpack_f32x2(add_f32x2(pack_f32x2(q[i] << 16, q[i] & 0xFFFF0000u),
+                                 pack_f32x2(y[i] << 16, y[i] & 0xFFFF0000u)),
+                       lo, hi);
+          q[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+        }
+        store16B(o, q);
+      }
+    }
+  }
+}
+
+template <bool kInPlace, int RS>
+cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t s) {
+  auto k = int4_key_decode_kernel<kInPlace, RS>;
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
+  if (occ < 1) occ = 1;
+  const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
+  int64_t need = (warps + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t cap = static_cast<int64_t>(num_sms()) * occ * 2;
+  if (need < 1) need = 1;
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("int4_key_decode_kernel", s, k<<<grid, kThreads, 0, s>>>(u); e = cudaGetLastError());
+  return e;
+}
+
 template <int L, int BPL, bool kV8, int kFmt, int kMode>
 cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   auto k = payload_kernel<L, BPL, kV8, kFmt, kMode>;
@@ -208,8 +299,8 @@ cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
   if (occ < 1) occ = 1;
   int64_t need;
-  if (kMode == 2)  // one warp per run of kRun tokens
-    need = ((static_cast<int64_t>(u.src_rows) + kRun - 1) / kRun + kThreads / 32 - 1) / (kThreads / 32);
+  if (kMode == 2)  // one warp per run of u.run tokens
+    need = ((static_cast<int64_t>(u.src_rows) + u.run - 1) / u.run + kThreads / 32 - 1) / (kThreads / 32);
   else
     need = (static_cast<int64_t>(u.total_rows) + (kThreads / 32) * (32 / L) - 1) / ((kThreads / 32) * (32 / L));
   const int64_t cap = static_cast<int64_t>(num_sms()) * occ * 2;
@@ -236,7 +327,17 @@ cudaError_t pl_dispatch_fm(const UnpackParams& u, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_payload_decode(const UnpackParams& u, int /*lanes*/, bool v8, cudaStream_t s) {
+cudaError_t launch_payload_decode(const UnpackParams& u_in, int /*lanes*/, bool v8, cudaStream_t s) {
+  UnpackParams u = u_in;
+  // copy mode: runs of 4..64 tokens, about 32 runs per SM
+  const int64_t per = (static_cast<int64_t>(u.src_rows) + num_sms() * 32 - 1) / (num_sms() * 32);
+  u.run = static_cast<int32_t>(per < 4 ? 4 : (per > 64 ? 64 : per));
+  if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode != 2) {
+    const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
+    const bool small = ntask * 4 < static_cast<int64_t>(num_sms()) * 2048;
+    if (u.mode == 0) return small ? key_decode_launch<false, 8>(u, ntask, s) : key_decode_launch<false, 4>(u, ntask, s);
+    return small ? key_decode_launch<true, 8>(u, ntask, s) : key_decode_launch<true, 4>(u, ntask, s);
+  }
   const int bpl = (u.nb % 2 == 0) ? 2 : 1;
   int lanes = 1;
   while (lanes < u.nb / bpl) lanes <<= 1;
