@@ -50,6 +50,32 @@ __device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float
 
 __device__ __forceinline__ float int4_rcp(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }
 
+// Codes of the two bf16 of w (lo, hi) -> one byte (lo | hi << 4), the same integers
+// as int4_code (0 for a constant group, sc == 0), with the estimate done in f32x2.
+__device__ __forceinline__ uint32_t int4_pair(uint32_t w, float mnl, float mnh, float scl, float sch,
+                                              float rscl, float rsch) {
+  const uint64_t d2 = add_f32x2(pack_f32x2(w << 16, w & 0xFFFF0000u),
+                                pack_f32x2(__float_as_uint(-mnl), __float_as_uint(-mnh)));
+  uint32_t ql, qh;
+  unpack_f32x2(mul_f32x2(d2, pack_f32x2(__float_as_uint(rscl), __float_as_uint(rsch))), ql, qh);
+  const float qcl = fminf(__uint_as_float(ql), 15.0f), qch = fminf(__uint_as_float(qh), 15.0f);
+  const uint64_t q2 = pack_f32x2(__float_as_uint(qcl), __float_as_uint(qch));
+  const uint64_t k2 = pack_f32x2(__float_as_uint(kRound), __float_as_uint(kRound));
+  const uint64_t t2 = add_f32x2(q2, k2);
+  uint32_t tl, th;
+  unpack_f32x2(t2, tl, th);
+  // distance of each estimate to its rounded integer
+  const float rl = __fsub_rn(__uint_as_float(tl), kRound), rh = __fsub_rn(__uint_as_float(th), kRound);
+  const bool okl = (scl >= 0x1p-126f || scl == 0.0f) && fabsf(__fsub_rn(qcl, rl)) < 0.49999237f;
+  const bool okh = (sch >= 0x1p-126f || sch == 0.0f) && fabsf(__fsub_rn(qch, rh)) < 0.49999237f;
+  uint32_t cl = tl & 15u, ch = th & 15u;
+  if (!(okl && okh)) {
+    cl = scl != 0.0f ? int4_code(bf16lo(w), mnl, scl, rscl) : 0u;
+    ch = sch != 0.0f ? int4_code(bf16hi(w), mnh, sch, rsch) : 0u;
+  }
+  return cl | (ch << 4);
+}
+
 // The 8 bf16 values of one 16-byte chunk of a compact row (residual: bf16(cur-prev)).
 // Returns false for a residual row whose position is out of range (values zero).
 template <bool kResidual>
@@ -87,12 +113,12 @@ __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row
   }
 }
 
-// KEY kind: a column task is (group of G rows, head, 8-channel chunk).  RS lanes
-// share a task, each walking every RS-th row of the group twice (min/max, then
-// codes); the RS partial minima/maxima meet in a xor butterfly.  A warp holds 32/RS
-// consecutive tasks (consecutive chunks of one row), so each row read is one
-// coalesced span per row split.
-template <bool kResidual, int RS>
+// KEY kind: a column task is (group of G rows, head, 8-channel chunk).  RS = G / RPL
+// lanes share a task; each holds its RPL rows of the chunk in registers (all loads
+// issued together), so every row is read once.  The RS partial minima/maxima meet in
+// a xor butterfly, then each lane codes its own rows.  A warp holds 32/RS
+// consecutive chunks of a row, so each row read is one coalesced span per row split.
+template <bool kResidual, int RS, int RPL>
 __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
   constexpr int CW = 32 / RS;
   const int lane = threadIdx.x & 31;
@@ -115,22 +141,31 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
     const int32_t r1 = valid ? min(p.rows, r0 + p.G) : r0;
     const int32_t col = chunk * 8;
 
+    uint32_t v[RPL][4];
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int32_t r = r0 + rs + k * RS;
+      if (r < r1) {
+        load_chunk8<kResidual>(p, r, h, col, v[k]);
+      } else {
+        v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0u;
+      }
+    }
     float mn[8], mx[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       mn[i] = __int_as_float(0x7F800000);  // +inf
       mx[i] = __int_as_float(0xFF800000);  // -inf
     }
-#pragma unroll 4
-    for (int32_t r = r0 + rs; r < r1; r += RS) {
-      uint32_t w[4];
-      load_chunk8<kResidual>(p, r, h, col, w);
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      if (r0 + rs + k * RS >= r1) continue;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        mn[2 * i] = fminf(mn[2 * i], bf16lo(w[i]));
-        mx[2 * i] = fmaxf(mx[2 * i], bf16lo(w[i]));
-        mn[2 * i + 1] = fminf(mn[2 * i + 1], bf16hi(w[i]));
-        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16hi(w[i]));
+        mn[2 * i] = fminf(mn[2 * i], bf16lo(v[k][i]));
+        mx[2 * i] = fmaxf(mx[2 * i], bf16lo(v[k][i]));
+        mn[2 * i + 1] = fminf(mn[2 * i + 1], bf16hi(v[k][i]));
+        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16hi(v[k][i]));
       }
     }
 #pragma unroll
@@ -148,20 +183,17 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
       sc[i] = __fdiv_rn(__fsub_rn(mx[i], mn[i]), 15.0f);
       rsc[i] = int4_rcp(sc[i]);
     }
-
-#pragma unroll 4
-    for (int32_t r = r0 + rs; r < r1; r += RS) {
-      uint32_t w[4];
-      load_chunk8<kResidual>(p, r, h, col, w);
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int32_t r = r0 + rs + k * RS;
+      if (r >= r1) continue;
       if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
       uint32_t packed = 0u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t cl0 = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i], rsc[2 * i]) : 0u;
-        const uint32_t ch0 =
-            sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1], rsc[2 * i + 1]) : 0u;
-        packed |= (cl0 | (ch0 << 4)) << (8 * i);
-      }
+      for (int i = 0; i < 4; ++i)
+        packed |= int4_pair(v[k][i], mn[2 * i], mn[2 * i + 1], sc[2 * i], sc[2 * i + 1], rsc[2 * i],
+                            rsc[2 * i + 1])
+                  << (8 * i);
       STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
                                       col / 2),
           packed);
@@ -200,8 +232,9 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
   for (uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
        row - sub < total; row += stride) {
     const bool valid = row < total && has;
-    const int32_t r = static_cast<int32_t>((valid ? row : 0u) / static_cast<uint32_t>(p.H));
-    const int32_t h = static_cast<int32_t>((valid ? row : 0u) % static_cast<uint32_t>(p.H));
+    uint32_t ru, hu;
+    p.div_h.divmod(valid ? row : 0u, ru, hu);
+    const int32_t r = static_cast<int32_t>(ru), h = static_cast<int32_t>(hu);
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = 0u;
@@ -224,14 +257,9 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
         lmx = fmaxf(lmx, fmaxf(bf16lo(w[i]), bf16hi(w[i])));
       }
     }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float omn = __shfl_xor_sync(0xFFFFFFFFu, lmn, o);
-      const float omx = __shfl_xor_sync(0xFFFFFFFFu, lmx, o);
-      if (o < W) {
-        lmn = fminf(lmn, omn);
-        lmx = fmaxf(lmx, omx);
-      }
+    for (int o = 1; o < W; o <<= 1) {  // W is uniform: every lane runs the same shuffles
+      lmn = fminf(lmn, __shfl_xor_sync(0xFFFFFFFFu, lmn, o));
+      lmx = fmaxf(lmx, __shfl_xor_sync(0xFFFFFFFFu, lmx, o));
     }
     if (!valid) continue;
     const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
@@ -239,12 +267,11 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     uint32_t c0 = 0u, c1 = 0u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t cl = sc != 0.0f ? int4_code(bf16lo(w[i]), lmn, sc, rsc) : 0u;
-      const uint32_t ch = sc != 0.0f ? int4_code(bf16hi(w[i]), lmn, sc, rsc) : 0u;
+      const uint32_t byte = int4_pair(w[i], lmn, lmn, sc, sc, rsc, rsc);
       if (i < 4)
-        c0 |= (cl | (ch << 4)) << (8 * i);
+        c0 |= byte << (8 * i);
       else
-        c1 |= (cl | (ch << 4)) << (8 * (i - 4));
+        c1 |= byte << (8 * (i - 4));
     }
     const int64_t drow = static_cast<int64_t>(r) * p.H + h;
     store8B(p.dst.codes + drow * (p.D / 2) + 8 * b, c0, c1);
@@ -291,9 +318,9 @@ cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-template <bool kRes, int RS>
+template <bool kRes, int RS, int RPL>
 cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s) {
-  auto k = int4_key_kernel<kRes, RS>;
+  auto k = int4_key_kernel<kRes, RS, RPL>;
   const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
   const int grid = grid_cap(k, warps, kThreads / 32);
   cudaError_t e = cudaSuccess;
@@ -301,17 +328,24 @@ cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s)
   return e;
 }
 
+template <bool kRes>
+cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
+  const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
+  switch (p.G) {  // RS = G / RPL lanes per column task
+    case 16: return key_launch<kRes, 2, 8>(p, ntask, s);
+    case 32: return key_launch<kRes, 4, 8>(p, ntask, s);
+    case 64: return key_launch<kRes, 8, 8>(p, ntask, s);
+    case 128: return key_launch<kRes, 16, 8>(p, ntask, s);
+    case 256: return key_launch<kRes, 32, 8>(p, ntask, s);
+    case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s) {
-  if (p.kind == 0) {
-    // column tasks; with few of them (short tensors) each gets 8 row splits so the
-    // launch still fills the GPU, otherwise 4
-    const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
-    const bool small = ntask * 4 < static_cast<int64_t>(num_sms()) * 2048;
-    if (p.residual) return small ? key_launch<true, 8>(p, ntask, s) : key_launch<true, 4>(p, ntask, s);
-    return small ? key_launch<false, 8>(p, ntask, s) : key_launch<false, 4>(p, ntask, s);
-  }
+  if (p.kind == 0) return p.residual ? key_dispatch<true>(p, s) : key_dispatch<false>(p, s);
   return p.residual ? value_dispatch<true>(p, s) : value_dispatch<false>(p, s);
 }
 

@@ -365,6 +365,7 @@ KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_str
   p.dst = Int4Payload{out->codes, static_cast<uint16_t*>(out->meta0),
                       static_cast<uint16_t*>(out->meta1)};
   p.rows = out->rows;
+  p.div_h = FastDiv(static_cast<uint32_t>(out->heads));
   p.H = out->heads;
   p.D = out->dim;
   p.G = out->group_size;
@@ -459,6 +460,7 @@ KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in
   p.dst = Int4Payload{payload->codes, static_cast<uint16_t*>(payload->meta0),
                       static_cast<uint16_t*>(payload->meta1)};
   p.rows = num_pos;
+  p.div_h = FastDiv(static_cast<uint32_t>(payload->heads));
   p.H = payload->heads;
   p.D = payload->dim;
   p.G = payload->group_size;

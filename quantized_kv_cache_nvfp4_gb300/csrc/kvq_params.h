@@ -121,6 +121,7 @@ struct Int4EncodeParams {
   int64_t prev_row_pitch, prev_head_pitch;
   Int4Payload dst;
   int32_t rows;       // compact rows (T, or num_pos)
+  FastDiv div_h;      // by H
   int32_t H, D, G;
   int32_t kind;       // 0 key, 1 value
   int32_t residual;   // 0/1

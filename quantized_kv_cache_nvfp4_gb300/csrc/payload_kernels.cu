@@ -205,10 +205,11 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
 
 // INT4 K payloads, unpack (kInPlace = false) or residual decode in place: a column
 // task is (group of G compact rows, head, 8-channel chunk); its FP16 minimum and
-// scale are read once, then RS lanes walk every RS-th row of the group: 4 bytes of
-// codes in, 16 bytes of bf16 out (plus 16 bytes of prev in place).  A warp holds
-// 32/RS consecutive chunks of a row, so every row access is one coalesced span.
-template <bool kInPlace, int RS>
+// scale are read once.  RS = G / RPL lanes share a task; each loads the codes of its
+// RPL rows together (4 bytes per row), then writes 16 bytes of bf16 per row (in
+// place: adds to the 16 bytes of prev it also loaded up front).  A warp holds 32/RS
+// consecutive chunks of a row, so every row access is one coalesced span.
+template <bool kInPlace, int RS, int RPL>
 __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackParams u) {
   constexpr int CW = 32 / RS;
   const int lane = threadIdx.x & 31;
@@ -234,6 +235,30 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
     uint32_t a[4], c[4];
     load16B(static_cast<const uint16_t*>(P.meta0) + m, a);
     load16B(static_cast<const uint16_t*>(P.meta1) + m, c);
+    // all loads of this lane's rows first
+    uint32_t cw[RPL];
+    int64_t t[RPL];
+    uint32_t q[RPL][4];
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      const int32_t r = r0 + rs + k * RS;
+      t[k] = -1;
+      if (r >= r1) continue;
+      cw[k] = LDX(reinterpret_cast<const uint32_t*>(P.codes + (static_cast<int64_t>(r) * u.H + h) * (u.D / 2) + col / 2));
+      t[k] = r;
+      if constexpr (kInPlace) {
+        if (u.pos != nullptr) {
+          t[k] = LDX(u.pos + r);
+          if (chunk == 0 && h == 0 && r > 0 && LDX(u.pos + r - 1) >= t[k]) set_status(u.status, 4u);
+          if (t[k] < 0 || t[k] >= u.src_rows) {
+            if (chunk == 0 && h == 0) set_status(u.status, 4u);
+            t[k] = -1;
+            continue;
+          }
+        }
+        load16B_rw(u.y + t[k] * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col, q[k]);
+      }
+    }
     float mn[8], sc[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -242,43 +267,30 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
       sc[2 * i] = f16_bits_to_f32(static_cast<uint16_t>(c[i] & 0xFFFFu));
       sc[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(c[i] >> 16));
     }
-#pragma unroll 4
-    for (int32_t r = r0 + rs; r < r1; r += RS) {
-      const uint32_t cw = LDX(reinterpret_cast<const uint32_t*>(P.codes + (static_cast<int64_t>(r) * u.H + h) * (u.D / 2) + col / 2));
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      if (t[k] < 0) continue;
       uint32_t y[4];
-      int4_decode8(cw, mn, sc, y);
-      if constexpr (!kInPlace) {
-        store16B(u.y + static_cast<int64_t>(r) * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col, y);
-      } else {
-        int64_t t = r;
-        if (u.pos != nullptr) {
-          t = LDX(u.pos + r);
-          if (chunk == 0 && h == 0 && r > 0 && LDX(u.pos + r - 1) >= t) set_status(u.status, 4u);
-          if (t < 0 || t >= u.src_rows) {
-            if (chunk == 0 && h == 0) set_status(u.status, 4u);
-            continue;
-          }
-        }
-        uint16_t* o = u.y + t * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col;
-        uint32_t q[4];
-        load16B_rw(o, q);
+      int4_decode8(cw[k], mn, sc, y);
+      uint16_t* o = u.y + t[k] * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col;
+      if constexpr (kInPlace) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t lo, hi;
-          unpack_f32x2(add_f32x2(pack_f32x2(q[i] << 16, q[i] & 0xFFFF0000u),
+          unpack_f32x2(add_f32x2(pack_f32x2(q[k][i] << 16, q[k][i] & 0xFFFF0000u),
                                  pack_f32x2(y[i] << 16, y[i] & 0xFFFF0000u)),
                        lo, hi);
-          q[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+          y[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
         }
-        store16B(o, q);
       }
+      store16B(o, y);
     }
   }
 }
 
-template <bool kInPlace, int RS>
+template <bool kInPlace, int RS, int RPL>
 cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t s) {
-  auto k = int4_key_decode_kernel<kInPlace, RS>;
+  auto k = int4_key_decode_kernel<kInPlace, RS, RPL>;
   int occ = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
   if (occ < 1) occ = 1;
@@ -290,6 +302,20 @@ cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t
   cudaError_t e = cudaSuccess;
   KVQ_LAUNCH("int4_key_decode_kernel", s, k<<<grid, kThreads, 0, s>>>(u); e = cudaGetLastError());
   return e;
+}
+
+template <bool kInPlace>
+cudaError_t key_decode_dispatch(const UnpackParams& u, cudaStream_t s) {
+  const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
+  switch (u.pay.G) {  // RS = G / RPL lanes per column task
+    case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
+    case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
+    case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
+    case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
+    case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
+    case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int L, int BPL, bool kV8, int kFmt, int kMode>
@@ -332,12 +358,8 @@ cudaError_t launch_payload_decode(const UnpackParams& u_in, int /*lanes*/, bool 
   // copy mode: runs of 4..64 tokens, about 32 runs per SM
   const int64_t per = (static_cast<int64_t>(u.src_rows) + num_sms() * 32 - 1) / (num_sms() * 32);
   u.run = static_cast<int32_t>(per < 4 ? 4 : (per > 64 ? 64 : per));
-  if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode != 2) {
-    const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
-    const bool small = ntask * 4 < static_cast<int64_t>(num_sms()) * 2048;
-    if (u.mode == 0) return small ? key_decode_launch<false, 8>(u, ntask, s) : key_decode_launch<false, 4>(u, ntask, s);
-    return small ? key_decode_launch<true, 8>(u, ntask, s) : key_decode_launch<true, 4>(u, ntask, s);
-  }
+  if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode != 2)
+    return u.mode == 0 ? key_decode_dispatch<false>(u, s) : key_decode_dispatch<true>(u, s);
   const int bpl = (u.nb % 2 == 0) ? 2 : 1;
   int lanes = 1;
   while (lanes < u.nb / bpl) lanes <<= 1;
