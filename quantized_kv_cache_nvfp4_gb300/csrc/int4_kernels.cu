@@ -214,6 +214,90 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
   }
 }
 
+// KEY kind, tiled through shared memory: a block takes one tile (a group of up to G
+// rows x the D channels of one head) at a time.
+//  1. every thread loads 16-byte chunks of the tile (consecutive threads, consecutive
+//     chunks of a row: coalesced; residual mode gathers rows at pos[] and subtracts
+//     prev here) into shared memory;
+//  2. thread (rq, cp) takes channel pair cp over rows rq, rq + RQ, ... (RQ = 512 / D
+//     row splits; a warp reads consecutive words: no bank conflicts) and leaves its
+//     partial minimum/maximum in shared memory; after a barrier every thread combines
+//     the RQ partials of its pair, so the group's FP32 minimum and scale are known;
+//  3. each thread codes its rows of the pair (one byte per row, a warp writes 32
+//     consecutive bytes) and the rq == 0 threads write the FP16 metadata.
+template <bool kResidual>
+__global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4EncodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int D = p.D;
+  const int nchunk = D / 8;     // 16-byte chunks per row
+  const int npair = D / 2;      // channel pairs
+  const int RQ = kThreads / npair;
+  const int tid = threadIdx.x;
+  const int cp = tid % npair;
+  const int rq = tid / npair;
+  uint32_t* tile = reinterpret_cast<uint32_t*>(smem);                 // [G][D/2] bf16x2
+  float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(p.G) * D * 2);  // [2][RQ][D]
+  const int32_t ngroups = (p.rows + p.G - 1) / p.G;
+  const int64_t ntiles = static_cast<int64_t>(ngroups) * p.H;
+  for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
+    const int32_t g = static_cast<int32_t>(tile_id / p.H);
+    const int32_t h = static_cast<int32_t>(tile_id % p.H);
+    const int32_t r0 = g * p.G;
+    const int32_t nr = min(p.G, p.rows - r0);
+    // 1. load the tile
+    for (int c = tid; c < nr * nchunk; c += kThreads) {
+      const int row = c / nchunk;
+      const int col = (c % nchunk) * 8;
+      uint32_t w[4];
+      load_chunk8<kResidual>(p, r0 + row, h, col, w);
+      if (col == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
+      *reinterpret_cast<uint4*>(tile + row * npair + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+    // 2. column minimum and maximum of the pair
+    float mnl = __int_as_float(0x7F800000), mnh = mnl;
+    float mxl = __int_as_float(0xFF800000), mxh = mxl;
+    if (rq < RQ) {
+      for (int row = rq; row < nr; row += RQ) {
+        const uint32_t v = tile[row * npair + cp];
+        mnl = fminf(mnl, bf16lo(v));
+        mxl = fmaxf(mxl, bf16lo(v));
+        mnh = fminf(mnh, bf16hi(v));
+        mxh = fmaxf(mxh, bf16hi(v));
+      }
+      part[(0 * RQ + rq) * D + 2 * cp] = mnl;
+      part[(0 * RQ + rq) * D + 2 * cp + 1] = mnh;
+      part[(1 * RQ + rq) * D + 2 * cp] = mxl;
+      part[(1 * RQ + rq) * D + 2 * cp + 1] = mxh;
+    }
+    __syncthreads();
+    if (rq < RQ) {
+      for (int k = 0; k < RQ; ++k) {
+        mnl = fminf(mnl, part[(0 * RQ + k) * D + 2 * cp]);
+        mnh = fminf(mnh, part[(0 * RQ + k) * D + 2 * cp + 1]);
+        mxl = fmaxf(mxl, part[(1 * RQ + k) * D + 2 * cp]);
+        mxh = fmaxf(mxh, part[(1 * RQ + k) * D + 2 * cp + 1]);
+      }
+      const float scl = __fdiv_rn(__fsub_rn(mxl, mnl), 15.0f);
+      const float sch = __fdiv_rn(__fsub_rn(mxh, mnh), 15.0f);
+      const float rsl = int4_rcp(scl), rsh = int4_rcp(sch);
+      // 3. codes of this thread's rows
+      for (int row = rq; row < nr; row += RQ) {
+        const uint32_t byte = int4_pair(tile[row * npair + cp], mnl, mnh, scl, sch, rsl, rsh);
+        STX(p.dst.codes + (static_cast<int64_t>(r0 + row) * p.H + h) * npair + cp, static_cast<uint8_t>(byte));
+      }
+      if (rq == 0) {
+        const int64_t m = (static_cast<int64_t>(g) * p.H + h) * D + 2 * cp;
+        STX(reinterpret_cast<uint32_t*>(p.dst.mn + m),
+            static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
+        STX(reinterpret_cast<uint32_t*>(p.dst.sc + m),
+            static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16));
+      }
+    }
+    __syncthreads();  // the tile buffer is reused
+  }
+}
+
 // VALUE kind: one lane per 16-channel block of a row; a group spans W = min(G/16, L)
 // aligned lanes, reduced with a xor butterfly of uniform width.
 template <int L, bool kResidual>
@@ -229,26 +313,34 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
   const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
   const bool has = b < nb;
 
-  for (uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
-       row - sub < total; row += stride) {
+  // the 16 values of this lane's block of row `rw` (zeros when there is none)
+  auto load_row = [&](uint32_t rw, uint32_t (&w)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
+    if (rw >= total || !has) return;
+    uint32_t ru, hu;
+    p.div_h.divmod(rw, ru, hu);
+    uint32_t a[4], c[4];
+    load_chunk8<kResidual>(p, static_cast<int32_t>(ru), static_cast<int32_t>(hu), 16 * b, a);
+    load_chunk8<kResidual>(p, static_cast<int32_t>(ru), static_cast<int32_t>(hu), 16 * b + 8, c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i] = a[i];
+      w[4 + i] = c[i];
+    }
+  };
+
+  uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
+  uint32_t w[8];
+  load_row(row, w);
+  for (; row - sub < total; row += stride) {
     const bool valid = row < total && has;
     uint32_t ru, hu;
     p.div_h.divmod(valid ? row : 0u, ru, hu);
     const int32_t r = static_cast<int32_t>(ru), h = static_cast<int32_t>(hu);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0u;
-    if (valid) {
-      uint32_t a[4], c[4];
-      load_chunk8<kResidual>(p, r, h, 16 * b, a);
-      load_chunk8<kResidual>(p, r, h, 16 * b + 8, c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[i] = a[i];
-        w[4 + i] = c[i];
-      }
-      if (b == 0 && h == 0) check_pos<kResidual>(p, r);
-    }
+    uint32_t nw[8];
+    load_row(row + stride, nw);  // the next row's loads before this row's arithmetic
+    if (valid && b == 0 && h == 0) check_pos<kResidual>(p, r);
     float lmn = __int_as_float(0x7F800000), lmx = __int_as_float(0xFF800000);
     if (valid) {
 #pragma unroll
@@ -261,7 +353,11 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
       lmn = fminf(lmn, __shfl_xor_sync(0xFFFFFFFFu, lmn, o));
       lmx = fmaxf(lmx, __shfl_xor_sync(0xFFFFFFFFu, lmx, o));
     }
-    if (!valid) continue;
+    if (!valid) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = nw[i];
+      continue;
+    }
     const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
     const float rsc = int4_rcp(sc);
     uint32_t c0 = 0u, c1 = 0u;
@@ -280,6 +376,8 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
       STX(p.dst.mn + m, f32_to_f16_bits(lmn));
       STX(p.dst.sc + m, f32_to_f16_bits(sc));
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = nw[i];
   }
 }
 
@@ -328,8 +426,34 @@ cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s)
   return e;
 }
 
+// Shared memory of one tile: G x D bf16 plus the [2][RQ][D] float partials.
+size_t key_tile_smem(int G, int D) {
+  return static_cast<size_t>(G) * D * 2 + 2 * static_cast<size_t>(kThreads / (D / 2)) * D * 4;
+}
+
+template <bool kRes>
+cudaError_t key_tile_launch(const Int4EncodeParams& p, cudaStream_t s) {
+  auto k = int4_key_tile_kernel<kRes>;
+  const size_t smem = key_tile_smem(p.G, p.D);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem);
+  if (occ < 1) occ = 1;
+  const int64_t tiles = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+  const int grid = static_cast<int>(tiles < cap ? (tiles < 1 ? 1 : tiles) : cap);
+  cudaError_t e = cudaSuccess;
+  KVQ_LAUNCH("int4_key_tile_kernel", s, k<<<grid, kThreads, smem, s>>>(p); e = cudaGetLastError());
+  return e;
+}
+
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
+  // a tile of up to 96 KB of shared memory (64 rows x 256 channels, 128 x 128, ...)
+  if (p.D >= 16 && key_tile_smem(p.G, p.D) <= 96 * 1024) return key_tile_launch<kRes>(p, s);
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
   switch (p.G) {  // RS = G / RPL lanes per column task
     case 16: return key_launch<kRes, 2, 8>(p, ntask, s);
