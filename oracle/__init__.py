@@ -25,6 +25,7 @@ LIB = os.path.join(HERE, "liboracle.so")
 
 FMT_NVFP4 = 1
 FMT_INT4 = 2
+FMT_FP8 = 3
 KIND_KEY = 0
 KIND_VALUE = 1
 
@@ -84,6 +85,10 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_residual_encode": (_U32, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
         "orc_residual_decode": (_U32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _P]),
         "orc_storage_bytes": (_I64, [_I, _I, _I, _I64, _I, _I]),
+        "orc_fp8_encode_rows": (None, [_P, _I64, _I, _P, _P]),
+        "orc_fp8_decode_rows": (None, [_P, _P, _I64, _I, _P]),
+        "orc_fp8_scatter": (_U32, [_P, _I64, _I64, _I, _I, _I, _P, _I64, _P, _P]),
+        "orc_fp8_restore": (_U32, [_P, _P, _I64, _I, _I, _I, _P, _I, _I, _P, _I, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -223,6 +228,58 @@ def nvfp4_restore(pool, block_size, block_table, seq_lens, Tmax, out=None):
 
 
 # --------------------------------------------------------------------------
+# FP8 E4M3 row codec
+# --------------------------------------------------------------------------
+def fp8_encode_rows(x_bf16: np.ndarray):
+    """x [..., D] uint16 (bf16 bits) -> codes [..., D] (E4M3 bytes), rscale [...]."""
+    x = _c(x_bf16, np.uint16)
+    D = x.shape[-1]
+    lead = x.shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    codes = np.zeros(lead + (D,), np.uint8)
+    rscale = np.zeros(lead, np.float32)
+    lib().orc_fp8_encode_rows(_ptr(x), n, D, _ptr(codes), _ptr(rscale))
+    return codes, rscale
+
+
+def fp8_decode_rows(codes, rscale) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    rscale = _c(rscale, np.float32)
+    D = codes.shape[-1]
+    lead = codes.shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    y = np.empty(lead + (D,), np.uint16)
+    lib().orc_fp8_decode_rows(_ptr(codes), _ptr(rscale), n, D, _ptr(y))
+    return y
+
+
+def new_fp8_pool(num_slots: int, H: int, D: int):
+    """Zero-filled FP8 planes for one tensor: codes, rscale."""
+    return np.zeros((num_slots, H, D), np.uint8), np.zeros((num_slots, H), np.float32)
+
+
+def fp8_scatter(x_flat, row_pitch, head_pitch, T, H, D, slot_ids, pool) -> int:
+    x = _c(x_flat, np.uint16).ravel()
+    slot_ids = _c(slot_ids, np.int64)
+    codes, rscale = pool
+    return int(lib().orc_fp8_scatter(_ptr(x), row_pitch, head_pitch, T, H, D, _ptr(slot_ids),
+                                     codes.shape[0], _ptr(codes), _ptr(rscale)))
+
+
+def fp8_restore(pool, block_size, block_table, seq_lens, Tmax, out=None):
+    codes, rscale = pool
+    num_slots, H, D = codes.shape
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    S, max_blocks = block_table.shape
+    if out is None:
+        out = np.zeros((S, Tmax, H, D), np.uint16)
+    st = lib().orc_fp8_restore(_ptr(codes), _ptr(rscale), num_slots, H, D, block_size,
+                               _ptr(block_table), S, max_blocks, _ptr(seq_lens), Tmax, _ptr(out))
+    return out, int(st)
+
+
+# --------------------------------------------------------------------------
 # INT4 affine codec
 # --------------------------------------------------------------------------
 def int4_meta_shape(kind, T, H, D, G):
@@ -258,6 +315,8 @@ def int4_unpack(codes, mn, sc, kind: int, G: int = 64):
 # residual encode / decode
 # --------------------------------------------------------------------------
 def _payload_buffers(fmt, kind, P, H, D, G):
+    if fmt == FMT_FP8:
+        return np.zeros((P, H, D), np.uint8), None, None, np.zeros((P, H), np.float32)
     codes = np.zeros((P, H, D // 2), np.uint8)
     if fmt == FMT_NVFP4:
         return codes, np.zeros((P, H, D // 16), np.uint8), None, np.zeros((P, H), np.float32)

@@ -256,6 +256,48 @@ void orc_nvfp4_decode_rows(const uint8_t* codes, const uint8_t* bscale, const fl
 }
 
 /* ------------------------------------------------------------------------- */
+/* FP8 E4M3 row codec ("feat(kvcache): add nvfp4 kv quantization (FreeToken PR */
+/* #408)", fp8 store notes: a row becomes head_dim e4m3 codes plus one FP32    */
+/* symmetric scale).  Readings, as for NVFP4: rs = amax / 448 stored as the    */
+/* decode multiplier; q = x * (1 / rs), or x / rs when the reciprocal          */
+/* overflows; code = e4m3_rne(q) (saturating at 448, sign of x);               */
+/* decode y = bf16(e4m3 * rs).                                                 */
+/* ------------------------------------------------------------------------- */
+void orc_fp8_encode_row(const uint16_t* x, int D, uint8_t* codes, float* rscale) {
+  float amax = 0.0f;
+  for (int i = 0; i < D; i++) amax = fmaxf(amax, fabsf(orc_bf16_to_f32(x[i])));
+  const float E4M3_MAX = 448.0f;
+  float rs = amax / E4M3_MAX;
+  *rscale = rs;
+  float inv = 0.0f;
+  if (rs != 0.0f) inv = 1.0f / rs;
+  for (int i = 0; i < D; i++) {
+    float xi = orc_bf16_to_f32(x[i]);
+    float q;
+    if (rs == 0.0f)
+      q = copysignf(0.0f, xi);
+    else if (isinf(inv))
+      q = xi / rs;
+    else
+      q = xi * inv;
+    uint8_t c = orc_e4m3_encode(q);
+    codes[i] = (uint8_t)((c & 0x7F) | (signbit(xi) ? 0x80 : 0));
+  }
+}
+
+void orc_fp8_decode_row(const uint8_t* codes, float rscale, int D, uint16_t* y) {
+  for (int i = 0; i < D; i++) y[i] = orc_f32_to_bf16(orc_e4m3_value(codes[i]) * rscale);
+}
+
+void orc_fp8_encode_rows(const uint16_t* x, int64_t n, int D, uint8_t* codes, float* rscale) {
+  for (int64_t r = 0; r < n; r++) orc_fp8_encode_row(x + r * D, D, codes + r * D, rscale + r);
+}
+
+void orc_fp8_decode_rows(const uint8_t* codes, const float* rscale, int64_t n, int D, uint16_t* y) {
+  for (int64_t r = 0; r < n; r++) orc_fp8_decode_row(codes + r * D, rscale[r], D, y + r * D);
+}
+
+/* ------------------------------------------------------------------------- */
 /* paged store and restore                                                    */
 /* ------------------------------------------------------------------------- */
 uint32_t orc_nvfp4_scatter(const uint16_t* x, int64_t row_pitch, int64_t head_pitch, int T,
@@ -304,6 +346,56 @@ uint32_t orc_nvfp4_restore(const uint8_t* codes, const uint8_t* bscale, const fl
         int64_t r = slot * H + h;
         uint16_t* y = out + (((int64_t)s * Tmax + t) * H + h) * D;
         orc_nvfp4_decode_row(codes + r * (D / 2), bscale + r * (D / 16), rscale[r], D, y);
+      }
+    }
+  }
+  return status;
+}
+
+uint32_t orc_fp8_scatter(const uint16_t* x, int64_t row_pitch, int64_t head_pitch, int T, int H,
+                         int D, const int64_t* slot_ids, int64_t num_slots, uint8_t* codes,
+                         float* rscale) {
+  uint32_t status = 0;
+  uint16_t row[4096];
+  for (int t = 0; t < T; t++) {
+    int64_t slot = slot_ids[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      status |= ORC_BAD_SLOT;
+      continue;
+    }
+    for (int h = 0; h < H; h++) {
+      for (int d = 0; d < D; d++) row[d] = x[(int64_t)t * row_pitch + (int64_t)h * head_pitch + d];
+      int64_t r = slot * H + h;
+      orc_fp8_encode_row(row, D, codes + r * D, rscale + r);
+    }
+  }
+  return status;
+}
+
+uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_slots, int H,
+                         int D, int block_size, const int32_t* block_table, int S,
+                         int max_blocks, const int32_t* seq_lens, int Tmax, uint16_t* out) {
+  uint32_t status = 0;
+  int64_t num_blocks = num_slots / block_size;
+  int64_t cap = (int64_t)max_blocks * block_size;
+  if (cap > Tmax) cap = Tmax;
+  for (int s = 0; s < S; s++) {
+    int len = seq_lens[s];
+    if (len < 0 || len > cap) {
+      status |= ORC_BAD_SEQLEN;
+      continue;
+    }
+    for (int t = 0; t < len; t++) {
+      int32_t block = block_table[(int64_t)s * max_blocks + t / block_size];
+      if (block < 0 || block >= num_blocks) {
+        status |= ORC_BAD_BLOCK;
+        continue;
+      }
+      int64_t slot = (int64_t)block * block_size + t % block_size;
+      for (int h = 0; h < H; h++) {
+        int64_t r = slot * H + h;
+        orc_fp8_decode_row(codes + r * D, rscale[r], D, out + (((int64_t)s * Tmax + t) * H + h) * D);
       }
     }
   }
@@ -427,6 +519,8 @@ uint32_t orc_residual_encode(const uint16_t* cur, const uint16_t* prev, int T, i
   if (P > 0) {
     if (fmt == ORC_FMT_NVFP4)
       orc_nvfp4_encode_rows(r, (int64_t)P * H, D, codes, (uint8_t*)meta_a, rscale);
+    else if (fmt == ORC_FMT_FP8)
+      orc_fp8_encode_rows(r, (int64_t)P * H, D, codes, rscale);
     else
       orc_int4_pack(r, P, H, D, kind, G, codes, (uint16_t*)meta_a, (uint16_t*)meta_b);
   }
@@ -446,6 +540,8 @@ uint32_t orc_residual_decode(const uint8_t* codes, const void* meta_a, const voi
   uint16_t* y = (uint16_t*)malloc((size_t)P * (size_t)row * sizeof(uint16_t));
   if (fmt == ORC_FMT_NVFP4)
     orc_nvfp4_decode_rows(codes, (const uint8_t*)meta_a, rscale, (int64_t)P * H, D, y);
+  else if (fmt == ORC_FMT_FP8)
+    orc_fp8_decode_rows(codes, rscale, (int64_t)P * H, D, y);
   else
     orc_int4_unpack(codes, (const uint16_t*)meta_a, (const uint16_t*)meta_b, P, H, D, kind, G, y);
   for (int p = 0; p < P; p++) {
@@ -467,6 +563,8 @@ uint32_t orc_residual_decode(const uint8_t* codes, const void* meta_a, const voi
 int64_t orc_storage_bytes(int fmt, int kind, int G, int64_t T, int H, int D) {
   if (fmt == ORC_FMT_NVFP4) /* codes D/2 + one E4M3 per 16 + one FP32 per row */
     return T * H * (D / 2 + D / 16 + 4);
+  if (fmt == ORC_FMT_FP8) /* one E4M3 per value + one FP32 per row */
+    return T * H * (D + 4);
   int64_t code_bytes = T * H * (D / 2);
   int64_t groups = (kind == ORC_KIND_KEY) ? ((T + G - 1) / G) * H * D
                                           : T * H * ((D + G - 1) / G);

@@ -35,7 +35,7 @@ extern "C" {
 #define ORC_BAD_POS 4u     /* position out of [0, T) or not strictly increasing */
 #define ORC_BAD_SEQLEN 8u  /* sequence length outside [0, min(Tmax, max_blocks*block_size)] */
 
-enum { ORC_FMT_NVFP4 = 1, ORC_FMT_INT4 = 2 };
+enum { ORC_FMT_NVFP4 = 1, ORC_FMT_INT4 = 2, ORC_FMT_FP8 = 3 };
 enum { ORC_KIND_KEY = 0, ORC_KIND_VALUE = 1 };
 
 /* ---- scalar format primitives ---- */
@@ -65,6 +65,12 @@ void orc_nvfp4_encode_rows(const uint16_t* x, int64_t n, int D, uint8_t* codes,
 void orc_nvfp4_decode_rows(const uint8_t* codes, const uint8_t* bscale, const float* rscale,
                            int64_t n, int D, uint16_t* y);
 
+/* ---- FP8 E4M3 row codec: one row of D bf16 -> D E4M3 codes + one FP32 scale ---- */
+void orc_fp8_encode_row(const uint16_t* x, int D, uint8_t* codes, float* rscale);
+void orc_fp8_decode_row(const uint8_t* codes, float rscale, int D, uint16_t* y);
+void orc_fp8_encode_rows(const uint16_t* x, int64_t n, int D, uint8_t* codes, float* rscale);
+void orc_fp8_decode_rows(const uint8_t* codes, const float* rscale, int64_t n, int D, uint16_t* y);
+
 /* ---- paged store / restore (one tensor, K or V) ----
  * x is addressed x[t*row_pitch + h*head_pitch + d] (elements).
  * Pool planes: codes [num_slots][H][D/2], bscale [num_slots][H][D/16], rscale [num_slots][H].
@@ -77,6 +83,13 @@ uint32_t orc_nvfp4_restore(const uint8_t* codes, const uint8_t* bscale, const fl
                            int64_t num_slots, int H, int D, int block_size,
                            const int32_t* block_table, int S, int max_blocks,
                            const int32_t* seq_lens, int Tmax, uint16_t* out);
+/* FP8 pool planes: codes [num_slots][H][D], rscale [num_slots][H]. */
+uint32_t orc_fp8_scatter(const uint16_t* x, int64_t row_pitch, int64_t head_pitch, int T, int H,
+                         int D, const int64_t* slot_ids, int64_t num_slots, uint8_t* codes,
+                         float* rscale);
+uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_slots, int H,
+                         int D, int block_size, const int32_t* block_table, int S,
+                         int max_blocks, const int32_t* seq_lens, int Tmax, uint16_t* out);
 
 /* ---- INT4 affine codec, group size G, x contiguous [T][H][D] (D even) ----
  * codes [T][H][D/2] (low nibble = even channel)
@@ -92,6 +105,7 @@ void orc_int4_unpack(const uint8_t* codes, const uint16_t* mn16, const uint16_t*
  * NULL for the dense case (P must equal T).  The payload covers the P compact rows:
  *   NVFP4: codes [P][H][D/2], meta_a = bscale [P][H][D/16] (uint8), rscale [P][H]
  *   INT4 : codes [P][H][D/2], meta_a = mn16, meta_b = sc16 (uint16, shapes as orc_int4_pack)
+ *   FP8  : codes [P][H][D], rscale [P][H]
  * pos_out receives the owned copy of the positions (may be NULL when pos is NULL). */
 uint32_t orc_residual_encode(const uint16_t* cur, const uint16_t* prev, int T, int H, int D,
                              const int32_t* pos, int P, int fmt, int kind, int G,

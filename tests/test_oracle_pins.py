@@ -374,7 +374,7 @@ def test_storage_figures_printed_on_the_pages(case):
     if fmt == "bf16":
         got = T * H * D * 2
     else:
-        f = O.FMT_NVFP4 if fmt == "nvfp4" else O.FMT_INT4
+        f = {"nvfp4": O.FMT_NVFP4, "int4": O.FMT_INT4, "fp8": O.FMT_FP8}[fmt]
         got = O.storage_bytes(f, k, G, T, H, D)
     if name.endswith("_bits"):
         got = 8.0 * got / (T * H * D)
@@ -641,3 +641,79 @@ def test_negative_slot_skips_and_bad_ids_are_flagged():
     assert st == O.BAD_BLOCK
     _, st = O.nvfp4_restore(pool, 4, table, np.array([9], np.int32), 8)
     assert st == O.BAD_SEQLEN
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 row codec
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D", [16, 128, 256])
+@pytest.mark.parametrize("k", [-100, 0, 40])
+def test_fp8_identity_on_exact_inputs(D, k):
+    """Rows of E4M3 values times 2^k with one entry at +-448 * 2^k decode exactly and
+    carry the row scale 2^k."""
+    rng = np.random.default_rng(D + 7 * k + 900)
+    tab = e4m3_table()
+    x = tab[rng.integers(0, 127, (16, D))] * rng.choice([-1, 1], (16, D))
+    x[np.arange(16), rng.integers(0, D, 16)] = 448.0 * rng.choice([-1, 1], 16)
+    x = x * 2.0 ** k
+    xb = _bits(x)
+    assert np.array_equal(O.bf16_to_f32(xb).astype(np.float64), x)
+    codes, rs = O.fp8_encode_rows(xb)
+    np.testing.assert_array_equal(rs, np.float32(2.0 ** k))
+    np.testing.assert_array_equal(O.fp8_decode_rows(codes, rs), xb)
+
+
+def test_fp8_codes_are_nearest_e4m3_of_x_over_scale():
+    x = synth.bf16_bits(synth.normal_bf16((256, 128), seed=31, stream=1, outlier_frac=0.01, outlier_scale=20.0))
+    codes, rs = O.fp8_encode_rows(x)
+    xf = O.bf16_to_f32(x).astype(np.float64)
+    q = xf / rs[:, None].astype(np.float64)
+    tab = e4m3_table()
+    want = brute_nearest_even(q, tab) | np.where(np.signbit(xf), 0x80, 0)
+    mids = (tab[:-1] + tab[1:]) / 2
+    near = np.abs(np.abs(q)[..., None] - mids).min(-1) <= 1e-6 * np.abs(q)
+    assert not ((codes != want) & ~near).any()
+    # the row maximum lands on 448 exactly (rs = amax / 448)
+    assert (codes.max(axis=1) & 0x7F).max() == 0x7E
+
+
+def test_fp8_zero_and_tiny_rows():
+    x = np.zeros((3, 32))
+    x[1] = -0.0
+    x[2, 0] = 2.0 ** -125          # rs subnormal: its reciprocal overflows
+    x[2, 1] = 2.0 ** -126
+    x[2, 2] = -(2.0 ** -127)
+    xb = _bits(x)
+    codes, rs = O.fp8_encode_rows(xb)
+    assert rs[0] == 0 and (codes[0] == 0).all() and (codes[1] == 0x80).all()
+    assert 0 < rs[2] < np.finfo(np.float32).tiny
+    with np.errstate(over="ignore", divide="ignore"):
+        assert np.isinf(np.float32(1.0) / rs[2])
+    q = x[2, :3] / float(rs[2])
+    want = brute_nearest_even(q, e4m3_table()) | np.where(q < 0, 0x80, 0)
+    assert list(codes[2, :3]) == list(want) and (np.abs(q) < 448).any()
+    np.testing.assert_array_equal(O.fp8_decode_rows(codes[:2], rs[:2]), xb[:2])
+
+
+def test_fp8_paged_round_trip_and_residuals():
+    S, Tmax, H, D, bsz = 2, 48, 2, 32, 16
+    lens = np.array([48, 20], np.int32)
+    perm = synth.block_permutation(8, 32).numpy()
+    table = perm[:6].reshape(2, 3).astype(np.int32)
+    k = synth.bf16_bits(synth.normal_bf16((S, Tmax, H, D), 32, 1))
+    pool = O.new_fp8_pool(8 * bsz, H, D)
+    for s in range(S):
+        t = np.arange(lens[s])
+        assert O.fp8_scatter(k[s], H * D, D, int(lens[s]), H, D, table[s, t // bsz].astype(np.int64) * bsz + t % bsz, pool) == 0
+    out, st = O.fp8_restore(pool, bsz, table, lens, Tmax)
+    assert st == 0
+    for s in range(S):
+        n = lens[s]
+        np.testing.assert_array_equal(out[s, :n], O.fp8_decode_rows(*O.fp8_encode_rows(k[s, :n])))
+    prev = synth.bf16_bits(synth.normal_bf16((40, H, D), 33, 1))
+    pay, st = O.residual_encode(prev, prev, None, O.FMT_FP8, 0)
+    np.testing.assert_array_equal(O.residual_decode(pay, prev)[0], prev)
+    cur = synth.bf16_bits(synth.normal_bf16((40, H, D), 33, 2))
+    a, _ = O.residual_encode(cur, prev, np.arange(40, dtype=np.int32), O.FMT_FP8, 0)
+    b, _ = O.residual_encode(cur, prev, None, O.FMT_FP8, 0)
+    np.testing.assert_array_equal(O.residual_decode(a, prev)[0], O.residual_decode(b, prev)[0])
