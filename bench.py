@@ -373,7 +373,7 @@ def run_e2e(args, kvq, device, k, v, slots, table, lens, pool, dist, T):
     hs.copy_(slots)
     ht.copy_(table)
     ok = torch.empty((T, H, D), dtype=torch.bfloat16, pin_memory=True)
-    ov = torch.empty_like(ok)
+    ov = torch.empty((T, H, D), dtype=torch.bfloat16, pin_memory=True)  # empty_like would not pin
     dk, dv, ds, dt = (torch.empty_like(x) for x in (k, v, slots, table))
     dl = torch.empty((nch,), dtype=torch.int32, device=device)
     yk = torch.empty((T, H, D), dtype=torch.bfloat16, device=device)

@@ -14,6 +14,9 @@
  *     packing/unpacking and cross-loop residual reconstruction", Purpose.
  *   - Residual encode/decode against the reconstructed predecessor with a compact
  *     int32 position map (same page, Purpose).
+ *   - FP8 E4M3 row codec: head_dim E4M3 codes plus one FP32 symmetric scale per
+ *     (token, KV head) row, in a code buffer with the geometry of the bf16 one.
+ *     Source: FreeToken PR #408, the fp8 store notes.
  *
  * Conventions shared by every entry point
  *   Memory   every pointer argument that a kernel touches is DEVICE memory
@@ -67,7 +70,7 @@ typedef enum {
   KVQ_ERR_CUDA = 5            /* the CUDA runtime reported an error at launch */
 } kvq_status;
 
-typedef enum { KVQ_FMT_NVFP4 = 1, KVQ_FMT_INT4 = 2 } kvq_format;
+typedef enum { KVQ_FMT_NVFP4 = 1, KVQ_FMT_INT4 = 2, KVQ_FMT_FP8 = 3 } kvq_format;
 typedef enum { KVQ_KIND_KEY = 0, KVQ_KIND_VALUE = 1 } kvq_kind;
 
 /* Bits ORed into *dev_status by the kernels. */
@@ -90,29 +93,34 @@ typedef struct {
   int64_t head_pitch;
 } kvq_bf16_out;
 
-/* One tensor's NVFP4 planes in a paged pool, slot-major:
+/* One tensor's planes in a paged pool, slot-major.  fmt NVFP4:
  *   codes  [num_slots][num_heads][head_dim/2]   E2M1 nibbles, low nibble = even element
  *   bscale [num_slots][num_heads][head_dim/16]  E4M3 block scales
  *   rscale [num_slots][num_heads]               FP32 row scales
- * Slot = block * block_size + offset.  All three must be 16-byte aligned. */
+ * fmt FP8: codes [num_slots][num_heads][head_dim] E4M3 bytes, rscale as above, bscale
+ * unused (may be NULL).
+ * Slot = block * block_size + offset.  Every plane used must be 16-byte aligned. */
 typedef struct {
   uint8_t* codes;
   uint8_t* bscale;
   float* rscale;
-} kvq_nvfp4_plane;
+} kvq_plane;
 
 typedef struct {
-  kvq_nvfp4_plane k;
-  kvq_nvfp4_plane v;
+  kvq_plane k;
+  kvq_plane v;
   int64_t num_slots;  /* a multiple of block_size */
   int32_t block_size; /* tokens per page (16 in the pages' pools) */
   int32_t num_heads;
   int32_t head_dim;   /* a multiple of 16, at most 512 */
-} kvq_nvfp4_pool;
+  int32_t fmt;        /* KVQ_FMT_NVFP4 or KVQ_FMT_FP8 */
+} kvq_pool;
 
 /* A logical (non-paged) packed tensor [rows][heads][dim], caller-allocated.
  *   fmt NVFP4: codes [rows][heads][dim/2], meta0 = bscale uint8 [rows][heads][dim/16],
  *              rscale float [rows][heads], meta1 unused; group_size must be 16.
+ *   fmt FP8  : codes [rows][heads][dim] E4M3, rscale float [rows][heads]; meta0 and
+ *              meta1 unused; group_size ignored.
  *   fmt INT4 : codes [rows][heads][dim/2], meta0 = FP16 minimum, meta1 = FP16 scale,
  *              each [ceil(rows/G)][heads][dim] for kind KEY (groups of G token rows
  *              per head and channel) or [rows][heads][ceil(dim/G)] for kind VALUE
@@ -132,7 +140,8 @@ typedef struct {
   float* rscale;
 } kvq_packed;
 
-/* Fused NVFP4 quantise + scatter of K and V into a paged pool (the encode hot path).
+/* Fused quantise + scatter of K and V into a paged pool (the encode hot path), in
+ * the pool's format (NVFP4, or FP8 E4M3 with one FP32 scale per row).
  * Source: FreeToken PR #408, Summary ("CUDA Graph-safe KV writes") and the fp8 store
  * notes (slot ids arrive as a device tensor; one launch under graph capture).
  *   k, v       bf16 [num_tokens][num_heads][head_dim] views; either may be NULL
@@ -143,11 +152,10 @@ typedef struct {
  *   pool       planes written in place (only the rows of the given slots).
  * One kernel launch; num_tokens == 0 launches nothing. */
 KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v, int32_t num_tokens,
-                             const int64_t* slot_ids, const kvq_nvfp4_pool* pool,
+                             const int64_t* slot_ids, const kvq_pool* pool,
                              uint32_t* dev_status, kvq_stream_t stream);
 
-/* Paged NVFP4 restore: gather and dequantise pool rows back to bf16 (the decode
- * side).  Source: FreeToken PR #408, Summary ("Triton restore paths"); vllm-rlt
+/* Paged restore: gather and dequantise pool rows back to bf16 (the decode side).  Source: FreeToken PR #408, Summary ("Triton restore paths"); vllm-rlt
  * PR #166 review (pack_paged / unpack_paged over [pages, page_size, heads, dim]).
  *   block_table  device int32 [num_seqs][max_blocks]; token t of sequence s lives in
  *                slot block_table[s][t / block_size] * block_size + t % block_size.
@@ -155,10 +163,11 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
  *   k_out/v_out  bf16 views of [num_seqs * max_seq_len][num_heads][head_dim]: row
  *                s * max_seq_len + t receives token t of sequence s.  Either may be
  *                NULL (that tensor is not restored); not both.
- * y = bf16(e2m1 * block_scale * row_scale), the product rounded once in fp32.
+ * NVFP4: y = bf16(e2m1 * block_scale * row_scale), the product rounded once in fp32;
+ * FP8: y = bf16(e4m3 * row_scale).
  * Rows with a bad block id are skipped (KVQ_DEV_BAD_BLOCK); a sequence with a bad
  * length is skipped whole (KVQ_DEV_BAD_SEQLEN). */
-KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_table, int32_t num_seqs,
+KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table, int32_t num_seqs,
                        int32_t max_blocks, const int32_t* seq_lens, int32_t max_seq_len,
                        const kvq_bf16_out* k_out, const kvq_bf16_out* v_out,
                        uint32_t* dev_status, kvq_stream_t stream);

@@ -19,13 +19,13 @@ from typing import Optional
 import torch
 
 from . import _abi
-from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT_INT4, FMT_NVFP4,
-                   KIND_KEY, KIND_VALUE)
+from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT_FP8, FMT_INT4,
+                   FMT_NVFP4, KIND_KEY, KIND_VALUE)
 
 __all__ = [
-    "KvqError", "Nvfp4Pool", "Packed", "kvq_quant_scatter", "kvq_restore", "kvq_pack",
+    "KvqError", "KvPool", "Nvfp4Pool", "Packed", "kvq_quant_scatter", "kvq_restore", "kvq_pack",
     "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_storage_bytes",
-    "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "KIND_KEY",
+    "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "FMT_FP8", "KIND_KEY",
     "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN",
 ]
 
@@ -82,21 +82,24 @@ def _bf16_out(t: torch.Tensor, name: str):
 # device memory holders
 # ---------------------------------------------------------------------------
 @dataclass
-class Nvfp4Pool:
-    """Paged NVFP4 planes for K and V: codes [slots, H, D/2] u8, bscale [slots, H, D/16]
-    u8 (E4M3), rscale [slots, H] f32.  Slot = block * block_size + offset."""
+class KvPool:
+    """Paged K/V planes of one format, slot-major (slot = block * block_size + offset).
+
+    NVFP4: codes [slots, H, D/2] u8, bscale [slots, H, D/16] u8 (E4M3), rscale [slots, H] f32.
+    FP8:   codes [slots, H, D] u8 (E4M3), rscale [slots, H] f32 (no block scales)."""
 
     k_codes: torch.Tensor
-    k_bscale: torch.Tensor
+    k_bscale: Optional[torch.Tensor]
     k_rscale: torch.Tensor
     v_codes: torch.Tensor
-    v_bscale: torch.Tensor
+    v_bscale: Optional[torch.Tensor]
     v_rscale: torch.Tensor
     block_size: int
+    fmt: int = FMT_NVFP4
 
     @classmethod
     def empty(cls, num_slots: int, num_heads: int, head_dim: int, block_size: int = 16,
-              device="cuda", fill: Optional[int] = None) -> "Nvfp4Pool":
+              device="cuda", fill: Optional[int] = None, fmt: int = FMT_NVFP4) -> "KvPool":
         def u8(*shape):
             t = torch.empty(shape, dtype=torch.uint8, device=device)
             return t.fill_(fill) if fill is not None else t
@@ -107,9 +110,12 @@ class Nvfp4Pool:
                 t.view(torch.uint8).fill_(fill)
             return t
 
+        if fmt == FMT_FP8:
+            return cls(u8(num_slots, num_heads, head_dim), None, f32(num_slots, num_heads),
+                       u8(num_slots, num_heads, head_dim), None, f32(num_slots, num_heads), block_size, fmt)
         return cls(u8(num_slots, num_heads, head_dim // 2), u8(num_slots, num_heads, head_dim // 16),
                    f32(num_slots, num_heads), u8(num_slots, num_heads, head_dim // 2),
-                   u8(num_slots, num_heads, head_dim // 16), f32(num_slots, num_heads), block_size)
+                   u8(num_slots, num_heads, head_dim // 16), f32(num_slots, num_heads), block_size, fmt)
 
     @property
     def num_slots(self) -> int:
@@ -121,20 +127,27 @@ class Nvfp4Pool:
 
     @property
     def head_dim(self) -> int:
-        return self.k_codes.size(2) * 2
+        return self.k_codes.size(2) * (1 if self.fmt == FMT_FP8 else 2)
+
+    def _planes(self):
+        return [t for t in (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale,
+                            self.v_rscale) if t is not None]
 
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in
-                   (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale, self.v_rscale))
+        return sum(t.numel() * t.element_size() for t in self._planes())
 
-    def _struct(self) -> _abi.Nvfp4Pool:
-        for t in (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale, self.v_rscale):
+    def _struct(self) -> _abi.Pool:
+        for t in self._planes():
             if not t.is_contiguous():
                 raise ValueError("pool planes must be contiguous")
-        return _abi.Nvfp4Pool(
-            _abi.Nvfp4Plane(self.k_codes.data_ptr(), self.k_bscale.data_ptr(), self.k_rscale.data_ptr()),
-            _abi.Nvfp4Plane(self.v_codes.data_ptr(), self.v_bscale.data_ptr(), self.v_rscale.data_ptr()),
-            self.num_slots, self.block_size, self.num_heads, self.head_dim)
+        bs = lambda t: None if t is None else t.data_ptr()
+        return _abi.Pool(
+            _abi.Plane(self.k_codes.data_ptr(), bs(self.k_bscale), self.k_rscale.data_ptr()),
+            _abi.Plane(self.v_codes.data_ptr(), bs(self.v_bscale), self.v_rscale.data_ptr()),
+            self.num_slots, self.block_size, self.num_heads, self.head_dim, self.fmt)
+
+
+Nvfp4Pool = KvPool  # the NVFP4 pool is the default format of KvPool
 
 
 @dataclass
@@ -148,13 +161,17 @@ class Packed:
     heads: int
     dim: int
     codes: torch.Tensor
-    meta0: torch.Tensor
+    meta0: Optional[torch.Tensor]
     meta1: Optional[torch.Tensor] = None
     rscale: Optional[torch.Tensor] = None
 
     @classmethod
     def empty(cls, fmt: int, kind: int, rows: int, heads: int, dim: int, group_size: int = 64,
               device="cuda") -> "Packed":
+        if fmt == FMT_FP8:
+            return cls(fmt, kind, 0, rows, heads, dim,
+                       torch.empty((rows, heads, dim), dtype=torch.uint8, device=device), None, None,
+                       torch.empty((rows, heads), dtype=torch.float32, device=device))
         codes = torch.empty((rows, heads, dim // 2), dtype=torch.uint8, device=device)
         if fmt == FMT_NVFP4:
             return cls(fmt, kind, 16, rows, heads, dim, codes,
@@ -177,7 +194,7 @@ class Packed:
             if t is not None and not t.is_contiguous():
                 raise ValueError("packed buffers must be contiguous")
         return _abi.Packed(self.fmt, self.kind, self.group_size, self.rows, self.heads, self.dim,
-                           self.codes.data_ptr(), self.meta0.data_ptr(),
+                           self.codes.data_ptr(), None if self.meta0 is None else self.meta0.data_ptr(),
                            None if self.meta1 is None else self.meta1.data_ptr(),
                            None if self.rscale is None else self.rscale.data_ptr())
 
@@ -186,8 +203,9 @@ class Packed:
 # entry points (same names as the C ABI)
 # ---------------------------------------------------------------------------
 def kvq_quant_scatter(k: Optional[torch.Tensor], v: Optional[torch.Tensor], slot_ids: torch.Tensor,
-                      pool: Nvfp4Pool, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """NVFP4 quantise + scatter of K/V [T, H, D] bf16 into pool slots slot_ids[T] (int64)."""
+                      pool: KvPool, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantise + scatter of K/V [T, H, D] bf16 into pool slots slot_ids[T] (int64), in the
+    pool's format (NVFP4 or FP8)."""
     src = k if k is not None else v
     if src is None:
         raise ValueError("k and v are both None")
@@ -211,10 +229,10 @@ def _seq_view(t: torch.Tensor, S: int, Tmax: int, name: str):
     return _bf16_out(t, name)
 
 
-def kvq_restore(pool: Nvfp4Pool, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+def kvq_restore(pool: KvPool, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                 k_out: Optional[torch.Tensor], v_out: Optional[torch.Tensor],
                 dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Paged NVFP4 restore into k_out / v_out [S, max_seq_len, H, D] bf16."""
+    """Paged restore into k_out / v_out [S, max_seq_len, H, D] bf16."""
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_table and seq_lens must be int32")
     if not block_table.is_contiguous():

@@ -19,6 +19,7 @@ STATUS_NAMES = {
 
 FMT_NVFP4 = 1
 FMT_INT4 = 2
+FMT_FP8 = 3
 KIND_KEY = 0
 KIND_VALUE = 1
 
@@ -36,18 +37,19 @@ class Bf16Out(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("row_pitch", ctypes.c_int64), ("head_pitch", ctypes.c_int64)]
 
 
-class Nvfp4Plane(ctypes.Structure):
+class Plane(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("bscale", ctypes.c_void_p), ("rscale", ctypes.c_void_p)]
 
 
-class Nvfp4Pool(ctypes.Structure):
+class Pool(ctypes.Structure):
     _fields_ = [
-        ("k", Nvfp4Plane),
-        ("v", Nvfp4Plane),
+        ("k", Plane),
+        ("v", Plane),
         ("num_slots", ctypes.c_int64),
         ("block_size", ctypes.c_int32),
         ("num_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
+        ("fmt", ctypes.c_int32),
     ]
 
 
@@ -73,8 +75,8 @@ _ST = ctypes.c_int
 
 SIGNATURES = {
     "kvq_quant_scatter": (_ST, [ctypes.POINTER(Bf16In), ctypes.POINTER(Bf16In), _I32, _P,
-                                ctypes.POINTER(Nvfp4Pool), _P, _P]),
-    "kvq_restore": (_ST, [ctypes.POINTER(Nvfp4Pool), _P, _I32, _I32, _P, _I32,
+                                ctypes.POINTER(Pool), _P, _P]),
+    "kvq_restore": (_ST, [ctypes.POINTER(Pool), _P, _I32, _I32, _P, _I32,
                           ctypes.POINTER(Bf16Out), ctypes.POINTER(Bf16Out), _P, _P]),
     "kvq_pack": (_ST, [ctypes.POINTER(Bf16In), ctypes.POINTER(Packed), _P]),
     "kvq_unpack": (_ST, [ctypes.POINTER(Packed), ctypes.POINTER(Bf16Out), _P]),

@@ -42,6 +42,11 @@ int64_t view_bytes(int64_t rows, int64_t row_pitch, int64_t heads, int64_t head_
 }
 void dbg_packed(const kvq_packed* pk) {
   const int64_t rh = static_cast<int64_t>(pk->rows) * pk->heads;
+  if (pk->fmt == KVQ_FMT_FP8) {
+    dbg_add(pk->codes, rh * pk->dim, "codes");
+    dbg_add(pk->rscale, rh * 4, "rscale");
+    return;
+  }
   dbg_add(pk->codes, rh * (pk->dim / 2), "codes");
   if (pk->fmt == KVQ_FMT_NVFP4) {
     dbg_add(pk->meta0, rh * (pk->dim / 16), "bscale");
@@ -115,6 +120,20 @@ kvq_status check_head_dim(int32_t H, int32_t D) {
   return KVQ_OK;
 }
 
+// A pool's format and planes (the bscale plane only for NVFP4).
+kvq_status check_pool_fmt(const kvq_pool* pool) {
+  if (pool->fmt != KVQ_FMT_NVFP4 && pool->fmt != KVQ_FMT_FP8)
+    return fail(KVQ_ERR_INVALID_ARG, "pool fmt must be KVQ_FMT_NVFP4 or KVQ_FMT_FP8 (got %d)", pool->fmt);
+  return KVQ_OK;
+}
+kvq_status check_pool_plane(const kvq_pool* pool, const kvq_plane* pl) {
+  kvq_status st;
+  if ((st = check_plane(pl->codes, "pool codes")) != KVQ_OK) return st;
+  if (pool->fmt == KVQ_FMT_NVFP4 && (st = check_plane(pl->bscale, "pool bscale")) != KVQ_OK) return st;
+  return check_plane(pl->rscale, "pool rscale");
+}
+int64_t code_bytes_per_row(int32_t fmt, int32_t D) { return fmt == KVQ_FMT_FP8 ? D : D / 2; }
+
 int lanes_for(int32_t D) {
   int nb = D / 16, L = 1;
   while (L < nb) L <<= 1;
@@ -140,6 +159,10 @@ kvq_status check_packed(const kvq_packed* pk, const char* what) {
     if (pk->rows == 0) return KVQ_OK;
     if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
     if ((st = check_plane(pk->meta0, "meta0 (block scales)")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->rscale, "rscale")) != KVQ_OK) return st;
+  } else if (pk->fmt == KVQ_FMT_FP8) {
+    if (pk->rows == 0) return KVQ_OK;
+    if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
     if ((st = check_plane(pk->rscale, "rscale")) != KVQ_OK) return st;
   } else if (pk->fmt == KVQ_FMT_INT4) {
     const int G = pk->group_size;
@@ -200,9 +223,10 @@ extern "C" {
 
 KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
                                      int32_t num_tokens, const int64_t* slot_ids,
-                                     const kvq_nvfp4_pool* pool, uint32_t* dev_status,
+                                     const kvq_pool* pool, uint32_t* dev_status,
                                      kvq_stream_t stream) {
   if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
   if (k == nullptr && v == nullptr) return fail(KVQ_ERR_INVALID_ARG, "both k and v are NULL");
   if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_tokens");
   kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
@@ -220,15 +244,13 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
   bool v8 = true;
   int i = 0;
   const kvq_bf16_in* src[2] = {k, v};
-  const kvq_nvfp4_plane* dst[2] = {&pool->k, &pool->v};
+  const kvq_plane* dst[2] = {&pool->k, &pool->v};
   const char* names[2] = {"k", "v"};
   for (int j = 0; j < 2; ++j) {
     if (src[j] == nullptr) continue;
     if ((st = check_view(src[j]->ptr, src[j]->row_pitch, src[j]->head_pitch, names[j], v8)) != KVQ_OK)
       return st;
-    if ((st = check_plane(dst[j]->codes, "pool codes")) != KVQ_OK) return st;
-    if ((st = check_plane(dst[j]->bscale, "pool bscale")) != KVQ_OK) return st;
-    if ((st = check_plane(dst[j]->rscale, "pool rscale")) != KVQ_OK) return st;
+    if ((st = check_pool_plane(pool, dst[j])) != KVQ_OK) return st;
     EncodeTensor& t = p.ten[i++];
     t.x = static_cast<const uint16_t*>(src[j]->ptr);
     t.row_pitch = src[j]->row_pitch;
@@ -248,17 +270,17 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
     if (src[j] == nullptr) continue;
     dbg_add(src[j]->ptr, view_bytes(num_tokens, src[j]->row_pitch, pool->num_heads, src[j]->head_pitch, pool->head_dim), names[j]);
     const int64_t rh = pool->num_slots * pool->num_heads;
-    dbg_add(dst[j]->codes, rh * (pool->head_dim / 2), "pool codes");
-    dbg_add(dst[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(dst[j]->codes, rh * code_bytes_per_row(pool->fmt, pool->head_dim), "pool codes");
+    if (pool->fmt == KVQ_FMT_NVFP4) dbg_add(dst[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
     dbg_add(dst[j]->rscale, rh * 4, "pool rscale");
   }
   dbg_add(slot_ids, 8ll * num_tokens, "slot_ids");
   dbg_add(dev_status, 4, "status");
-  return launched(launch_nvfp4_encode(p, kEncScatter, lanes_for(pool->head_dim), v8,
+  return launched(launch_nvfp4_encode(p, kEncScatter, pool->fmt, v8,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
-KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_table,
+KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table,
                                int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
                                int32_t max_seq_len, const kvq_bf16_out* k_out,
                                const kvq_bf16_out* v_out, uint32_t* dev_status,
@@ -266,6 +288,7 @@ KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_
   if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
   if (k_out == nullptr && v_out == nullptr)
     return fail(KVQ_ERR_INVALID_ARG, "both k_out and v_out are NULL");
+  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
   kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
   if (st != KVQ_OK) return st;
   if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
@@ -284,15 +307,13 @@ KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_
   bool v8 = true;
   int i = 0;
   const kvq_bf16_out* out[2] = {k_out, v_out};
-  const kvq_nvfp4_plane* src[2] = {&pool->k, &pool->v};
+  const kvq_plane* src[2] = {&pool->k, &pool->v};
   const char* names[2] = {"k_out", "v_out"};
   for (int j = 0; j < 2; ++j) {
     if (out[j] == nullptr) continue;
     if ((st = check_view(out[j]->ptr, out[j]->row_pitch, out[j]->head_pitch, names[j], v8)) != KVQ_OK)
       return st;
-    if ((st = check_plane(src[j]->codes, "pool codes")) != KVQ_OK) return st;
-    if ((st = check_plane(src[j]->bscale, "pool bscale")) != KVQ_OK) return st;
-    if ((st = check_plane(src[j]->rscale, "pool rscale")) != KVQ_OK) return st;
+    if ((st = check_pool_plane(pool, src[j])) != KVQ_OK) return st;
     DecodeTensor& t = p.ten[i++];
     t.codes = src[j]->codes;
     t.bscale = src[j]->bscale;
@@ -323,14 +344,14 @@ KVQ_API kvq_status kvq_restore(const kvq_nvfp4_pool* pool, const int32_t* block_
     if (out[j] == nullptr) continue;
     dbg_add(out[j]->ptr, view_bytes(static_cast<int64_t>(num_seqs) * max_seq_len, out[j]->row_pitch, pool->num_heads, out[j]->head_pitch, pool->head_dim), names[j]);
     const int64_t rh = pool->num_slots * pool->num_heads;
-    dbg_add(src[j]->codes, rh * (pool->head_dim / 2), "pool codes");
-    dbg_add(src[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(src[j]->codes, rh * code_bytes_per_row(pool->fmt, pool->head_dim), "pool codes");
+    if (pool->fmt == KVQ_FMT_NVFP4) dbg_add(src[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
     dbg_add(src[j]->rscale, rh * 4, "pool rscale");
   }
   dbg_add(block_table, 4ll * num_seqs * max_blocks, "block_table");
   dbg_add(seq_lens, 4ll * num_seqs, "seq_lens");
   dbg_add(dev_status, 4, "status");
-  return launched(launch_nvfp4_decode(p, kDecRestore, lanes_for(pool->head_dim), v8,
+  return launched(launch_nvfp4_decode(p, kDecRestore, pool->fmt, v8,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -345,7 +366,7 @@ KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_str
   dbg_clear();
   dbg_add(x->ptr, view_bytes(out->rows, x->row_pitch, out->heads, x->head_pitch, out->dim), "x");
   dbg_packed(out);
-  if (out->fmt == KVQ_FMT_NVFP4) {
+  if (out->fmt == KVQ_FMT_NVFP4 || out->fmt == KVQ_FMT_FP8) {
     EncodeParams p{};
     p.ten[0].x = static_cast<const uint16_t*>(x->ptr);
     p.ten[0].row_pitch = x->row_pitch;
@@ -356,7 +377,7 @@ KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_str
     p.div_h = FastDiv(static_cast<uint32_t>(out->heads));
     p.H = out->heads;
     p.nb = out->dim / 16;
-    return launched(launch_nvfp4_encode(p, kEncPack, lanes_for(out->dim), v8, s));
+    return launched(launch_nvfp4_encode(p, kEncPack, out->fmt, v8, s));
   }
   Int4EncodeParams p{};
   p.x = static_cast<const uint16_t*>(x->ptr);
@@ -429,7 +450,7 @@ KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in
   dbg_add(pos, 4ll * num_pos, "pos");
   dbg_add(pos_out, 4ll * num_pos, "pos_out");
   dbg_add(dev_status, 4, "status");
-  if (payload->fmt == KVQ_FMT_NVFP4) {
+  if (payload->fmt == KVQ_FMT_NVFP4 || payload->fmt == KVQ_FMT_FP8) {
     EncodeParams p{};
     EncodeTensor& t = p.ten[0];
     t.x = static_cast<const uint16_t*>(cur->ptr);
@@ -448,7 +469,7 @@ KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in
     p.pos_out = pos_out;
     p.src_rows = num_rows;
     p.status = dev_status;
-    return launched(launch_nvfp4_encode(p, kEncResidual, lanes_for(payload->dim), v8, s));
+    return launched(launch_nvfp4_encode(p, kEncResidual, payload->fmt, v8, s));
   }
   Int4EncodeParams p{};
   p.x = static_cast<const uint16_t*>(cur->ptr);
@@ -552,6 +573,7 @@ KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_si
     if (dim % 16 != 0) return 0;
     return static_cast<size_t>(rh * (dim / 2 + dim / 16 + 4));
   }
+  if (fmt == KVQ_FMT_FP8) return static_cast<size_t>(rh * (dim + 4));
   if (fmt == KVQ_FMT_INT4) {
     if (dim % 2 != 0 || group_size <= 0) return 0;
     const int64_t codes = rh * (dim / 2);

@@ -373,6 +373,43 @@ __device__ __forceinline__ void nvfp4_decode16(uint32_t cw0, uint32_t cw1, uint3
   }
 }
 
+// FP8 E4M3 row codec, one 16-element block: q = x * inv (or x / rs when inv is
+// infinite), codes E4M3 nearest even, saturating at 448, sign of x; the 16 code
+// bytes land in c (element 0 in the low byte of c[0]).
+__device__ __forceinline__ void fp8_quantize16(const uint32_t (&w)[8], float rs, float inv,
+                                               uint32_t (&c)[4]) {
+  c[0] = c[1] = c[2] = c[3] = 0u;
+  if (!isinf(inv)) {
+    const uint64_t inv2 = pack_f32x2(__float_as_uint(inv), __float_as_uint(inv));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t ql, qh;
+      unpack_f32x2(mul_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), inv2), ql, qh);
+      c[i / 2] |= e4m3x2_from_f32(__uint_as_float(ql), __uint_as_float(qh)) << (16 * (i % 2));
+    }
+  } else {  // tiny scale: the reciprocal overflowed, divide directly
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i / 2] |= e4m3x2_from_f32(__fdiv_rn(bf16lo(w[i]), rs), __fdiv_rn(bf16hi(w[i]), rs)) << (16 * (i % 2));
+  }
+}
+
+// FP8 decode of one 16-element block: y = bf16(e4m3 * rs) (E4M3 -> fp16 is exact).
+__device__ __forceinline__ void fp8_decode16(const uint32_t (&c)[4], float rs, uint32_t (&out)[8]) {
+  const uint64_t rs2 = pack_f32x2(__float_as_uint(rs), __float_as_uint(rs));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t h2;
+    const uint16_t two = static_cast<uint16_t>((c[i / 2] >> (16 * (i % 2))) & 0xFFFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    float lo, hi;
+    f16x2_to_f32(h2, lo, hi);
+    uint32_t yl, yh;
+    unpack_f32x2(mul_f32x2(pack_f32x2(__float_as_uint(lo), __float_as_uint(hi)), rs2), yl, yh);
+    out[i] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+  }
+}
+
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));

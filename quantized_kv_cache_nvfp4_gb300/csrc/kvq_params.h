@@ -42,8 +42,8 @@ struct FastDiv {
 enum EncodeMode : int { kEncScatter = 0, kEncPack = 1, kEncResidual = 2 };
 
 struct Nvfp4Planes {
-  uint8_t* codes;   // [rows][D/2]  (rows = slot*H + h, or p*H + h)
-  uint8_t* bscale;  // [rows][D/16]
+  uint8_t* codes;   // NVFP4 [rows][D/2], FP8 [rows][D]  (rows = slot*H + h, or p*H + h)
+  uint8_t* bscale;  // NVFP4 [rows][D/16]
   float* rscale;    // [rows]
 };
 
@@ -133,7 +133,7 @@ struct Int4EncodeParams {
 
 // Decoder of a packed payload row into bf16, plus an optional residual add.
 struct PayloadRef {
-  int32_t fmt;         // 1 nvfp4, 2 int4
+  int32_t fmt;         // 1 nvfp4, 2 int4, 3 fp8
   int32_t kind;
   int32_t G;
   const uint8_t* codes;
@@ -172,10 +172,10 @@ struct HostRange {
 HostRange* pending(int* n);  // the list for the next launch (at most 32 entries)
 }  // namespace dbg
 
-// Launchers (return the cudaGetLastError() of the launch).
-cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int lanes, bool v8,
+// Launchers (return the cudaGetLastError() of the launch).  fmt: 1 NVFP4, 3 FP8.
+cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int fmt, bool v8,
                                 cudaStream_t s);
-cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int lanes, bool v8,
+cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int fmt, bool v8,
                                 cudaStream_t s);
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s);
 cudaError_t launch_payload_decode(const UnpackParams& p, int lanes, bool v8, cudaStream_t s);

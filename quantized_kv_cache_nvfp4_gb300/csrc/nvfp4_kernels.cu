@@ -15,6 +15,11 @@
 // The tiny-scale direct division follows "vllm-rlt PR #166: INT4 KV packing ...",
 // Purpose ("a direct-division fallback when their reciprocal overflows").
 //
+// FP8 E4M3 rows ("feat(kvcache): ... (FreeToken PR #408)", fp8 store notes) take the
+// same kernels with kFmt = 3: rs = amax / 448; q = x * (1 / rs) (x / rs when the
+// reciprocal overflows); code = e4m3(q) nearest even; decode y = bf16(e4m3 * rs);
+// D code bytes per row and no block scales.
+//
 // Work mapping: a lane owns BPL consecutive 16-element blocks of a row (BPL = 2 when
 // the row has an even number of blocks: two 256-bit loads, 64 contiguous bytes per
 // lane).  The L lanes of a row (L = next power of two of D/16/BPL) form an aligned
@@ -110,7 +115,7 @@ __device__ __forceinline__ void quantize_block(const uint32_t (&w)[8], float s, 
   c1 = bytes4(byte[4], byte[5], byte[6], byte[7]);
 }
 
-template <int L, int BPL, bool kV8, int kMode, int kMinBlocks>
+template <int L, int BPL, bool kV8, int kMode, int kMinBlocks, int kFmt>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(const EncodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
@@ -182,6 +187,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(cons
       lmax = fmaxf(lmax, vb[j]);
     }
     const float amax = group_max<L>(lmax);
+    if constexpr (kFmt == 3) {  // FP8 E4M3: one scale per row, no block scales
+      const float rs = __fdiv_rn(amax, kE4M3Max);
+      const float inv = (rs != 0.0f) ? __frcp_rn(rs) : 0.0f;
+      uint32_t c8[BPL][4];
+#pragma unroll
+      for (int j = 0; j < BPL; ++j) fp8_quantize16(w[j], rs, inv, c8[j]);
+      if (!skip && lane_active) {
+        const Nvfp4Planes& d = p.ten[loc.tensor].dst;
+        uint8_t* cp = d.codes + drow * (16 * p.nb) + 16 * b0;
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) store16B(cp + 16 * j, c8[j]);
+        if (li == 0) STX(d.rscale + drow, rs);
+      }
+#pragma unroll
+      for (int j = 0; j < BPL; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[j][i] = nw[j][i];
+      continue;
+    }
     const float rs = __fdiv_rn(amax, kE2M1Max * kE4M3Max);
     const float rinv = (rs != 0.0f) ? __frcp_rn(rs) : 0.0f;
 
@@ -258,7 +282,7 @@ __device__ __forceinline__ RestoreRow resolve_row(const DecodeParams& p, uint32_
 
 // R rows per lane per iteration: all R block-table lookups, then all R code loads,
 // then the arithmetic and stores, so R dependent load chains are in flight at once.
-template <int L, int BPL, bool kV8, int kMode, int R, int kMinBlocks>
+template <int L, int BPL, bool kV8, int kMode, int R, int kMinBlocks, int kFmt>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_decode_kernel(const DecodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
@@ -276,6 +300,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_decode_kernel(cons
     for (int r = 0; r < R; ++r) {
       const uint32_t row = row0 + r * stride;
       rr[r] = (row < total) ? resolve_row<kMode>(p, row, li) : RestoreRow{-1, nullptr, nullptr};
+    }
+    if constexpr (kFmt == 3) {  // FP8 E4M3 rows: 16 code bytes per block, one scale
+      uint32_t c8[R][BPL][4];
+      float rs8[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (rr[r].srow < 0) continue;
+        const DecodeTensor& T = *rr[r].ten;
+        rs8[r] = LDX(T.rscale + rr[r].srow);
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) load16B(T.codes + rr[r].srow * (16 * p.nb) + 16 * (b0 + j), c8[r][j]);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (rr[r].srow < 0) continue;
+        uint32_t out[8];
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) {
+          fp8_decode16(c8[r][j], rs8[r], out);
+          store32B<kV8>(rr[r].y + 16 * (b0 + j), out);
+        }
+      }
+      continue;
     }
     uint32_t cw[R][2 * BPL];
     uint32_t bsb[R];
@@ -332,9 +379,9 @@ constexpr int kDecRows = 2;
 constexpr int kDecMinBlocks = 1;
 constexpr int kDecGridFactor = 2;
 
-template <int L, int BPL, bool kV8, int kMode>
+template <int L, int BPL, bool kV8, int kMode, int kFmt>
 cudaError_t enc_launch(const EncodeParams& p, cudaStream_t s) {
-  auto k = nvfp4_encode_kernel<L, BPL, kV8, kMode, kEncMinBlocks>;
+  auto k = nvfp4_encode_kernel<L, BPL, kV8, kMode, kEncMinBlocks, kFmt>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L), kEncGridFactor);
   cudaError_t e = cudaSuccess;
@@ -342,9 +389,9 @@ cudaError_t enc_launch(const EncodeParams& p, cudaStream_t s) {
   return e;
 }
 
-template <int L, int BPL, bool kV8, int kMode>
+template <int L, int BPL, bool kV8, int kMode, int kFmt>
 cudaError_t dec_launch(const DecodeParams& p, cudaStream_t s) {
-  auto k = nvfp4_decode_kernel<L, BPL, kV8, kMode, kDecRows, kDecMinBlocks>;
+  auto k = nvfp4_decode_kernel<L, BPL, kV8, kMode, kDecRows, kDecMinBlocks, kFmt>;
   uint32_t rows = p.rows_per_tensor * p.ntensors;
   int grid = grid_for(k, rows, (kThreads / 32) * (32 / L) * kDecRows, kDecGridFactor);
   cudaError_t e = cudaSuccess;
@@ -363,25 +410,25 @@ void row_shape(int nb, int& lanes, int& bpl) {
 #define KVQ_SHAPES(X) X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) \
                       X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2)
 
-template <int kMode>
+template <int kMode, int kFmt>
 cudaError_t enc_dispatch(const EncodeParams& p, bool v8, cudaStream_t s) {
   int lanes, bpl;
   row_shape(p.nb, lanes, bpl);
 #define KVQ_ENC(LN, B)                                                                    \
   if (lanes == LN && bpl == B)                                                            \
-    return v8 ? enc_launch<LN, B, true, kMode>(p, s) : enc_launch<LN, B, false, kMode>(p, s);
+    return v8 ? enc_launch<LN, B, true, kMode, kFmt>(p, s) : enc_launch<LN, B, false, kMode, kFmt>(p, s);
   KVQ_SHAPES(KVQ_ENC)
 #undef KVQ_ENC
   return cudaErrorInvalidValue;
 }
 
-template <int kMode>
+template <int kMode, int kFmt>
 cudaError_t dec_dispatch(const DecodeParams& p, bool v8, cudaStream_t s) {
   int lanes, bpl;
   row_shape(p.nb, lanes, bpl);
 #define KVQ_DEC(LN, B)                                                                    \
   if (lanes == LN && bpl == B)                                                            \
-    return v8 ? dec_launch<LN, B, true, kMode>(p, s) : dec_launch<LN, B, false, kMode>(p, s);
+    return v8 ? dec_launch<LN, B, true, kMode, kFmt>(p, s) : dec_launch<LN, B, false, kMode, kFmt>(p, s);
   KVQ_SHAPES(KVQ_DEC)
 #undef KVQ_DEC
   return cudaErrorInvalidValue;
@@ -389,23 +436,22 @@ cudaError_t dec_dispatch(const DecodeParams& p, bool v8, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int /*lanes*/, bool v8,
-                                cudaStream_t s) {
+cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int fmt, bool v8, cudaStream_t s) {
+  const bool fp8 = fmt == 3;
   switch (mode) {
     case kEncScatter:
-      return enc_dispatch<kEncScatter>(p, v8, s);
+      return fp8 ? enc_dispatch<kEncScatter, 3>(p, v8, s) : enc_dispatch<kEncScatter, 1>(p, v8, s);
     case kEncPack:
-      return enc_dispatch<kEncPack>(p, v8, s);
+      return fp8 ? enc_dispatch<kEncPack, 3>(p, v8, s) : enc_dispatch<kEncPack, 1>(p, v8, s);
     case kEncResidual:
-      return enc_dispatch<kEncResidual>(p, v8, s);
+      return fp8 ? enc_dispatch<kEncResidual, 3>(p, v8, s) : enc_dispatch<kEncResidual, 1>(p, v8, s);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int /*lanes*/, bool v8,
-                                cudaStream_t s) {
-  if (mode == kDecRestore) return dec_dispatch<kDecRestore>(p, v8, s);
-  return cudaErrorInvalidValue;
+cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int fmt, bool v8, cudaStream_t s) {
+  if (mode != kDecRestore) return cudaErrorInvalidValue;
+  return fmt == 3 ? dec_dispatch<kDecRestore, 3>(p, v8, s) : dec_dispatch<kDecRestore, 1>(p, v8, s);
 }
 
 }  // namespace kvq

@@ -35,6 +35,16 @@ __device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, 
                                               uint32_t (&w)[BPL][8]) {
   const PayloadRef& P = u.pay;
   const int64_t prow = p * u.H + h;
+  if constexpr (kFmt == 3) {  // FP8: 16 E4M3 bytes per block, one scale per row
+    const float rs = LDX(P.rscale + prow);
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+      uint32_t c4[4];
+      load16B(P.codes + prow * u.D + 16 * (b0 + j), c4);
+      fp8_decode16(c4, rs, w[j]);
+    }
+    return;
+  }
   uint32_t cw[2 * BPL];
   if constexpr (BPL == 2) {
     uint32_t c4[4];
@@ -337,16 +347,22 @@ cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   return e;
 }
 
+template <int L, int BPL, bool kV8, int kFmt>
+cudaError_t pl_dispatch_mode(const UnpackParams& u, cudaStream_t s) {
+  switch (u.mode) {
+    case 0: return pl_launch<L, BPL, kV8, kFmt, 0>(u, s);
+    case 1: return pl_launch<L, BPL, kV8, kFmt, 1>(u, s);
+    case 2: return pl_launch<L, BPL, kV8, kFmt, 2>(u, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int L, int BPL, bool kV8>
 cudaError_t pl_dispatch_fm(const UnpackParams& u, cudaStream_t s) {
-  const int f = u.pay.fmt == 1 ? 1 : 2;
-  switch (u.mode * 2 + (f - 1)) {
-    case 0: return pl_launch<L, BPL, kV8, 1, 0>(u, s);
-    case 1: return pl_launch<L, BPL, kV8, 2, 0>(u, s);
-    case 2: return pl_launch<L, BPL, kV8, 1, 1>(u, s);
-    case 3: return pl_launch<L, BPL, kV8, 2, 1>(u, s);
-    case 4: return pl_launch<L, BPL, kV8, 1, 2>(u, s);
-    case 5: return pl_launch<L, BPL, kV8, 2, 2>(u, s);
+  switch (u.pay.fmt) {
+    case 1: return pl_dispatch_mode<L, BPL, kV8, 1>(u, s);
+    case 2: return pl_dispatch_mode<L, BPL, kV8, 2>(u, s);
+    case 3: return pl_dispatch_mode<L, BPL, kV8, 3>(u, s);
   }
   return cudaErrorInvalidValue;
 }

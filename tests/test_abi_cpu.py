@@ -41,11 +41,11 @@ def test_library_exports_every_declared_symbol(kvq_lib_path):
 def test_storage_bytes_agrees_with_the_oracle(kvq_lib_path):
     import quantized_kv_cache_nvfp4_gb300 as kvq
 
-    for fmt in (1, 2):
+    for fmt in (1, 2, 3):
         for kind in (0, 1):
             for G in (16, 64):
                 for (T, H, D) in [(1, 1, 128), (256, 8, 128), (4100, 8, 96), (1048576, 4, 256), (0, 2, 32)]:
-                    g = 16 if fmt == 1 else G
+                    g = {1: 16, 2: G, 3: 0}[fmt]
                     assert kvq.kvq_storage_bytes(fmt, kind, g, T, H, D) == O.storage_bytes(fmt, kind, g, T, H, D)
     assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 128) == 76
     assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 100) == 0
@@ -64,7 +64,7 @@ def test_host_checks_fail_before_any_cuda_call(kvq_lib_path):
     from quantized_kv_cache_nvfp4_gb300 import _abi
 
     lib = _abi.load()
-    pool = _abi.Nvfp4Pool(_abi.Nvfp4Plane(), _abi.Nvfp4Plane(), 64, 16, 2, 100)
+    pool = _abi.Pool(_abi.Plane(), _abi.Plane(), 64, 16, 2, 100, 1)
     x = _abi.Bf16In(None, 256, 128)
     assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
     assert b"multiple of 16" in lib.kvq_last_error()
@@ -78,6 +78,10 @@ def test_host_checks_fail_before_any_cuda_call(kvq_lib_path):
     assert lib.kvq_pack(ctypes.byref(x), ctypes.byref(pk), None) == 2
     pk = _abi.Packed(7, 0, 64, 4, 2, 128, None, None, None, None)
     assert lib.kvq_unpack(ctypes.byref(pk), None, None) == 1
+    pool.head_dim, pool.fmt = 128, 2  # INT4 is not a pool format
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
+    assert b"pool fmt" in lib.kvq_last_error()
+    pool.fmt = 1
     # zero-sized work is a no-op that needs no pointers
     pool.num_slots = 64
     assert lib.kvq_quant_scatter(ctypes.byref(x), None, 0, None, ctypes.byref(pool), None, None) == 0
