@@ -502,6 +502,28 @@ def other_rows(kvq, device, T=262144, H=8, D=128, G=64, P=None, iters=20, peak=6
           2 * P * H * 2 * D + 4 * P + pb)
     timed("kvq_decode_residual nvfp4 25% copy", lambda: kvq.kvq_decode_residual(pay, pos, prev, y),
           rows_b + pb + 4 * P + rows_b)
+    # FP8 E4M3 rows: D code bytes + one FP32 scale per (token, head)
+    f8 = kvq.Packed.empty(kvq.FMT_FP8, 0, T, H, D, device=device)
+    f8b = T * H * (D + 4)
+    timed("kvq_pack fp8", lambda: kvq.kvq_pack(cur, f8), rows_b + f8b)
+    timed("kvq_unpack fp8", lambda: kvq.kvq_unpack(f8, y), f8b + rows_b)
+    nblk = -(-T // 16)
+    perm = synth.block_permutation(nblk, 4).to(device)
+    t = torch.arange(T, device=device)
+    slots = perm[t // 16].long() * 16 + t % 16
+    pool = kvq.KvPool.empty(nblk * 16, H, D, 16, device=device, fmt=kvq.FMT_FP8)
+    timed("kvq_quant_scatter fp8 (K only)", lambda: kvq.kvq_quant_scatter(cur, None, slots, pool),
+          rows_b + 8 * T + f8b)
+    lens = torch.tensor([T], dtype=torch.int32, device=device)
+    table = perm.view(1, -1).contiguous()
+    timed("kvq_restore fp8 (K only)", lambda: kvq.kvq_restore(pool, table, lens, T, y, None),
+          f8b + 4 * nblk + rows_b)
+    pay = kvq.Packed.empty(kvq.FMT_FP8, 0, P, H, D, device=device)
+    pb = P * H * (D + 4)
+    timed("kvq_encode_residual fp8 25%", lambda: kvq.kvq_encode_residual(cur, prev, pos, pay),
+          2 * P * H * 2 * D + 4 * P + pb)
+    timed("kvq_decode_residual fp8 25% copy", lambda: kvq.kvq_decode_residual(pay, pos, prev, y),
+          rows_b + pb + 4 * P + rows_b)
     return {"workload": f"[{T} tokens, {H} KV heads, D{D}] bf16, INT4 G{G}, residual rows kept {P}/{T}",
             "kernels": out}
 

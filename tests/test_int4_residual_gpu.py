@@ -36,6 +36,8 @@ def check_payload(pay, opay):
     if pay.fmt == kvq.FMT_INT4:
         np.testing.assert_array_equal(f16bits(pay.meta0), opay["meta_a"], err_msg="payload min")
         np.testing.assert_array_equal(f16bits(pay.meta1), opay["meta_b"], err_msg="payload scale")
+    elif pay.fmt == kvq.FMT_FP8:
+        np.testing.assert_array_equal(f32bits(pay.rscale), f32bits(opay["rscale"]), err_msg="row scales")
     else:
         np.testing.assert_array_equal(u8(pay.meta0), opay["meta_a"], err_msg="payload block scales")
         np.testing.assert_array_equal(f32bits(pay.rscale), f32bits(opay["rscale"]), err_msg="row scales")
@@ -115,6 +117,12 @@ def test_dense_residual_chain(kind):
 def test_int4_base_nvfp4_residual_chain(kind):
     """A mixed chain: INT4 base, NVFP4 residual rows."""
     _chain(kind, kvq.FMT_NVFP4, T=600, H=3, D=96, P=150)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_base_fp8_residual_chain(kind):
+    """A mixed chain: INT4 base, FP8 E4M3 residual rows."""
+    _chain(kind, kvq.FMT_FP8, T=600, H=3, D=96, P=150)
 
 
 def test_ragged_compact_groups_and_odd_sizes():
