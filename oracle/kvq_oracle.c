@@ -417,14 +417,26 @@ static int get_nibble(const uint8_t* codes, int64_t elem) {
   return (elem % 2 == 0) ? (b & 15) : (b >> 4);
 }
 
+/* Minimum and maximum in the total order of IEEE 754-2019 minimum/maximum for finite
+ * values: -0 is below +0.  (C's fminf may return either zero for a (-0, +0) pair, and
+ * which one changes the sign bit of the stored FP16 minimum.) */
+static float min_signed0(float a, float b) {
+  if (a == 0.0f && b == 0.0f) return signbit(a) ? a : b;
+  return b < a ? b : a;
+}
+static float max_signed0(float a, float b) {
+  if (a == 0.0f && b == 0.0f) return signbit(a) ? b : a;
+  return b > a ? b : a;
+}
+
 /* One group of n elements at x[idx[k]] (R5). */
 static void int4_quantize_group(const uint16_t* x, const int64_t* idx, int n, uint8_t* codes,
                                 uint16_t* mn16, uint16_t* sc16) {
   float mn = orc_bf16_to_f32(x[idx[0]]), mx = mn;
   for (int k = 1; k < n; k++) {
     float v = orc_bf16_to_f32(x[idx[k]]);
-    mn = fminf(mn, v);
-    mx = fmaxf(mx, v);
+    mn = min_signed0(mn, v);
+    mx = max_signed0(mx, v);
   }
   float sc = (mx - mn) / 15.0f;
   for (int k = 0; k < n; k++) {

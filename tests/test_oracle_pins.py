@@ -437,6 +437,34 @@ def test_int4_constant_group_decodes_to_its_value():
         assert (y == want).all()
 
 
+def _f16bits(x):
+    """fp16 bits by numpy's own conversion (round to nearest even)."""
+    return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_int4_signed_zero_groups_order_minus_zero_first():
+    """A group whose minimum or maximum is a zero holding both signs: -0 orders below +0
+    whatever the order of the elements (IEEE 754-2019 minimum/maximum), so the stored
+    FP16 minimum is -0 (0x8000) and the maximum gives sc = (+0 - -0) / 15 = 0."""
+    for order in ((0x0000, 0x8000), (0x8000, 0x0000)):
+        xb = np.zeros((1, 1, 64), np.uint16)
+        xb[0, 0, :32] = order[0]
+        xb[0, 0, 32:] = order[1]
+        codes, mn, sc = O.int4_pack(xb, O.KIND_VALUE, 64)
+        assert mn[0, 0, 0] == 0x8000 and sc[0, 0, 0] == 0 and (codes == 0).all()
+        y = O.int4_unpack(codes, mn, sc, O.KIND_VALUE, 64)
+        assert (y == 0).all()  # (0 * 0) + (-0) = (+0) + (-0) = +0 in round-to-nearest
+        # a positive value above the zeros: min is -0, the codes are those of mn = 0
+        xb[0, 0, 7] = 0x3FC0  # bf16 1.5
+        codes, mn, sc = O.int4_pack(xb, O.KIND_VALUE, 64)
+        assert mn[0, 0, 0] == 0x8000 and sc[0, 0, 0] == _f16bits(np.float32(0.1))
+        assert (codes.reshape(-1) == np.where(np.arange(32) == 3, 0xF0, 0)).all()
+        # max over {-0, +0, negatives} is +0
+        xb[0, 0, 7] = 0xBFC0  # bf16 -1.5
+        codes, mn, sc = O.int4_pack(xb, O.KIND_VALUE, 64)
+        assert mn[0, 0, 0] == _f16bits(np.float32(-1.5)) and sc[0, 0, 0] == _f16bits(np.float32(0.1))
+
+
 def test_int4_nibble_order_low_is_even_channel():
     x = np.zeros((1, 1, 64), np.float32)
     x[0, 0, 1] = 15.0  # mn 0, sc 1: channel 1 -> code 15, channel 0 -> 0
