@@ -51,28 +51,24 @@ __device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float
 __device__ __forceinline__ float int4_rcp(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }
 
 // Codes of the two bf16 of w (lo, hi) -> one byte (lo | hi << 4), the same integers
-// as int4_code (0 for a constant group, sc == 0), with the estimate done in f32x2.
+// as int4_code (0 for a constant group, sc == 0).  The estimate, its rounding and its
+// distance to the rounded integer are formed two at a time in f32x2.  No clamp is
+// needed here: x <= max gives q <= 15 * (1 + 2^-22) < 15.5, which rounds to 15.
 __device__ __forceinline__ uint32_t int4_pair(uint32_t w, float mnl, float mnh, float scl, float sch,
                                               float rscl, float rsch) {
-  const uint64_t d2 = add_f32x2(pack_f32x2(w << 16, w & 0xFFFF0000u),
-                                pack_f32x2(__float_as_uint(-mnl), __float_as_uint(-mnh)));
-  uint32_t ql, qh;
-  unpack_f32x2(mul_f32x2(d2, pack_f32x2(__float_as_uint(rscl), __float_as_uint(rsch))), ql, qh);
-  const float qcl = fminf(__uint_as_float(ql), 15.0f), qch = fminf(__uint_as_float(qh), 15.0f);
-  const uint64_t q2 = pack_f32x2(__float_as_uint(qcl), __float_as_uint(qch));
   const uint64_t k2 = pack_f32x2(__float_as_uint(kRound), __float_as_uint(kRound));
+  const uint64_t q2 = mul_f32x2(add_f32x2(pack_f32x2(w << 16, w & 0xFFFF0000u),
+                                          pack_f32x2(__float_as_uint(-mnl), __float_as_uint(-mnh))),
+                                pack_f32x2(__float_as_uint(rscl), __float_as_uint(rsch)));
   const uint64_t t2 = add_f32x2(q2, k2);
-  uint32_t tl, th;
+  uint32_t el, eh, tl, th;
+  unpack_f32x2(sub_f32x2(q2, sub_f32x2(t2, k2)), el, eh);  // estimate - its rounded integer
   unpack_f32x2(t2, tl, th);
-  // distance of each estimate to its rounded integer
-  const float rl = __fsub_rn(__uint_as_float(tl), kRound), rh = __fsub_rn(__uint_as_float(th), kRound);
-  const bool okl = (scl >= 0x1p-126f || scl == 0.0f) && fabsf(__fsub_rn(qcl, rl)) < 0.49999237f;
-  const bool okh = (sch >= 0x1p-126f || sch == 0.0f) && fabsf(__fsub_rn(qch, rh)) < 0.49999237f;
-  uint32_t cl = tl & 15u, ch = th & 15u;
-  if (!(okl && okh)) {
-    cl = scl != 0.0f ? int4_code(bf16lo(w), mnl, scl, rscl) : 0u;
-    ch = sch != 0.0f ? int4_code(bf16hi(w), mnh, sch, rsch) : 0u;
-  }
+  const bool ok = fabsf(__uint_as_float(el)) < 0.49999237f && fabsf(__uint_as_float(eh)) < 0.49999237f &&
+                  (scl >= 0x1p-126f || scl == 0.0f) && (sch >= 0x1p-126f || sch == 0.0f);
+  if (ok) return (tl & 15u) | ((th & 15u) << 4);
+  const uint32_t cl = scl != 0.0f ? int4_code(bf16lo(w), mnl, scl, rscl) : 0u;
+  const uint32_t ch = sch != 0.0f ? int4_code(bf16hi(w), mnh, sch, rsch) : 0u;
   return cl | (ch << 4);
 }
 
@@ -151,30 +147,39 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0u;
       }
     }
-    float mn[8], mx[8];
+    // group minimum / maximum per channel, in the bf16 order keys (-0 below +0)
+    uint32_t kmn[4], kmx[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mn[i] = __int_as_float(0x7F800000);  // +inf
-      mx[i] = __int_as_float(0xFF800000);  // -inf
+    for (int i = 0; i < 4; ++i) {
+      kmn[i] = 0xFFFFFFFFu;
+      kmx[i] = 0u;
     }
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
       if (r0 + rs + k * RS >= r1) continue;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        mn[2 * i] = fminf(mn[2 * i], bf16lo(v[k][i]));
-        mx[2 * i] = fmaxf(mx[2 * i], bf16lo(v[k][i]));
-        mn[2 * i + 1] = fminf(mn[2 * i + 1], bf16hi(v[k][i]));
-        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], bf16hi(v[k][i]));
+        const uint32_t key = bf16x2_key(v[k][i]);
+        kmn[i] = min_u16x2(kmn[i], key);
+        kmx[i] = max_u16x2(kmx[i], key);
       }
     }
 #pragma unroll
     for (int o = CW; o < 32; o <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mn[i] = fminf(mn[i], __shfl_xor_sync(0xFFFFFFFFu, mn[i], o));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xFFFFFFFFu, mx[i], o));
+      for (int i = 0; i < 4; ++i) {
+        kmn[i] = min_u16x2(kmn[i], __shfl_xor_sync(0xFFFFFFFFu, kmn[i], o));
+        kmx[i] = max_u16x2(kmx[i], __shfl_xor_sync(0xFFFFFFFFu, kmx[i], o));
       }
+    }
+    float mn[8], mx[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = bf16x2_unkey(kmn[i]), b = bf16x2_unkey(kmx[i]);
+      mn[2 * i] = bf16lo(a);
+      mn[2 * i + 1] = bf16hi(a);
+      mx[2 * i] = bf16lo(b);
+      mx[2 * i + 1] = bf16hi(b);
     }
     if (!valid) continue;
     float sc[8], rsc[8];
@@ -215,74 +220,114 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
 }
 
 // KEY kind, tiled through shared memory: a block takes one tile (a group of up to G
-// rows x the D channels of one head) at a time.
-//  1. every thread loads 16-byte chunks of the tile (consecutive threads, consecutive
-//     chunks of a row: coalesced; residual mode gathers rows at pos[] and subtracts
-//     prev here) into shared memory;
+// rows x the D channels of one head) at a time, in kStages shared-memory buffers.
+//  1. the tile's rows are copied into shared memory with 16-byte cp.async copies,
+//     all issued at once (consecutive threads, consecutive chunks of a row); with two
+//     stages the next tile's copies are in flight while this tile is coded.  Residual
+//     mode gathers the rows at pos[] from cur and prev into two planes;
 //  2. thread (rq, cp) takes channel pair cp over rows rq, rq + RQ, ... (RQ = 512 / D
-//     row splits; a warp reads consecutive words: no bank conflicts) and leaves its
-//     partial minimum/maximum in shared memory; after a barrier every thread combines
-//     the RQ partials of its pair, so the group's FP32 minimum and scale are known;
+//     row splits; a warp reads consecutive words: no bank conflicts), forms the
+//     residual bf16(cur - prev) in place, and leaves its partial minimum/maximum in
+//     shared memory; after a barrier every thread combines the RQ partials of its
+//     pair, so the group's FP32 minimum and scale are known;
 //  3. each thread codes its rows of the pair (one byte per row, a warp writes 32
 //     consecutive bytes) and the rq == 0 threads write the FP16 metadata.
-template <bool kResidual>
+template <bool kResidual, int kStages>
 __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4EncodeParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int kPlanes = kResidual ? 2 : 1;
   const int D = p.D;
   const int nchunk = D / 8;     // 16-byte chunks per row
-  const int npair = D / 2;      // channel pairs
+  const int npair = D / 2;      // channel pairs = 32-bit words per row
   const int RQ = kThreads / npair;
   const int tid = threadIdx.x;
   const int cp = tid % npair;
   const int rq = tid / npair;
-  uint32_t* tile = reinterpret_cast<uint32_t*>(smem);                 // [G][D/2] bf16x2
-  float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(p.G) * D * 2);  // [2][RQ][D]
+  const int tile_words = p.G * npair;
+  uint32_t* const buf = reinterpret_cast<uint32_t*>(smem);  // [kStages][kPlanes][G][D/2]
+  uint32_t* const part = buf + kStages * kPlanes * tile_words;  // [2][RQ][D/2] keys
   const int32_t ngroups = (p.rows + p.G - 1) / p.G;
   const int64_t ntiles = static_cast<int64_t>(ngroups) * p.H;
-  for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
+
+  // copies of tile `tile_id` into stage `st` (nothing past the last tile)
+  auto issue = [&](int64_t tile_id, int st) {
+    if (tile_id >= ntiles) return;
     const int32_t g = static_cast<int32_t>(tile_id / p.H);
     const int32_t h = static_cast<int32_t>(tile_id % p.H);
     const int32_t r0 = g * p.G;
     const int32_t nr = min(p.G, p.rows - r0);
-    // 1. load the tile
+    uint32_t* const cur = buf + st * kPlanes * tile_words;
     for (int c = tid; c < nr * nchunk; c += kThreads) {
       const int row = c / nchunk;
       const int col = (c % nchunk) * 8;
-      uint32_t w[4];
-      load_chunk8<kResidual>(p, r0 + row, h, col, w);
-      if (col == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
-      *reinterpret_cast<uint4*>(tile + row * npair + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+      uint32_t* const dst = cur + row * npair + col / 2;
+      int64_t src = r0 + row;
+      if constexpr (kResidual) {
+        if (p.pos != nullptr) src = LDX(p.pos + r0 + row);
+        if (src < 0 || src >= p.src_rows) {  // a bad position codes zeros (and is flagged)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(dst + tile_words) = make_uint4(0u, 0u, 0u, 0u);
+          continue;
+        }
+        cp_async16(dst + tile_words,
+                   p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col);
+      }
+      cp_async16(dst, p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col);
+    }
+  };
+
+  int64_t tile_id = blockIdx.x;
+  issue(tile_id, 0);
+  cp_async_commit();
+  if constexpr (kStages == 2) {
+    issue(tile_id + gridDim.x, 1);
+    cp_async_commit();
+  }
+  for (int it = 0; tile_id < ntiles; tile_id += gridDim.x, ++it) {
+    const int st = kStages == 2 ? (it & 1) : 0;
+    if constexpr (kStages == 2) {
+      cp_async_wait<1>();  // this tile's group is complete; the next may be in flight
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    // 2. column minimum and maximum of the pair
-    float mnl = __int_as_float(0x7F800000), mnh = mnl;
-    float mxl = __int_as_float(0xFF800000), mxh = mxl;
+    const int32_t g = static_cast<int32_t>(tile_id / p.H);
+    const int32_t h = static_cast<int32_t>(tile_id % p.H);
+    const int32_t r0 = g * p.G;
+    const int32_t nr = min(p.G, p.rows - r0);
+    uint32_t* const tile = buf + st * kPlanes * tile_words;
+    // 2. column minimum and maximum of the pair in bf16 order keys (-0 below +0;
+    //    residual: the difference is formed first)
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
     if (rq < RQ) {
       for (int row = rq; row < nr; row += RQ) {
-        const uint32_t v = tile[row * npair + cp];
-        mnl = fminf(mnl, bf16lo(v));
-        mxl = fmaxf(mxl, bf16lo(v));
-        mnh = fminf(mnh, bf16hi(v));
-        mxh = fmaxf(mxh, bf16hi(v));
+        uint32_t v = tile[row * npair + cp];
+        if constexpr (kResidual) {
+          const uint32_t q = tile[tile_words + row * npair + cp];
+          v = pack_bf16x2(__fsub_rn(bf16lo(v), bf16lo(q)), __fsub_rn(bf16hi(v), bf16hi(q)));
+          tile[row * npair + cp] = v;  // read back by this same thread in step 3
+        }
+        const uint32_t key = bf16x2_key(v);
+        kmn = min_u16x2(kmn, key);
+        kmx = max_u16x2(kmx, key);
       }
-      part[(0 * RQ + rq) * D + 2 * cp] = mnl;
-      part[(0 * RQ + rq) * D + 2 * cp + 1] = mnh;
-      part[(1 * RQ + rq) * D + 2 * cp] = mxl;
-      part[(1 * RQ + rq) * D + 2 * cp + 1] = mxh;
+      part[rq * npair + cp] = kmn;
+      part[(RQ + rq) * npair + cp] = kmx;
     }
     __syncthreads();
     if (rq < RQ) {
       for (int k = 0; k < RQ; ++k) {
-        mnl = fminf(mnl, part[(0 * RQ + k) * D + 2 * cp]);
-        mnh = fminf(mnh, part[(0 * RQ + k) * D + 2 * cp + 1]);
-        mxl = fmaxf(mxl, part[(1 * RQ + k) * D + 2 * cp]);
-        mxh = fmaxf(mxh, part[(1 * RQ + k) * D + 2 * cp + 1]);
+        kmn = min_u16x2(kmn, part[k * npair + cp]);
+        kmx = max_u16x2(kmx, part[(RQ + k) * npair + cp]);
       }
+      const uint32_t wmn = bf16x2_unkey(kmn), wmx = bf16x2_unkey(kmx);
+      const float mnl = bf16lo(wmn), mnh = bf16hi(wmn), mxl = bf16lo(wmx), mxh = bf16hi(wmx);
       const float scl = __fdiv_rn(__fsub_rn(mxl, mnl), 15.0f);
       const float sch = __fdiv_rn(__fsub_rn(mxh, mnh), 15.0f);
       const float rsl = int4_rcp(scl), rsh = int4_rcp(sch);
       // 3. codes of this thread's rows
       for (int row = rq; row < nr; row += RQ) {
+        if (cp == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
         const uint32_t byte = int4_pair(tile[row * npair + cp], mnl, mnh, scl, sch, rsl, rsh);
         STX(p.dst.codes + (static_cast<int64_t>(r0 + row) * p.H + h) * npair + cp, static_cast<uint8_t>(byte));
       }
@@ -294,8 +339,11 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
             static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16));
       }
     }
-    __syncthreads();  // the tile buffer is reused
+    __syncthreads();  // stage st and the partials are free again
+    issue(tile_id + static_cast<int64_t>(kStages) * gridDim.x, st);
+    cp_async_commit();
   }
+  cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
 }
 
 // VALUE kind: one lane per 16-channel block of a row; a group spans W = min(G/16, L)
@@ -341,23 +389,30 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     uint32_t nw[8];
     load_row(row + stride, nw);  // the next row's loads before this row's arithmetic
     if (valid && b == 0 && h == 0) check_pos<kResidual>(p, r);
-    float lmn = __int_as_float(0x7F800000), lmx = __int_as_float(0xFF800000);
+    // the group's minimum and maximum in bf16 order keys (-0 below +0); one word
+    // carries the minimum key (low half) and the complemented maximum key (high half),
+    // so a single unsigned min per butterfly round reduces both
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
     if (valid) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        lmn = fminf(lmn, fminf(bf16lo(w[i]), bf16hi(w[i])));
-        lmx = fmaxf(lmx, fmaxf(bf16lo(w[i]), bf16hi(w[i])));
+        const uint32_t key = bf16x2_key(w[i]);
+        kmn = min_u16x2(kmn, key);
+        kmx = max_u16x2(kmx, key);
       }
     }
-    for (int o = 1; o < W; o <<= 1) {  // W is uniform: every lane runs the same shuffles
-      lmn = fminf(lmn, __shfl_xor_sync(0xFFFFFFFFu, lmn, o));
-      lmx = fmaxf(lmx, __shfl_xor_sync(0xFFFFFFFFu, lmx, o));
-    }
+    kmn = min_u16x2(kmn, __byte_perm(kmn, 0u, 0x1032));  // both halves: the lane minimum
+    kmx = max_u16x2(kmx, __byte_perm(kmx, 0u, 0x1032));
+    uint32_t mm = (kmn & 0xFFFFu) | (~kmx << 16);
+    for (int o = 1; o < W; o <<= 1)  // W is uniform: every lane runs the same shuffles
+      mm = min_u16x2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
     if (!valid) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = nw[i];
       continue;
     }
+    const uint32_t mnmx = bf16x2_unkey(mm ^ 0xFFFF0000u);  // low: minimum, high: maximum
+    const float lmn = bf16lo(mnmx), lmx = bf16hi(mnmx);
     const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
     const float rsc = int4_rcp(sc);
     uint32_t c0 = 0u, c1 = 0u;
@@ -426,15 +481,18 @@ cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s)
   return e;
 }
 
-// Shared memory of one tile: G x D bf16 plus the [2][RQ][D] float partials.
-size_t key_tile_smem(int G, int D) {
-  return static_cast<size_t>(G) * D * 2 + 2 * static_cast<size_t>(kThreads / (D / 2)) * D * 4;
+// Shared memory of the tile kernel: kStages x planes tiles of G x D bf16, plus the
+// [2][RQ][D/2] partial key words.
+size_t key_tile_smem(int G, int D, int stages, int planes) {
+  return static_cast<size_t>(stages) * planes * G * D * 2 + 2 * static_cast<size_t>(kThreads / (D / 2)) * D * 2;
 }
 
-template <bool kRes>
+constexpr size_t kTileSmemCap = 110 * 1024;  // two blocks per SM at least
+
+template <bool kRes, int kStages>
 cudaError_t key_tile_launch(const Int4EncodeParams& p, cudaStream_t s) {
-  auto k = int4_key_tile_kernel<kRes>;
-  const size_t smem = key_tile_smem(p.G, p.D);
+  auto k = int4_key_tile_kernel<kRes, kStages>;
+  const size_t smem = key_tile_smem(p.G, p.D, kStages, kRes ? 2 : 1);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -452,8 +510,9 @@ cudaError_t key_tile_launch(const Int4EncodeParams& p, cudaStream_t s) {
 
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
-  // a tile of up to 96 KB of shared memory (64 rows x 256 channels, 128 x 128, ...)
-  if (p.D >= 16 && key_tile_smem(p.G, p.D) <= 96 * 1024) return key_tile_launch<kRes>(p, s);
+  const int planes = kRes ? 2 : 1;
+  if (p.D >= 16 && key_tile_smem(p.G, p.D, 2, planes) <= kTileSmemCap) return key_tile_launch<kRes, 2>(p, s);
+  if (p.D >= 16 && key_tile_smem(p.G, p.D, 1, planes) <= kTileSmemCap) return key_tile_launch<kRes, 1>(p, s);
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
   switch (p.G) {  // RS = G / RPL lanes per column task
     case 16: return key_launch<kRes, 2, 8>(p, ntask, s);

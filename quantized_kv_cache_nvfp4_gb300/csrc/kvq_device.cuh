@@ -416,6 +416,33 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Order keys of two packed finite bf16: a positive value keeps its bits with the top
+// bit set, a negative one is complemented, so the unsigned order of the 16-bit keys
+// is the order of the values with -0 (key 0x7FFF) below +0 (key 0x8000) -- the total
+// order of IEEE 754-2019 minimum/maximum.  bf16x2_unkey inverts it.
+__device__ __forceinline__ uint32_t bf16x2_key(uint32_t w) {
+  return w ^ (((w >> 15) & 0x00010001u) * 0x7FFFu + 0x80008000u);
+}
+__device__ __forceinline__ uint32_t bf16x2_unkey(uint32_t k) {
+  return k ^ (((~k >> 15) & 0x00010001u) * 0x7FFFu + 0x80008000u);
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // INT4 decode of 8 codes (one word, low nibble first) with per-element minimum and
 // scale: y = bf16(code * sc + mn), a multiply then an add, each rounded (no FMA).
 __device__ __forceinline__ void int4_decode8(uint32_t cw, const float (&mn)[8], const float (&sc)[8],
@@ -466,6 +493,26 @@ __device__ __forceinline__ void load16B(const void* p, uint32_t (&w)[4]) {
   asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                : "l"(p));
+}
+
+// 16-byte asynchronous copy global -> shared memory through L2 only (cp.async.cg).
+// It lands by the cp.async.wait_group that covers its commit group; the hardware
+// tracks it, so no wait in this code spins.  The checked build stores zeros instead
+// of copying from outside a registered range.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  if (!KVQ_OK(gsrc, 16, 16)) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
+    return;
+  }
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // 16-byte load through the coherent path (for rows this launch also writes).

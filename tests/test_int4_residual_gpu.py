@@ -239,3 +239,43 @@ def test_int4_half_integer_quotients_round_to_even(scale):
         codes, mn, sc = O.int4_pack(xb, kind, 64)
         check_int4(pk, codes, mn, sc)
         np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
+
+
+def _signed_zero_mix(T, H, D, seed):
+    """bf16 bits: every element a zero of random sign, then 30% of the elements a
+    positive value, and in the second head's last 64 rows the values negative; the
+    first 64 rows of head 0 stay zeros only."""
+    rng = np.random.default_rng(seed)
+    xb = (rng.integers(0, 2, size=(T, H, D)).astype(np.uint16) << 15).astype(np.uint16)
+    mag = O.f32_to_bf16(np.abs(rng.standard_normal((T, H, D))).astype(np.float32) + 0.01)
+    pick = rng.random((T, H, D)) < 0.3
+    pick[:64, 0] = False
+    xb[pick] = mag[pick]
+    neg = pick.copy()
+    neg[:-64] = False
+    neg[:, 0] = False
+    xb[neg] |= 0x8000
+    return xb
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_signed_zero_groups_match_the_oracle(kind):
+    """Groups whose minimum is a zero held with both signs: the stored FP16 minimum is
+    -0 (the -0 < +0 order), in the plain pack and in the residual pack."""
+    T, H, D = 256, 2, 128
+    xb = _signed_zero_mix(T, H, D, seed=12)
+    x = synth.from_bits(xb).to(DEV)
+    pk, y = gpu_int4_pack(x, kind)
+    codes, mn, sc = O.int4_pack(xb, kind, 64)
+    assert (mn == 0x8000).any()
+    check_int4(pk, codes, mn, sc)
+    np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
+    # residual: cur - prev gives -0 where cur is -0 and prev is +0
+    prev_b = np.zeros_like(xb)
+    pos = torch.arange(0, T, 2, dtype=torch.int32)
+    pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 2, H, D, 64)
+    kvq.kvq_encode_residual(x, synth.from_bits(prev_b).to(DEV), pos.to(DEV), pay)
+    torch.cuda.synchronize()
+    opay, ost = O.residual_encode(xb, prev_b, pos.numpy(), kvq.FMT_INT4, kind, 64)
+    assert ost == 0
+    check_payload(pay, opay)
