@@ -93,12 +93,12 @@ typedef struct {
   int64_t head_pitch;
 } kvq_bf16_out;
 
-/* One tensor's planes in a paged pool, slot-major.  fmt NVFP4:
+/* One tensor's planes in a paged pool, slot-major.  Format NVFP4:
  *   codes  [num_slots][num_heads][head_dim/2]   E2M1 nibbles, low nibble = even element
  *   bscale [num_slots][num_heads][head_dim/16]  E4M3 block scales
  *   rscale [num_slots][num_heads]               FP32 row scales
- * fmt FP8: codes [num_slots][num_heads][head_dim] E4M3 bytes, rscale as above, bscale
- * unused (may be NULL).
+ * Format FP8: codes [num_slots][num_heads][head_dim] E4M3 bytes, rscale as above,
+ * bscale unused (may be NULL).
  * Slot = block * block_size + offset.  Every plane used must be 16-byte aligned. */
 typedef struct {
   uint8_t* codes;
@@ -113,7 +113,9 @@ typedef struct {
   int32_t block_size; /* tokens per page (16 in the pages' pools) */
   int32_t num_heads;
   int32_t head_dim;   /* a multiple of 16, at most 512 */
-  int32_t fmt;        /* KVQ_FMT_NVFP4 or KVQ_FMT_FP8 */
+  int32_t fmt;        /* format of the K plane: KVQ_FMT_NVFP4 or KVQ_FMT_FP8 */
+  int32_t v_fmt;      /* format of the V plane; 0 = the same as fmt.  FP8 K with NVFP4 V
+                         is the k8v4 split of the FreeToken page (fp8 store notes) */
 } kvq_pool;
 
 /* A logical (non-paged) packed tensor [rows][heads][dim], caller-allocated.
@@ -140,8 +142,8 @@ typedef struct {
   float* rscale;
 } kvq_packed;
 
-/* Fused quantise + scatter of K and V into a paged pool (the encode hot path), in
- * the pool's format (NVFP4, or FP8 E4M3 with one FP32 scale per row).
+/* Fused quantise + scatter of K and V into a paged pool (the encode hot path), each
+ * in its plane's format (NVFP4, or FP8 E4M3 with one FP32 scale per row).
  * Source: FreeToken PR #408, Summary ("CUDA Graph-safe KV writes") and the fp8 store
  * notes (slot ids arrive as a device tensor; one launch under graph capture).
  *   k, v       bf16 [num_tokens][num_heads][head_dim] views; either may be NULL
@@ -150,7 +152,8 @@ typedef struct {
  *              negative id skips the token (padding); an id >= num_slots skips it
  *              and sets KVQ_DEV_BAD_SLOT.  Duplicate ids: undefined last writer.
  *   pool       planes written in place (only the rows of the given slots).
- * One kernel launch; num_tokens == 0 launches nothing. */
+ * One kernel launch (two when K and V planes have different formats); num_tokens ==
+ * 0 launches nothing. */
 KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v, int32_t num_tokens,
                              const int64_t* slot_ids, const kvq_pool* pool,
                              uint32_t* dev_status, kvq_stream_t stream);
@@ -164,7 +167,8 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
  *                s * max_seq_len + t receives token t of sequence s.  Either may be
  *                NULL (that tensor is not restored); not both.
  * NVFP4: y = bf16(e2m1 * block_scale * row_scale), the product rounded once in fp32;
- * FP8: y = bf16(e4m3 * row_scale).
+ * FP8: y = bf16(e4m3 * row_scale).  One launch (two when K and V planes have
+ * different formats).
  * Rows with a bad block id are skipped (KVQ_DEV_BAD_BLOCK); a sequence with a bad
  * length is skipped whole (KVQ_DEV_BAD_SEQLEN). */
 KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table, int32_t num_seqs,

@@ -83,7 +83,8 @@ def _bf16_out(t: torch.Tensor, name: str):
 # ---------------------------------------------------------------------------
 @dataclass
 class KvPool:
-    """Paged K/V planes of one format, slot-major (slot = block * block_size + offset).
+    """Paged K/V planes, slot-major (slot = block * block_size + offset); each plane in
+    its own format (fmt for K, v_fmt for V; v_fmt None = the same as fmt).
 
     NVFP4: codes [slots, H, D/2] u8, bscale [slots, H, D/16] u8 (E4M3), rscale [slots, H] f32.
     FP8:   codes [slots, H, D] u8 (E4M3), rscale [slots, H] f32 (no block scales)."""
@@ -96,10 +97,12 @@ class KvPool:
     v_rscale: torch.Tensor
     block_size: int
     fmt: int = FMT_NVFP4
+    v_fmt: Optional[int] = None
 
     @classmethod
     def empty(cls, num_slots: int, num_heads: int, head_dim: int, block_size: int = 16,
-              device="cuda", fill: Optional[int] = None, fmt: int = FMT_NVFP4) -> "KvPool":
+              device="cuda", fill: Optional[int] = None, fmt: int = FMT_NVFP4,
+              v_fmt: Optional[int] = None) -> "KvPool":
         def u8(*shape):
             t = torch.empty(shape, dtype=torch.uint8, device=device)
             return t.fill_(fill) if fill is not None else t
@@ -110,12 +113,13 @@ class KvPool:
                 t.view(torch.uint8).fill_(fill)
             return t
 
-        if fmt == FMT_FP8:
-            return cls(u8(num_slots, num_heads, head_dim), None, f32(num_slots, num_heads),
-                       u8(num_slots, num_heads, head_dim), None, f32(num_slots, num_heads), block_size, fmt)
-        return cls(u8(num_slots, num_heads, head_dim // 2), u8(num_slots, num_heads, head_dim // 16),
-                   f32(num_slots, num_heads), u8(num_slots, num_heads, head_dim // 2),
-                   u8(num_slots, num_heads, head_dim // 16), f32(num_slots, num_heads), block_size, fmt)
+        def plane(f):
+            if f == FMT_FP8:
+                return u8(num_slots, num_heads, head_dim), None, f32(num_slots, num_heads)
+            return (u8(num_slots, num_heads, head_dim // 2), u8(num_slots, num_heads, head_dim // 16),
+                    f32(num_slots, num_heads))
+
+        return cls(*plane(fmt), *plane(fmt if v_fmt is None else v_fmt), block_size, fmt, v_fmt)
 
     @property
     def num_slots(self) -> int:
@@ -144,7 +148,8 @@ class KvPool:
         return _abi.Pool(
             _abi.Plane(self.k_codes.data_ptr(), bs(self.k_bscale), self.k_rscale.data_ptr()),
             _abi.Plane(self.v_codes.data_ptr(), bs(self.v_bscale), self.v_rscale.data_ptr()),
-            self.num_slots, self.block_size, self.num_heads, self.head_dim, self.fmt)
+            self.num_slots, self.block_size, self.num_heads, self.head_dim, self.fmt,
+            0 if self.v_fmt is None else self.v_fmt)
 
 
 Nvfp4Pool = KvPool  # the NVFP4 pool is the default format of KvPool

@@ -50,6 +50,7 @@ class Pool(ctypes.Structure):
         ("num_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("fmt", ctypes.c_int32),
+        ("v_fmt", ctypes.c_int32),
     ]
 
 

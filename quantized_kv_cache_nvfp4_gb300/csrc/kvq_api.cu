@@ -121,15 +121,26 @@ kvq_status check_head_dim(int32_t H, int32_t D) {
 }
 
 // A pool's format and planes (the bscale plane only for NVFP4).
+bool pool_fmt_ok(int32_t f) { return f == KVQ_FMT_NVFP4 || f == KVQ_FMT_FP8; }
+
 kvq_status check_pool_fmt(const kvq_pool* pool) {
-  if (pool->fmt != KVQ_FMT_NVFP4 && pool->fmt != KVQ_FMT_FP8)
+  if (!pool_fmt_ok(pool->fmt))
     return fail(KVQ_ERR_INVALID_ARG, "pool fmt must be KVQ_FMT_NVFP4 or KVQ_FMT_FP8 (got %d)", pool->fmt);
+  if (pool->v_fmt != 0 && !pool_fmt_ok(pool->v_fmt))
+    return fail(KVQ_ERR_INVALID_ARG, "pool v_fmt must be 0, KVQ_FMT_NVFP4 or KVQ_FMT_FP8 (got %d)",
+                pool->v_fmt);
   return KVQ_OK;
 }
-kvq_status check_pool_plane(const kvq_pool* pool, const kvq_plane* pl) {
+
+// Format of plane j (0 = K, 1 = V).
+int32_t plane_fmt(const kvq_pool* pool, int j) {
+  return (j == 1 && pool->v_fmt != 0) ? pool->v_fmt : pool->fmt;
+}
+
+kvq_status check_pool_plane(int32_t fmt, const kvq_plane* pl) {
   kvq_status st;
   if ((st = check_plane(pl->codes, "pool codes")) != KVQ_OK) return st;
-  if (pool->fmt == KVQ_FMT_NVFP4 && (st = check_plane(pl->bscale, "pool bscale")) != KVQ_OK) return st;
+  if (fmt == KVQ_FMT_NVFP4 && (st = check_plane(pl->bscale, "pool bscale")) != KVQ_OK) return st;
   return check_plane(pl->rscale, "pool rscale");
 }
 int64_t code_bytes_per_row(int32_t fmt, int32_t D) { return fmt == KVQ_FMT_FP8 ? D : D / 2; }
@@ -219,27 +230,14 @@ int num_sms() {
 
 using namespace kvq;
 
-extern "C" {
+namespace {
 
-KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
-                                     int32_t num_tokens, const int64_t* slot_ids,
-                                     const kvq_pool* pool, uint32_t* dev_status,
-                                     kvq_stream_t stream) {
-  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
-  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
-  if (k == nullptr && v == nullptr) return fail(KVQ_ERR_INVALID_ARG, "both k and v are NULL");
-  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_tokens");
-  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
-  if (st != KVQ_OK) return st;
-  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
-  if (num_tokens == 0) return KVQ_OK;
+// Scatter of the given tensors (K and/or V), whose planes share format fmt.
+kvq_status scatter_impl(const kvq_bf16_in* k, const kvq_bf16_in* v, int32_t num_tokens,
+                        const int64_t* slot_ids, const kvq_pool* pool, int32_t fmt,
+                        uint32_t* dev_status, kvq_stream_t stream) {
+  kvq_status st;
   const int ntensors = (k != nullptr) + (v != nullptr);
-  if (!fits_u31(static_cast<int64_t>(num_tokens) * pool->num_heads * ntensors))
-    return fail(KVQ_ERR_UNSUPPORTED, "num_tokens x heads too large");
-  if ((st = check_dev(slot_ids, "slot_ids")) != KVQ_OK) return st;
-  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
-
   EncodeParams p{};
   bool v8 = true;
   int i = 0;
@@ -250,7 +248,7 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
     if (src[j] == nullptr) continue;
     if ((st = check_view(src[j]->ptr, src[j]->row_pitch, src[j]->head_pitch, names[j], v8)) != KVQ_OK)
       return st;
-    if ((st = check_pool_plane(pool, dst[j])) != KVQ_OK) return st;
+    if ((st = check_pool_plane(fmt, dst[j])) != KVQ_OK) return st;
     EncodeTensor& t = p.ten[i++];
     t.x = static_cast<const uint16_t*>(src[j]->ptr);
     t.row_pitch = src[j]->row_pitch;
@@ -270,39 +268,22 @@ KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
     if (src[j] == nullptr) continue;
     dbg_add(src[j]->ptr, view_bytes(num_tokens, src[j]->row_pitch, pool->num_heads, src[j]->head_pitch, pool->head_dim), names[j]);
     const int64_t rh = pool->num_slots * pool->num_heads;
-    dbg_add(dst[j]->codes, rh * code_bytes_per_row(pool->fmt, pool->head_dim), "pool codes");
-    if (pool->fmt == KVQ_FMT_NVFP4) dbg_add(dst[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(dst[j]->codes, rh * code_bytes_per_row(fmt, pool->head_dim), "pool codes");
+    if (fmt == KVQ_FMT_NVFP4) dbg_add(dst[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
     dbg_add(dst[j]->rscale, rh * 4, "pool rscale");
   }
   dbg_add(slot_ids, 8ll * num_tokens, "slot_ids");
   dbg_add(dev_status, 4, "status");
-  return launched(launch_nvfp4_encode(p, kEncScatter, pool->fmt, v8,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  return launched(launch_nvfp4_encode(p, kEncScatter, fmt, v8, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table,
-                               int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
-                               int32_t max_seq_len, const kvq_bf16_out* k_out,
-                               const kvq_bf16_out* v_out, uint32_t* dev_status,
-                               kvq_stream_t stream) {
-  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
-  if (k_out == nullptr && v_out == nullptr)
-    return fail(KVQ_ERR_INVALID_ARG, "both k_out and v_out are NULL");
-  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
-  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
-  if (st != KVQ_OK) return st;
-  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
-  if (num_seqs < 0 || max_blocks < 0 || max_seq_len < 0)
-    return fail(KVQ_ERR_INVALID_ARG, "negative num_seqs, max_blocks or max_seq_len");
-  if (num_seqs == 0 || max_seq_len == 0) return KVQ_OK;
+// Restore of the given tensors (K and/or V), whose planes share format fmt.
+kvq_status restore_impl(const kvq_pool* pool, const int32_t* block_table, int32_t num_seqs,
+                        int32_t max_blocks, const int32_t* seq_lens, int32_t max_seq_len,
+                        const kvq_bf16_out* k_out, const kvq_bf16_out* v_out, int32_t fmt,
+                        uint32_t* dev_status, kvq_stream_t stream) {
+  kvq_status st;
   const int ntensors = (k_out != nullptr) + (v_out != nullptr);
-  if (!fits_u31(static_cast<int64_t>(num_seqs) * max_seq_len * pool->num_heads * ntensors))
-    return fail(KVQ_ERR_UNSUPPORTED, "num_seqs x max_seq_len x heads too large");
-  if ((st = check_dev(block_table, "block_table")) != KVQ_OK) return st;
-  if ((st = check_dev(seq_lens, "seq_lens")) != KVQ_OK) return st;
-  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
-
   DecodeParams p{};
   bool v8 = true;
   int i = 0;
@@ -313,7 +294,7 @@ KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table,
     if (out[j] == nullptr) continue;
     if ((st = check_view(out[j]->ptr, out[j]->row_pitch, out[j]->head_pitch, names[j], v8)) != KVQ_OK)
       return st;
-    if ((st = check_pool_plane(pool, src[j])) != KVQ_OK) return st;
+    if ((st = check_pool_plane(fmt, src[j])) != KVQ_OK) return st;
     DecodeTensor& t = p.ten[i++];
     t.codes = src[j]->codes;
     t.bscale = src[j]->bscale;
@@ -344,15 +325,80 @@ KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table,
     if (out[j] == nullptr) continue;
     dbg_add(out[j]->ptr, view_bytes(static_cast<int64_t>(num_seqs) * max_seq_len, out[j]->row_pitch, pool->num_heads, out[j]->head_pitch, pool->head_dim), names[j]);
     const int64_t rh = pool->num_slots * pool->num_heads;
-    dbg_add(src[j]->codes, rh * code_bytes_per_row(pool->fmt, pool->head_dim), "pool codes");
-    if (pool->fmt == KVQ_FMT_NVFP4) dbg_add(src[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
+    dbg_add(src[j]->codes, rh * code_bytes_per_row(fmt, pool->head_dim), "pool codes");
+    if (fmt == KVQ_FMT_NVFP4) dbg_add(src[j]->bscale, rh * (pool->head_dim / 16), "pool bscale");
     dbg_add(src[j]->rscale, rh * 4, "pool rscale");
   }
   dbg_add(block_table, 4ll * num_seqs * max_blocks, "block_table");
   dbg_add(seq_lens, 4ll * num_seqs, "seq_lens");
   dbg_add(dev_status, 4, "status");
-  return launched(launch_nvfp4_decode(p, kDecRestore, pool->fmt, v8,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  return launched(launch_nvfp4_decode(p, kDecRestore, fmt, v8, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+KVQ_API kvq_status kvq_quant_scatter(const kvq_bf16_in* k, const kvq_bf16_in* v,
+                                     int32_t num_tokens, const int64_t* slot_ids,
+                                     const kvq_pool* pool, uint32_t* dev_status,
+                                     kvq_stream_t stream) {
+  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
+  if (k == nullptr && v == nullptr) return fail(KVQ_ERR_INVALID_ARG, "both k and v are NULL");
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_tokens");
+  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
+  if (st != KVQ_OK) return st;
+  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
+  if (num_tokens == 0) return KVQ_OK;
+  const int ntensors = (k != nullptr) + (v != nullptr);
+  if (!fits_u31(static_cast<int64_t>(num_tokens) * pool->num_heads * ntensors))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_tokens x heads too large");
+  if ((st = check_dev(slot_ids, "slot_ids")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+  const int32_t fk = plane_fmt(pool, 0), fv = plane_fmt(pool, 1);
+  if (k != nullptr && v != nullptr && fk != fv) {  // split formats: one launch per plane
+    if ((st = scatter_impl(k, nullptr, num_tokens, slot_ids, pool, fk, dev_status, stream)) != KVQ_OK)
+      return st;
+    return scatter_impl(nullptr, v, num_tokens, slot_ids, pool, fv, dev_status, stream);
+  }
+  return scatter_impl(k, v, num_tokens, slot_ids, pool, k != nullptr ? fk : fv, dev_status, stream);
+}
+
+KVQ_API kvq_status kvq_restore(const kvq_pool* pool, const int32_t* block_table,
+                               int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
+                               int32_t max_seq_len, const kvq_bf16_out* k_out,
+                               const kvq_bf16_out* v_out, uint32_t* dev_status,
+                               kvq_stream_t stream) {
+  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (k_out == nullptr && v_out == nullptr)
+    return fail(KVQ_ERR_INVALID_ARG, "both k_out and v_out are NULL");
+  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
+  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
+  if (st != KVQ_OK) return st;
+  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
+  if (num_seqs < 0 || max_blocks < 0 || max_seq_len < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "negative num_seqs, max_blocks or max_seq_len");
+  if (num_seqs == 0 || max_seq_len == 0) return KVQ_OK;
+  const int ntensors = (k_out != nullptr) + (v_out != nullptr);
+  if (!fits_u31(static_cast<int64_t>(num_seqs) * max_seq_len * pool->num_heads * ntensors))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_seqs x max_seq_len x heads too large");
+  if ((st = check_dev(block_table, "block_table")) != KVQ_OK) return st;
+  if ((st = check_dev(seq_lens, "seq_lens")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+
+  const int32_t fk = plane_fmt(pool, 0), fv = plane_fmt(pool, 1);
+  if (k_out != nullptr && v_out != nullptr && fk != fv) {  // split formats: one launch per plane
+    if ((st = restore_impl(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, k_out,
+                           nullptr, fk, dev_status, stream)) != KVQ_OK)
+      return st;
+    return restore_impl(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, nullptr, v_out,
+                        fv, dev_status, stream);
+  }
+  return restore_impl(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, k_out, v_out,
+                      k_out != nullptr ? fk : fv, dev_status, stream);
 }
 
 KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_stream_t stream) {

@@ -81,9 +81,14 @@ def test_host_checks_fail_before_any_cuda_call(kvq_lib_path):
     pool.head_dim, pool.fmt = 128, 2  # INT4 is not a pool format
     assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
     assert b"pool fmt" in lib.kvq_last_error()
-    pool.fmt = 1
+    pool.fmt, pool.v_fmt = 1, 2  # nor is it a V-plane format
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
+    assert b"v_fmt" in lib.kvq_last_error()
+    pool.v_fmt, pool.num_slots = 3, 64  # FP8 V beside NVFP4 K is accepted ...
+    assert lib.kvq_quant_scatter(ctypes.byref(x), None, 4, None, ctypes.byref(pool), None, None) == 1
+    assert b"slot_ids is NULL" in lib.kvq_last_error()  # ... and the call stops at the slot ids
+    pool.v_fmt = 0
     # zero-sized work is a no-op that needs no pointers
-    pool.num_slots = 64
     assert lib.kvq_quant_scatter(ctypes.byref(x), None, 0, None, ctypes.byref(pool), None, None) == 0
     pk = _abi.Packed(2, 0, 64, 0, 2, 128, None, None, None, None)
     assert lib.kvq_pack(ctypes.byref(x), ctypes.byref(pk), None) == 0

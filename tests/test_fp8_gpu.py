@@ -294,3 +294,58 @@ def test_fp8_long_context_sampled():
     c, r = O.fp8_encode_rows(bits(k.index_select(0, ti)))
     assert_fp8_rows(u8(pk.codes.index_select(0, ti)), pk.rscale.index_select(0, ti), c, r)
     np.testing.assert_array_equal(bits(ko[0].index_select(0, ti)), O.fp8_decode_rows(c, r))
+
+
+# ---------------------------------------------------------------------------
+# k8v4: FP8 K beside NVFP4 V in one pool
+# ---------------------------------------------------------------------------
+def test_k8v4_split_pool_scatter_restore_and_graph():
+    """FP8 E4M3 keys and NVFP4 values in one pool (two launches per call), ragged
+    sequences through a shuffled block table; eager and graph-captured calls agree."""
+    H, D, bs, S, Tmax = 4, 128, 16, 3, 90
+    lens = torch.tensor([90, 47, 16], dtype=torch.int32)
+    mb = -(-Tmax // bs)
+    nblocks = S * mb + 2
+    table = synth.block_permutation(nblocks, 71)[: S * mb].view(S, mb).contiguous()
+    k = synth.normal_bf16((S, Tmax, H, D), 71, synth.STREAM_K, 0.01, 20.0)
+    v = synth.normal_bf16((S, Tmax, H, D), 71, synth.STREAM_V, 0.01, 20.0)
+    pool = kvq.KvPool.empty(nblocks * bs, H, D, bs, fill=POISON, fmt=FP8, v_fmt=kvq.FMT_NVFP4)
+    assert pool.k_bscale is None and pool.v_bscale.shape == (nblocks * bs, H, D // 16)
+    assert pool.nbytes() == nblocks * bs * H * ((D + 4) + (D // 2 + D // 16 + 4))
+    st = status_word()
+    for s in range(S):
+        n = int(lens[s])
+        t = torch.arange(n)
+        slots = (table[s, t // bs].long() * bs + t % bs).to(DEV)
+        kvq.kvq_quant_scatter(k[s, :n].to(DEV), v[s, :n].to(DEV), slots, pool, st)
+    ko, vo = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
+    kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko, vo, st)
+    ko2, vo2 = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko2, vo2, st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kpool = (np.ascontiguousarray(u8(pool.k_codes)), np.ascontiguousarray(pool.k_rscale.cpu().numpy()))
+    vpool = (np.ascontiguousarray(u8(pool.v_codes)), np.ascontiguousarray(u8(pool.v_bscale)),
+             np.ascontiguousarray(pool.v_rscale.cpu().numpy()))
+    for s in range(S):  # the pool rows are the oracle's encodings of the tokens
+        n = int(lens[s])
+        t = np.arange(n)
+        sl = table.numpy()[s, t // bs].astype(np.int64) * bs + t % bs
+        c, r = O.fp8_encode_rows(bits(k[s, :n]))
+        assert_fp8_rows(kpool[0][sl], kpool[1][sl], c, r, "K")
+        c, b, r = O.nvfp4_encode_rows(bits(v[s, :n]))
+        np.testing.assert_array_equal(vpool[0][sl], c)
+        np.testing.assert_array_equal(vpool[1][sl], b)
+        np.testing.assert_array_equal(f32bits(vpool[2][sl]), f32bits(r))
+    blank = lambda: np.full((S, Tmax, H, D), 0xA5A5, np.uint16)
+    wk, ost = O.fp8_restore(kpool, bs, table.numpy(), lens.numpy(), Tmax, out=blank())
+    assert ost == 0
+    wv, ost = O.nvfp4_restore(vpool, bs, table.numpy(), lens.numpy(), Tmax, out=blank())
+    assert ost == 0
+    for out in (ko, ko2):
+        np.testing.assert_array_equal(bits(out), wk)
+    for out in (vo, vo2):
+        np.testing.assert_array_equal(bits(out), wv)
