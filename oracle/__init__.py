@@ -85,6 +85,8 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_residual_encode": (_U32, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
         "orc_residual_decode": (_U32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _P]),
         "orc_storage_bytes": (_I64, [_I, _I, _I, _I64, _I, _I]),
+        "orc_decode_attention": (_U32, [_P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I, _I, _P, _I, _I,
+                                        _P, _P, _I, ctypes.c_double, _P]),
         "orc_fp8_encode_rows": (None, [_P, _I64, _I, _P, _P]),
         "orc_fp8_decode_rows": (None, [_P, _P, _I64, _I, _P]),
         "orc_fp8_scatter": (_U32, [_P, _I64, _I64, _I, _I, _I, _P, _I64, _P, _P]),
@@ -365,6 +367,36 @@ def residual_decode(payload, prev, out=None):
         _ptr(payload["rscale"]), payload["fmt"], payload["kind"], payload["G"],
         _pos_ptr(pos), P, _ptr(prev), T, H, D, _ptr(out),
     )
+    return out, int(st)
+
+
+# --------------------------------------------------------------------------
+# paged decode attention over a quantised pool (fp64)
+# --------------------------------------------------------------------------
+def _plane(plane, fmt):
+    """(codes, bscale or None, rscale) numpy planes -> C-contiguous arrays."""
+    codes, bscale, rscale = plane
+    return (_c(codes, np.uint8), None if fmt == FMT_FP8 else _c(bscale, np.uint8), _c(rscale, np.float32))
+
+
+def decode_attention(k_plane, v_plane, fmt_k, fmt_v, block_size, block_table, seq_lens, q_bf16,
+                     scale, out=None):
+    """o[s][qh] = softmax over the sequence's tokens of scale * q . k, applied to v, with
+    k / v the exact decoded pool rows.  Planes: (codes, bscale, rscale) as the pool holds
+    them ([slots][H][...]); q: bf16 bits [S][Hq][D].  Returns (out float64, status)."""
+    kc, kb, kr = _plane(k_plane, fmt_k)
+    vc, vb, vr = _plane(v_plane, fmt_v)
+    num_slots, H = kr.shape
+    q = _c(q_bf16, np.uint16)
+    S, Hq, D = q.shape
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    if out is None:
+        out = np.zeros((S, Hq, D), np.float64)
+    st = lib().orc_decode_attention(
+        _ptr(kc), _ptr(kb), _ptr(kr), fmt_k, _ptr(vc), _ptr(vb), _ptr(vr), fmt_v, num_slots, H, D,
+        block_size, _ptr(block_table), S, block_table.shape[1], _ptr(seq_lens), _ptr(q), Hq,
+        float(scale), _ptr(out))
     return out, int(st)
 
 

@@ -403,6 +403,82 @@ uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_
 }
 
 /* ------------------------------------------------------------------------- */
+/* paged decode attention (NEXT row f1: "feat(kvcache): add nvfp4 kv quantization */
+/* (FreeToken PR #408)", Summary and fp8 store notes -- dequantise in registers,  */
+/* the row scale applied to the score / output -- and the vllm-rlt review's note  */
+/* to dequantise in registers and keep the 16-bit MMA).  The definition is plain  */
+/* softmax attention of one query over the decoded rows, in double precision.     */
+/* ------------------------------------------------------------------------- */
+/* Exact value of element d of a pool row (double holds every product exactly). */
+static double pool_value(const uint8_t* codes, const uint8_t* bscale, const float* rscale, int fmt,
+                         int64_t r, int D, int d) {
+  if (fmt == ORC_FMT_FP8) return (double)orc_e4m3_value(codes[r * D + d]) * (double)rscale[r];
+  uint8_t byte = codes[r * (D / 2) + d / 2];
+  uint8_t nib = (d % 2 == 0) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4);
+  return (double)orc_e2m1_value(nib) * (double)orc_e4m3_value(bscale[r * (D / 16) + d / 16]) *
+         (double)rscale[r];
+}
+
+uint32_t orc_decode_attention(const uint8_t* k_codes, const uint8_t* k_bscale, const float* k_rscale,
+                              int fmt_k, const uint8_t* v_codes, const uint8_t* v_bscale,
+                              const float* v_rscale, int fmt_v, int64_t num_slots, int H, int D,
+                              int block_size, const int32_t* block_table, int S, int max_blocks,
+                              const int32_t* seq_lens, const uint16_t* q, int Hq, double scale,
+                              double* out) {
+  uint32_t status = 0;
+  int64_t num_blocks = num_slots / block_size;
+  int64_t cap = (int64_t)max_blocks * block_size;
+  int group = Hq / H;
+  for (int s = 0; s < S; s++) {
+    int len = seq_lens[s];
+    if (len < 0 || len > cap) {
+      status |= ORC_BAD_SEQLEN;
+      continue;
+    }
+    int bad = 0;
+    for (int t = 0; t < len && !bad; t++) {
+      int32_t block = block_table[(int64_t)s * max_blocks + t / block_size];
+      if (block < 0 || block >= num_blocks) bad = 1;
+    }
+    if (bad) {
+      status |= ORC_BAD_BLOCK;
+      continue;
+    }
+    double* sc = (double*)malloc(sizeof(double) * (len > 0 ? len : 1));
+    for (int qh = 0; qh < Hq; qh++) {
+      int h = qh / group;
+      const uint16_t* qv = q + ((int64_t)s * Hq + qh) * D;
+      double* o = out + ((int64_t)s * Hq + qh) * D;
+      for (int d = 0; d < D; d++) o[d] = 0.0;
+      if (len == 0) continue;
+      double mx = -INFINITY;
+      for (int t = 0; t < len; t++) {
+        int64_t slot = (int64_t)block_table[(int64_t)s * max_blocks + t / block_size] * block_size + t % block_size;
+        int64_t r = slot * H + h;
+        double dot = 0.0;
+        for (int d = 0; d < D; d++)
+          dot += (double)orc_bf16_to_f32(qv[d]) * pool_value(k_codes, k_bscale, k_rscale, fmt_k, r, D, d);
+        sc[t] = scale * dot;
+        if (sc[t] > mx) mx = sc[t];
+      }
+      double l = 0.0;
+      for (int t = 0; t < len; t++) {
+        sc[t] = exp(sc[t] - mx);
+        l += sc[t];
+      }
+      for (int t = 0; t < len; t++) {
+        int64_t slot = (int64_t)block_table[(int64_t)s * max_blocks + t / block_size] * block_size + t % block_size;
+        int64_t r = slot * H + h;
+        double p = sc[t] / l;
+        for (int d = 0; d < D; d++) o[d] += p * pool_value(v_codes, v_bscale, v_rscale, fmt_v, r, D, d);
+      }
+    }
+    free(sc);
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------- */
 /* INT4 affine codec                                                          */
 /* ------------------------------------------------------------------------- */
 static void put_nibble(uint8_t* codes, int64_t elem, int code) {

@@ -115,6 +115,23 @@ uint32_t orc_residual_decode(const uint8_t* codes, const void* meta_a, const voi
                              const float* rscale, int fmt, int kind, int G, const int32_t* pos,
                              int P, const uint16_t* prev, int T, int H, int D, uint16_t* out);
 
+/* ---- paged decode attention over a quantised pool (fp64) ----
+ * One query token per sequence.  Query head qh reads KV head qh / (Hq / H) (Hq a
+ * multiple of H).  K and V rows are the exact decoded values: NVFP4 e2m1 * bs * rs,
+ * FP8 e4m3 * rs (fmt_k / fmt_v per plane; bscale NULL for FP8).  For every sequence s
+ * with 0 < len = seq_lens[s]:
+ *   s_t = scale * sum_d q[s][qh][d] * k[t][d],  p = softmax_t(s),  out = sum_t p_t v[t]
+ * over tokens t < len (slot = block_table[s][t / block_size] * block_size + t % block_size).
+ * len == 0 writes zeros.  A bad length, or a block entry outside the pool, flags the
+ * status and leaves that sequence's output untouched.
+ * q: bf16 bits [S][Hq][D]; out: double [S][Hq][D]. */
+uint32_t orc_decode_attention(const uint8_t* k_codes, const uint8_t* k_bscale, const float* k_rscale,
+                              int fmt_k, const uint8_t* v_codes, const uint8_t* v_bscale,
+                              const float* v_rscale, int fmt_v, int64_t num_slots, int H, int D,
+                              int block_size, const int32_t* block_table, int S, int max_blocks,
+                              const int32_t* seq_lens, const uint16_t* q, int Hq, double scale,
+                              double* out);
+
 /* ---- storage accounting (bytes held by the codes and their scale sidecars) ---- */
 int64_t orc_storage_bytes(int fmt, int kind, int G, int64_t T, int H, int D);
 
