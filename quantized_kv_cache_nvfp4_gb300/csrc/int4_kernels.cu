@@ -9,6 +9,7 @@
 //   mn = min x;  mx = max x;  sc = (mx - mn) / 15
 //   code = 0 if sc == 0, else clamp(rint((x - mn) / sc), 0, 15)   (rint: ties even)
 //   stored: fp16(mn), fp16(sc); two codes per byte, low nibble = even channel.
+// The minimum and maximum order -0 below +0 (IEEE 754-2019 minimum/maximum).
 // Residual encode feeds the same codec with r = bf16(cur - prev) of the kept rows
 // (same page, Purpose: residuals subtract the reconstructed predecessor in the
 // input dtype; K groups follow the compact row order).
@@ -21,56 +22,121 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Code of x in a group with FP32 minimum mn and scale sc > 0, rsc = RN(1 / sc):
-// clamp(rint(RN(RN(x - mn) / sc)), 0, 15), usually without dividing.
+// Code of x in a group with FP32 minimum mn and scale sc > 0, and rsc within one ulp
+// of 1 / sc: clamp(rint(RN(RN(x - mn) / sc)), 0, 15), usually without dividing.
 //
-// With d = RN(x - mn) >= 0, the estimate qe = RN(d * rsc) and the defined quotient
-// q = RN(d / sc) both lie within 2 * 2^-24 (relative) of d / sc, and d / sc <= 15 *
-// (1 + 2^-23) because x <= max; so after clamping to 15, |qe - q| < 2.9e-6 < 2^-17.
-// When qe is more than 2^-17 away from the half-integers around it, q rounds to the
-// same integer as qe (rint is ties-to-even, and no tie is possible there).
-// Otherwise, and whenever sc is not a normal binary32 (rsc could overflow), the
-// quotient is formed by the division itself.
+// With d = RN(x - mn) >= 0, the estimate qe = RN(d * rsc) lies within 2^-23 + 2^-24
+// (relative) of d / sc and the defined quotient q = RN(d / sc) within 2^-24, and
+// d / sc <= 15 * (1 + 2^-23) because x <= max; so after clamping to 15,
+// |qe - q| < 15 * 2^-22 < 3.6e-6 < 2^-17.  When qe is more than 2^-17 away from the
+// half-integers around it, q rounds to the same integer as qe (rint is ties-to-even,
+// and no tie is possible there).  Otherwise, and whenever sc is not a normal binary32
+// (rsc could overflow), the quotient is formed by the division itself.
 //
-// Rounding to an integer: for 0 <= v <= 15, RN(v + 1.5 * 2^23) has unit spacing, so
+// Rounding to an integer: for 0 <= v < 15.5, RN(v + 1.5 * 2^23) has unit spacing, so
 // it is v rounded to nearest with ties to even, and its low four mantissa bits are
 // that integer.
-constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+constexpr float kRound = 12582912.0f;     // 1.5 * 2^23
+constexpr float kNearHalf = 0.49999237f;  // 0.5 - 2^-17
 
 __device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float rsc) {
   const float d = __fsub_rn(x, mn);
   if (sc >= 0x1p-126f) {
     const float qe = fminf(__fmul_rn(d, rsc), 15.0f);
     const float t = __fadd_rn(qe, kRound);
-    if (fabsf(__fsub_rn(qe, __fsub_rn(t, kRound))) < 0.49999237f)  // 0.5 - 2^-17
-      return __float_as_uint(t) & 15u;
+    if (fabsf(__fsub_rn(qe, __fsub_rn(t, kRound))) < kNearHalf) return __float_as_uint(t) & 15u;
   }
   return __float_as_uint(__fadd_rn(fminf(__fdiv_rn(d, sc), 15.0f), kRound)) & 15u;
 }
 
-__device__ __forceinline__ float int4_rcp(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }
-
-// Codes of the two bf16 of w (lo, hi) -> one byte (lo | hi << 4), the same integers
-// as int4_code (0 for a constant group, sc == 0).  The estimate, its rounding and its
-// distance to the rounded integer are formed two at a time in f32x2.  No clamp is
-// needed here: x <= max gives q <= 15 * (1 + 2^-22) < 15.5, which rounds to 15.
-__device__ __forceinline__ uint32_t int4_pair(uint32_t w, float mnl, float mnh, float scl, float sch,
-                                              float rscl, float rsch) {
-  const uint64_t k2 = pack_f32x2(__float_as_uint(kRound), __float_as_uint(kRound));
-  const uint64_t q2 = mul_f32x2(add_f32x2(pack_f32x2(w << 16, w & 0xFFFF0000u),
-                                          pack_f32x2(__float_as_uint(-mnl), __float_as_uint(-mnh))),
-                                pack_f32x2(__float_as_uint(rscl), __float_as_uint(rsch)));
-  const uint64_t t2 = add_f32x2(q2, k2);
-  uint32_t el, eh, tl, th;
-  unpack_f32x2(sub_f32x2(q2, sub_f32x2(t2, k2)), el, eh);  // estimate - its rounded integer
-  unpack_f32x2(t2, tl, th);
-  const bool ok = fabsf(__uint_as_float(el)) < 0.49999237f && fabsf(__uint_as_float(eh)) < 0.49999237f &&
-                  (scl >= 0x1p-126f || scl == 0.0f) && (sch >= 0x1p-126f || sch == 0.0f);
-  if (ok) return (tl & 15u) | ((th & 15u) << 4);
-  const uint32_t cl = scl != 0.0f ? int4_code(bf16lo(w), mnl, scl, rscl) : 0u;
-  const uint32_t ch = sch != 0.0f ? int4_code(bf16hi(w), mnh, sch, rsch) : 0u;
-  return cl | (ch << 4);
+// Reciprocal of a group scale for the estimate: the hardware approximation, within
+// one ulp (the bound above allows it); 0 for a constant group (sc == 0).
+__device__ __forceinline__ float int4_rcp(float sc) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(sc));
+  return sc != 0.0f ? r : 0.0f;
 }
+
+// True when the estimate path may be used for a group scale: normal or zero.
+__device__ __forceinline__ bool int4_fast_scale(float sc) { return sc >= 0x1p-126f || sc == 0.0f; }
+
+// Codes of the 8 bf16 of words w[0..3] (channel 2i in the low half of w[i], 2i + 1 in
+// the high half), with nmn2[i] = the negated minima and rs2[i] = the reciprocal
+// scales of w[i]'s two channels, as f32x2 pairs.  Byte i of the result holds w[i]'s
+// two codes, low nibble = even channel.  Raises `emax` to the largest distance of an
+// estimate from its rounded integer: the codes are int4_code's while emax stays below
+// kNearHalf and every scale passes int4_fast_scale (constant groups: rs = 0 gives
+// code 0).  No clamp is needed: q < 15.5 rounds into [0, 15].
+__device__ __forceinline__ uint32_t int4_codes4(const uint32_t (&w)[4], const uint64_t (&nmn2)[4],
+                                                const uint64_t (&rs2)[4], float& emax) {
+  const uint64_t k2 = pack_f32x2(__float_as_uint(kRound), __float_as_uint(kRound));
+  uint32_t out = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t q2 = mul_f32x2(add_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), nmn2[i]), rs2[i]);
+    const uint64_t t2 = add_f32x2(q2, k2);
+    uint32_t el, eh, tl, th;
+    unpack_f32x2(sub_f32x2(q2, sub_f32x2(t2, k2)), el, eh);
+    emax = fmaxf(emax, fmaxf(fabsf(__uint_as_float(el)), fabsf(__uint_as_float(eh))));
+    unpack_f32x2(t2, tl, th);
+    out |= ((tl & 15u) | ((th & 15u) << 4)) << (8 * i);
+  }
+  return out;
+}
+
+// The same 8 codes by int4_code, element by element (the rare exact path).
+__device__ __forceinline__ uint32_t int4_codes4_exact(const uint32_t (&w)[4], const float (&mn)[8],
+                                                   const float (&sc)[8], const float (&rs)[8]) {
+  uint32_t out = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t cl = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i], rs[2 * i]) : 0u;
+    const uint32_t ch =
+        sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1], rs[2 * i + 1]) : 0u;
+    out |= (cl | (ch << 4)) << (8 * i);
+  }
+  return out;
+}
+
+// Codes of one chunk (4 words) against per-channel parameters, with the exact path
+// taken only when the estimate check fails.
+__device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&w)[4], const float (&mn)[8], const float (&sc)[8],
+                                                const float (&rs)[8], bool fast) {
+  uint64_t nmn2[4], rs2[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    nmn2[i] = pack_f32x2(__float_as_uint(-mn[2 * i]), __float_as_uint(-mn[2 * i + 1]));
+    rs2[i] = pack_f32x2(__float_as_uint(rs[2 * i]), __float_as_uint(rs[2 * i + 1]));
+  }
+  float emax = 0.0f;
+  const uint32_t c = int4_codes4(w, nmn2, rs2, emax);
+  return (fast && emax < kNearHalf) ? c : int4_codes4_exact(w, mn, sc, rs);
+}
+
+// Group minimum and maximum of packed bf16 words: min/max.bf16x2 (a minimum or
+// maximum of bf16 values is one of them, so nothing rounds) and the OR of the words.
+// The hardware may return either zero for a (-0, +0) pair; only the sign of a zero
+// MINIMUM is stored, and a zero minimum means no element is negative, so the group
+// holds a -0 exactly when a sign bit is set in the OR.  (The sign of a zero maximum
+// never matters: sc = mx - mn is +0 either way.)
+__device__ __forceinline__ uint32_t hmin2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// A group minimum in FP32 from its bf16 bits (low 16 bits of m) and the group's OR of
+// sign bits (nonzero when some element has its sign bit set).
+__device__ __forceinline__ float group_min(uint32_t m, uint32_t any_sign) {
+  const float v = __uint_as_float(m << 16);
+  return v == 0.0f ? __uint_as_float(any_sign != 0u ? 0x80000000u : 0u) : v;
+}
+constexpr uint32_t kPosInf2 = 0x7F807F80u;  // bf16x2 +inf, +inf
+constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // bf16x2 -inf, -inf
 
 // The 8 bf16 values of one 16-byte chunk of a compact row (residual: bf16(cur-prev)).
 // Returns false for a residual row whose position is out of range (values zero).
@@ -109,11 +175,11 @@ __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row
   }
 }
 
-// KEY kind: a column task is (group of G rows, head, 8-channel chunk).  RS = G / RPL
-// lanes share a task; each holds its RPL rows of the chunk in registers (all loads
-// issued together), so every row is read once.  The RS partial minima/maxima meet in
-// a xor butterfly, then each lane codes its own rows.  A warp holds 32/RS
-// consecutive chunks of a row, so each row read is one coalesced span per row split.
+// KEY kind, register fallback for tiles too large for shared memory: a column task is
+// (group of G rows, head, 8-channel chunk).  RS = G / RPL lanes share a task; each
+// holds its RPL rows of the chunk in registers (all loads issued together), so every
+// row is read once.  The RS partial minima/maxima meet in a xor butterfly (in bf16
+// order keys, -0 below +0), then each lane codes its own rows.
 template <bool kResidual, int RS, int RPL>
 __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
   constexpr int CW = 32 / RS;
@@ -147,7 +213,6 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0u;
       }
     }
-    // group minimum / maximum per channel, in the bf16 order keys (-0 below +0)
     uint32_t kmn[4], kmx[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -172,36 +237,29 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         kmx[i] = max_u16x2(kmx[i], __shfl_xor_sync(0xFFFFFFFFu, kmx[i], o));
       }
     }
-    float mn[8], mx[8];
+    if (!valid) continue;
+    float mn[8], sc[8], rsc[8];
+    bool fast = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t a = bf16x2_unkey(kmn[i]), b = bf16x2_unkey(kmx[i]);
       mn[2 * i] = bf16lo(a);
       mn[2 * i + 1] = bf16hi(a);
-      mx[2 * i] = bf16lo(b);
-      mx[2 * i + 1] = bf16hi(b);
+      sc[2 * i] = __fdiv_rn(__fsub_rn(bf16lo(b), mn[2 * i]), 15.0f);
+      sc[2 * i + 1] = __fdiv_rn(__fsub_rn(bf16hi(b), mn[2 * i + 1]), 15.0f);
     }
-    if (!valid) continue;
-    float sc[8], rsc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      sc[i] = __fdiv_rn(__fsub_rn(mx[i], mn[i]), 15.0f);
       rsc[i] = int4_rcp(sc[i]);
+      fast = fast && int4_fast_scale(sc[i]);
     }
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
       const int32_t r = r0 + rs + k * RS;
       if (r >= r1) continue;
       if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
-      uint32_t packed = 0u;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        packed |= int4_pair(v[k][i], mn[2 * i], mn[2 * i + 1], sc[2 * i], sc[2 * i + 1], rsc[2 * i],
-                            rsc[2 * i + 1])
-                  << (8 * i);
-      STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) +
-                                      col / 2),
-          packed);
+      STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) + col / 2),
+          chunk_codes(v[k], mn, sc, rsc, fast));
     }
     if (rs == 0) {
       uint32_t m16[4], s16[4];
@@ -221,46 +279,45 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
 
 // KEY kind, tiled through shared memory: a block takes one tile (a group of up to G
 // rows x the D channels of one head) at a time, in kStages shared-memory buffers.
-//  1. the tile's rows are copied into shared memory with 16-byte cp.async copies,
-//     all issued at once (consecutive threads, consecutive chunks of a row); with two
-//     stages the next tile's copies are in flight while this tile is coded.  Residual
-//     mode gathers the rows at pos[] from cur and prev into two planes;
-//  2. thread (rq, cp) takes channel pair cp over rows rq, rq + RQ, ... (RQ = 512 / D
-//     row splits; a warp reads consecutive words: no bank conflicts), forms the
-//     residual bf16(cur - prev) in place, and leaves its partial minimum/maximum in
-//     shared memory; after a barrier every thread combines the RQ partials of its
-//     pair, so the group's FP32 minimum and scale are known;
-//  3. each thread codes its rows of the pair (one byte per row, a warp writes 32
-//     consecutive bytes) and the rq == 0 threads write the FP16 metadata.
+// Thread (rq, ch) owns 16-byte chunk ch (channels 8ch .. 8ch + 7) of rows rq,
+// rq + RP, ... (RP = 256 / (D / 8) rows per pass) through every step:
+//  1. the tile's rows are copied into shared memory with 16-byte cp.async copies; with
+//     two stages the next tile's copies are in flight while this tile is coded.
+//     Residual mode gathers the rows at pos[] from cur and prev into two planes;
+//  2. each thread reduces its rows of its chunk (residual: forms bf16(cur - prev) in
+//     place first) to partial min / max / sign-OR words;
+//  3. one thread per channel pair combines the RP partials, computes the group's
+//     minimum, scale and reciprocal, keeps them in shared memory and writes the FP16
+//     metadata;
+//  4. each thread codes its rows of its chunk: 8 codes -> one 32-bit store.
 template <bool kResidual, int kStages>
 __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4EncodeParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int kPlanes = kResidual ? 2 : 1;
   const int D = p.D;
-  const int nchunk = D / 8;     // 16-byte chunks per row
-  const int npair = D / 2;      // channel pairs = 32-bit words per row
-  const int RQ = kThreads / npair;
+  const int nchunk = D / 8;  // 16-byte chunks per row
+  const int npair = D / 2;   // 32-bit words per row
+  const int RP = kThreads / nchunk;
   const int tid = threadIdx.x;
-  const int cp = tid % npair;
-  const int rq = tid / npair;
+  const bool worker = tid < RP * nchunk;
+  const int ch = tid % nchunk;
+  const int rq = tid / nchunk;
   const int tile_words = p.G * npair;
-  uint32_t* const buf = reinterpret_cast<uint32_t*>(smem);  // [kStages][kPlanes][G][D/2]
-  uint32_t* const part = buf + kStages * kPlanes * tile_words;  // [2][RQ][D/2] keys
-  const int32_t ngroups = (p.rows + p.G - 1) / p.G;
-  const int64_t ntiles = static_cast<int64_t>(ngroups) * p.H;
+  uint32_t* const buf = reinterpret_cast<uint32_t*>(smem);                             // [kStages][kPlanes][G][D/2]
+  uint4* const part = reinterpret_cast<uint4*>(buf + kStages * kPlanes * tile_words);  // [3][RP][D/8]
+  float2* const prm = reinterpret_cast<float2*>(part + 3 * RP * nchunk);               // [3][D/2]
+  const uint32_t ntiles = static_cast<uint32_t>((p.rows + p.G - 1) / p.G) * static_cast<uint32_t>(p.H);
 
-  // copies of tile `tile_id` into stage `st` (nothing past the last tile)
-  auto issue = [&](int64_t tile_id, int st) {
-    if (tile_id >= ntiles) return;
-    const int32_t g = static_cast<int32_t>(tile_id / p.H);
-    const int32_t h = static_cast<int32_t>(tile_id % p.H);
-    const int32_t r0 = g * p.G;
+  // copies of tile `tile` into stage `st` (nothing past the last tile)
+  auto issue = [&](uint32_t tile, int st) {
+    if (!worker || tile >= ntiles) return;
+    uint32_t g, h;
+    p.div_h.divmod(tile, g, h);
+    const int32_t r0 = static_cast<int32_t>(g) * p.G;
     const int32_t nr = min(p.G, p.rows - r0);
-    uint32_t* const cur = buf + st * kPlanes * tile_words;
-    for (int c = tid; c < nr * nchunk; c += kThreads) {
-      const int row = c / nchunk;
-      const int col = (c % nchunk) * 8;
-      uint32_t* const dst = cur + row * npair + col / 2;
+    uint32_t* const cur = buf + st * kPlanes * tile_words + ch * 4;
+    for (int row = rq; row < nr; row += RP) {
+      uint32_t* const dst = cur + row * npair;
       int64_t src = r0 + row;
       if constexpr (kResidual) {
         if (p.pos != nullptr) src = LDX(p.pos + r0 + row);
@@ -270,20 +327,20 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
           continue;
         }
         cp_async16(dst + tile_words,
-                   p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col);
+                   p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + ch * 8);
       }
-      cp_async16(dst, p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + col);
+      cp_async16(dst, p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + ch * 8);
     }
   };
 
-  int64_t tile_id = blockIdx.x;
-  issue(tile_id, 0);
+  uint32_t tile = blockIdx.x;
+  issue(tile, 0);
   cp_async_commit();
   if constexpr (kStages == 2) {
-    issue(tile_id + gridDim.x, 1);
+    issue(tile + gridDim.x, 1);
     cp_async_commit();
   }
-  for (int it = 0; tile_id < ntiles; tile_id += gridDim.x, ++it) {
+  for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
     const int st = kStages == 2 ? (it & 1) : 0;
     if constexpr (kStages == 2) {
       cp_async_wait<1>();  // this tile's group is complete; the next may be in flight
@@ -291,56 +348,87 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
       cp_async_wait<0>();
     }
     __syncthreads();
-    const int32_t g = static_cast<int32_t>(tile_id / p.H);
-    const int32_t h = static_cast<int32_t>(tile_id % p.H);
-    const int32_t r0 = g * p.G;
+    uint32_t g, h;
+    p.div_h.divmod(tile, g, h);
+    const int32_t r0 = static_cast<int32_t>(g) * p.G;
     const int32_t nr = min(p.G, p.rows - r0);
-    uint32_t* const tile = buf + st * kPlanes * tile_words;
-    // 2. column minimum and maximum of the pair in bf16 order keys (-0 below +0;
-    //    residual: the difference is formed first)
-    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
-    if (rq < RQ) {
-      for (int row = rq; row < nr; row += RQ) {
-        uint32_t v = tile[row * npair + cp];
+    uint32_t* const tw = buf + st * kPlanes * tile_words + ch * 4;  // this thread's column
+    // 2. partial minimum / maximum / sign-OR of this thread's rows of its chunk
+    if (worker) {
+      uint32_t mn[4] = {kPosInf2, kPosInf2, kPosInf2, kPosInf2};
+      uint32_t mx[4] = {kNegInf2, kNegInf2, kNegInf2, kNegInf2};
+      uint32_t sg[4] = {0u, 0u, 0u, 0u};
+      for (int row = rq; row < nr; row += RP) {
+        uint4 v = *reinterpret_cast<const uint4*>(tw + row * npair);
         if constexpr (kResidual) {
-          const uint32_t q = tile[tile_words + row * npair + cp];
-          v = pack_bf16x2(__fsub_rn(bf16lo(v), bf16lo(q)), __fsub_rn(bf16hi(v), bf16hi(q)));
-          tile[row * npair + cp] = v;  // read back by this same thread in step 3
+          const uint4 q = *reinterpret_cast<const uint4*>(tw + tile_words + row * npair);
+          v.x = pack_bf16x2(__fsub_rn(bf16lo(v.x), bf16lo(q.x)), __fsub_rn(bf16hi(v.x), bf16hi(q.x)));
+          v.y = pack_bf16x2(__fsub_rn(bf16lo(v.y), bf16lo(q.y)), __fsub_rn(bf16hi(v.y), bf16hi(q.y)));
+          v.z = pack_bf16x2(__fsub_rn(bf16lo(v.z), bf16lo(q.z)), __fsub_rn(bf16hi(v.z), bf16hi(q.z)));
+          v.w = pack_bf16x2(__fsub_rn(bf16lo(v.w), bf16lo(q.w)), __fsub_rn(bf16hi(v.w), bf16hi(q.w)));
+          *reinterpret_cast<uint4*>(tw + row * npair) = v;  // read back by this thread in step 4
         }
-        const uint32_t key = bf16x2_key(v);
-        kmn = min_u16x2(kmn, key);
-        kmx = max_u16x2(kmx, key);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mn[i] = hmin2(mn[i], w[i]);
+          mx[i] = hmax2(mx[i], w[i]);
+          sg[i] |= w[i];
+        }
       }
-      part[rq * npair + cp] = kmn;
-      part[(RQ + rq) * npair + cp] = kmx;
+      part[(0 * RP + rq) * nchunk + ch] = make_uint4(mn[0], mn[1], mn[2], mn[3]);
+      part[(1 * RP + rq) * nchunk + ch] = make_uint4(mx[0], mx[1], mx[2], mx[3]);
+      part[(2 * RP + rq) * nchunk + ch] = make_uint4(sg[0], sg[1], sg[2], sg[3]);
     }
     __syncthreads();
-    if (rq < RQ) {
-      for (int k = 0; k < RQ; ++k) {
-        kmn = min_u16x2(kmn, part[k * npair + cp]);
-        kmx = max_u16x2(kmx, part[(RQ + k) * npair + cp]);
+    // 3. per channel pair: the group's minimum, scale and reciprocal; FP16 metadata
+    if (tid < npair) {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(part);  // [3][RP][D/2] words
+      uint32_t m = kPosInf2, M = kNegInf2, s = 0u;
+      for (int k = 0; k < RP; ++k) {
+        m = hmin2(m, pw[(0 * RP + k) * npair + tid]);
+        M = hmax2(M, pw[(1 * RP + k) * npair + tid]);
+        s |= pw[(2 * RP + k) * npair + tid];
       }
-      const uint32_t wmn = bf16x2_unkey(kmn), wmx = bf16x2_unkey(kmx);
-      const float mnl = bf16lo(wmn), mnh = bf16hi(wmn), mxl = bf16lo(wmx), mxh = bf16hi(wmx);
-      const float scl = __fdiv_rn(__fsub_rn(mxl, mnl), 15.0f);
-      const float sch = __fdiv_rn(__fsub_rn(mxh, mnh), 15.0f);
-      const float rsl = int4_rcp(scl), rsh = int4_rcp(sch);
-      // 3. codes of this thread's rows
-      for (int row = rq; row < nr; row += RQ) {
-        if (cp == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
-        const uint32_t byte = int4_pair(tile[row * npair + cp], mnl, mnh, scl, sch, rsl, rsh);
-        STX(p.dst.codes + (static_cast<int64_t>(r0 + row) * p.H + h) * npair + cp, static_cast<uint8_t>(byte));
+      const float mnl = group_min(m, s & 0x8000u), mnh = group_min(m >> 16, s & 0x80000000u);
+      const float scl = __fdiv_rn(__fsub_rn(bf16lo(M), mnl), 15.0f);
+      const float sch = __fdiv_rn(__fsub_rn(bf16hi(M), mnh), 15.0f);
+      prm[tid] = make_float2(mnl, mnh);
+      prm[npair + tid] = make_float2(scl, sch);
+      prm[2 * npair + tid] = make_float2(int4_rcp(scl), int4_rcp(sch));
+      const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * D + 2 * tid;
+      STX(reinterpret_cast<uint32_t*>(p.dst.mn + mi),
+          static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
+      STX(reinterpret_cast<uint32_t*>(p.dst.sc + mi),
+          static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16));
+    }
+    __syncthreads();
+    // 4. codes of this thread's rows of its chunk
+    if (worker) {
+      float mn[8], sc[8], rs[8];
+      bool fast = true;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = prm[ch * 4 + i], b = prm[npair + ch * 4 + i], c = prm[2 * npair + ch * 4 + i];
+        mn[2 * i] = a.x;
+        mn[2 * i + 1] = a.y;
+        sc[2 * i] = b.x;
+        sc[2 * i + 1] = b.y;
+        rs[2 * i] = c.x;
+        rs[2 * i + 1] = c.y;
+        fast = fast && int4_fast_scale(b.x) && int4_fast_scale(b.y);
       }
-      if (rq == 0) {
-        const int64_t m = (static_cast<int64_t>(g) * p.H + h) * D + 2 * cp;
-        STX(reinterpret_cast<uint32_t*>(p.dst.mn + m),
-            static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
-        STX(reinterpret_cast<uint32_t*>(p.dst.sc + m),
-            static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16));
+      uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(h) * npair + ch * 4;
+      const int64_t cstride = static_cast<int64_t>(p.H) * npair;
+      for (int row = rq; row < nr; row += RP) {
+        if (ch == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
+        const uint4 v = *reinterpret_cast<const uint4*>(tw + row * npair);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        STX(reinterpret_cast<uint32_t*>(cbase + (r0 + row) * cstride), chunk_codes(w, mn, sc, rs, fast));
       }
     }
-    __syncthreads();  // stage st and the partials are free again
-    issue(tile_id + static_cast<int64_t>(kStages) * gridDim.x, st);
+    __syncthreads();  // stage st, the partials and the parameters are free again
+    issue(tile + static_cast<uint32_t>(kStages) * gridDim.x, st);
     cp_async_commit();
   }
   cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
@@ -389,21 +477,24 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     uint32_t nw[8];
     load_row(row + stride, nw);  // the next row's loads before this row's arithmetic
     if (valid && b == 0 && h == 0) check_pos<kResidual>(p, r);
-    // the group's minimum and maximum in bf16 order keys (-0 below +0); one word
-    // carries the minimum key (low half) and the complemented maximum key (high half),
-    // so a single unsigned min per butterfly round reduces both
-    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+    // the lane's minimum / maximum (bf16x2 min/max, sign-OR for a zero minimum), then
+    // the group's over W lanes in bf16 order keys (-0 below +0): one word carries the
+    // minimum key (low half) and the complemented maximum key (high half), so a single
+    // unsigned min per butterfly round reduces both
+    uint32_t mm = 0xFFFFFFFFu;
     if (valid) {
+      uint32_t m = w[0], M = w[0], s = w[0];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t key = bf16x2_key(w[i]);
-        kmn = min_u16x2(kmn, key);
-        kmx = max_u16x2(kmx, key);
+      for (int i = 1; i < 8; ++i) {
+        m = hmin2(m, w[i]);
+        M = hmax2(M, w[i]);
+        s |= w[i];
       }
+      m = hmin2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the lane's extremes
+      M = hmax2(M, __byte_perm(M, 0u, 0x1032));
+      const uint32_t mbits = __float_as_uint(group_min(m, s & 0x80008000u)) >> 16;
+      mm = (bf16x2_key(mbits) & 0xFFFFu) | (~bf16x2_key(M) << 16);
     }
-    kmn = min_u16x2(kmn, __byte_perm(kmn, 0u, 0x1032));  // both halves: the lane minimum
-    kmx = max_u16x2(kmx, __byte_perm(kmx, 0u, 0x1032));
-    uint32_t mm = (kmn & 0xFFFFu) | (~kmx << 16);
     for (int o = 1; o < W; o <<= 1)  // W is uniform: every lane runs the same shuffles
       mm = min_u16x2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
     if (!valid) {
@@ -412,18 +503,20 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
       continue;
     }
     const uint32_t mnmx = bf16x2_unkey(mm ^ 0xFFFF0000u);  // low: minimum, high: maximum
-    const float lmn = bf16lo(mnmx), lmx = bf16hi(mnmx);
-    const float sc = __fdiv_rn(__fsub_rn(lmx, lmn), 15.0f);
+    const float lmn = bf16lo(mnmx);
+    const float sc = __fdiv_rn(__fsub_rn(bf16hi(mnmx), lmn), 15.0f);
     const float rsc = int4_rcp(sc);
-    uint32_t c0 = 0u, c1 = 0u;
+    float mn8[8], sc8[8], rs8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = int4_pair(w[i], lmn, lmn, sc, sc, rsc, rsc);
-      if (i < 4)
-        c0 |= byte << (8 * i);
-      else
-        c1 |= byte << (8 * (i - 4));
+      mn8[i] = lmn;
+      sc8[i] = sc;
+      rs8[i] = rsc;
     }
+    const bool fast = int4_fast_scale(sc);
+    const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
+    const uint32_t c0 = chunk_codes(w0, mn8, sc8, rs8, fast);
+    const uint32_t c1 = chunk_codes(w1, mn8, sc8, rs8, fast);
     const int64_t drow = static_cast<int64_t>(r) * p.H + h;
     store8B(p.dst.codes + drow * (p.D / 2) + 8 * b, c0, c1);
     if ((16 * b) % p.G == 0) {
@@ -481,10 +574,12 @@ cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s)
   return e;
 }
 
-// Shared memory of the tile kernel: kStages x planes tiles of G x D bf16, plus the
-// [2][RQ][D/2] partial key words.
+// Shared memory of the tile kernel: kStages x planes tiles of G x D bf16, the
+// [3][RP][D/8] partial chunks and the [3][D/2] float2 group parameters.
 size_t key_tile_smem(int G, int D, int stages, int planes) {
-  return static_cast<size_t>(stages) * planes * G * D * 2 + 2 * static_cast<size_t>(kThreads / (D / 2)) * D * 2;
+  const size_t nchunk = static_cast<size_t>(D / 8);
+  return static_cast<size_t>(stages) * planes * G * D * 2 + 3 * (kThreads / nchunk) * nchunk * 16 +
+         3 * static_cast<size_t>(D / 2) * 8;
 }
 
 constexpr size_t kTileSmemCap = 110 * 1024;  // two blocks per SM at least
@@ -511,8 +606,8 @@ cudaError_t key_tile_launch(const Int4EncodeParams& p, cudaStream_t s) {
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   const int planes = kRes ? 2 : 1;
-  if (p.D >= 16 && key_tile_smem(p.G, p.D, 2, planes) <= kTileSmemCap) return key_tile_launch<kRes, 2>(p, s);
-  if (p.D >= 16 && key_tile_smem(p.G, p.D, 1, planes) <= kTileSmemCap) return key_tile_launch<kRes, 1>(p, s);
+  if (key_tile_smem(p.G, p.D, 2, planes) <= kTileSmemCap) return key_tile_launch<kRes, 2>(p, s);
+  if (key_tile_smem(p.G, p.D, 1, planes) <= kTileSmemCap) return key_tile_launch<kRes, 1>(p, s);
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
   switch (p.G) {  // RS = G / RPL lanes per column task
     case 16: return key_launch<kRes, 2, 8>(p, ntask, s);

@@ -319,11 +319,12 @@ def test_k8v4_split_pool_scatter_restore_and_graph():
         slots = (table[s, t // bs].long() * bs + t % bs).to(DEV)
         kvq.kvq_quant_scatter(k[s, :n].to(DEV), v[s, :n].to(DEV), slots, pool, st)
     ko, vo = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
-    kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko, vo, st)
+    td, ld = table.to(DEV), lens.to(DEV)  # device inputs before capture (no copies inside it)
+    kvq.kvq_restore(pool, td, ld, Tmax, ko, vo, st)
     ko2, vo2 = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko2, vo2, st)
+        kvq.kvq_restore(pool, td, ld, Tmax, ko2, vo2, st)
     g.replay()
     torch.cuda.synchronize()
     assert int(st.item()) == 0

@@ -279,3 +279,24 @@ def test_int4_signed_zero_groups_match_the_oracle(kind):
     opay, ost = O.residual_encode(xb, prev_b, pos.numpy(), kvq.FMT_INT4, kind, 64)
     assert ost == 0
     check_payload(pay, opay)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_tiny_and_subnormal_groups(kind):
+    """Groups at scales 2^-140 .. 2^-100 (bf16 subnormals, subnormal and tiny normal
+    scales: the exact division path) beside ordinary groups, against the oracle."""
+    T, H, D = 512, 2, 128
+    x = synth.normal_bf16((T, H, D), seed=13, stream=1).float()
+    exps = torch.tensor([-140, -133, -128, -126, -120, -110, -100, 0], dtype=torch.float32)
+    if kind == kvq.KIND_KEY:  # one scale per 64-row group
+        s = exps.repeat_interleave(64)[:T].view(T, 1, 1)
+    else:  # one scale per 64-channel group
+        s = exps[torch.arange(T) % 8].view(T, 1, 1).repeat(1, H, 1)
+        s = torch.cat([s.expand(T, H, 64), torch.zeros(T, H, 64)], dim=2)
+    xb = (x * torch.exp2(s)).to(torch.bfloat16)
+    bits_in = bits(xb)
+    assert ((bits_in & 0x7F80) == 0).any() and ((bits_in & 0x7FFF) != 0).any()  # subnormals present
+    pk, y = gpu_int4_pack(xb.to(DEV), kind)
+    codes, mn, sc = O.int4_pack(bits_in, kind, 64)
+    check_int4(pk, codes, mn, sc)
+    np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
