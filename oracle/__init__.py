@@ -26,6 +26,7 @@ LIB = os.path.join(HERE, "liboracle.so")
 FMT_NVFP4 = 1
 FMT_INT4 = 2
 FMT_FP8 = 3
+FMT_NVFP4_TENSOR = 4
 KIND_KEY = 0
 KIND_VALUE = 1
 
@@ -85,6 +86,8 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_residual_encode": (_U32, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
         "orc_residual_decode": (_U32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _P]),
         "orc_storage_bytes": (_I64, [_I, _I, _I, _I64, _I, _I]),
+        "orc_nvfp4t_pack": (None, [_P, _I, _I, _I, _I, _P, _P, _P]),
+        "orc_nvfp4t_unpack": (None, [_P, _P, _P, _I, _I, _I, _I, _P]),
         "orc_decode_attention": (_U32, [_P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I, _I, _P, _I, _I,
                                         _P, _P, _I, ctypes.c_double, _P]),
         "orc_fp8_encode_rows": (None, [_P, _I64, _I, _P, _P]),
@@ -368,6 +371,34 @@ def residual_decode(payload, prev, out=None):
         _pos_ptr(pos), P, _ptr(prev), T, H, D, _ptr(out),
     )
     return out, int(st)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 with one FP32 scale per tensor, G16 blocks along the kind's axis
+# --------------------------------------------------------------------------
+def nvfp4t_bscale_shape(kind, T, H, D):
+    return (-(-T // 16), H, D) if kind == KIND_KEY else (T, H, D // 16)
+
+
+def nvfp4t_pack(x_bf16, kind: int):
+    """x [T][H][D] bf16 bits -> codes [T][H][D/2], bscale (by kind), rscale [1]."""
+    x = _c(x_bf16, np.uint16)
+    T, H, D = x.shape
+    codes = np.zeros((T, H, D // 2), np.uint8)
+    bscale = np.zeros(nvfp4t_bscale_shape(kind, T, H, D), np.uint8)
+    rscale = np.zeros(1, np.float32)
+    lib().orc_nvfp4t_pack(_ptr(x), T, H, D, kind, _ptr(codes), _ptr(bscale), _ptr(rscale))
+    return codes, bscale, rscale
+
+
+def nvfp4t_unpack(codes, bscale, rscale, kind: int):
+    codes = _c(codes, np.uint8)
+    bscale = _c(bscale, np.uint8)
+    rscale = _c(rscale, np.float32)
+    T, H, half = codes.shape
+    y = np.empty((T, H, 2 * half), np.uint16)
+    lib().orc_nvfp4t_unpack(_ptr(codes), _ptr(bscale), _ptr(rscale), T, H, 2 * half, kind, _ptr(y))
+    return y
 
 
 # --------------------------------------------------------------------------

@@ -403,6 +403,79 @@ uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_
 }
 
 /* ------------------------------------------------------------------------- */
+/* NVFP4 with one FP32 scale per tensor ("vllm-rlt PR #166", Purpose: E4M3     */
+/* block scales and a scalar FP32 global encoding multiplier after vLLM's      */
+/* reference; G16 blocks along the kind's axis, K over token rows, V over      */
+/* channels; partial groups allowed).  The scale is the tensor's amax / 2688,  */
+/* stored as the decode multiplier (R1 read per tensor); each block follows    */
+/* R2-R3 against it.                                                           */
+/* ------------------------------------------------------------------------- */
+static int64_t nvfp4t_elem(int kind, int H, int D, int g, int h, int j, int k) {
+  /* element k (0..15) of block j: VALUE block j = (t, h, 16-channel block), KEY block = (group, h, d) */
+  if (kind == ORC_KIND_VALUE) return ((int64_t)g * H + h) * D + 16 * j + k;
+  return ((int64_t)(16 * g + k) * H + h) * D + j;
+}
+
+void orc_nvfp4t_pack(const uint16_t* x, int T, int H, int D, int kind, uint8_t* codes,
+                     uint8_t* bscale, float* rscale) {
+  const float E2M1_MAX = 6.0f, E4M3_MAX = 448.0f;
+  int64_t n = (int64_t)T * H * D;
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; i++) amax = fmaxf(amax, fabsf(orc_bf16_to_f32(x[i])));
+  float rs = amax / (E2M1_MAX * E4M3_MAX);
+  rscale[0] = rs;
+  for (int64_t i = 0; i < n / 2; i++) codes[i] = 0;
+  int groups = (kind == ORC_KIND_VALUE) ? T : (T + 15) / 16; /* outer index of a block */
+  int per = (kind == ORC_KIND_VALUE) ? D / 16 : D;            /* blocks per (outer, h) */
+  for (int g = 0; g < groups; g++)
+    for (int h = 0; h < H; h++)
+      for (int j = 0; j < per; j++) {
+        int len = (kind == ORC_KIND_VALUE) ? 16 : (T - 16 * g < 16 ? T - 16 * g : 16);
+        /* block amax and the E4M3 block scale (R2) */
+        float vb = 0.0f;
+        for (int k = 0; k < len; k++) vb = fmaxf(vb, fabsf(orc_bf16_to_f32(x[nvfp4t_elem(kind, H, D, g, h, j, k)])));
+        float t = 0.0f;
+        if (rs != 0.0f) t = (vb / E2M1_MAX) / rs;
+        if (t > E4M3_MAX) t = E4M3_MAX;
+        uint8_t bsb = orc_e4m3_encode(t);
+        bscale[((int64_t)g * H + h) * per + j] = bsb;
+        float bs = orc_e4m3_value(bsb);
+        /* element codes against s = bs * rs (R3) */
+        float s = bs * rs;
+        float inv = 0.0f;
+        if (s != 0.0f) inv = 1.0f / s;
+        for (int k = 0; k < len; k++) {
+          int64_t e = nvfp4t_elem(kind, H, D, g, h, j, k);
+          float xi = orc_bf16_to_f32(x[e]);
+          float q;
+          if (s == 0.0f)
+            q = copysignf(0.0f, xi);
+          else if (isinf(inv))
+            q = xi / s;
+          else
+            q = xi * inv;
+          uint8_t c = orc_e2m1_encode(q);
+          c = (uint8_t)((c & 7) | (signbit(xi) ? 8 : 0));
+          codes[e / 2] |= (uint8_t)((e % 2 == 0) ? c : (c << 4)); /* low nibble = even channel */
+        }
+      }
+}
+
+void orc_nvfp4t_unpack(const uint8_t* codes, const uint8_t* bscale, const float* rscale, int T, int H,
+                       int D, int kind, uint16_t* y) {
+  for (int t = 0; t < T; t++)
+    for (int h = 0; h < H; h++)
+      for (int d = 0; d < D; d++) {
+        int64_t e = ((int64_t)t * H + h) * D + d;
+        uint8_t c = (e % 2 == 0) ? (uint8_t)(codes[e / 2] & 15) : (uint8_t)(codes[e / 2] >> 4);
+        int64_t b = (kind == ORC_KIND_VALUE) ? ((int64_t)t * H + h) * (D / 16) + d / 16
+                                             : ((int64_t)(t / 16) * H + h) * D + d;
+        float v = orc_e2m1_value(c) * orc_e4m3_value(bscale[b]); /* exact */
+        y[e] = orc_f32_to_bf16(v * rscale[0]);                    /* R4 */
+      }
+}
+
+/* ------------------------------------------------------------------------- */
 /* paged decode attention (NEXT row f1: "feat(kvcache): add nvfp4 kv quantization */
 /* (FreeToken PR #408)", Summary and fp8 store notes -- dequantise in registers,  */
 /* the row scale applied to the score / output -- and the vllm-rlt review's note  */
@@ -653,6 +726,10 @@ int64_t orc_storage_bytes(int fmt, int kind, int G, int64_t T, int H, int D) {
     return T * H * (D / 2 + D / 16 + 4);
   if (fmt == ORC_FMT_FP8) /* one E4M3 per value + one FP32 per row */
     return T * H * (D + 4);
+  if (fmt == ORC_FMT_NVFP4_TENSOR) { /* codes D/2 + one E4M3 per 16-block + one FP32 per tensor */
+    int64_t blocks = (kind == ORC_KIND_KEY) ? ((T + 15) / 16) * H * D : T * H * (D / 16);
+    return T * H * (D / 2) + blocks + 4;
+  }
   int64_t code_bytes = T * H * (D / 2);
   int64_t groups = (kind == ORC_KIND_KEY) ? ((T + G - 1) / G) * H * D
                                           : T * H * ((D + G - 1) / G);

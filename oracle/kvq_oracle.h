@@ -35,7 +35,7 @@ extern "C" {
 #define ORC_BAD_POS 4u     /* position out of [0, T) or not strictly increasing */
 #define ORC_BAD_SEQLEN 8u  /* sequence length outside [0, min(Tmax, max_blocks*block_size)] */
 
-enum { ORC_FMT_NVFP4 = 1, ORC_FMT_INT4 = 2, ORC_FMT_FP8 = 3 };
+enum { ORC_FMT_NVFP4 = 1, ORC_FMT_INT4 = 2, ORC_FMT_FP8 = 3, ORC_FMT_NVFP4_TENSOR = 4 };
 enum { ORC_KIND_KEY = 0, ORC_KIND_VALUE = 1 };
 
 /* ---- scalar format primitives ---- */
@@ -90,6 +90,19 @@ uint32_t orc_fp8_scatter(const uint16_t* x, int64_t row_pitch, int64_t head_pitc
 uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_slots, int H,
                          int D, int block_size, const int32_t* block_table, int S,
                          int max_blocks, const int32_t* seq_lens, int Tmax, uint16_t* out);
+
+/* ---- NVFP4 with one FP32 scale per tensor (vllm-rlt PR #166's logical layout) ----
+ * x contiguous [T][H][D] (D % 16 == 0).  rs = amax over the whole tensor / 2688.
+ * Blocks of 16 run along the kind's axis: kind VALUE over 16 channels per (t, h),
+ * kind KEY over 16 token rows per (h, d) (the last group may be partial).  Per block
+ * the row codec's steps R2-R3 against the tensor's rs.  Layout:
+ *   codes [T][H][D/2] (low nibble = even channel)
+ *   bscale: VALUE [T][H][D/16], KEY [ceil(T/16)][H][D]
+ *   rscale [1] */
+void orc_nvfp4t_pack(const uint16_t* x, int T, int H, int D, int kind, uint8_t* codes,
+                     uint8_t* bscale, float* rscale);
+void orc_nvfp4t_unpack(const uint8_t* codes, const uint8_t* bscale, const float* rscale, int T, int H,
+                       int D, int kind, uint16_t* y);
 
 /* ---- INT4 affine codec, group size G, x contiguous [T][H][D] (D even) ----
  * codes [T][H][D/2] (low nibble = even channel)

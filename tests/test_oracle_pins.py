@@ -374,7 +374,7 @@ def test_storage_figures_printed_on_the_pages(case):
     if fmt == "bf16":
         got = T * H * D * 2
     else:
-        f = {"nvfp4": O.FMT_NVFP4, "int4": O.FMT_INT4, "fp8": O.FMT_FP8}[fmt]
+        f = {"nvfp4": O.FMT_NVFP4, "int4": O.FMT_INT4, "fp8": O.FMT_FP8, "nvfp4t": O.FMT_NVFP4_TENSOR}[fmt]
         got = O.storage_bytes(f, k, G, T, H, D)
     if name.endswith("_bits"):
         got = 8.0 * got / (T * H * D)
