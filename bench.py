@@ -290,6 +290,7 @@ def run_ours(args):
     if not args.no_other_rows and rank == 0:
         rows_other = other_rows(kvq, device, peak=measured_peaks()[0])
         rows_other["latency_us_one_residual_loop"] = residual_loop_latency(kvq, device)
+        rows_other["decode_attention"] = attention_rows(kvq, device, peak=measured_peaks()[0])
 
     if rank != 0:
         if dist is not None:
@@ -526,6 +527,73 @@ def other_rows(kvq, device, T=262144, H=8, D=128, G=64, P=None, iters=20, peak=6
           rows_b + pb + 4 * P + rows_b)
     return {"workload": f"[{T} tokens, {H} KV heads, D{D}] bf16, INT4 G{G}, residual rows kept {P}/{T}",
             "kernels": out}
+
+
+def attention_rows(kvq, device, peak=6795.5, iters=20, S=32, T=8192, H=8, Hq=32, D=128):
+    """Decode attention reading the quantised pool (K and V decoded in registers) on the
+    paged-restore workload's pool: S sequences x T tokens, H KV heads, Hq query heads,
+    D128.  Bytes: the pool rows read (K and V) + q + out + block table.  The unfused
+    path (restore to bf16, then torch SDPA) is timed beside it for context."""
+    import math
+
+    from quantized_kv_cache_nvfp4_gb300 import synth
+
+    bs = BLOCK
+    nblocks = S * T // bs
+    perm = synth.block_permutation(nblocks, 3).to(device)
+    table = perm.view(S, T // bs).contiguous()
+    t = torch.arange(T, device=device)
+    slots = (table[:, t // bs].long() * bs + t % bs).reshape(-1)
+    lens = torch.full((S,), T, dtype=torch.int32, device=device)
+    q = synth.normal_bf16((S, Hq, D), 3, 9, device=str(device))
+    out = torch.empty_like(q)
+    res = {}
+    for name, fk, fv in (("nvfp4", kvq.FMT_NVFP4, None), ("fp8", kvq.FMT_FP8, None),
+                         ("k8v4 (FP8 K, NVFP4 V)", kvq.FMT_FP8, kvq.FMT_NVFP4)):
+        pool = kvq.KvPool.empty(nblocks * bs, H, D, bs, device=device, fmt=fk, v_fmt=fv)
+        k = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_K, device=str(device))
+        v = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_V, device=str(device))
+        kvq.kvq_quant_scatter(k, v, slots, pool)
+        del k, v
+        ws = torch.empty(max(kvq.kvq_decode_attention_workspace(S, H, Hq, D, T), 16), dtype=torch.uint8,
+                         device=device)
+        fn = lambda: kvq.kvq_decode_attention(pool, table, lens, T, q, 1.0 / math.sqrt(D), out, workspace=ws)
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize(device)
+        ms = a.elapsed_time(b) / iters
+        nbytes = pool.nbytes() + 2 * q.numel() * 2 + table.numel() * 4
+        res[f"kvq_decode_attention {name}"] = {"ms": round(ms, 4), "bytes": nbytes,
+                                               "GB/s": round(nbytes / ms / 1e6, 1),
+                                               "frac": round(nbytes / ms / 1e6 / peak, 4)}
+        if name == "nvfp4":  # the unfused path on the same pool, for context
+            ko = torch.empty((S, T, H, D), dtype=torch.bfloat16, device=device)
+            vo = torch.empty_like(ko)
+
+            def unfused():
+                kvq.kvq_restore(pool, table, lens, T, ko, vo)
+                kk = ko.permute(0, 2, 1, 3).repeat_interleave(Hq // H, dim=1)
+                vv = vo.permute(0, 2, 1, 3).repeat_interleave(Hq // H, dim=1)
+                return torch.nn.functional.scaled_dot_product_attention(q[:, :, None], kk, vv,
+                                                                        scale=1.0 / math.sqrt(D))
+
+            for _ in range(2):
+                unfused()
+            a.record()
+            for _ in range(5):
+                unfused()
+            b.record()
+            torch.cuda.synchronize(device)
+            res["unfused restore + torch SDPA (nvfp4)"] = {"ms": round(a.elapsed_time(b) / 5, 4)}
+            del ko, vo
+        del pool
+    return {"workload": f"decode attention: {S} sequences x {T} tokens, {H} KV heads, {Hq} query heads, "
+                        f"D{D}, block size {bs}, shuffled block table", "kernels": res}
 
 
 def residual_loop_latency(kvq, device, iters=50):

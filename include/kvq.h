@@ -214,6 +214,42 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
                                const kvq_bf16_out* out, uint32_t* dev_status,
                                kvq_stream_t stream);
 
+/* Paged decode attention over a quantised pool: the step downstream of the
+ * restore, with K and V dequantised in registers instead of restored to bf16.
+ * Source: FreeToken PR #408, Summary (restore paths) and fp8 store notes (the row
+ * scale multiplies the score and the output); vllm-rlt PR #166, review by 0z5a
+ * (dequantise to 16 bits in registers and keep the 16-bit MMA).
+ * One query token per sequence.  For query head qh (KV head qh / (num_q_heads /
+ * pool->num_heads)):
+ *   out[s][qh] = softmax_t(scale * q[s][qh] . k_t) . v_t   over t < seq_lens[s],
+ * with k_t, v_t the decoded pool rows (each plane in its own format, NVFP4 or FP8).
+ *   q    bf16 [num_seqs][num_q_heads][head_dim] through q->row_pitch (per sequence)
+ *        and q->head_pitch (per head), inner stride 1; 16-byte aligned.
+ *   out  bf16, indexed the same way through its own pitches.
+ *   head_dim 64, 128 or 256; num_q_heads a multiple of num_heads, at most 16 query
+ *   heads per KV head.  seq_lens[s] <= min(max_seq_len, max_blocks * block_size).
+ *   workspace  device memory of kvq_decode_attention_workspace(...) bytes, 16-byte
+ *              aligned (may be NULL when that is 0); caller-owned, reused by the next
+ *              call on the same stream.
+ * Accuracy: K and V decode exactly; the products run in f16 with f32 accumulation
+ * (P rounded to f16 relative to a running maximum), so the output is within a few
+ * bf16 ulps of the exact attention of the decoded rows (tests/test_attention_gpu.py
+ * states the bound).
+ * An empty sequence writes zeros.  A bad length (KVQ_DEV_BAD_SEQLEN) or a block
+ * entry outside the pool (KVQ_DEV_BAD_BLOCK) leaves that sequence's output untouched.
+ * One or two kernel launches. */
+KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* block_table,
+                                        int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
+                                        int32_t max_seq_len, const kvq_bf16_in* q, int32_t num_q_heads,
+                                        float scale, const kvq_bf16_out* out, void* workspace,
+                                        size_t workspace_bytes, uint32_t* dev_status,
+                                        kvq_stream_t stream);
+
+/* Workspace bytes kvq_decode_attention needs for these sizes on the current device
+ * (0 when the call runs without one).  Host-only query. */
+KVQ_API size_t kvq_decode_attention_workspace(int32_t num_seqs, int32_t num_heads, int32_t num_q_heads,
+                                              int32_t head_dim, int32_t max_seq_len);
+
 /* Bytes held by codes plus scale sidecars for rows x heads x dim in a format,
  * excluding allocator overhead (vllm-rlt PR #166 review: storage_bytes).  76 per
  * NVFP4 row at dim 128; INT4 G64: 4 + 32/64 bits per element for full groups.

@@ -24,7 +24,8 @@ from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT
 
 __all__ = [
     "KvqError", "KvPool", "Nvfp4Pool", "Packed", "kvq_quant_scatter", "kvq_restore", "kvq_pack",
-    "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_storage_bytes",
+    "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_decode_attention",
+    "kvq_decode_attention_workspace", "kvq_storage_bytes",
     "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "FMT_FP8", "KIND_KEY",
     "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN",
 ]
@@ -297,6 +298,35 @@ def kvq_decode_residual(payload: Packed, pos: Optional[torch.Tensor], prev: torc
     _check(_lib().kvq_decode_residual(
         ctypes.byref(ps), pos_ptr, n, ctypes.byref(pi), prev.size(0), ctypes.byref(oo),
         _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def kvq_decode_attention_workspace(num_seqs: int, num_heads: int, num_q_heads: int, head_dim: int,
+                                   max_seq_len: int) -> int:
+    return int(_lib().kvq_decode_attention_workspace(num_seqs, num_heads, num_q_heads, head_dim, max_seq_len))
+
+
+def kvq_decode_attention(pool: KvPool, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                         q: torch.Tensor, scale: float, out: torch.Tensor,
+                         workspace: Optional[torch.Tensor] = None,
+                         dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention of q [S, Hq, D] bf16 over the pool's K/V (decoded in registers)
+    into out [S, Hq, D] bf16.  A workspace tensor is allocated when none is given."""
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [S, max_blocks]")
+    S, max_blocks = block_table.shape
+    qi, oo = _bf16_in(q, "q"), _bf16_out(out, "out")
+    Hq = q.size(1)
+    need = kvq_decode_attention_workspace(S, pool.num_heads, Hq, pool.head_dim, max_seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ps = pool._struct()
+    _check(_lib().kvq_decode_attention(
+        ctypes.byref(ps), _ptr(block_table), S, max_blocks, _ptr(seq_lens), max_seq_len, ctypes.byref(qi), Hq,
+        float(scale), ctypes.byref(oo), _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
     return out
 
 

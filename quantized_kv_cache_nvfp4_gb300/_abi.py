@@ -85,6 +85,10 @@ SIGNATURES = {
                                   ctypes.POINTER(Packed), _P, _P, _P]),
     "kvq_decode_residual": (_ST, [ctypes.POINTER(Packed), _P, _I32, ctypes.POINTER(Bf16In), _I32,
                                   ctypes.POINTER(Bf16Out), _P, _P]),
+    "kvq_decode_attention": (_ST, [ctypes.POINTER(Pool), _P, _I32, _I32, _P, _I32, ctypes.POINTER(Bf16In),
+                                   _I32, ctypes.c_float, ctypes.POINTER(Bf16Out), _P, ctypes.c_size_t,
+                                   _P, _P]),
+    "kvq_decode_attention_workspace": (ctypes.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "kvq_storage_bytes": (ctypes.c_size_t, [_ST, _ST, _I32, _I64, _I32, _I32]),
     "kvq_status_string": (ctypes.c_char_p, [_ST]),
     "kvq_last_error": (ctypes.c_char_p, []),

@@ -1,0 +1,514 @@
+// attn_kernels.cu -- paged decode attention that reads the quantised pool directly.
+//
+// The step downstream of the paged restore: instead of restoring K and V to bf16,
+// decode attention dequantises them in registers ("feat(kvcache): add nvfp4 kv
+// quantization (FreeToken PR #408)", Summary -- the restore paths -- and fp8 store
+// notes, where the row scale multiplies the score and the output; "vllm-rlt PR #166",
+// review by 0z5a: dequantise to 16 bits in registers and keep the 16-bit MMA).
+//
+// One query token per sequence; query head qh reads KV head qh / group:
+//   o[s][qh] = softmax_t(scale * q . k_t) . v_t   over tokens t < seq_lens[s].
+//
+// Mapping (mma.sync m16n8k16, f16 operands, f32 accumulators).  A CTA takes one
+// (split of a sequence's tokens, KV head, sequence); its 4 warps take 16-token tiles
+// in turn, each through its own cp.async ring of pool tiles in shared memory.
+//  * M = the group's query heads (padded to 16): a warp's S = Q K^T tile is 16 heads
+//    x 16 tokens, and its P feeds P V directly as the A operand.
+//  * Q K^T contracts over the head dimension in a permuted order: k-step kb of lane c
+//    (c = lane % 4) covers dims c*D/4 + 4kb .. + 3, so a lane's K operand for one token
+//    is one contiguous run of code bytes; Q is permuted the same way.
+//  * P V writes column n of n-tile nt to dim n*D/8 + nt, so a lane's V operand for
+//    one token is again one contiguous run; the nibbles (or bytes) of the two tokens a
+//    register pairs are interleaved by a mask-and-shift (or byte-permute) transpose.
+//  * K and V decode exactly to f16: e2m1 x e4m3 has at most 2 x 4 significant bits,
+//    and e4m3 fits f16.  K's FP32 row scale multiplies the score; V's multiplies P
+//    relative to a running maximum R of the tile row scales (P' = p * rs / R <= 1, so
+//    f16 holds it), and O is rescaled when R grows, like the softmax running maximum.
+//  * Q enters f16 exactly: each query row is scaled by a power of two that puts its
+//    largest element in [2^14, 2^15), undone in the score multiplier.
+//  * The warps of a CTA merge through shared memory; several splits of a sequence
+//    merge through the caller's workspace in a second small kernel.
+#include "kvq_device.cuh"
+#include "kvq_params.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Both E4M3 bytes of `two` (low byte -> low half) to f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  const uint16_t in = static_cast<uint16_t>(two & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+  return r;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Asynchronous 4- / 8-byte copies into shared memory (cp.async.ca; 16-byte copies use
+// cp_async16).  The checked build stores zeros instead of copying from outside a
+// registered range.
+template <int N>
+__device__ __forceinline__ void cp_async_small(void* smem_dst, const void* gsrc) {
+  static_assert(N == 4 || N == 8, "4 or 8 bytes");
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  if (!KVQ_OK(gsrc, N, N)) {
+    if constexpr (N == 4) {
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(d), "r"(0u) : "memory");
+    } else {
+      asm volatile("st.shared.v2.b32 [%0], {%1, %1};" ::"r"(d), "r"(0u) : "memory");
+    }
+    return;
+  }
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gsrc), "n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_n(void* smem_dst, const void* gsrc) {
+  if constexpr (N == 16) {
+    cp_async16(smem_dst, gsrc);
+  } else {
+    cp_async_small<N>(smem_dst, gsrc);
+  }
+}
+
+__device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
+  const int lo = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v & 0xFFFFFFFF), src);
+  const int hi = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v >> 32), src);
+  return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
+// Shared-memory layout of one 16-token tile of one KV head (both K and V).
+template <int D, int kFK, int kFV>
+struct AttnTile {
+  static constexpr int kCK = kFK == 3 ? D : D / 2;  // code bytes per row
+  static constexpr int kCV = kFV == 3 ? D : D / 2;
+  static constexpr int kBK = kFK == 3 ? 0 : D / 16;  // block-scale bytes per row
+  static constexpr int kBV = kFV == 3 ? 0 : D / 16;
+  static constexpr int kOffKC = 0;
+  static constexpr int kOffVC = kOffKC + 16 * kCK;
+  static constexpr int kOffKB = kOffVC + 16 * kCV;
+  static constexpr int kOffVB = kOffKB + 16 * kBK;
+  static constexpr int kOffKR = kOffVB + 16 * kBV;
+  static constexpr int kOffVR = kOffKR + 64;
+  static constexpr int kBytes = kOffVR + 64;
+  static constexpr int kStages = kBytes > 4096 ? 3 : 4;
+  static constexpr int kRing = kAttnWarps * kStages * kBytes;
+  static constexpr int kMerge = kAttnWarps * 16 * (D + 2) * 4;  // per warp: 16 rows x (O, m, l)
+  static constexpr int kSmem = kRing > kMerge ? kRing : kMerge;
+};
+
+template <int D, int kFK, int kFV>
+__global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnParams p) {
+  using T = AttnTile<D, kFK, kFV>;
+  constexpr int kKS = D / 16;  // Q K^T k-steps
+  constexpr int kNT = D / 8;   // P V n-tiles
+  extern __shared__ __align__(16) unsigned char smem[];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+
+  const int len = LDX(p.seq_lens + s);
+  const bool bad_len = len < 0 || len > p.seq_cap;
+  const int t_begin = split * p.split_len;
+  const int t_end = bad_len ? t_begin : min(t_begin + p.split_len, len);
+  const int ntile = t_end > t_begin ? (t_end - t_begin + 15) / 16 : 0;
+  if (bad_len && threadIdx.x == 0 && split == 0 && h == 0) set_status(p.status, 8u);
+
+  // ---- Q fragments: rows g and g + 8 of the group, scaled by 2^k into f16 ----
+  uint32_t qa[kKS][4];
+  float qmul[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int row = g + 8 * hr;
+    uint32_t w[D / 8];  // this lane's D/4 dims as bf16 pairs
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) w[i] = 0u;
+    if (row < p.group) {
+      const uint16_t* qp =
+          p.q + static_cast<int64_t>(s) * p.q_row_pitch + static_cast<int64_t>(h * p.group + row) * p.q_head_pitch + c * (D / 4);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        uint32_t v4[4];
+        load16B(qp + 8 * i, v4);
+        w[4 * i] = v4[0];
+        w[4 * i + 1] = v4[1];
+        w[4 * i + 2] = v4[2];
+        w[4 * i + 3] = v4[3];
+      }
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) am = fmaxf(am, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    int k = 0;
+    if (am > 0.0f) k = 14 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127);
+    k = max(-100, min(120, k));
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+    qmul[hr] = p.scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+#pragma unroll
+    for (int kb = 0; kb < kKS; ++kb) {
+      qa[kb][hr] = f32x2_to_f16x2(bf16lo(w[2 * kb]) * up, bf16hi(w[2 * kb]) * up);          // dims 4kb, +1
+      qa[kb][2 + hr] = f32x2_to_f16x2(bf16lo(w[2 * kb + 1]) * up, bf16hi(w[2 * kb + 1]) * up);  // dims 4kb+2, +3
+    }
+  }
+
+  // ---- the warp's tiles through its cp.async ring ----
+  unsigned char* const ring = smem + warp * T::kStages * T::kBytes;
+  bool bad = false;
+  auto issue = [&](int it, int st) {
+    const int tile = warp + it * kAttnWarps;
+    if (tile >= ntile) return;
+    unsigned char* const sb = ring + st * T::kBytes;
+    const int tt = lane & 15;
+    int t = t_begin + tile * 16 + tt;
+    if (t >= t_end) t = t_end - 1;  // a valid token's address; masked later
+    uint32_t bi, bo;
+    p.div_bs.divmod(static_cast<uint32_t>(t), bi, bo);
+    int64_t blk = LDX(p.block_table + static_cast<int64_t>(s) * p.max_blocks + bi);
+    if (blk < 0 || blk >= p.num_blocks) {
+      bad = true;
+      blk = 0;
+    }
+    const int64_t row = (blk * p.block_size + bo) * p.H + h;  // pool row of token tt
+    constexpr int kPK = T::kCK / 16, kPV = T::kCV / 16;
+#pragma unroll
+    for (int i = lane; i < 16 * kPK; i += 32) {
+      const int64_t rr = shfl64(row, i / kPK);
+      cp_async16(sb + T::kOffKC + (i / kPK) * T::kCK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
+    }
+#pragma unroll
+    for (int i = lane; i < 16 * kPV; i += 32) {
+      const int64_t rr = shfl64(row, i / kPV);
+      cp_async16(sb + T::kOffVC + (i / kPV) * T::kCV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
+    }
+    if (lane < 16) {
+      if constexpr (T::kBK > 0) cp_async_n<T::kBK>(sb + T::kOffKB + tt * T::kBK, p.k.bscale + row * T::kBK);
+      cp_async_small<4>(sb + T::kOffKR + tt * 4, p.k.rscale + row);
+    } else {
+      if constexpr (T::kBV > 0) cp_async_n<T::kBV>(sb + T::kOffVB + tt * T::kBV, p.v.bscale + row * T::kBV);
+      cp_async_small<4>(sb + T::kOffVR + tt * 4, p.v.rscale + row);
+    }
+  };
+
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.0f, 0.0f}, R = 0.0f;
+  float o[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
+
+#pragma unroll
+  for (int j = 0; j < T::kStages - 1; ++j) {
+    issue(j, j);
+    cp_async_commit();
+  }
+  const int my_tiles = ntile > warp ? (ntile - warp + kAttnWarps - 1) / kAttnWarps : 0;
+  for (int it = 0; it < my_tiles; ++it) {
+    cp_async_wait<T::kStages - 2>();
+    __syncwarp();
+    const unsigned char* const sb = ring + (it % T::kStages) * T::kBytes;
+    const int t0 = t_begin + (warp + it * kAttnWarps) * 16;
+
+    // S = Q K^T over the 16 tokens: n-tile j holds tokens 8j .. 8j + 7
+    float sc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
+      const int tk = 8 * j + g;
+      if constexpr (kFK == 3) {
+        const uint32_t* kw = reinterpret_cast<const uint32_t*>(sb + T::kOffKC + tk * T::kCK + c * (D / 4));
+#pragma unroll
+        for (int kb = 0; kb < kKS; ++kb) {
+          const uint32_t wv = kw[kb];
+          mma_f16_16816(sc[j], qa[kb], e4m3x2_to_f16x2(wv), e4m3x2_to_f16x2(wv >> 16));
+        }
+      } else {
+        const uint32_t* kw = reinterpret_cast<const uint32_t*>(sb + T::kOffKC + tk * T::kCK + c * (D / 8));
+        const uint8_t* kbs = sb + T::kOffKB + tk * T::kBK + c * (D / 64);
+#pragma unroll
+        for (int kb = 0; kb < kKS; ++kb) {
+          const uint32_t wv = kw[kb / 2] >> (16 * (kb % 2));
+          const uint32_t bsh = e4m3_to_f16x2(kbs[kb / 4]) & 0xFFFFu;
+          const uint32_t bs2 = bsh | (bsh << 16);
+          mma_f16_16816(sc[j], qa[kb], hmul2(e2m1x2_to_f16x2(wv & 0xFFu), bs2),
+                        hmul2(e2m1x2_to_f16x2((wv >> 8) & 0xFFu), bs2));
+        }
+      }
+    }
+    // scores (log2 domain): row scale of K, query scale; tokens past the end masked
+    const float* krs = reinterpret_cast<const float*>(sb + T::kOffKR);
+    const float* vrs = reinterpret_cast<const float*>(sb + T::kOffVR);
+    float rv[2][2];
+    float mt[2] = {kNegInf, kNegInf};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 8 * j + 2 * c + (e & 1);
+        const float v = sc[j][e] * krs[tok] * qmul[e >> 1];
+        sc[j][e] = (t0 + tok < t_end) ? v : kNegInf;
+        mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
+      }
+      rv[j][0] = vrs[8 * j + 2 * c];
+      rv[j][1] = vrs[8 * j + 2 * c + 1];
+    }
+    float rmax = fmaxf(fmaxf(rv[0][0], rv[0][1]), fmaxf(rv[1][0], rv[1][1]));
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xFFFFFFFFu, mt[0], off));
+      mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xFFFFFFFFu, mt[1], off));
+      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
+    }
+    // running maxima: softmax m per row, V row-scale reference R
+    const float mn0 = fmaxf(m[0], mt[0]), mn1 = fmaxf(m[1], mt[1]);
+    const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
+    const float a0 = ex2(m[0] - mn0), a1 = ex2(m[1] - mn1);  // 0 while m is -inf
+    const float rr = R / Rn;
+    if (__any_sync(0xFFFFFFFFu, a0 != 1.0f || a1 != 1.0f || rr != 1.0f)) {
+      const float f0 = a0 * rr, f1 = a1 * rr;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        o[nt][0] *= f0;
+        o[nt][1] *= f0;
+        o[nt][2] *= f1;
+        o[nt][3] *= f1;
+      }
+    }
+    l[0] *= a0;
+    l[1] *= a1;
+    m[0] = mn0;
+    m[1] = mn1;
+    R = Rn;
+    // P' = exp2(s - m) * rs_v / R as the A operand of P V
+    const float rR = rcp_approx(Rn);
+    uint32_t pa[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float p0 = ex2(sc[j][0] - mn0), p1 = ex2(sc[j][1] - mn0);
+      const float p2 = ex2(sc[j][2] - mn1), p3 = ex2(sc[j][3] - mn1);
+      l[0] += p0 + p1;
+      l[1] += p2 + p3;
+      const float r0 = rv[j][0] * rR, r1 = rv[j][1] * rR;
+      pa[2 * j] = f32x2_to_f16x2(p0 * r0, p1 * r1);      // row g, tokens 8j + 2c, +1
+      pa[2 * j + 1] = f32x2_to_f16x2(p2 * r0, p3 * r1);  // row g + 8
+    }
+    // O += P' V: n-tile nt, column n = dim n * D/8 + nt; this lane supplies V for
+    // tokens (2c, 2c + 1) and (2c + 8, 2c + 9) at dims g * D/8 + nt
+    {
+      // the two token pairs of this lane
+      const int ta0 = 2 * c, ta1 = 2 * c + 8;
+      if constexpr (kFV == 3) {
+        const uint32_t* v0 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta0 * T::kCV + g * (D / 8));
+        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta0 + 1) * T::kCV + g * (D / 8));
+        const uint32_t* v2 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta1 * T::kCV + g * (D / 8));
+        const uint32_t* v3 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta1 + 1) * T::kCV + g * (D / 8));
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          const uint32_t sel = (nt % 4) | ((4 + nt % 4) << 4);
+          const uint32_t b01 = e4m3x2_to_f16x2(__byte_perm(v0[nt / 4], v1[nt / 4], sel) & 0xFFFFu);
+          const uint32_t b23 = e4m3x2_to_f16x2(__byte_perm(v2[nt / 4], v3[nt / 4], sel) & 0xFFFFu);
+          mma_f16_16816(o[nt], pa, b01, b23);
+        }
+      } else {
+        constexpr int kW = D / 64;  // code words per lane per token (D/16 bytes)
+        const uint32_t* v0 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta0 * T::kCV + g * (D / 16));
+        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta0 + 1) * T::kCV + g * (D / 16));
+        const uint32_t* v2 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta1 * T::kCV + g * (D / 16));
+        const uint32_t* v3 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta1 + 1) * T::kCV + g * (D / 16));
+        // nibble transpose: X byte j = (dim 2j of token a | dim 2j of token b << 4), Y: dims 2j + 1
+        uint32_t x01[kW > 0 ? kW : 1], y01[kW > 0 ? kW : 1], x23[kW > 0 ? kW : 1], y23[kW > 0 ? kW : 1];
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+          x01[i] = (v0[i] & 0x0F0F0F0Fu) | ((v1[i] & 0x0F0F0F0Fu) << 4);
+          y01[i] = ((v0[i] >> 4) & 0x0F0F0F0Fu) | (v1[i] & 0xF0F0F0F0u);
+          x23[i] = (v2[i] & 0x0F0F0F0Fu) | ((v3[i] & 0x0F0F0F0Fu) << 4);
+          y23[i] = ((v2[i] >> 4) & 0x0F0F0F0Fu) | (v3[i] & 0xF0F0F0F0u);
+        }
+        const uint8_t* vbs = sb + T::kOffVB;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          const int blk = (g * (D / 8) + nt) / 16;
+          const uint32_t bs01 = e4m3x2_to_f16x2(vbs[ta0 * T::kBV + blk] | (vbs[(ta0 + 1) * T::kBV + blk] << 8));
+          const uint32_t bs23 = e4m3x2_to_f16x2(vbs[ta1 * T::kBV + blk] | (vbs[(ta1 + 1) * T::kBV + blk] << 8));
+          const int bi = nt / 2;  // byte of the transposed words
+          const uint32_t w01 = (nt % 2 == 0) ? x01[bi / 4] : y01[bi / 4];
+          const uint32_t w23 = (nt % 2 == 0) ? x23[bi / 4] : y23[bi / 4];
+          const uint32_t b01 = hmul2(e2m1x2_to_f16x2((w01 >> (8 * (bi % 4))) & 0xFFu), bs01);
+          const uint32_t b23 = hmul2(e2m1x2_to_f16x2((w23 >> (8 * (bi % 4))) & 0xFFu), bs23);
+          mma_f16_16816(o[nt], pa, b01, b23);
+        }
+      }
+    }
+    __syncwarp();  // every lane has read this stage before it is refilled
+    issue(it + T::kStages - 1, (it + T::kStages - 1) % T::kStages);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, 2u);
+  l[0] += __shfl_xor_sync(0xFFFFFFFFu, l[0], 1);
+  l[0] += __shfl_xor_sync(0xFFFFFFFFu, l[0], 2);
+  l[1] += __shfl_xor_sync(0xFFFFFFFFu, l[1], 1);
+  l[1] += __shfl_xor_sync(0xFFFFFFFFu, l[1], 2);
+  const bool cta_bad = __syncthreads_or(bad ? 1 : 0) != 0 || bad_len;  // the ring is free after this
+
+  // per warp: O (true scale: O * R) by natural dim, and m, l per row
+  float* const mo = reinterpret_cast<float*>(smem) + warp * 16 * (D + 2);
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = g + 8 * (e >> 1);
+      const int n = 2 * c + (e & 1);
+      mo[row * (D + 2) + n * (D / 8) + nt] = o[nt][e] * R;
+    }
+  }
+  if (c == 0) {
+    mo[g * (D + 2) + D] = m[0];
+    mo[g * (D + 2) + D + 1] = l[0];
+    mo[(g + 8) * (D + 2) + D] = m[1];
+    mo[(g + 8) * (D + 2) + D + 1] = l[1];
+  }
+  __syncthreads();
+  const float* const mall = reinterpret_cast<const float*>(smem);
+  for (int idx = threadIdx.x; idx < p.group * D; idx += kAttnThreads) {
+    const int row = idx / D, d = idx % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[(w * 16 + row) * (D + 2) + D]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float mw = mall[(w * 16 + row) * (D + 2) + D];
+      const float f = mw == kNegInf ? 0.0f : ex2(mw - M);
+      L += mall[(w * 16 + row) * (D + 2) + D + 1] * f;
+      O += mall[(w * 16 + row) * (D + 2) + d] * f;
+    }
+    const int qh = h * p.group + row;
+    if (p.nsplit == 1) {
+      if (cta_bad) continue;  // a bad sequence leaves its output untouched
+      const float y = L > 0.0f ? O / L : 0.0f;
+      STX(p.out + static_cast<int64_t>(s) * p.o_row_pitch + static_cast<int64_t>(qh) * p.o_head_pitch + d,
+          static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu));
+    } else {
+      float* const wsr = p.ws + ((static_cast<int64_t>(s) * p.Hq + qh) * p.nsplit + split) * (D + 2);
+      STX(wsr + d, O);
+      if (d == 0) {
+        STX(wsr + D, M);
+        STX(wsr + D + 1, cta_bad ? __int_as_float(0x7FC00000) : L);  // NaN marks a bad sequence
+      }
+    }
+  }
+}
+
+// Merge of the splits of each (sequence, query head): o = sum_k O_k 2^(M_k - M) /
+// sum_k L_k 2^(M_k - M).  A NaN L (bad sequence) leaves the output untouched.
+template <int D>
+__global__ void __launch_bounds__(D) decode_attn_merge_kernel(const AttnParams p) {
+  const int sq = blockIdx.x;  // s * Hq + qh
+  const int s = sq / p.Hq, qh = sq % p.Hq;
+  const int d = threadIdx.x;
+  const float* const base = p.ws + static_cast<int64_t>(sq) * p.nsplit * (D + 2);
+  float M = kNegInf;
+  bool bad = false;
+  for (int k = 0; k < p.nsplit; ++k) {
+    M = fmaxf(M, LDX(base + k * (D + 2) + D));
+    bad = bad || isnan(LDX(base + k * (D + 2) + D + 1));
+  }
+  if (bad) return;
+  float L = 0.0f, O = 0.0f;
+  for (int k = 0; k < p.nsplit; ++k) {
+    const float mk = LDX(base + k * (D + 2) + D);
+    const float f = mk == kNegInf ? 0.0f : ex2(mk - M);
+    L += LDX(base + k * (D + 2) + D + 1) * f;
+    O += LDX(base + k * (D + 2) + d) * f;
+  }
+  const float y = L > 0.0f ? O / L : 0.0f;
+  STX(p.out + static_cast<int64_t>(s) * p.o_row_pitch + static_cast<int64_t>(qh) * p.o_head_pitch + d,
+      static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu));
+}
+
+template <int D, int kFK, int kFV>
+cudaError_t attn_launch(const AttnParams& p, cudaStream_t s) {
+  using T = AttnTile<D, kFK, kFV>;
+  auto k = decode_attn_kernel<D, kFK, kFV>;
+  if (T::kSmem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaSuccess;
+  const dim3 grid(p.nsplit, p.H, p.S);
+  KVQ_LAUNCH("decode_attn_kernel", s, k<<<grid, kAttnThreads, T::kSmem, s>>>(p); e = cudaGetLastError());
+  if (e != cudaSuccess || p.nsplit == 1) return e;
+  KVQ_LAUNCH("decode_attn_merge_kernel", s,
+             decode_attn_merge_kernel<D><<<p.S * p.Hq, D, 0, s>>>(p); e = cudaGetLastError());
+  return e;
+}
+
+template <int D>
+cudaError_t attn_dispatch_fmt(const AttnParams& p, cudaStream_t s) {
+  const bool k8 = p.fmt_k == 3, v8 = p.fmt_v == 3;
+  if (!k8 && !v8) return attn_launch<D, 1, 1>(p, s);
+  if (k8 && !v8) return attn_launch<D, 3, 1>(p, s);
+  if (!k8 && v8) return attn_launch<D, 1, 3>(p, s);
+  return attn_launch<D, 3, 3>(p, s);
+}
+
+}  // namespace
+
+int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len) {
+  const int64_t pairs = static_cast<int64_t>(S) * H;
+  if (pairs <= 0 || max_seq_len <= 0) return 1;
+  const int64_t want = (3LL * num_sms() + pairs - 1) / pairs;  // about 3 CTAs per SM
+  const int64_t cap = (max_seq_len + 255) / 256;               // at least 256 tokens per split
+  int64_t n = want < cap ? want : cap;
+  return static_cast<int>(n < 1 ? 1 : (n > 64 ? 64 : n));
+}
+
+cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s) {
+  switch (p.D) {
+    case 64: return attn_dispatch_fmt<64>(p, s);
+    case 128: return attn_dispatch_fmt<128>(p, s);
+    case 256: return attn_dispatch_fmt<256>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

@@ -611,6 +611,111 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Splits and tokens per split of a decode-attention call (tokens per split a multiple
+// of 64: whole 16-token tiles for each of the 4 warps).
+static void attn_geometry(int32_t S, int32_t H, int32_t max_seq_len, int* nsplit, int* split_len) {
+  *nsplit = attn_num_splits(S, H, max_seq_len);
+  const int64_t per = (static_cast<int64_t>(max_seq_len) + *nsplit - 1) / *nsplit;
+  *split_len = static_cast<int>(((per + 63) / 64) * 64);
+  if (*split_len <= 0) *split_len = 64;
+}
+
+KVQ_API size_t kvq_decode_attention_workspace(int32_t num_seqs, int32_t num_heads, int32_t num_q_heads,
+                                              int32_t head_dim, int32_t max_seq_len) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+  int nsplit = 1, split_len = 64;
+  attn_geometry(num_seqs, num_heads, max_seq_len, &nsplit, &split_len);
+  if (nsplit <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * num_q_heads * nsplit * (head_dim + 2) * sizeof(float);
+}
+
+KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* block_table,
+                                        int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
+                                        int32_t max_seq_len, const kvq_bf16_in* q, int32_t num_q_heads,
+                                        float scale, const kvq_bf16_out* out, void* workspace,
+                                        size_t workspace_bytes, uint32_t* dev_status,
+                                        kvq_stream_t stream) {
+  if (pool == nullptr || q == nullptr || out == nullptr)
+    return fail(KVQ_ERR_INVALID_ARG, "pool, q and out must not be NULL");
+  if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
+  kvq_status st = check_head_dim(pool->num_heads, pool->head_dim);
+  if (st != KVQ_OK) return st;
+  const int32_t D = pool->head_dim, H = pool->num_heads;
+  if (D != 64 && D != 128 && D != 256)
+    return fail(KVQ_ERR_UNSUPPORTED, "decode attention supports head_dim 64, 128 or 256 (got %d)", D);
+  if (pool->block_size <= 0 || pool->num_slots < 0 || pool->num_slots % pool->block_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_slots must be a non-negative multiple of block_size");
+  if (num_seqs < 0 || max_blocks < 0 || max_seq_len < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "negative num_seqs, max_blocks or max_seq_len");
+  if (num_q_heads <= 0 || num_q_heads % H != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_heads");
+  if (num_q_heads / H > 16) return fail(KVQ_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+  if (num_seqs > 65535 || H > 65535) return fail(KVQ_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
+  if (num_seqs == 0) return KVQ_OK;
+  if (!fits_u31(static_cast<int64_t>(num_seqs) * num_q_heads * D))
+    return fail(KVQ_ERR_UNSUPPORTED, "num_seqs x num_q_heads x head_dim too large");
+  bool v8 = true;
+  if ((st = check_view(q->ptr, q->row_pitch, q->head_pitch, "q", v8)) != KVQ_OK) return st;
+  if ((st = check_view(out->ptr, out->row_pitch, out->head_pitch, "out", v8)) != KVQ_OK) return st;
+  const int32_t fk = plane_fmt(pool, 0), fv = plane_fmt(pool, 1);
+  if ((st = check_pool_plane(fk, &pool->k)) != KVQ_OK) return st;
+  if ((st = check_pool_plane(fv, &pool->v)) != KVQ_OK) return st;
+  if ((st = check_dev(block_table, "block_table")) != KVQ_OK) return st;
+  if ((st = check_dev(seq_lens, "seq_lens")) != KVQ_OK) return st;
+  if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
+
+  AttnParams p{};
+  attn_geometry(num_seqs, H, max_seq_len, &p.nsplit, &p.split_len);
+  const size_t need = kvq_decode_attention_workspace(num_seqs, H, num_q_heads, D, max_seq_len);
+  if (need > 0) {
+    if ((st = check_dev(workspace, "workspace")) != KVQ_OK) return st;
+    if (!aligned(workspace, 16)) return fail(KVQ_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need)
+      return fail(KVQ_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, need);
+  }
+  p.k = AttnPlane{pool->k.codes, pool->k.bscale, pool->k.rscale};
+  p.v = AttnPlane{pool->v.codes, pool->v.bscale, pool->v.rscale};
+  p.fmt_k = fk;
+  p.fmt_v = fv;
+  p.q = static_cast<const uint16_t*>(q->ptr);
+  p.q_row_pitch = q->row_pitch;
+  p.q_head_pitch = q->head_pitch;
+  p.out = static_cast<uint16_t*>(out->ptr);
+  p.o_row_pitch = out->row_pitch;
+  p.o_head_pitch = out->head_pitch;
+  p.ws = static_cast<float*>(workspace);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks;
+  const int64_t cap = static_cast<int64_t>(max_blocks) * pool->block_size;
+  p.seq_cap = static_cast<int32_t>(cap < max_seq_len ? cap : max_seq_len);
+  p.block_size = pool->block_size;
+  p.div_bs = FastDiv(static_cast<uint32_t>(pool->block_size));
+  p.num_blocks = pool->num_slots / pool->block_size;
+  p.S = num_seqs;
+  p.H = H;
+  p.Hq = num_q_heads;
+  p.D = D;
+  p.group = num_q_heads / H;
+  p.scale = scale;
+  p.status = dev_status;
+  dbg_clear();
+  const int64_t rh = pool->num_slots * H;
+  dbg_add(pool->k.codes, rh * code_bytes_per_row(fk, D), "k codes");
+  if (fk == KVQ_FMT_NVFP4) dbg_add(pool->k.bscale, rh * (D / 16), "k bscale");
+  dbg_add(pool->k.rscale, rh * 4, "k rscale");
+  dbg_add(pool->v.codes, rh * code_bytes_per_row(fv, D), "v codes");
+  if (fv == KVQ_FMT_NVFP4) dbg_add(pool->v.bscale, rh * (D / 16), "v bscale");
+  dbg_add(pool->v.rscale, rh * 4, "v rscale");
+  dbg_add(q->ptr, view_bytes(num_seqs, q->row_pitch, num_q_heads, q->head_pitch, D), "q");
+  dbg_add(out->ptr, view_bytes(num_seqs, out->row_pitch, num_q_heads, out->head_pitch, D), "out");
+  dbg_add(block_table, 4ll * num_seqs * max_blocks, "block_table");
+  dbg_add(seq_lens, 4ll * num_seqs, "seq_lens");
+  if (need > 0) dbg_add(workspace, static_cast<int64_t>(need), "workspace");
+  dbg_add(dev_status, 4, "status");
+  return launched(launch_decode_attention(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_size, int64_t rows,
                                  int32_t heads, int32_t dim) {
   if (rows < 0 || heads <= 0 || dim <= 0) return 0;

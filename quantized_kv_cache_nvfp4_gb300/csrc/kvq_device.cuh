@@ -354,6 +354,29 @@ __device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) 
   hi = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
 }
 
+// Codes of one 16-element block against s = bs * rs; returns the 8 code bytes as
+// two words (low nibble of each byte = the even element).
+__device__ __forceinline__ void quantize_block(const uint32_t (&w)[8], float s, uint32_t& c0,
+                                               uint32_t& c1) {
+  const float inv = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
+  uint32_t byte[8];
+  if (!isinf(inv)) {
+    const uint64_t inv2 = pack_f32x2(__float_as_uint(inv), __float_as_uint(inv));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t ql, qh;
+      unpack_f32x2(mul_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), inv2), ql, qh);
+      byte[i] = e2m1x2_from_f32(__uint_as_float(ql), __uint_as_float(qh));
+    }
+  } else {  // tiny scale: the reciprocal overflowed, divide directly
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      byte[i] = e2m1x2_from_f32(__fdiv_rn(bf16lo(w[i]), s), __fdiv_rn(bf16hi(w[i]), s));
+  }
+  c0 = bytes4(byte[0], byte[1], byte[2], byte[3]);
+  c1 = bytes4(byte[4], byte[5], byte[6], byte[7]);
+}
+
 // NVFP4 decode of one 16-element block: y = bf16((e2m1 * bs) * rs).  e2m1 * bs is
 // exact (fma.rn.f32.f16 of two fp16 values, at most 6 significant bits), then one
 // binary32 rounding by the row scale, then bf16.

@@ -178,6 +178,41 @@ cudaError_t launch_nvfp4_encode(const EncodeParams& p, int mode, int fmt, bool v
 cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int fmt, bool v8,
                                 cudaStream_t s);
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Paged decode attention over the quantised pool.
+// ---------------------------------------------------------------------------
+struct AttnPlane {
+  const uint8_t* codes;   // [slots][H][D/2] (NVFP4) or [slots][H][D] (FP8)
+  const uint8_t* bscale;  // [slots][H][D/16] (NVFP4)
+  const float* rscale;    // [slots][H]
+};
+
+struct AttnParams {
+  AttnPlane k, v;
+  int32_t fmt_k, fmt_v;
+  const uint16_t* q;        // bf16 [S][Hq][D] through the pitches below
+  int64_t q_row_pitch, q_head_pitch;
+  uint16_t* out;            // bf16, same indexing through its own pitches
+  int64_t o_row_pitch, o_head_pitch;
+  float* ws;                // split partials [S][Hq][nsplit][D + 2] (nsplit > 1)
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t max_blocks;
+  int32_t seq_cap;          // max_blocks * block_size
+  int32_t block_size;
+  FastDiv div_bs;
+  int64_t num_blocks;
+  int32_t S, H, Hq, D, group;  // group = Hq / H query heads per KV head
+  int32_t nsplit;
+  int32_t split_len;        // tokens per split, a multiple of 64
+  float scale;              // softmax scale applied to q . k
+  uint32_t* status;
+};
+
+// Split count for a call: enough CTAs to fill the GPU, each split at least 256 tokens.
+int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len);
+cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_payload_decode(const UnpackParams& p, int lanes, bool v8, cudaStream_t s);
 
 int num_sms();

@@ -92,28 +92,6 @@ __device__ __forceinline__ void load_source(const EncodeParams& p, const RowLoc&
   }
 }
 
-// Codes of one 16-element block against s = bs * rs; returns the 8 code bytes as
-// two words (low nibble of each byte = the even element).
-__device__ __forceinline__ void quantize_block(const uint32_t (&w)[8], float s, uint32_t& c0,
-                                               uint32_t& c1) {
-  const float inv = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
-  uint32_t byte[8];
-  if (!isinf(inv)) {
-    const uint64_t inv2 = pack_f32x2(__float_as_uint(inv), __float_as_uint(inv));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t ql, qh;
-      unpack_f32x2(mul_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), inv2), ql, qh);
-      byte[i] = e2m1x2_from_f32(__uint_as_float(ql), __uint_as_float(qh));
-    }
-  } else {  // tiny scale: the reciprocal overflowed, divide directly
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      byte[i] = e2m1x2_from_f32(__fdiv_rn(bf16lo(w[i]), s), __fdiv_rn(bf16hi(w[i]), s));
-  }
-  c0 = bytes4(byte[0], byte[1], byte[2], byte[3]);
-  c1 = bytes4(byte[4], byte[5], byte[6], byte[7]);
-}
 
 template <int L, int BPL, bool kV8, int kMode, int kMinBlocks, int kFmt>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(const EncodeParams p) {

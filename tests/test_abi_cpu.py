@@ -92,3 +92,23 @@ def test_host_checks_fail_before_any_cuda_call(kvq_lib_path):
     assert lib.kvq_quant_scatter(ctypes.byref(x), None, 0, None, ctypes.byref(pool), None, None) == 0
     pk = _abi.Packed(2, 0, 64, 0, 2, 128, None, None, None, None)
     assert lib.kvq_pack(ctypes.byref(x), ctypes.byref(pk), None) == 0
+
+
+def test_decode_attention_host_checks(kvq_lib_path):
+    from quantized_kv_cache_nvfp4_gb300 import _abi
+
+    lib = _abi.load()
+    assert lib.kvq_decode_attention_workspace(0, 8, 32, 128, 8192) == 0
+    assert lib.kvq_decode_attention_workspace(32, 8, 32, 128, 0) == 0
+    pool = _abi.Pool(_abi.Plane(), _abi.Plane(), 64, 16, 2, 96, 1)
+    q = _abi.Bf16In(None, 8 * 96, 96)
+    o = _abi.Bf16Out(None, 8 * 96, 96)
+    call = lambda hq: lib.kvq_decode_attention(ctypes.byref(pool), None, 1, 4, None, 64, ctypes.byref(q), hq,
+                                               0.1, ctypes.byref(o), None, 0, None, None)
+    assert call(8) == 2 and b"head_dim" in lib.kvq_last_error()  # 96 is not 64/128/256
+    pool.head_dim = 128
+    assert call(3) == 1 and b"multiple of num_heads" in lib.kvq_last_error()
+    assert call(34) == 2 and b"16 query heads" in lib.kvq_last_error()
+    assert call(8) == 1 and b"NULL" in lib.kvq_last_error()  # q's pointer
+    assert lib.kvq_decode_attention(None, None, 1, 4, None, 64, ctypes.byref(q), 8, 0.1, ctypes.byref(o), None,
+                                    0, None, None) == 1
