@@ -687,6 +687,69 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+CASES = ("attention_nvfp4", "attention_fp8", "attention_k8v4", "int4_pack_key", "int4_pack_value",
+         "int4_residual_key", "nvfp4t_pack_key", "nvfp4t_pack_value")
+
+
+def run_case(args):
+    """One kernel's workload alone (for profiler captures): `args.warmup` untimed calls,
+    then `args.steps` timed ones; prints one JSON line with the mean time per call.
+    attention_*: the decode-attention pool of 32 x 8192 tokens, 8 KV / 32 query heads,
+    D128; int4_* and nvfp4t_*: a [131072, 8, 128] bf16 tensor (residual: 25% of rows)."""
+    import math
+
+    import quantized_kv_cache_nvfp4_gb300 as kvq
+    from quantized_kv_cache_nvfp4_gb300 import synth
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    name = args.case
+    if name.startswith("attention"):
+        S, T, H, Hq, D, bs = 32, 8192, 8, 32, 128, BLOCK
+        fk, fv = {"attention_nvfp4": (kvq.FMT_NVFP4, None), "attention_fp8": (kvq.FMT_FP8, None),
+                  "attention_k8v4": (kvq.FMT_FP8, kvq.FMT_NVFP4)}[name]
+        nblocks = S * T // bs
+        perm = synth.block_permutation(nblocks, 3).to(device)
+        table = perm.view(S, T // bs).contiguous()
+        t = torch.arange(T, device=device)
+        slots = (table[:, t // bs].long() * bs + t % bs).reshape(-1)
+        lens = torch.full((S,), T, dtype=torch.int32, device=device)
+        q = synth.normal_bf16((S, Hq, D), 3, 9, device=str(device))
+        out = torch.empty_like(q)
+        pool = kvq.KvPool.empty(nblocks * bs, H, D, bs, device=device, fmt=fk, v_fmt=fv)
+        k = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_K, device=str(device))
+        v = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_V, device=str(device))
+        kvq.kvq_quant_scatter(k, v, slots, pool)
+        del k, v
+        ws = torch.empty(max(kvq.kvq_decode_attention_workspace(S, H, Hq, D, T), 16), dtype=torch.uint8,
+                         device=device)
+        fn = lambda: kvq.kvq_decode_attention(pool, table, lens, T, q, 1.0 / math.sqrt(D), out, workspace=ws)
+    else:
+        T, H, D, G = 131072, 8, 128, 64
+        cur, prev = synth.layer_kv(T, H, D, seed=4, device=str(device))
+        kind = kvq.KIND_KEY if name.endswith("key") else kvq.KIND_VALUE
+        if name.startswith("int4_pack"):
+            pk = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G, device=device)
+            fn = lambda: kvq.kvq_pack(cur, pk)
+        elif name.startswith("int4_residual"):
+            pos = synth.sorted_positions(T, T // 4, 4).to(device)
+            pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 4, H, D, G, device=device)
+            fn = lambda: kvq.kvq_encode_residual(cur, prev, pos, pay)
+        else:
+            pk = kvq.Packed.empty(kvq.FMT_NVFP4_TENSOR, kind, T, H, D, device=device)
+            fn = lambda: kvq.kvq_pack(cur, pk)
+    for _ in range(max(args.warmup, 1)):
+        fn()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(max(args.steps, 1)):
+        fn()
+    b.record()
+    torch.cuda.synchronize(device)
+    print(json.dumps({"case": name, "steps": args.steps, "ms_per_call": round(a.elapsed_time(b) / max(args.steps, 1), 4)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -704,10 +767,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run one kernel's workload alone (for profiler captures) instead of the bench")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case is not None:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

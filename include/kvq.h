@@ -70,7 +70,12 @@ typedef enum {
   KVQ_ERR_CUDA = 5            /* the CUDA runtime reported an error at launch */
 } kvq_status;
 
-typedef enum { KVQ_FMT_NVFP4 = 1, KVQ_FMT_INT4 = 2, KVQ_FMT_FP8 = 3 } kvq_format;
+typedef enum {
+  KVQ_FMT_NVFP4 = 1,        /* row codec: E2M1 + E4M3 per 16 + one FP32 scale per row */
+  KVQ_FMT_INT4 = 2,         /* affine INT4, FP16 minimum and scale per group of G */
+  KVQ_FMT_FP8 = 3,          /* E4M3 + one FP32 scale per row */
+  KVQ_FMT_NVFP4_TENSOR = 4  /* E2M1 + E4M3 per 16 along the kind's axis + one FP32 scale per tensor */
+} kvq_format;
 typedef enum { KVQ_KIND_KEY = 0, KVQ_KIND_VALUE = 1 } kvq_kind;
 
 /* Bits ORed into *dev_status by the kernels. */
@@ -123,6 +128,11 @@ typedef struct {
  *              rscale float [rows][heads], meta1 unused; group_size must be 16.
  *   fmt FP8  : codes [rows][heads][dim] E4M3, rscale float [rows][heads]; meta0 and
  *              meta1 unused; group_size ignored.
+ *   fmt NVFP4_TENSOR: the logical NVFP4 layout of vllm-rlt PR #166 (Purpose): codes
+ *              [rows][heads][dim/2], meta0 = bscale uint8, [ceil(rows/16)][heads][dim]
+ *              for kind KEY (16 token rows per head and channel) or [rows][heads][dim/16]
+ *              for kind VALUE (16 channels), rscale float [1] = tensor amax / 2688;
+ *              group_size 16.  Logical pack / unpack only.
  *   fmt INT4 : codes [rows][heads][dim/2], meta0 = FP16 minimum, meta1 = FP16 scale,
  *              each [ceil(rows/G)][heads][dim] for kind KEY (groups of G token rows
  *              per head and channel) or [rows][heads][ceil(dim/G)] for kind VALUE
@@ -231,10 +241,11 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
  *   workspace  device memory of kvq_decode_attention_workspace(...) bytes, 16-byte
  *              aligned (may be NULL when that is 0); caller-owned, reused by the next
  *              call on the same stream.
- * Accuracy: K and V decode exactly; the products run in f16 with f32 accumulation
- * (P rounded to f16 relative to a running maximum), so the output is within a few
- * bf16 ulps of the exact attention of the decoded rows (tests/test_attention_gpu.py
- * states the bound).
+ * Accuracy: K, V and Q enter the f16 MMA exactly (Q through a power-of-two
+ * prescale); products and sums are fp32; P is rounded once to f16 (relative 2^-11,
+ * against a running maximum of V's row scales) and the output once to bf16, so
+ * |out - exact| <= 2^-9 |exact| + 2^-11 max|v| plus fp32 rounding, where exact is
+ * the attention of the decoded rows.
  * An empty sequence writes zeros.  A bad length (KVQ_DEV_BAD_SEQLEN) or a block
  * entry outside the pool (KVQ_DEV_BAD_BLOCK) leaves that sequence's output untouched.
  * One or two kernel launches. */
@@ -244,6 +255,21 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
                                         float scale, const kvq_bf16_out* out, void* workspace,
                                         size_t workspace_bytes, uint32_t* dev_status,
                                         kvq_stream_t stream);
+
+/* kvq_decode_attention without a workspace argument: it allocates nothing and uses
+ * the library's built-in scratch (48 MiB of device memory in the library image)
+ * for the split partials.  The split policy keeps the partials under 40.2 MB on a
+ * 152-SM GPU for every supported shape; KVQ_ERR_UNSUPPORTED if they would not fit
+ * (kvq_decode_attention_workspace(...) > 48 MiB).  The scratch is one per device:
+ * calls of this entry point must not overlap (different streams, or graphs
+ * replayed concurrently); kvq_decode_attention with a caller workspace has no
+ * such limit.  Same arguments, results and errors otherwise. */
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_pool* pool, const int32_t* block_table,
+                                                int32_t num_seqs, int32_t max_blocks,
+                                                const int32_t* seq_lens, int32_t max_seq_len,
+                                                const kvq_bf16_in* q, int32_t num_q_heads, float scale,
+                                                const kvq_bf16_out* out, uint32_t* dev_status,
+                                                kvq_stream_t stream);
 
 /* Workspace bytes kvq_decode_attention needs for these sizes on the current device
  * (0 when the call runs without one).  Host-only query. */

@@ -20,13 +20,14 @@ import torch
 
 from . import _abi
 from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT_FP8, FMT_INT4,
+                   FMT_NVFP4_TENSOR,
                    FMT_NVFP4, KIND_KEY, KIND_VALUE)
 
 __all__ = [
     "KvqError", "KvPool", "Nvfp4Pool", "Packed", "kvq_quant_scatter", "kvq_restore", "kvq_pack",
     "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_decode_attention",
-    "kvq_decode_attention_workspace", "kvq_storage_bytes",
-    "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "FMT_FP8", "KIND_KEY",
+    "kvq_decode_attention_workspace", "kvq_decode_attention_noalloc", "kvq_storage_bytes",
+    "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "FMT_FP8", "FMT_NVFP4_TENSOR", "KIND_KEY",
     "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN",
 ]
 
@@ -174,6 +175,12 @@ class Packed:
     @classmethod
     def empty(cls, fmt: int, kind: int, rows: int, heads: int, dim: int, group_size: int = 64,
               device="cuda") -> "Packed":
+        if fmt == FMT_NVFP4_TENSOR:
+            bs = (math.ceil(rows / 16), heads, dim) if kind == KIND_KEY else (rows, heads, dim // 16)
+            return cls(fmt, kind, 16, rows, heads, dim,
+                       torch.empty((rows, heads, dim // 2), dtype=torch.uint8, device=device),
+                       torch.empty(bs, dtype=torch.uint8, device=device), None,
+                       torch.empty((1,), dtype=torch.float32, device=device))
         if fmt == FMT_FP8:
             return cls(fmt, kind, 0, rows, heads, dim,
                        torch.empty((rows, heads, dim), dtype=torch.uint8, device=device), None, None,
@@ -327,6 +334,24 @@ def kvq_decode_attention(pool: KvPool, block_table: torch.Tensor, seq_lens: torc
     _check(_lib().kvq_decode_attention(
         ctypes.byref(ps), _ptr(block_table), S, max_blocks, _ptr(seq_lens), max_seq_len, ctypes.byref(qi), Hq,
         float(scale), ctypes.byref(oo), _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def kvq_decode_attention_noalloc(pool: KvPool, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                 max_seq_len: int, q: torch.Tensor, scale: float, out: torch.Tensor,
+                                 dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kvq_decode_attention with the library's built-in split scratch: no workspace and no
+    allocation (calls must not overlap on one device)."""
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [S, max_blocks]")
+    S, max_blocks = block_table.shape
+    qi, oo = _bf16_in(q, "q"), _bf16_out(out, "out")
+    ps = pool._struct()
+    _check(_lib().kvq_decode_attention_noalloc(
+        ctypes.byref(ps), _ptr(block_table), S, max_blocks, _ptr(seq_lens), max_seq_len, ctypes.byref(qi),
+        q.size(1), float(scale), ctypes.byref(oo), _ptr(dev_status), _stream(stream)))
     return out
 
 

@@ -20,6 +20,7 @@ STATUS_NAMES = {
 FMT_NVFP4 = 1
 FMT_INT4 = 2
 FMT_FP8 = 3
+FMT_NVFP4_TENSOR = 4
 KIND_KEY = 0
 KIND_VALUE = 1
 
@@ -89,6 +90,8 @@ SIGNATURES = {
                                    _I32, ctypes.c_float, ctypes.POINTER(Bf16Out), _P, ctypes.c_size_t,
                                    _P, _P]),
     "kvq_decode_attention_workspace": (ctypes.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
+    "kvq_decode_attention_noalloc": (_ST, [ctypes.POINTER(Pool), _P, _I32, _I32, _P, _I32, ctypes.POINTER(Bf16In),
+                                           _I32, ctypes.c_float, ctypes.POINTER(Bf16Out), _P, _P]),
     "kvq_storage_bytes": (ctypes.c_size_t, [_ST, _ST, _I32, _I64, _I32, _I32]),
     "kvq_status_string": (ctypes.c_char_p, [_ST]),
     "kvq_last_error": (ctypes.c_char_p, []),

@@ -48,6 +48,13 @@ void dbg_packed(const kvq_packed* pk) {
     return;
   }
   dbg_add(pk->codes, rh * (pk->dim / 2), "codes");
+  if (pk->fmt == KVQ_FMT_NVFP4_TENSOR) {
+    const int64_t nb = pk->kind == KVQ_KIND_KEY ? static_cast<int64_t>((pk->rows + 15) / 16) * pk->heads * pk->dim
+                                                : rh * (pk->dim / 16);
+    dbg_add(pk->meta0, nb, "bscale");
+    dbg_add(pk->rscale, 4, "rscale");
+    return;
+  }
   if (pk->fmt == KVQ_FMT_NVFP4) {
     dbg_add(pk->meta0, rh * (pk->dim / 16), "bscale");
     dbg_add(pk->rscale, rh * 4, "rscale");
@@ -174,6 +181,17 @@ kvq_status check_packed(const kvq_packed* pk, const char* what) {
   } else if (pk->fmt == KVQ_FMT_FP8) {
     if (pk->rows == 0) return KVQ_OK;
     if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->rscale, "rscale")) != KVQ_OK) return st;
+  } else if (pk->fmt == KVQ_FMT_NVFP4_TENSOR) {
+    if (pk->group_size != 16 && pk->group_size != 0)
+      return fail(KVQ_ERR_INVALID_ARG, "%s: NVFP4 groups are 16 values", what);
+    if (pk->kind != KVQ_KIND_KEY && pk->kind != KVQ_KIND_VALUE)
+      return fail(KVQ_ERR_INVALID_ARG, "%s: kind must be KEY or VALUE", what);
+    if (!fits_u31(static_cast<int64_t>(pk->rows) * pk->heads * pk->dim))
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: rows x heads x dim too large", what);
+    if (pk->rows == 0) return KVQ_OK;
+    if ((st = check_plane(pk->codes, "codes")) != KVQ_OK) return st;
+    if ((st = check_plane(pk->meta0, "meta0 (block scales)")) != KVQ_OK) return st;
     if ((st = check_plane(pk->rscale, "rscale")) != KVQ_OK) return st;
   } else if (pk->fmt == KVQ_FMT_INT4) {
     const int G = pk->group_size;
@@ -412,6 +430,23 @@ KVQ_API kvq_status kvq_pack(const kvq_bf16_in* x, const kvq_packed* out, kvq_str
   dbg_clear();
   dbg_add(x->ptr, view_bytes(out->rows, x->row_pitch, out->heads, x->head_pitch, out->dim), "x");
   dbg_packed(out);
+  if (out->fmt == KVQ_FMT_NVFP4_TENSOR) {
+    TensorNvfp4Params p{};
+    p.x = static_cast<const uint16_t*>(x->ptr);
+    p.row_pitch = x->row_pitch;
+    p.head_pitch = x->head_pitch;
+    p.codes = out->codes;
+    p.bscale = static_cast<uint8_t*>(out->meta0);
+    p.rscale = out->rscale;
+    p.rows = out->rows;
+    p.H = out->heads;
+    p.D = out->dim;
+    p.kind = out->kind;
+    p.div_h = FastDiv(static_cast<uint32_t>(out->heads));
+    p.div_nb = FastDiv(static_cast<uint32_t>(out->dim / 16));
+    p.div_np = FastDiv(static_cast<uint32_t>(out->dim / 2));
+    return launched(launch_tensor_nvfp4_pack(p, s));
+  }
   if (out->fmt == KVQ_FMT_NVFP4 || out->fmt == KVQ_FMT_FP8) {
     EncodeParams p{};
     p.ten[0].x = static_cast<const uint16_t*>(x->ptr);
@@ -449,6 +484,26 @@ KVQ_API kvq_status kvq_unpack(const kvq_packed* in, const kvq_bf16_out* y, kvq_s
   if (in->rows == 0) return KVQ_OK;
   bool v8 = true;
   if ((st = check_view(y->ptr, y->row_pitch, y->head_pitch, "y", v8)) != KVQ_OK) return st;
+  if (in->fmt == KVQ_FMT_NVFP4_TENSOR) {
+    TensorNvfp4Params p{};
+    p.codes = in->codes;
+    p.bscale = static_cast<uint8_t*>(in->meta0);
+    p.rscale = in->rscale;
+    p.y = static_cast<uint16_t*>(y->ptr);
+    p.y_row_pitch = y->row_pitch;
+    p.y_head_pitch = y->head_pitch;
+    p.rows = in->rows;
+    p.H = in->heads;
+    p.D = in->dim;
+    p.kind = in->kind;
+    p.div_h = FastDiv(static_cast<uint32_t>(in->heads));
+    p.div_nb = FastDiv(static_cast<uint32_t>(in->dim / 16));
+    p.div_np = FastDiv(static_cast<uint32_t>(in->dim / 2));
+    dbg_clear();
+    dbg_add(y->ptr, view_bytes(in->rows, y->row_pitch, in->heads, y->head_pitch, in->dim), "y");
+    dbg_packed(in);
+    return launched(launch_tensor_nvfp4_unpack(p, reinterpret_cast<cudaStream_t>(stream)));
+  }
   UnpackParams u{};
   u.pay = payload_ref(in);
   u.H = in->heads;
@@ -472,6 +527,8 @@ KVQ_API kvq_status kvq_encode_residual(const kvq_bf16_in* cur, const kvq_bf16_in
                                        const kvq_packed* payload, int32_t* pos_out,
                                        uint32_t* dev_status, kvq_stream_t stream) {
   kvq_status st = check_packed(payload, "payload");
+  if (st == KVQ_OK && payload->fmt == KVQ_FMT_NVFP4_TENSOR)
+    return fail(KVQ_ERR_UNSUPPORTED, "residual payloads are NVFP4 rows, FP8 rows or INT4");
   if (st != KVQ_OK) return st;
   if (cur == nullptr || prev == nullptr) return fail(KVQ_ERR_INVALID_ARG, "cur or prev is NULL");
   if (num_rows < 0 || num_pos < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_rows or num_pos");
@@ -545,6 +602,8 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
                                        int32_t num_rows, const kvq_bf16_out* out,
                                        uint32_t* dev_status, kvq_stream_t stream) {
   kvq_status st = check_packed(payload, "payload");
+  if (st == KVQ_OK && payload->fmt == KVQ_FMT_NVFP4_TENSOR)
+    return fail(KVQ_ERR_UNSUPPORTED, "residual payloads are NVFP4 rows, FP8 rows or INT4");
   if (st != KVQ_OK) return st;
   if (prev == nullptr || out == nullptr) return fail(KVQ_ERR_INVALID_ARG, "prev or out is NULL");
   if (num_rows < 0 || num_pos < 0) return fail(KVQ_ERR_INVALID_ARG, "negative num_rows or num_pos");
@@ -716,6 +775,30 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
   return launched(launch_decode_attention(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_pool* pool, const int32_t* block_table,
+                                                int32_t num_seqs, int32_t max_blocks,
+                                                const int32_t* seq_lens, int32_t max_seq_len,
+                                                const kvq_bf16_in* q, int32_t num_q_heads, float scale,
+                                                const kvq_bf16_out* out, uint32_t* dev_status,
+                                                kvq_stream_t stream) {
+  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
+  if (num_seqs <= 0) return kvq_decode_attention(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len,
+                                                 q, num_q_heads, scale, out, nullptr, 0, dev_status, stream);
+  const size_t need = kvq_decode_attention_workspace(num_seqs, pool->num_heads, num_q_heads, pool->head_dim,
+                                                     max_seq_len);
+  if (need > attn_builtin_scratch_bytes())
+    return fail(KVQ_ERR_UNSUPPORTED, "split partials need %zu bytes, more than the built-in %zu", need,
+                attn_builtin_scratch_bytes());
+  void* scratch = nullptr;
+  size_t cap = 0;
+  if (need > 0) {
+    const cudaError_t e = attn_builtin_scratch(&scratch, &cap);
+    if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "built-in scratch: %s", cudaGetErrorString(e));
+  }
+  return kvq_decode_attention(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, q, num_q_heads,
+                              scale, out, scratch, cap, dev_status, stream);
+}
+
 KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_size, int64_t rows,
                                  int32_t heads, int32_t dim) {
   if (rows < 0 || heads <= 0 || dim <= 0) return 0;
@@ -725,6 +808,11 @@ KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_si
     return static_cast<size_t>(rh * (dim / 2 + dim / 16 + 4));
   }
   if (fmt == KVQ_FMT_FP8) return static_cast<size_t>(rh * (dim + 4));
+  if (fmt == KVQ_FMT_NVFP4_TENSOR) {
+    if (dim % 16 != 0 || (kind != KVQ_KIND_KEY && kind != KVQ_KIND_VALUE)) return 0;
+    const int64_t blocks = kind == KVQ_KIND_KEY ? ((rows + 15) / 16) * heads * dim : rh * (dim / 16);
+    return static_cast<size_t>(rh * (dim / 2) + blocks + 4);
+  }
   if (fmt == KVQ_FMT_INT4) {
     if (dim % 2 != 0 || group_size <= 0) return 0;
     const int64_t codes = rh * (dim / 2);

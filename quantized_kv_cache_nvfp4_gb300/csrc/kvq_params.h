@@ -180,6 +180,26 @@ cudaError_t launch_nvfp4_decode(const DecodeParams& p, int mode, int fmt, bool v
 cudaError_t launch_int4_encode(const Int4EncodeParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// NVFP4 with one FP32 scale per tensor (logical pack / unpack).
+// ---------------------------------------------------------------------------
+struct TensorNvfp4Params {
+  const uint16_t* x;        // pack source [rows][H][D] through the pitches
+  int64_t row_pitch, head_pitch;
+  uint8_t* codes;           // [rows][H][D/2]
+  uint8_t* bscale;          // KEY [ceil(rows/16)][H][D], VALUE [rows][H][D/16]
+  float* rscale;            // [1]
+  uint16_t* y;              // unpack output through its pitches
+  int64_t y_row_pitch, y_head_pitch;
+  int32_t rows, H, D, kind;
+  FastDiv div_h;            // by H
+  FastDiv div_nb;           // by D/16
+  FastDiv div_np;           // by D/2
+};
+
+cudaError_t launch_tensor_nvfp4_pack(const TensorNvfp4Params& p, cudaStream_t s);
+cudaError_t launch_tensor_nvfp4_unpack(const TensorNvfp4Params& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // Paged decode attention over the quantised pool.
 // ---------------------------------------------------------------------------
 struct AttnPlane {
@@ -213,6 +233,10 @@ struct AttnParams {
 // Split count for a call: enough CTAs to fill the GPU, each split at least 256 tokens.
 int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len);
 cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s);
+// The library's built-in split scratch (device memory in the library image, for the
+// entry point that allocates nothing): its device address and size in bytes.
+cudaError_t attn_builtin_scratch(void** ptr, size_t* bytes);
+size_t attn_builtin_scratch_bytes();
 cudaError_t launch_payload_decode(const UnpackParams& p, int lanes, bool v8, cudaStream_t s);
 
 int num_sms();

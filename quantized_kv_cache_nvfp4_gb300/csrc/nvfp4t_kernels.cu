@@ -1,0 +1,246 @@
+// nvfp4t_kernels.cu -- NVFP4 with one FP32 scale per tensor: the logical layout of
+// "vllm-rlt PR #166: INT4 KV packing/unpacking and cross-loop residual reconstruction"
+// (Purpose: E4M3 block scales and a scalar FP32 global encoding multiplier; G16
+// blocks along the kind's axis, K over token rows per head/channel, V over channels
+// per token/head; partial groups allowed).
+//
+// rs = amax of the whole tensor / 2688, kept as the decode multiplier; each block of
+// 16 takes the row codec's steps against it: block scale e4m3(min((vb/6)/rs, 448)),
+// codes e2m1(x * 1/(bs*rs)) (x / (bs*rs) when the reciprocal overflows), decode
+// bf16((e2m1 * bs) * rs).
+//
+// Encoding runs as three kernels on the caller's stream (the scale slot is zeroed by
+// a memset first): the tensor's amax, gathered with atomicMax on the float bits into
+// the packed tensor's own scale slot (non-negative floats order as their bits); the
+// block codes, which read that amax; and one thread that turns the slot into rs.  No
+// scratch memory, and safe under graph capture.
+#include "kvq_device.cuh"
+#include "kvq_params.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kRowScaleDiv = 2688.0f;  // 6 * 448
+
+__device__ __forceinline__ void tensor_scale(const float* slot, float& rs, float& rinv) {
+  const float amax = LDX(slot);
+  rs = __fdiv_rn(amax, kRowScaleDiv);
+  rinv = rs != 0.0f ? __frcp_rn(rs) : 0.0f;
+}
+
+// The 16 bf16 of block b of row (r, h): 32 bytes, 16-byte aligned.
+__device__ __forceinline__ void load_block(const TensorNvfp4Params& p, uint32_t r, uint32_t h, uint32_t b,
+                                           uint32_t (&w)[8]) {
+  const uint16_t* src = p.x + static_cast<int64_t>(r) * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + 16 * b;
+  uint32_t a[4], c[4];
+  load16B(src, a);
+  load16B(src + 8, c);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w[i] = a[i];
+    w[4 + i] = c[i];
+  }
+}
+
+// 1. amax of the tensor (every block of 16 of every row), into the scale slot.
+__global__ void __launch_bounds__(kThreads) tensor_amax_kernel(const TensorNvfp4Params p) {
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * static_cast<uint32_t>(p.D / 16);
+  float m = 0.0f;
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nblk; i += gridDim.x * kThreads) {
+    uint32_t rh, b, r, h;
+    p.div_nb.divmod(i, rh, b);
+    p.div_h.divmod(rh, r, h);
+    uint32_t w[8];
+    load_block(p, r, h, b, w);
+    m = fmaxf(m, absmax16(w));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.rscale), __float_as_uint(m));
+}
+
+// 2a. VALUE kind: one thread per 16-channel block of a row.
+__global__ void __launch_bounds__(kThreads) tensor_value_encode_kernel(const TensorNvfp4Params p) {
+  const uint32_t nb = static_cast<uint32_t>(p.D / 16);
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * nb;
+  float rs, rinv;
+  tensor_scale(p.rscale, rs, rinv);
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nblk; i += gridDim.x * kThreads) {
+    uint32_t rh, b, r, h;
+    p.div_nb.divmod(i, rh, b);
+    p.div_h.divmod(rh, r, h);
+    uint32_t w[8];
+    load_block(p, r, h, b, w);
+    const uint32_t bsb = block_scale_code(absmax16(w), rs, rinv);
+    uint32_t c0, c1;
+    quantize_block(w, __fmul_rn(e4m3_to_f32(bsb), rs), c0, c1);
+    store8B(p.codes + static_cast<int64_t>(rh) * (p.D / 2) + 8 * b, c0, c1);
+    STX(p.bscale + static_cast<int64_t>(rh) * nb + b, static_cast<uint8_t>(bsb));
+  }
+}
+
+// 2b. KEY kind: one thread per (group of 16 token rows, head, channel pair); the pair's
+// two blocks are its two channels over the group's rows (fewer in a partial group).
+__global__ void __launch_bounds__(kThreads) tensor_key_encode_kernel(const TensorNvfp4Params p) {
+  const uint32_t npair = static_cast<uint32_t>(p.D / 2);
+  const uint32_t ngroups = static_cast<uint32_t>((p.rows + 15) / 16);
+  const uint32_t ntask = ngroups * static_cast<uint32_t>(p.H) * npair;
+  float rs, rinv;
+  tensor_scale(p.rscale, rs, rinv);
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < ntask; i += gridDim.x * kThreads) {
+    uint32_t gh, pr, g, h;
+    p.div_np.divmod(i, gh, pr);
+    p.div_h.divmod(gh, g, h);
+    const int r0 = static_cast<int>(g) * 16;
+    const int n = min(16, p.rows - r0);
+    uint32_t w[16];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      w[k] = 0u;
+      if (k < n)
+        w[k] = LDX(reinterpret_cast<const uint32_t*>(p.x + static_cast<int64_t>(r0 + k) * p.row_pitch +
+                                                       static_cast<int64_t>(h) * p.head_pitch + 2 * pr));
+      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(w[k]));
+    }
+    m &= 0x7FFF7FFFu;
+    const uint32_t bl = block_scale_code(bf16lo(m), rs, rinv);
+    const uint32_t bh = block_scale_code(bf16hi(m), rs, rinv);
+    const float sl = __fmul_rn(e4m3_to_f32(bl), rs), sh = __fmul_rn(e4m3_to_f32(bh), rs);
+    const float il = sl != 0.0f ? __frcp_rn(sl) : 0.0f, ih = sh != 0.0f ? __frcp_rn(sh) : 0.0f;
+    const bool direct = isinf(il) || isinf(ih);  // a tiny scale: divide instead
+    const uint64_t inv2 = pack_f32x2(__float_as_uint(il), __float_as_uint(ih));
+    uint8_t* const cp = p.codes + (static_cast<int64_t>(r0) * p.H + h) * npair + pr;
+    const int64_t cstride = static_cast<int64_t>(p.H) * npair;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (k >= n) break;
+      float ql, qh;
+      if (!direct) {
+        uint32_t a, b;
+        unpack_f32x2(mul_f32x2(pack_f32x2(w[k] << 16, w[k] & 0xFFFF0000u), inv2), a, b);
+        ql = __uint_as_float(a);
+        qh = __uint_as_float(b);
+      } else {
+        ql = isinf(il) ? __fdiv_rn(bf16lo(w[k]), sl) : __fmul_rn(bf16lo(w[k]), il);
+        qh = isinf(ih) ? __fdiv_rn(bf16hi(w[k]), sh) : __fmul_rn(bf16hi(w[k]), ih);
+      }
+      STX(cp + k * cstride, static_cast<uint8_t>(e2m1x2_from_f32(ql, qh)));
+    }
+    STX(reinterpret_cast<uint16_t*>(p.bscale + (static_cast<int64_t>(g) * p.H + h) * p.D + 2 * pr),
+        static_cast<uint16_t>(bl | (bh << 8)));
+  }
+}
+
+// 3. The scale slot: amax -> rs (the decode multiplier).
+__global__ void tensor_scale_finalize_kernel(float* slot) {
+  STX(slot, __fdiv_rn(LDX(slot), kRowScaleDiv));
+}
+
+// Unpack, VALUE kind: one thread per 16-channel block.
+__global__ void __launch_bounds__(kThreads) tensor_value_decode_kernel(const TensorNvfp4Params p) {
+  const uint32_t nb = static_cast<uint32_t>(p.D / 16);
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * nb;
+  const float rs = LDX(p.rscale);
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nblk; i += gridDim.x * kThreads) {
+    uint32_t rh, b, r, h;
+    p.div_nb.divmod(i, rh, b);
+    p.div_h.divmod(rh, r, h);
+    uint32_t c0, c1;
+    load8B(p.codes + static_cast<int64_t>(rh) * (p.D / 2) + 8 * b, c0, c1);
+    uint32_t out[8];
+    nvfp4_decode16(c0, c1, LDX(p.bscale + static_cast<int64_t>(rh) * nb + b), rs, out);
+    uint16_t* dst = p.y + static_cast<int64_t>(r) * p.y_row_pitch + static_cast<int64_t>(h) * p.y_head_pitch + 16 * b;
+    store16B(dst, *reinterpret_cast<const uint32_t(*)[4]>(&out[0]));
+    store16B(dst + 8, *reinterpret_cast<const uint32_t(*)[4]>(&out[4]));
+  }
+}
+
+// Unpack, KEY kind: one thread per 16 channels of a row; each channel has its own
+// block scale (of the row's 16-row group).
+__global__ void __launch_bounds__(kThreads) tensor_key_decode_kernel(const TensorNvfp4Params p) {
+  const uint32_t nb = static_cast<uint32_t>(p.D / 16);
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * nb;
+  const float rs = LDX(p.rscale);
+  const uint64_t rs2 = pack_f32x2(__float_as_uint(rs), __float_as_uint(rs));
+  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nblk; i += gridDim.x * kThreads) {
+    uint32_t rh, j, r, h;
+    p.div_nb.divmod(i, rh, j);
+    p.div_h.divmod(rh, r, h);
+    uint32_t c0, c1, bsw[4];
+    load8B(p.codes + static_cast<int64_t>(rh) * (p.D / 2) + 8 * j, c0, c1);
+    load16B(p.bscale + (static_cast<int64_t>(r / 16) * p.H + h) * p.D + 16 * j, bsw);
+    uint32_t out[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t byte = ((e < 4 ? c0 : c1) >> (8 * (e & 3))) & 0xFFu;
+      const uint32_t h2 = e2m1x2_to_f16x2(byte);
+      const uint32_t two = (bsw[e / 2] >> (16 * (e % 2))) & 0xFFFFu;  // scales of channels 2e, 2e + 1
+      const float lo = mul_f16_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu),
+                                      static_cast<uint16_t>(e4m3_to_f16x2(two & 0xFFu) & 0xFFFFu));
+      const float hi = mul_f16_to_f32(static_cast<uint16_t>(h2 >> 16),
+                                      static_cast<uint16_t>(e4m3_to_f16x2(two >> 8) & 0xFFFFu));
+      uint32_t yl, yh;
+      unpack_f32x2(mul_f32x2(pack_f32x2(__float_as_uint(lo), __float_as_uint(hi)), rs2), yl, yh);
+      out[e] = pack_bf16x2(__uint_as_float(yl), __uint_as_float(yh));
+    }
+    uint16_t* dst = p.y + static_cast<int64_t>(r) * p.y_row_pitch + static_cast<int64_t>(h) * p.y_head_pitch + 16 * j;
+    store16B(dst, *reinterpret_cast<const uint32_t(*)[4]>(&out[0]));
+    store16B(dst + 8, *reinterpret_cast<const uint32_t(*)[4]>(&out[4]));
+  }
+}
+
+template <typename K>
+int grid_for(K kernel, uint32_t work) {
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+  if (occ < 1) occ = 1;
+  const int64_t need = (static_cast<int64_t>(work) + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+  return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_tensor_nvfp4_pack(const TensorNvfp4Params& p, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p.rscale, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * static_cast<uint32_t>(p.D / 16);
+  KVQ_LAUNCH("tensor_amax_kernel", s,
+             tensor_amax_kernel<<<grid_for(tensor_amax_kernel, nblk), kThreads, 0, s>>>(p); e = cudaGetLastError());
+  if (e != cudaSuccess) return e;
+  if (p.kind == 0) {
+    const uint32_t ntask = static_cast<uint32_t>((p.rows + 15) / 16) * static_cast<uint32_t>(p.H) *
+                           static_cast<uint32_t>(p.D / 2);
+    KVQ_LAUNCH("tensor_key_encode_kernel", s,
+               tensor_key_encode_kernel<<<grid_for(tensor_key_encode_kernel, ntask), kThreads, 0, s>>>(p);
+               e = cudaGetLastError());
+  } else {
+    KVQ_LAUNCH("tensor_value_encode_kernel", s,
+               tensor_value_encode_kernel<<<grid_for(tensor_value_encode_kernel, nblk), kThreads, 0, s>>>(p);
+               e = cudaGetLastError());
+  }
+  if (e != cudaSuccess) return e;
+  KVQ_LAUNCH("tensor_scale_finalize_kernel", s,
+             tensor_scale_finalize_kernel<<<1, 1, 0, s>>>(p.rscale); e = cudaGetLastError());
+  return e;
+}
+
+cudaError_t launch_tensor_nvfp4_unpack(const TensorNvfp4Params& p, cudaStream_t s) {
+  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * static_cast<uint32_t>(p.D / 16);
+  cudaError_t e = cudaSuccess;
+  if (p.kind == 0) {
+    KVQ_LAUNCH("tensor_key_decode_kernel", s,
+               tensor_key_decode_kernel<<<grid_for(tensor_key_decode_kernel, nblk), kThreads, 0, s>>>(p);
+               e = cudaGetLastError());
+  } else {
+    KVQ_LAUNCH("tensor_value_decode_kernel", s,
+               tensor_value_decode_kernel<<<grid_for(tensor_value_decode_kernel, nblk), kThreads, 0, s>>>(p);
+               e = cudaGetLastError());
+  }
+  return e;
+}
+
+}  // namespace kvq

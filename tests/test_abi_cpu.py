@@ -41,11 +41,11 @@ def test_library_exports_every_declared_symbol(kvq_lib_path):
 def test_storage_bytes_agrees_with_the_oracle(kvq_lib_path):
     import quantized_kv_cache_nvfp4_gb300 as kvq
 
-    for fmt in (1, 2, 3):
+    for fmt in (1, 2, 3, 4):
         for kind in (0, 1):
             for G in (16, 64):
                 for (T, H, D) in [(1, 1, 128), (256, 8, 128), (4100, 8, 96), (1048576, 4, 256), (0, 2, 32)]:
-                    g = {1: 16, 2: G, 3: 0}[fmt]
+                    g = {1: 16, 2: G, 3: 0, 4: 16}[fmt]
                     assert kvq.kvq_storage_bytes(fmt, kind, g, T, H, D) == O.storage_bytes(fmt, kind, g, T, H, D)
     assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 128) == 76
     assert kvq.kvq_storage_bytes(1, 0, 16, 1, 1, 100) == 0
@@ -112,3 +112,19 @@ def test_decode_attention_host_checks(kvq_lib_path):
     assert call(8) == 1 and b"NULL" in lib.kvq_last_error()  # q's pointer
     assert lib.kvq_decode_attention(None, None, 1, 4, None, 64, ctypes.byref(q), 8, 0.1, ctypes.byref(o), None,
                                     0, None, None) == 1
+
+
+def test_noalloc_scratch_covers_every_split_workspace(kvq_lib_path):
+    """The built-in 48 MiB scratch of kvq_decode_attention_noalloc holds the split
+    partials of every supported shape (the workspace query is host-only)."""
+    from quantized_kv_cache_nvfp4_gb300 import _abi
+
+    lib = _abi.load()
+    worst = 0
+    for S in (1, 2, 3, 7, 32, 75, 151, 300, 455, 456, 1000):
+        for H in (1, 2, 8):
+            for group in (1, 4, 16):
+                for D in (64, 128, 256):
+                    for T in (1, 255, 256, 4096, 1 << 20):
+                        worst = max(worst, lib.kvq_decode_attention_workspace(S, H, H * group, D, T))
+    assert 0 < worst <= 48 << 20
