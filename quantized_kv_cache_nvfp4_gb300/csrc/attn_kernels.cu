@@ -68,6 +68,24 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return r;
 }
 
+// The four E2M1 pairs of a word, byte i -> f16x2 i (low nibble in the low half),
+// exactly; the bytes go to the conversions as .b8 registers (no shifts or masks).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// The two E4M3 pairs of a word, bytes 0-1 -> f16x2 0 and bytes 2-3 -> f16x2 1, exactly.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t (&h)[2]) {
+  asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, u;\n\t}"
+      : "=r"(h[0]), "=r"(h[1])
+      : "r"(w));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float r;
   asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -113,16 +131,22 @@ __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
   return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
 }
 
-// Shared-memory layout of one 16-token tile of one KV head (both K and V).
+// Shared-memory layout of one 16-token tile of one KV head (both K and V).  Row
+// strides are chosen so that each access phase of a warp covers 32 distinct banks:
+// a K read is one lane's contiguous chunk (D/8 or D/4 bytes at lane c's offset) of
+// token 8j + g; a V read is D/16 or D/8 bytes at lane g's offset of token 2c (+1,
+// +8, +9), which needs a row stride of 4 mod 16 words (the code bytes + 16).
 template <int D, int kFK, int kFV>
 struct AttnTile {
   static constexpr int kCK = kFK == 3 ? D : D / 2;  // code bytes per row
   static constexpr int kCV = kFV == 3 ? D : D / 2;
+  static constexpr int kSK = kFK == 3 ? (D == 128 ? 144 : D) : (D == 256 ? 144 : D / 2);  // smem row strides
+  static constexpr int kSV = kCV + 16;
   static constexpr int kBK = kFK == 3 ? 0 : D / 16;  // block-scale bytes per row
   static constexpr int kBV = kFV == 3 ? 0 : D / 16;
   static constexpr int kOffKC = 0;
-  static constexpr int kOffVC = kOffKC + 16 * kCK;
-  static constexpr int kOffKB = kOffVC + 16 * kCV;
+  static constexpr int kOffVC = kOffKC + 16 * kSK;
+  static constexpr int kOffKB = kOffVC + 16 * kSV;
   static constexpr int kOffVB = kOffKB + 16 * kBK;
   static constexpr int kOffKR = kOffVB + 16 * kBV;
   static constexpr int kOffVR = kOffKR + 64;
@@ -130,8 +154,30 @@ struct AttnTile {
   static constexpr int kStages = kBytes > 4096 ? 3 : 4;
   static constexpr int kRing = kAttnWarps * kStages * kBytes;
   static constexpr int kMerge = kAttnWarps * 16 * (D + 2) * 4;  // per warp: 16 rows x (O, m, l)
-  static constexpr int kSmem = kRing > kMerge ? kRing : kMerge;
+  static constexpr int kQ = (D / 16) * 32 * 16 + 64;             // Q fragments [k-step][lane] + 16 row factors
+  static constexpr int kSmem = kQ + (kRing > kMerge ? kRing : kMerge);
 };
+
+// NW words from shared memory at p (aligned to the access), in 16-, 8- or 4-byte loads.
+template <int NW>
+__device__ __forceinline__ void lds_words(const unsigned char* p, uint32_t (&w)[NW]) {
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+  } else if constexpr (NW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
 
 template <int D, int kFK, int kFV>
 __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnParams p) {
@@ -153,47 +199,55 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   const int ntile = t_end > t_begin ? (t_end - t_begin + 15) / 16 : 0;
   if (bad_len && threadIdx.x == 0 && split == 0 && h == 0) set_status(p.status, 8u);
 
-  // ---- Q fragments: rows g and g + 8 of the group, scaled by 2^k into f16 ----
-  uint32_t qa[kKS][4];
-  float qmul[2];
+  // ---- Q fragments (rows g and g + 8 of the group, scaled by 2^k into f16) and the
+  // per-row score factors, built once by warp 0 into shared memory ----
+  uint4* const qfrag = reinterpret_cast<uint4*>(smem);                   // [D/16][32 lanes]
+  float* const qfac = reinterpret_cast<float*>(smem + (D / 16) * 32 * 16);  // [16 rows]
+  if (warp == 0) {
+    uint32_t qa[kKS][4];
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int row = g + 8 * hr;
-    uint32_t w[D / 8];  // this lane's D/4 dims as bf16 pairs
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = g + 8 * hr;
+      uint32_t w[D / 8];  // this lane's D/4 dims as bf16 pairs
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) w[i] = 0u;
-    if (row < p.group) {
-      const uint16_t* qp =
-          p.q + static_cast<int64_t>(s) * p.q_row_pitch + static_cast<int64_t>(h * p.group + row) * p.q_head_pitch + c * (D / 4);
+      for (int i = 0; i < D / 8; ++i) w[i] = 0u;
+      if (row < p.group) {
+        const uint16_t* qp = p.q + static_cast<int64_t>(s) * p.q_row_pitch +
+                             static_cast<int64_t>(h * p.group + row) * p.q_head_pitch + c * (D / 4);
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        uint32_t v4[4];
-        load16B(qp + 8 * i, v4);
-        w[4 * i] = v4[0];
-        w[4 * i + 1] = v4[1];
-        w[4 * i + 2] = v4[2];
-        w[4 * i + 3] = v4[3];
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t v4[4];
+          load16B(qp + 8 * i, v4);
+          w[4 * i] = v4[0];
+          w[4 * i + 1] = v4[1];
+          w[4 * i + 2] = v4[2];
+          w[4 * i + 3] = v4[3];
+        }
+      }
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) am = fmaxf(am, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+      int k = 0;
+      if (am > 0.0f) k = 14 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127);
+      k = max(-100, min(120, k));
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+      if (c == 0) qfac[row] = p.scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+#pragma unroll
+      for (int kb = 0; kb < kKS; ++kb) {
+        qa[kb][hr] = f32x2_to_f16x2(bf16lo(w[2 * kb]) * up, bf16hi(w[2 * kb]) * up);              // dims 4kb, +1
+        qa[kb][2 + hr] = f32x2_to_f16x2(bf16lo(w[2 * kb + 1]) * up, bf16hi(w[2 * kb + 1]) * up);  // dims 4kb+2, +3
       }
     }
-    float am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) am = fmaxf(am, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
-    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-    int k = 0;
-    if (am > 0.0f) k = 14 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127);
-    k = max(-100, min(120, k));
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-    qmul[hr] = p.scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
-#pragma unroll
-    for (int kb = 0; kb < kKS; ++kb) {
-      qa[kb][hr] = f32x2_to_f16x2(bf16lo(w[2 * kb]) * up, bf16hi(w[2 * kb]) * up);          // dims 4kb, +1
-      qa[kb][2 + hr] = f32x2_to_f16x2(bf16lo(w[2 * kb + 1]) * up, bf16hi(w[2 * kb + 1]) * up);  // dims 4kb+2, +3
-    }
+    for (int kb = 0; kb < kKS; ++kb) qfrag[kb * 32 + lane] = make_uint4(qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3]);
   }
+  __syncthreads();
+  const float qmul[2] = {qfac[g], qfac[g + 8]};
 
   // ---- the warp's tiles through its cp.async ring ----
-  unsigned char* const ring = smem + warp * T::kStages * T::kBytes;
+  unsigned char* const ring = smem + T::kQ + warp * T::kStages * T::kBytes;
   bool bad = false;
   auto issue = [&](int it, int st) {
     const int tile = warp + it * kAttnWarps;
@@ -210,21 +264,18 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       blk = 0;
     }
     const int64_t row = (blk * p.block_size + bo) * p.H + h;  // pool row of token tt
-    constexpr int kPK = T::kCK / 16, kPV = T::kCV / 16;
-#pragma unroll
-    for (int i = lane; i < 16 * kPK; i += 32) {
-      const int64_t rr = shfl64(row, i / kPK);
-      cp_async16(sb + T::kOffKC + (i / kPK) * T::kCK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
-    }
-#pragma unroll
-    for (int i = lane; i < 16 * kPV; i += 32) {
-      const int64_t rr = shfl64(row, i / kPV);
-      cp_async16(sb + T::kOffVC + (i / kPV) * T::kCV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
-    }
+    // lanes 0-15 copy token tt's K row, lanes 16-31 its V row (code bytes in 16-byte
+    // pieces, the block scales, the row scale)
     if (lane < 16) {
+#pragma unroll
+      for (int pc = 0; pc < T::kCK / 16; ++pc)
+        cp_async16(sb + T::kOffKC + tt * T::kSK + pc * 16, p.k.codes + row * T::kCK + pc * 16);
       if constexpr (T::kBK > 0) cp_async_n<T::kBK>(sb + T::kOffKB + tt * T::kBK, p.k.bscale + row * T::kBK);
       cp_async_small<4>(sb + T::kOffKR + tt * 4, p.k.rscale + row);
     } else {
+#pragma unroll
+      for (int pc = 0; pc < T::kCV / 16; ++pc)
+        cp_async16(sb + T::kOffVC + tt * T::kSV + pc * 16, p.v.codes + row * T::kCV + pc * 16);
       if constexpr (T::kBV > 0) cp_async_n<T::kBV>(sb + T::kOffVB + tt * T::kBV, p.v.bscale + row * T::kBV);
       cp_async_small<4>(sb + T::kOffVR + tt * 4, p.v.rscale + row);
     }
@@ -247,29 +298,55 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     const unsigned char* const sb = ring + (it % T::kStages) * T::kBytes;
     const int t0 = t_begin + (warp + it * kAttnWarps) * 16;
 
-    // S = Q K^T over the 16 tokens: n-tile j holds tokens 8j .. 8j + 7
-    float sc[2][4];
+    // S = Q K^T over the 16 tokens: n-tile j holds tokens 8j .. 8j + 7 (this lane
+    // supplies token 8j + g); each Q fragment is read once for both n-tiles
+    float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    if constexpr (kFK == 3) {
+      uint32_t kw[2][D / 16];  // this lane's D/4 code bytes of tokens g and 8 + g
+      lds_words<D / 16>(sb + T::kOffKC + g * T::kSK + c * (D / 4), kw[0]);
+      lds_words<D / 16>(sb + T::kOffKC + (8 + g) * T::kSK + c * (D / 4), kw[1]);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
-      const int tk = 8 * j + g;
-      if constexpr (kFK == 3) {
-        const uint32_t* kw = reinterpret_cast<const uint32_t*>(sb + T::kOffKC + tk * T::kCK + c * (D / 4));
+      for (int kb = 0; kb < kKS; ++kb) {
+        const uint4 qv = qfrag[kb * 32 + lane];
+        const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int kb = 0; kb < kKS; ++kb) {
-          const uint32_t wv = kw[kb];
-          mma_f16_16816(sc[j], qa[kb], e4m3x2_to_f16x2(wv), e4m3x2_to_f16x2(wv >> 16));
+        for (int j = 0; j < 2; ++j) {
+          uint32_t b2[2];
+          e4m3x4_to_f16x2(kw[j][kb], b2);  // dims 4kb, 4kb+1 | 4kb+2, 4kb+3
+          mma_f16_16816(sc[j], qa, b2[0], b2[1]);
         }
-      } else {
-        const uint32_t* kw = reinterpret_cast<const uint32_t*>(sb + T::kOffKC + tk * T::kCK + c * (D / 8));
-        const uint8_t* kbs = sb + T::kOffKB + tk * T::kBK + c * (D / 64);
+      }
+    } else {
+      uint32_t kw[2][D / 32];  // this lane's D/8 code bytes of tokens g and 8 + g
+      lds_words<D / 32>(sb + T::kOffKC + g * T::kSK + c * (D / 8), kw[0]);
+      lds_words<D / 32>(sb + T::kOffKC + (8 + g) * T::kSK + c * (D / 8), kw[1]);
+      constexpr int kNB = D / 64 > 0 ? D / 64 : 1;  // blocks of this lane's dims
+      uint32_t bsb[2][kNB];                         // their scales, f16 in both halves
 #pragma unroll
-        for (int kb = 0; kb < kKS; ++kb) {
-          const uint32_t wv = kw[kb / 2] >> (16 * (kb % 2));
-          const uint32_t bsh = e4m3_to_f16x2(kbs[kb / 4]) & 0xFFFFu;
-          const uint32_t bs2 = bsh | (bsh << 16);
-          mma_f16_16816(sc[j], qa[kb], hmul2(e2m1x2_to_f16x2(wv & 0xFFu), bs2),
-                        hmul2(e2m1x2_to_f16x2((wv >> 8) & 0xFFu), bs2));
+      for (int j = 0; j < 2; ++j) {
+        const uint8_t* kbs = sb + T::kOffKB + (8 * j + g) * T::kBK + c * (D / 64);
+#pragma unroll
+        for (int i = 0; i < kNB; ++i) {
+          const uint32_t bsh = e4m3_to_f16x2(kbs[i]) & 0xFFFFu;
+          bsb[j][i] = bsh | (bsh << 16);
+        }
+      }
+#pragma unroll
+      for (int wi = 0; wi < D / 32; ++wi) {  // one code word = k-steps 2wi and 2wi + 1
+        uint32_t hk[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          e2m1x8_to_f16x2(kw[j][wi], hk[j]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) hk[j][i] = hmul2(hk[j][i], bsb[j][(2 * wi) / 4]);
+        }
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const int kb = 2 * wi + hs;
+          const uint4 qv = qfrag[kb * 32 + lane];
+          const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) mma_f16_16816(sc[j], qa, hk[j][2 * hs], hk[j][2 * hs + 1]);
         }
       }
     }
@@ -336,44 +413,51 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       // the two token pairs of this lane
       const int ta0 = 2 * c, ta1 = 2 * c + 8;
       if constexpr (kFV == 3) {
-        const uint32_t* v0 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta0 * T::kCV + g * (D / 8));
-        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta0 + 1) * T::kCV + g * (D / 8));
-        const uint32_t* v2 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta1 * T::kCV + g * (D / 8));
-        const uint32_t* v3 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta1 + 1) * T::kCV + g * (D / 8));
+        uint32_t v0[D / 32], v1[D / 32], v2[D / 32], v3[D / 32];  // D/8 bytes of each token
+        lds_words<D / 32>(sb + T::kOffVC + ta0 * T::kSV + g * (D / 8), v0);
+        lds_words<D / 32>(sb + T::kOffVC + (ta0 + 1) * T::kSV + g * (D / 8), v1);
+        lds_words<D / 32>(sb + T::kOffVC + ta1 * T::kSV + g * (D / 8), v2);
+        lds_words<D / 32>(sb + T::kOffVC + (ta1 + 1) * T::kSV + g * (D / 8), v3);
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          const uint32_t sel = (nt % 4) | ((4 + nt % 4) << 4);
-          const uint32_t b01 = e4m3x2_to_f16x2(__byte_perm(v0[nt / 4], v1[nt / 4], sel) & 0xFFFFu);
-          const uint32_t b23 = e4m3x2_to_f16x2(__byte_perm(v2[nt / 4], v3[nt / 4], sel) & 0xFFFFu);
-          mma_f16_16816(o[nt], pa, b01, b23);
+        for (int np = 0; np < kNT / 2; ++np) {  // n-tiles 2np, 2np + 1: bytes of one half word
+          const int wd = np / 2, bo2 = 2 * (np % 2);
+          const uint32_t sel = bo2 | ((4 + bo2) << 4) | ((bo2 + 1) << 8) | ((5 + bo2) << 12);
+          uint32_t h01[2], h23[2];
+          e4m3x4_to_f16x2(__byte_perm(v0[wd], v1[wd], sel), h01);
+          e4m3x4_to_f16x2(__byte_perm(v2[wd], v3[wd], sel), h23);
+          mma_f16_16816(o[2 * np], pa, h01[0], h23[0]);
+          mma_f16_16816(o[2 * np + 1], pa, h01[1], h23[1]);
         }
       } else {
         constexpr int kW = D / 64;  // code words per lane per token (D/16 bytes)
-        const uint32_t* v0 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta0 * T::kCV + g * (D / 16));
-        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta0 + 1) * T::kCV + g * (D / 16));
-        const uint32_t* v2 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + ta1 * T::kCV + g * (D / 16));
-        const uint32_t* v3 = reinterpret_cast<const uint32_t*>(sb + T::kOffVC + (ta1 + 1) * T::kCV + g * (D / 16));
-        // nibble transpose: X byte j = (dim 2j of token a | dim 2j of token b << 4), Y: dims 2j + 1
-        uint32_t x01[kW > 0 ? kW : 1], y01[kW > 0 ? kW : 1], x23[kW > 0 ? kW : 1], y23[kW > 0 ? kW : 1];
-#pragma unroll
-        for (int i = 0; i < kW; ++i) {
-          x01[i] = (v0[i] & 0x0F0F0F0Fu) | ((v1[i] & 0x0F0F0F0Fu) << 4);
-          y01[i] = ((v0[i] >> 4) & 0x0F0F0F0Fu) | (v1[i] & 0xF0F0F0F0u);
-          x23[i] = (v2[i] & 0x0F0F0F0Fu) | ((v3[i] & 0x0F0F0F0Fu) << 4);
-          y23[i] = ((v2[i] >> 4) & 0x0F0F0F0Fu) | (v3[i] & 0xF0F0F0F0u);
-        }
+        uint32_t v0[kW], v1[kW], v2[kW], v3[kW];
+        lds_words<kW>(sb + T::kOffVC + ta0 * T::kSV + g * (D / 16), v0);
+        lds_words<kW>(sb + T::kOffVC + (ta0 + 1) * T::kSV + g * (D / 16), v1);
+        lds_words<kW>(sb + T::kOffVC + ta1 * T::kSV + g * (D / 16), v2);
+        lds_words<kW>(sb + T::kOffVC + (ta1 + 1) * T::kSV + g * (D / 16), v3);
         const uint8_t* vbs = sb + T::kOffVB;
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          const int blk = (g * (D / 8) + nt) / 16;
-          const uint32_t bs01 = e4m3x2_to_f16x2(vbs[ta0 * T::kBV + blk] | (vbs[(ta0 + 1) * T::kBV + blk] << 8));
-          const uint32_t bs23 = e4m3x2_to_f16x2(vbs[ta1 * T::kBV + blk] | (vbs[(ta1 + 1) * T::kBV + blk] << 8));
-          const int bi = nt / 2;  // byte of the transposed words
-          const uint32_t w01 = (nt % 2 == 0) ? x01[bi / 4] : y01[bi / 4];
-          const uint32_t w23 = (nt % 2 == 0) ? x23[bi / 4] : y23[bi / 4];
-          const uint32_t b01 = hmul2(e2m1x2_to_f16x2((w01 >> (8 * (bi % 4))) & 0xFFu), bs01);
-          const uint32_t b23 = hmul2(e2m1x2_to_f16x2((w23 >> (8 * (bi % 4))) & 0xFFu), bs23);
-          mma_f16_16816(o[nt], pa, b01, b23);
+        for (int i = 0; i < kW; ++i) {
+          // nibble transpose: X byte b = (dim 2(4i+b) of token a | the same dim of token
+          // b << 4), Y: the odd dims; then byte b of X / Y is n-tile 8i + 2b / 8i + 2b + 1
+          const uint32_t x01 = (v0[i] & 0x0F0F0F0Fu) | ((v1[i] & 0x0F0F0F0Fu) << 4);
+          const uint32_t y01 = ((v0[i] >> 4) & 0x0F0F0F0Fu) | (v1[i] & 0xF0F0F0F0u);
+          const uint32_t x23 = (v2[i] & 0x0F0F0F0Fu) | ((v3[i] & 0x0F0F0F0Fu) << 4);
+          const uint32_t y23 = ((v2[i] >> 4) & 0x0F0F0F0Fu) | (v3[i] & 0xF0F0F0F0u);
+          uint32_t hx01[4], hy01[4], hx23[4], hy23[4];
+          e2m1x8_to_f16x2(x01, hx01);
+          e2m1x8_to_f16x2(y01, hy01);
+          e2m1x8_to_f16x2(x23, hx23);
+          e2m1x8_to_f16x2(y23, hy23);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int nt = 8 * i + 2 * bb;  // and nt + 1: one 16-block for both
+            const int blk = (g * (D / 8) + nt) / 16;
+            const uint32_t bs01 = e4m3x2_to_f16x2(vbs[ta0 * T::kBV + blk] | (vbs[(ta0 + 1) * T::kBV + blk] << 8));
+            const uint32_t bs23 = e4m3x2_to_f16x2(vbs[ta1 * T::kBV + blk] | (vbs[(ta1 + 1) * T::kBV + blk] << 8));
+            mma_f16_16816(o[nt], pa, hmul2(hx01[bb], bs01), hmul2(hx23[bb], bs23));
+            mma_f16_16816(o[nt + 1], pa, hmul2(hy01[bb], bs01), hmul2(hy23[bb], bs23));
+          }
         }
       }
     }
@@ -390,7 +474,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   const bool cta_bad = __syncthreads_or(bad ? 1 : 0) != 0 || bad_len;  // the ring is free after this
 
   // per warp: O (true scale: O * R) by natural dim, and m, l per row
-  float* const mo = reinterpret_cast<float*>(smem) + warp * 16 * (D + 2);
+  float* const mo = reinterpret_cast<float*>(smem + T::kQ) + warp * 16 * (D + 2);
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
@@ -407,7 +491,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     mo[(g + 8) * (D + 2) + D + 1] = l[1];
   }
   __syncthreads();
-  const float* const mall = reinterpret_cast<const float*>(smem);
+  const float* const mall = reinterpret_cast<const float*>(smem + T::kQ);
   for (int idx = threadIdx.x; idx < p.group * D; idx += kAttnThreads) {
     const int row = idx / D, d = idx % D;
     float M = kNegInf;
@@ -493,13 +577,47 @@ cudaError_t attn_dispatch_fmt(const AttnParams& p, cudaStream_t s) {
 
 }  // namespace
 
+// Split policy: CTAs resident per SM assumed by the wave count (4 at D <= 128), and
+// the most waves a split may create.
+constexpr int kAttnCtasPerSm = 4;
+constexpr int kAttnMaxWaves = 4;
+
+// Built-in split scratch for kvq_decode_attention_noalloc: part of the library image,
+// so no call allocates.  One per device; calls that use it must not overlap.  The
+// policy above keeps S*H*nsplit <= 4 waves = 16 * SMs CTAs, so the partials take at
+// most 16 * SMs * 16 query heads * (256 + 2) * 4 bytes: 40.2 MB on 152 SMs, inside
+// these 48 MiB.
+constexpr size_t kAttnScratchBytes = size_t{48} << 20;
+static __device__ __align__(256) float g_attn_scratch[kAttnScratchBytes / sizeof(float)];
+
+cudaError_t attn_builtin_scratch(void** ptr, size_t* bytes) {
+  *bytes = kAttnScratchBytes;
+  return cudaGetSymbolAddress(ptr, g_attn_scratch);
+}
+
+size_t attn_builtin_scratch_bytes() { return kAttnScratchBytes; }
+
 int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len) {
   const int64_t pairs = static_cast<int64_t>(S) * H;
   if (pairs <= 0 || max_seq_len <= 0) return 1;
-  const int64_t want = (3LL * num_sms() + pairs - 1) / pairs;  // about 3 CTAs per SM
-  const int64_t cap = (max_seq_len + 255) / 256;               // at least 256 tokens per split
-  int64_t n = want < cap ? want : cap;
-  return static_cast<int>(n < 1 ? 1 : (n > 64 ? 64 : n));
+  const int64_t slots = static_cast<int64_t>(kAttnCtasPerSm) * num_sms();  // CTAs resident at once
+  int64_t cap = (max_seq_len + 255) / 256;                                  // >= 256 tokens per split
+  const int64_t waves_cap = (kAttnMaxWaves * slots) / pairs;                  // <= kAttnMaxWaves waves
+  if (waves_cap < cap) cap = waves_cap;
+  if (cap > 64) cap = 64;
+  // the split count whose last wave is fullest (least idle CTA time), the smallest on ties
+  int best = 1;
+  double best_fill = 0.0;
+  for (int64_t n = 1; n <= cap; ++n) {
+    const int64_t ctas = pairs * n;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (fill > best_fill + 0.01) {
+      best_fill = fill;
+      best = static_cast<int>(n);
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s) {
