@@ -249,12 +249,13 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   // ---- the warp's tiles through its cp.async ring ----
   unsigned char* const ring = smem + T::kQ + warp * T::kStages * T::kBytes;
   bool bad = false;
-  auto issue = [&](int it, int st) {
+  // pool row of token (lane & 15) of the warp's tile number `it` (-1 past the end); the
+  // block-table load is issued a tile ahead of its copies, so its latency overlaps
+  // the current tile's arithmetic
+  auto row_of = [&](int it) -> int64_t {
     const int tile = warp + it * kAttnWarps;
-    if (tile >= ntile) return;
-    unsigned char* const sb = ring + st * T::kBytes;
-    const int tt = lane & 15;
-    int t = t_begin + tile * 16 + tt;
+    if (tile >= ntile) return -1;
+    int t = t_begin + tile * 16 + (lane & 15);
     if (t >= t_end) t = t_end - 1;  // a valid token's address; masked later
     uint32_t bi, bo;
     p.div_bs.divmod(static_cast<uint32_t>(t), bi, bo);
@@ -263,19 +264,30 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       bad = true;
       blk = 0;
     }
-    const int64_t row = (blk * p.block_size + bo) * p.H + h;  // pool row of token tt
-    // lanes 0-15 copy token tt's K row, lanes 16-31 its V row (code bytes in 16-byte
-    // pieces, the block scales, the row scale)
-    if (lane < 16) {
+    return (blk * p.block_size + bo) * p.H + h;
+  };
+  // copies of a tile (rows from row_of, uniform -1 when there is none) into stage st:
+  // the 32 lanes take consecutive 16-byte pieces of the 16 rows (whole sectors), then
+  // lanes 0-15 the K block and row scales and lanes 16-31 the V ones
+  auto issue = [&](int64_t row, int st) {
+    if (__shfl_sync(0xFFFFFFFFu, row, 0) < 0) return;
+    unsigned char* const sb = ring + st * T::kBytes;
+    const int tt = lane & 15;
+    constexpr int kPK = T::kCK / 16, kPV = T::kCV / 16;
 #pragma unroll
-      for (int pc = 0; pc < T::kCK / 16; ++pc)
-        cp_async16(sb + T::kOffKC + tt * T::kSK + pc * 16, p.k.codes + row * T::kCK + pc * 16);
+    for (int i = lane; i < 16 * kPK; i += 32) {
+      const int64_t rr = shfl64(row, i / kPK);
+      cp_async16(sb + T::kOffKC + (i / kPK) * T::kSK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
+    }
+#pragma unroll
+    for (int i = lane; i < 16 * kPV; i += 32) {
+      const int64_t rr = shfl64(row, i / kPV);
+      cp_async16(sb + T::kOffVC + (i / kPV) * T::kSV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
+    }
+    if (lane < 16) {
       if constexpr (T::kBK > 0) cp_async_n<T::kBK>(sb + T::kOffKB + tt * T::kBK, p.k.bscale + row * T::kBK);
       cp_async_small<4>(sb + T::kOffKR + tt * 4, p.k.rscale + row);
     } else {
-#pragma unroll
-      for (int pc = 0; pc < T::kCV / 16; ++pc)
-        cp_async16(sb + T::kOffVC + tt * T::kSV + pc * 16, p.v.codes + row * T::kCV + pc * 16);
       if constexpr (T::kBV > 0) cp_async_n<T::kBV>(sb + T::kOffVB + tt * T::kBV, p.v.bscale + row * T::kBV);
       cp_async_small<4>(sb + T::kOffVR + tt * 4, p.v.rscale + row);
     }
@@ -288,11 +300,12 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 
 #pragma unroll
   for (int j = 0; j < T::kStages - 1; ++j) {
-    issue(j, j);
+    issue(row_of(j), j);
     cp_async_commit();
   }
   const int my_tiles = ntile > warp ? (ntile - warp + kAttnWarps - 1) / kAttnWarps : 0;
   for (int it = 0; it < my_tiles; ++it) {
+    const int64_t row_next = row_of(it + T::kStages - 1);  // the refill's rows, loaded early
     cp_async_wait<T::kStages - 2>();
     __syncwarp();
     const unsigned char* const sb = ring + (it % T::kStages) * T::kBytes;
@@ -462,7 +475,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       }
     }
     __syncwarp();  // every lane has read this stage before it is refilled
-    issue(it + T::kStages - 1, (it + T::kStages - 1) % T::kStages);
+    issue(row_next, (it + T::kStages - 1) % T::kStages);
     cp_async_commit();
   }
   cp_async_wait<0>();

@@ -381,21 +381,24 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
       part[(2 * RP + rq) * nchunk + ch] = make_uint4(sg[0], sg[1], sg[2], sg[3]);
     }
     __syncthreads();
-    // 3. per channel pair: the group's minimum, scale and reciprocal; FP16 metadata
+    // 3. per channel pair (32-bit word w = tid): the group's minimum, scale and
+    //    reciprocal, kept in shared memory at [param][w % 4][w / 4] (so step 4 reads
+    //    consecutive words), and the FP16 metadata
     if (tid < npair) {
       const uint32_t* pw = reinterpret_cast<const uint32_t*>(part);  // [3][RP][D/2] words
-      uint32_t m = kPosInf2, M = kNegInf2, s = 0u;
+      uint32_t m = kPosInf2, M = kNegInf2, sgn = 0u;
       for (int k = 0; k < RP; ++k) {
         m = hmin2(m, pw[(0 * RP + k) * npair + tid]);
         M = hmax2(M, pw[(1 * RP + k) * npair + tid]);
-        s |= pw[(2 * RP + k) * npair + tid];
+        sgn |= pw[(2 * RP + k) * npair + tid];
       }
-      const float mnl = group_min(m, s & 0x8000u), mnh = group_min(m >> 16, s & 0x80000000u);
+      const float mnl = group_min(m, sgn & 0x8000u), mnh = group_min(m >> 16, sgn & 0x80000000u);
       const float scl = __fdiv_rn(__fsub_rn(bf16lo(M), mnl), 15.0f);
       const float sch = __fdiv_rn(__fsub_rn(bf16hi(M), mnh), 15.0f);
-      prm[tid] = make_float2(mnl, mnh);
-      prm[npair + tid] = make_float2(scl, sch);
-      prm[2 * npair + tid] = make_float2(int4_rcp(scl), int4_rcp(sch));
+      const int slot = (tid % 4) * nchunk + tid / 4;
+      prm[slot] = make_float2(mnl, mnh);
+      prm[4 * nchunk + slot] = make_float2(scl, sch);
+      prm[8 * nchunk + slot] = make_float2(int4_rcp(scl), int4_rcp(sch));
       const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * D + 2 * tid;
       STX(reinterpret_cast<uint32_t*>(p.dst.mn + mi),
           static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
       bool fast = true;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 a = prm[ch * 4 + i], b = prm[npair + ch * 4 + i], c = prm[2 * npair + ch * 4 + i];
+        const float2 a = prm[i * nchunk + ch], b = prm[(4 + i) * nchunk + ch], c = prm[(8 + i) * nchunk + ch];
         mn[2 * i] = a.x;
         mn[2 * i + 1] = a.y;
         sc[2 * i] = b.x;
