@@ -22,95 +22,93 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Code of x in a group with FP32 minimum mn and scale sc > 0, and rsc within one ulp
-// of 1 / sc: clamp(rint(RN(RN(x - mn) / sc)), 0, 15), usually without dividing.
+// Quotients without dividing.  Both divisions of the format are formed from a
+// correctly rounded reciprocal y = RN(1/b) and FMA residuals (Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev.
+// 34(1), 1990: when q is within one ulp of a/b and y = RN(1/b), the residual
+// a - b*q is exact and RN(q + (a - b*q)*y) = RN(a/b), barring underflow).
 //
-// With d = RN(x - mn) >= 0, the estimate qe = RN(d * rsc) lies within 2^-23 + 2^-24
-// (relative) of d / sc and the defined quotient q = RN(d / sc) within 2^-24, and
-// d / sc <= 15 * (1 + 2^-23) because x <= max; so after clamping to 15,
-// |qe - q| < 15 * 2^-22 < 3.6e-6 < 2^-17.  When qe is more than 2^-17 away from the
-// half-integers around it, q rounds to the same integer as qe (rint is ties-to-even,
-// and no tie is possible there).  Otherwise, and whenever sc is not a normal binary32
-// (rsc could overflow), the quotient is formed by the division itself.
-//
-// Rounding to an integer: for 0 <= v < 15.5, RN(v + 1.5 * 2^23) has unit spacing, so
-// it is v rounded to nearest with ties to even, and its low four mantissa bits are
-// that integer.
-constexpr float kRound = 12582912.0f;     // 1.5 * 2^23
-constexpr float kNearHalf = 0.49999237f;  // 0.5 - 2^-17
+// Group scale: sc = RN(D / 15) for D = RN(mx - mn).  q0 = RN(D * RN(1/15)) plus one
+// residual step equals the IEEE quotient for every binary32 D in [2^-64, FLT_MAX]
+// (checked for all of them, 1.6e9 values); smaller D divide.
+constexpr float kRcp15 = 0x1.111112p-4f;  // RN(1/15)
 
-__device__ __forceinline__ uint32_t int4_code(float x, float mn, float sc, float rsc) {
-  const float d = __fsub_rn(x, mn);
-  if (sc >= 0x1p-126f) {
-    const float qe = fminf(__fmul_rn(d, rsc), 15.0f);
-    const float t = __fadd_rn(qe, kRound);
-    if (fabsf(__fsub_rn(qe, __fsub_rn(t, kRound))) < kNearHalf) return __float_as_uint(t) & 15u;
+__device__ __forceinline__ float int4_scale(float D) {
+  if (D >= 0x1p-64f && D <= 3.4028235e38f) {
+    const float q0 = __fmul_rn(D, kRcp15);
+    return __fmaf_rn(__fmaf_rn(-q0, 15.0f, D), kRcp15, q0);
   }
-  return __float_as_uint(__fadd_rn(fminf(__fdiv_rn(d, sc), 15.0f), kRound)) & 15u;
+  return __fdiv_rn(D, 15.0f);
 }
 
-// Reciprocal of a group scale for the estimate: the hardware approximation, within
-// one ulp (the bound above allows it); 0 for a constant group (sc == 0).
-__device__ __forceinline__ float int4_rcp(float sc) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(sc));
-  return sc != 0.0f ? r : 0.0f;
-}
+// Element quotient q = RN(d / sc), d = RN(x - mn) >= 0, for a scale sc >= 2^-64 with
+// y = RN(1/sc): q0 = RN(d*y) is within 2u + u^2 of d/sc (u = 2^-24); one residual
+// step leaves a relative error below 4u^2, so q1 is within one ulp and a second step
+// returns RN(d/sc) by the theorem above.  The second residual is exact while
+// e(sc) + e(q) >= -103 (binary exponents), i.e. for every q >= 2^-39 here; a smaller
+// q codes 0 either way (every step stays far below 0.5).  Scales under 2^-64 divide.
+// A constant group (sc = 0, so d = 0) uses y = 0, which gives q = 0.
+__device__ __forceinline__ bool int4_fast_scale(float sc) { return sc >= 0x1p-64f || sc == 0.0f; }
+__device__ __forceinline__ float int4_recip(float sc) { return sc != 0.0f ? __frcp_rn(sc) : 0.0f; }
 
-// True when the estimate path may be used for a group scale: normal or zero.
-__device__ __forceinline__ bool int4_fast_scale(float sc) { return sc >= 0x1p-126f || sc == 0.0f; }
+// Rounding to an integer: for 0 <= q < 15.5, RN(q + 1.5 * 2^23) has unit spacing, so
+// it is q rounded to nearest with ties to even, and its low four mantissa bits are
+// that integer.  q <= D / sc <= 15 / (1 - 2^-24) < 15.5 (d <= D), so no clamp applies.
+constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t dup_f32x2(float v) {
+  return pack_f32x2(__float_as_uint(v), __float_as_uint(v));
+}
 
 // Codes of the 8 bf16 of words w[0..3] (channel 2i in the low half of w[i], 2i + 1 in
-// the high half), with nmn2[i] = the negated minima and rs2[i] = the reciprocal
-// scales of w[i]'s two channels, as f32x2 pairs.  Byte i of the result holds w[i]'s
-// two codes, low nibble = even channel.  Raises `emax` to the largest distance of an
-// estimate from its rounded integer: the codes are int4_code's while emax stays below
-// kNearHalf and every scale passes int4_fast_scale (constant groups: rs = 0 gives
-// code 0).  No clamp is needed: q < 15.5 rounds into [0, 15].
-__device__ __forceinline__ uint32_t int4_codes4(const uint32_t (&w)[4], const uint64_t (&nmn2)[4],
-                                                const uint64_t (&rs2)[4], float& emax) {
-  const uint64_t k2 = pack_f32x2(__float_as_uint(kRound), __float_as_uint(kRound));
+// the high half) for fast scales, with per-channel-pair parameters as f32x2 pairs:
+// nmn = -minimum, nsc = -scale, y = RN(1/scale).  Byte i of the result holds w[i]'s
+// two codes, low nibble = even channel.  With t = K + n (n <= 15) the float bits end in
+// n, so t_hi * 16 + t_lo carries nothing out of its low byte, which is n_lo | n_hi << 4.
+__device__ __forceinline__ uint32_t int4_codes8(const uint32_t (&w)[4], const uint64_t (&nmn)[4],
+                                                const uint64_t (&nsc)[4], const uint64_t (&y)[4]) {
+  const uint64_t k2 = dup_f32x2(kRound);
+  uint32_t byte[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t d = add_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), nmn[i]);
+    const uint64_t q0 = mul_f32x2(d, y[i]);
+    const uint64_t q1 = fma_f32x2(fma_f32x2(q0, nsc[i], d), y[i], q0);
+    const uint64_t q2 = fma_f32x2(fma_f32x2(q1, nsc[i], d), y[i], q1);
+    uint32_t tl, th;
+    unpack_f32x2(add_f32x2(q2, k2), tl, th);
+    byte[i] = th * 16u + tl;
+  }
+  return __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
+}
+
+// The same codes by division, element by element (the defined arithmetic), for chunks
+// holding a scale below 2^-64; same parameters.
+__device__ __forceinline__ uint32_t int4_codes8_div(const uint32_t (&w)[4], const uint64_t (&nmn)[4],
+                                                    const uint64_t (&nsc)[4]) {
   uint32_t out = 0u;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint64_t q2 = mul_f32x2(add_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), nmn2[i]), rs2[i]);
-    const uint64_t t2 = add_f32x2(q2, k2);
-    uint32_t el, eh, tl, th;
-    unpack_f32x2(sub_f32x2(q2, sub_f32x2(t2, k2)), el, eh);
-    emax = fmaxf(emax, fmaxf(fabsf(__uint_as_float(el)), fabsf(__uint_as_float(eh))));
-    unpack_f32x2(t2, tl, th);
-    out |= ((tl & 15u) | ((th & 15u) << 4)) << (8 * i);
+    uint32_t ml, mh, sl, sh;
+    unpack_f32x2(nmn[i], ml, mh);
+    unpack_f32x2(nsc[i], sl, sh);
+    const float x[2] = {bf16lo(w[i]), bf16hi(w[i])};
+    const float m[2] = {-__uint_as_float(ml), -__uint_as_float(mh)};
+    const float s[2] = {-__uint_as_float(sl), -__uint_as_float(sh)};
+    uint32_t c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      c[j] = s[j] != 0.0f
+                 ? __float_as_uint(__fadd_rn(fminf(__fdiv_rn(__fsub_rn(x[j], m[j]), s[j]), 15.0f), kRound)) & 15u
+                 : 0u;
+    out |= (c[0] | (c[1] << 4)) << (8 * i);
   }
   return out;
-}
-
-// The same 8 codes by int4_code, element by element (the rare exact path).
-__device__ __forceinline__ uint32_t int4_codes4_exact(const uint32_t (&w)[4], const float (&mn)[8],
-                                                   const float (&sc)[8], const float (&rs)[8]) {
-  uint32_t out = 0u;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t cl = sc[2 * i] != 0.0f ? int4_code(bf16lo(w[i]), mn[2 * i], sc[2 * i], rs[2 * i]) : 0u;
-    const uint32_t ch =
-        sc[2 * i + 1] != 0.0f ? int4_code(bf16hi(w[i]), mn[2 * i + 1], sc[2 * i + 1], rs[2 * i + 1]) : 0u;
-    out |= (cl | (ch << 4)) << (8 * i);
-  }
-  return out;
-}
-
-// Codes of one chunk (4 words) against per-channel parameters, with the exact path
-// taken only when the estimate check fails.
-__device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&w)[4], const float (&mn)[8], const float (&sc)[8],
-                                                const float (&rs)[8], bool fast) {
-  uint64_t nmn2[4], rs2[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    nmn2[i] = pack_f32x2(__float_as_uint(-mn[2 * i]), __float_as_uint(-mn[2 * i + 1]));
-    rs2[i] = pack_f32x2(__float_as_uint(rs[2 * i]), __float_as_uint(rs[2 * i + 1]));
-  }
-  float emax = 0.0f;
-  const uint32_t c = int4_codes4(w, nmn2, rs2, emax);
-  return (fast && emax < kNearHalf) ? c : int4_codes4_exact(w, mn, sc, rs);
 }
 
 // Group minimum and maximum of packed bf16 words: min/max.bf16x2 (a minimum or
@@ -238,20 +236,20 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
       }
     }
     if (!valid) continue;
-    float mn[8], sc[8], rsc[8];
+    float mn[8], sc[8];
+    uint64_t nmn[4], nsc[4], y[4];
     bool fast = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t a = bf16x2_unkey(kmn[i]), b = bf16x2_unkey(kmx[i]);
       mn[2 * i] = bf16lo(a);
       mn[2 * i + 1] = bf16hi(a);
-      sc[2 * i] = __fdiv_rn(__fsub_rn(bf16lo(b), mn[2 * i]), 15.0f);
-      sc[2 * i + 1] = __fdiv_rn(__fsub_rn(bf16hi(b), mn[2 * i + 1]), 15.0f);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      rsc[i] = int4_rcp(sc[i]);
-      fast = fast && int4_fast_scale(sc[i]);
+      sc[2 * i] = int4_scale(__fsub_rn(bf16lo(b), mn[2 * i]));
+      sc[2 * i + 1] = int4_scale(__fsub_rn(bf16hi(b), mn[2 * i + 1]));
+      nmn[i] = pack_f32x2(__float_as_uint(-mn[2 * i]), __float_as_uint(-mn[2 * i + 1]));
+      nsc[i] = pack_f32x2(__float_as_uint(-sc[2 * i]), __float_as_uint(-sc[2 * i + 1]));
+      y[i] = pack_f32x2(__float_as_uint(int4_recip(sc[2 * i])), __float_as_uint(int4_recip(sc[2 * i + 1])));
+      fast = fast && int4_fast_scale(sc[2 * i]) && int4_fast_scale(sc[2 * i + 1]);
     }
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
@@ -259,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
       if (r >= r1) continue;
       if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
       STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) + col / 2),
-          chunk_codes(v[k], mn, sc, rsc, fast));
+          fast ? int4_codes8(v[k], nmn, nsc, y) : int4_codes8_div(v[k], nmn, nsc));
     }
     if (rs == 0) {
       uint32_t m16[4], s16[4];
@@ -382,8 +380,8 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
     }
     __syncthreads();
     // 3. per channel pair (32-bit word w = tid): the group's minimum, scale and
-    //    reciprocal, kept in shared memory at [param][w % 4][w / 4] (so step 4 reads
-    //    consecutive words), and the FP16 metadata
+    //    reciprocal, kept in shared memory (minimum and scale negated) at
+    //    [param][w % 4][w / 4] (so step 4 reads consecutive words), and the FP16 metadata
     if (tid < npair) {
       const uint32_t* pw = reinterpret_cast<const uint32_t*>(part);  // [3][RP][D/2] words
       uint32_t m = kPosInf2, M = kNegInf2, sgn = 0u;
@@ -393,12 +391,12 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
         sgn |= pw[(2 * RP + k) * npair + tid];
       }
       const float mnl = group_min(m, sgn & 0x8000u), mnh = group_min(m >> 16, sgn & 0x80000000u);
-      const float scl = __fdiv_rn(__fsub_rn(bf16lo(M), mnl), 15.0f);
-      const float sch = __fdiv_rn(__fsub_rn(bf16hi(M), mnh), 15.0f);
+      const float scl = int4_scale(__fsub_rn(bf16lo(M), mnl));
+      const float sch = int4_scale(__fsub_rn(bf16hi(M), mnh));
       const int slot = (tid % 4) * nchunk + tid / 4;
-      prm[slot] = make_float2(mnl, mnh);
-      prm[4 * nchunk + slot] = make_float2(scl, sch);
-      prm[8 * nchunk + slot] = make_float2(int4_rcp(scl), int4_rcp(sch));
+      prm[slot] = make_float2(-mnl, -mnh);
+      prm[4 * nchunk + slot] = make_float2(-scl, -sch);
+      prm[8 * nchunk + slot] = make_float2(int4_recip(scl), int4_recip(sch));
       const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * D + 2 * tid;
       STX(reinterpret_cast<uint32_t*>(p.dst.mn + mi),
           static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
@@ -408,18 +406,17 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
     __syncthreads();
     // 4. codes of this thread's rows of its chunk
     if (worker) {
-      float mn[8], sc[8], rs[8];
+      const uint64_t* const pq = reinterpret_cast<const uint64_t*>(prm);
+      uint64_t nmn[4], nsc[4], y[4];
       bool fast = true;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 a = prm[i * nchunk + ch], b = prm[(4 + i) * nchunk + ch], c = prm[(8 + i) * nchunk + ch];
-        mn[2 * i] = a.x;
-        mn[2 * i + 1] = a.y;
-        sc[2 * i] = b.x;
-        sc[2 * i + 1] = b.y;
-        rs[2 * i] = c.x;
-        rs[2 * i + 1] = c.y;
-        fast = fast && int4_fast_scale(b.x) && int4_fast_scale(b.y);
+        nmn[i] = pq[i * nchunk + ch];
+        nsc[i] = pq[(4 + i) * nchunk + ch];
+        y[i] = pq[(8 + i) * nchunk + ch];
+        uint32_t sl, sh;
+        unpack_f32x2(nsc[i], sl, sh);
+        fast = fast && int4_fast_scale(-__uint_as_float(sl)) && int4_fast_scale(-__uint_as_float(sh));
       }
       uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(h) * npair + ch * 4;
       const int64_t cstride = static_cast<int64_t>(p.H) * npair;
@@ -427,7 +424,8 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
         if (ch == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
         const uint4 v = *reinterpret_cast<const uint4*>(tw + row * npair);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        STX(reinterpret_cast<uint32_t*>(cbase + (r0 + row) * cstride), chunk_codes(w, mn, sc, rs, fast));
+        STX(reinterpret_cast<uint32_t*>(cbase + (r0 + row) * cstride),
+            fast ? int4_codes8(w, nmn, nsc, y) : int4_codes8_div(w, nmn, nsc));
       }
     }
     __syncthreads();  // stage st, the partials and the parameters are free again
@@ -437,31 +435,44 @@ __global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4Encod
   cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
 }
 
-// VALUE kind: one lane per 16-channel block of a row; a group spans W = min(G/16, L)
-// aligned lanes, reduced with a xor butterfly of uniform width.
+// Signed-integer order keys of binary32 values: the integer order is the float order
+// with -0 below +0 (IEEE 754-2019 minimum/maximum); the map is its own inverse.
+__device__ __forceinline__ int32_t f32_key(float f) {
+  const int32_t b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float f32_unkey(int32_t k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
+
+// VALUE kind: one lane per 16-channel block of a row, kRowsPerWarp = 32 / L rows per
+// warp; a group spans W = min(G/16, L) aligned lanes, reduced with a xor butterfly of
+// uniform width.  Each lane holds two rows' words (the next row's loads are issued
+// before this row's arithmetic), alternating between two register sets.  Rows past
+// the end and lanes past the last block load a valid row / block (the last one) and
+// store nothing; a repeated block lies in its own group or in one that stores nothing.
 template <int L, bool kResidual>
 __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & 31;
-  const int b = lane % L;
   const int sub = lane / L;
   const int nb = p.D / 16;
+  const bool has = lane % L < nb;
+  const int b = has ? lane % L : nb - 1;
   const int W = min(p.G / 16, L);
   const int ngv = (p.D + p.G - 1) / p.G;
+  const bool lead = has && (16 * b) % p.G == 0;  // writes its group's metadata
+  const int gidx = (16 * b) / p.G;
   const uint32_t total = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H);
   const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
-  const bool has = b < nb;
+  if (total == 0u) return;
 
-  // the 16 values of this lane's block of row `rw` (zeros when there is none)
-  auto load_row = [&](uint32_t rw, uint32_t (&w)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0u;
-    if (rw >= total || !has) return;
+  // the 16 values of this lane's block of row min(rw, total - 1); r = its compact row
+  auto load = [&](uint32_t rw, uint32_t (&w)[8], int32_t& r) {
     uint32_t ru, hu;
-    p.div_h.divmod(rw, ru, hu);
+    p.div_h.divmod(min(rw, total - 1u), ru, hu);
+    r = static_cast<int32_t>(ru);
     uint32_t a[4], c[4];
-    load_chunk8<kResidual>(p, static_cast<int32_t>(ru), static_cast<int32_t>(hu), 16 * b, a);
-    load_chunk8<kResidual>(p, static_cast<int32_t>(ru), static_cast<int32_t>(hu), 16 * b + 8, c);
+    load_chunk8<kResidual>(p, r, static_cast<int32_t>(hu), 16 * b, a);
+    load_chunk8<kResidual>(p, r, static_cast<int32_t>(hu), 16 * b + 8, c);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       w[i] = a[i];
@@ -469,66 +480,67 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     }
   };
 
-  uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
-  uint32_t w[8];
-  load_row(row, w);
-  for (; row - sub < total; row += stride) {
-    const bool valid = row < total && has;
-    uint32_t ru, hu;
-    p.div_h.divmod(valid ? row : 0u, ru, hu);
-    const int32_t r = static_cast<int32_t>(ru), h = static_cast<int32_t>(hu);
-    uint32_t nw[8];
-    load_row(row + stride, nw);  // the next row's loads before this row's arithmetic
-    if (valid && b == 0 && h == 0) check_pos<kResidual>(p, r);
+  auto code = [&](uint32_t rw, const uint32_t (&w)[8], int32_t r) {
+    const bool store = rw < total && has;
+    if constexpr (kResidual) {
+      if (store && b == 0 && static_cast<uint32_t>(r) * static_cast<uint32_t>(p.H) == rw) check_pos<kResidual>(p, r);
+    }
     // the lane's minimum / maximum (bf16x2 min/max, sign-OR for a zero minimum), then
-    // the group's over W lanes in bf16 order keys (-0 below +0): one word carries the
-    // minimum key (low half) and the complemented maximum key (high half), so a single
-    // unsigned min per butterfly round reduces both
-    uint32_t mm = 0xFFFFFFFFu;
-    if (valid) {
-      uint32_t m = w[0], M = w[0], s = w[0];
+    // the group's over W lanes in order keys
+    uint32_t m = w[0], M = w[0], s = w[0];
 #pragma unroll
-      for (int i = 1; i < 8; ++i) {
-        m = hmin2(m, w[i]);
-        M = hmax2(M, w[i]);
-        s |= w[i];
+    for (int i = 1; i < 8; ++i) {
+      m = hmin2(m, w[i]);
+      M = hmax2(M, w[i]);
+      s |= w[i];
+    }
+    m = hmin2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the lane's extremes
+    M = hmax2(M, __byte_perm(M, 0u, 0x1032));
+    int32_t kmn = f32_key(group_min(m, s & 0x80008000u)), kmx = f32_key(bf16lo(M));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      if (o < W) {  // W is uniform: every lane runs the same shuffles
+        kmn = min(kmn, __shfl_xor_sync(0xFFFFFFFFu, kmn, o));
+        kmx = max(kmx, __shfl_xor_sync(0xFFFFFFFFu, kmx, o));
       }
-      m = hmin2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the lane's extremes
-      M = hmax2(M, __byte_perm(M, 0u, 0x1032));
-      const uint32_t mbits = __float_as_uint(group_min(m, s & 0x80008000u)) >> 16;
-      mm = (bf16x2_key(mbits) & 0xFFFFu) | (~bf16x2_key(M) << 16);
     }
-    for (int o = 1; o < W; o <<= 1)  // W is uniform: every lane runs the same shuffles
-      mm = min_u16x2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
-    if (!valid) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = nw[i];
-      continue;
-    }
-    const uint32_t mnmx = bf16x2_unkey(mm ^ 0xFFFF0000u);  // low: minimum, high: maximum
-    const float lmn = bf16lo(mnmx);
-    const float sc = __fdiv_rn(__fsub_rn(bf16hi(mnmx), lmn), 15.0f);
-    const float rsc = int4_rcp(sc);
-    float mn8[8], sc8[8], rs8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mn8[i] = lmn;
-      sc8[i] = sc;
-      rs8[i] = rsc;
-    }
-    const bool fast = int4_fast_scale(sc);
+    const float mn = f32_unkey(kmn);
+    const float sc = int4_scale(__fsub_rn(f32_unkey(kmx), mn));
+    const uint64_t nmn2[4] = {dup_f32x2(-mn), dup_f32x2(-mn), dup_f32x2(-mn), dup_f32x2(-mn)};
+    const uint64_t nsc2[4] = {dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc)};
+    const float yv = int4_recip(sc);
+    const uint64_t y2[4] = {dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv)};
     const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
-    const uint32_t c0 = chunk_codes(w0, mn8, sc8, rs8, fast);
-    const uint32_t c1 = chunk_codes(w1, mn8, sc8, rs8, fast);
-    const int64_t drow = static_cast<int64_t>(r) * p.H + h;
-    store8B(p.dst.codes + drow * (p.D / 2) + 8 * b, c0, c1);
-    if ((16 * b) % p.G == 0) {
-      const int64_t m = drow * ngv + (16 * b) / p.G;
-      STX(p.dst.mn + m, f32_to_f16_bits(lmn));
-      STX(p.dst.sc + m, f32_to_f16_bits(sc));
+    uint32_t c0, c1;
+    if (int4_fast_scale(sc)) {
+      c0 = int4_codes8(w0, nmn2, nsc2, y2);
+      c1 = int4_codes8(w1, nmn2, nsc2, y2);
+    } else {
+      c0 = int4_codes8_div(w0, nmn2, nsc2);
+      c1 = int4_codes8_div(w1, nmn2, nsc2);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = nw[i];
+    if (store) {
+      store8B(p.dst.codes + static_cast<int64_t>(rw) * (p.D / 2) + 8 * b, c0, c1);
+      if (lead) {
+        const int64_t mi = static_cast<int64_t>(rw) * ngv + gidx;
+        STX(p.dst.mn + mi, f32_to_f16_bits(mn));
+        STX(p.dst.sc + mi, f32_to_f16_bits(sc));
+      }
+    }
+  };
+
+  uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
+  uint32_t wa[8], wb[8];
+  int32_t ra, rb;
+  load(row, wa, ra);
+  while (row - sub < total) {  // row - sub is uniform across the warp
+    load(row + stride, wb, rb);
+    code(row, wa, ra);
+    row += stride;
+    if (row - sub >= total) break;
+    load(row + stride, wa, ra);
+    code(row, wb, rb);
+    row += stride;
   }
 }
 

@@ -282,12 +282,15 @@ def test_int4_signed_zero_groups_match_the_oracle(kind):
 
 
 @pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
-def test_int4_tiny_and_subnormal_groups(kind):
+@pytest.mark.parametrize("exps", [(-140, -133, -128, -126, -120, -110, -100, 0),
+                                  (-80, -70, -67, -66, -65, -63, -60, -40)])
+def test_int4_tiny_and_subnormal_groups(kind, exps):
     """Groups at scales 2^-140 .. 2^-100 (bf16 subnormals, subnormal and tiny normal
-    scales: the exact division path) beside ordinary groups, against the oracle."""
+    scales) and around 2^-64 (where the kernels switch from dividing to the reciprocal
+    and residual steps) beside ordinary groups, against the oracle."""
     T, H, D = 512, 2, 128
     x = synth.normal_bf16((T, H, D), seed=13, stream=1).float()
-    exps = torch.tensor([-140, -133, -128, -126, -120, -110, -100, 0], dtype=torch.float32)
+    exps = torch.tensor(exps, dtype=torch.float32)
     if kind == kvq.KIND_KEY:  # one scale per 64-row group
         s = exps.repeat_interleave(64)[:T].view(T, 1, 1)
     else:  # one scale per 64-channel group
@@ -295,7 +298,8 @@ def test_int4_tiny_and_subnormal_groups(kind):
         s = torch.cat([s.expand(T, H, 64), torch.zeros(T, H, 64)], dim=2)
     xb = (x * torch.exp2(s)).to(torch.bfloat16)
     bits_in = bits(xb)
-    assert ((bits_in & 0x7F80) == 0).any() and ((bits_in & 0x7FFF) != 0).any()  # subnormals present
+    if float(exps.min()) < -126:  # subnormals present
+        assert (((bits_in & 0x7F80) == 0) & ((bits_in & 0x7FFF) != 0)).any()
     pk, y = gpu_int4_pack(xb.to(DEV), kind)
     codes, mn, sc = O.int4_pack(bits_in, kind, 64)
     check_int4(pk, codes, mn, sc)
