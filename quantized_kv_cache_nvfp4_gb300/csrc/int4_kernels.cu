@@ -64,6 +64,17 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
 __device__ __forceinline__ uint64_t dup_f32x2(float v) {
   return pack_f32x2(__float_as_uint(v), __float_as_uint(v));
 }
+// (x_lo + c_lo, x_hi + c_hi) in binary32 for the two bf16 of w and the pair c, each sum
+// rounded once (the bf16 -> f32 widening is exact): mixed-precision adds.
+__device__ __forceinline__ uint64_t add_bf16x2_f32x2(uint32_t w, uint64_t c) {
+  uint32_t cl, ch;
+  unpack_f32x2(c, cl, ch);
+  float dl, dh;
+  asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(dl), "=f"(dh)
+      : "r"(w), "f"(__uint_as_float(cl)), "f"(__uint_as_float(ch)));
+  return pack_f32x2(__float_as_uint(dl), __float_as_uint(dh));
+}
 
 // Codes of the 8 bf16 of words w[0..3] (channel 2i in the low half of w[i], 2i + 1 in
 // the high half) for fast scales, with per-channel-pair parameters as f32x2 pairs:
@@ -76,7 +87,7 @@ __device__ __forceinline__ uint32_t int4_codes8(const uint32_t (&w)[4], const ui
   uint32_t byte[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint64_t d = add_f32x2(pack_f32x2(w[i] << 16, w[i] & 0xFFFF0000u), nmn[i]);
+    const uint64_t d = add_bf16x2_f32x2(w[i], nmn[i]);
     const uint64_t q0 = mul_f32x2(d, y[i]);
     const uint64_t q1 = fma_f32x2(fma_f32x2(q0, nsc[i], d), y[i], q0);
     const uint64_t q2 = fma_f32x2(fma_f32x2(q1, nsc[i], d), y[i], q1);
@@ -443,44 +454,47 @@ __device__ __forceinline__ int32_t f32_key(float f) {
 }
 __device__ __forceinline__ float f32_unkey(int32_t k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
 
-// VALUE kind: one lane per 16-channel block of a row, kRowsPerWarp = 32 / L rows per
-// warp; a group spans W = min(G/16, L) aligned lanes, reduced with a xor butterfly of
-// uniform width.  Each lane holds two rows' words (the next row's loads are issued
-// before this row's arithmetic), alternating between two register sets.  Rows past
-// the end and lanes past the last block load a valid row / block (the last one) and
-// store nothing; a repeated block lies in its own group or in one that stores nothing.
-template <int L, bool kResidual>
-__global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodeParams p) {
+// VALUE kind: one lane per kBlk consecutive 16-channel blocks of a row (C = 16 kBlk
+// channels; kBlk = 2 when D % 32 == 0 and G >= 32, so a lane's channels lie in one
+// group), kRowsPerWarp = 32 / L rows per warp; a group spans W = min(G/C, L) aligned
+// lanes, reduced with a xor butterfly of uniform width.  Each lane holds two rows'
+// words (the next row's loads are issued before this row's arithmetic), alternating
+// between two register sets.  Rows past the end and lanes past the last block load a
+// valid row / block (the last one) and store nothing; a repeated block lies in its own
+// group or in one that stores nothing.
+template <int L, int kBlk, bool kResidual>
+__global__ void __launch_bounds__(kThreads, kBlk == 2 ? 3 : 4) int4_value_kernel(const Int4EncodeParams p) {
   constexpr int kRowsPerWarp = 32 / L;
+  constexpr int C = 16 * kBlk;     // channels per lane
+  constexpr int NW = 8 * kBlk;     // 32-bit words per lane
   const int lane = threadIdx.x & 31;
   const int sub = lane / L;
-  const int nb = p.D / 16;
+  const int nb = p.D / C;
   const bool has = lane % L < nb;
   const int b = has ? lane % L : nb - 1;
-  const int W = min(p.G / 16, L);
+  const int W = min(p.G / C, L);
   const int ngv = (p.D + p.G - 1) / p.G;
-  const bool lead = has && (16 * b) % p.G == 0;  // writes its group's metadata
-  const int gidx = (16 * b) / p.G;
+  const bool lead = has && (C * b) % p.G == 0;  // writes its group's metadata
+  const int gidx = (C * b) / p.G;
   const uint32_t total = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H);
   const uint32_t stride = gridDim.x * (kThreads / 32) * kRowsPerWarp;
   if (total == 0u) return;
 
-  // the 16 values of this lane's block of row min(rw, total - 1); r = its compact row
-  auto load = [&](uint32_t rw, uint32_t (&w)[8], int32_t& r) {
+  // the C values of this lane's blocks of row min(rw, total - 1); r = its compact row
+  auto load = [&](uint32_t rw, uint32_t (&w)[NW], int32_t& r) {
     uint32_t ru, hu;
     p.div_h.divmod(min(rw, total - 1u), ru, hu);
     r = static_cast<int32_t>(ru);
-    uint32_t a[4], c[4];
-    load_chunk8<kResidual>(p, r, static_cast<int32_t>(hu), 16 * b, a);
-    load_chunk8<kResidual>(p, r, static_cast<int32_t>(hu), 16 * b + 8, c);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[i] = a[i];
-      w[4 + i] = c[i];
+    for (int k = 0; k < 2 * kBlk; ++k) {
+      uint32_t a[4];
+      load_chunk8<kResidual>(p, r, static_cast<int32_t>(hu), C * b + 8 * k, a);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[4 * k + i] = a[i];
     }
   };
 
-  auto code = [&](uint32_t rw, const uint32_t (&w)[8], int32_t r) {
+  auto code = [&](uint32_t rw, const uint32_t (&w)[NW], int32_t r) {
     const bool store = rw < total && has;
     if constexpr (kResidual) {
       if (store && b == 0 && static_cast<uint32_t>(r) * static_cast<uint32_t>(p.H) == rw) check_pos<kResidual>(p, r);
@@ -489,7 +503,7 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     // the group's over W lanes in order keys
     uint32_t m = w[0], M = w[0], s = w[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) {
+    for (int i = 1; i < NW; ++i) {
       m = hmin2(m, w[i]);
       M = hmax2(M, w[i]);
       s |= w[i];
@@ -510,17 +524,20 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
     const uint64_t nsc2[4] = {dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc)};
     const float yv = int4_recip(sc);
     const uint64_t y2[4] = {dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv)};
-    const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
-    uint32_t c0, c1;
-    if (int4_fast_scale(sc)) {
-      c0 = int4_codes8(w0, nmn2, nsc2, y2);
-      c1 = int4_codes8(w1, nmn2, nsc2, y2);
-    } else {
-      c0 = int4_codes8_div(w0, nmn2, nsc2);
-      c1 = int4_codes8_div(w1, nmn2, nsc2);
+    const bool fast = int4_fast_scale(sc);
+    uint32_t cw[2 * kBlk];
+#pragma unroll
+    for (int k = 0; k < 2 * kBlk; ++k) {
+      const uint32_t wk[4] = {w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]};
+      cw[k] = fast ? int4_codes8(wk, nmn2, nsc2, y2) : int4_codes8_div(wk, nmn2, nsc2);
     }
     if (store) {
-      store8B(p.dst.codes + static_cast<int64_t>(rw) * (p.D / 2) + 8 * b, c0, c1);
+      uint8_t* const dst = p.dst.codes + static_cast<int64_t>(rw) * (p.D / 2) + (C / 2) * b;
+      if constexpr (kBlk == 2) {
+        store16B(dst, cw);
+      } else {
+        store8B(dst, cw[0], cw[1]);
+      }
       if (lead) {
         const int64_t mi = static_cast<int64_t>(rw) * ngv + gidx;
         STX(p.dst.mn + mi, f32_to_f16_bits(mn));
@@ -530,7 +547,7 @@ __global__ void __launch_bounds__(kThreads) int4_value_kernel(const Int4EncodePa
   };
 
   uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
-  uint32_t wa[8], wb[8];
+  uint32_t wa[NW], wb[NW];
   int32_t ra, rb;
   load(row, wa, ra);
   while (row - sub < total) {  // row - sub is uniform across the warp
@@ -555,28 +572,35 @@ int grid_cap(K kernel, int64_t work_items, int items_per_cta) {
   return static_cast<int>(need < cap ? need : cap);
 }
 
-template <int L, bool kRes>
+template <int L, int kBlk, bool kRes>
 cudaError_t value_launch(const Int4EncodeParams& p, cudaStream_t s) {
-  auto k = int4_value_kernel<L, kRes>;
+  auto k = int4_value_kernel<L, kBlk, kRes>;
   int grid = grid_cap(k, static_cast<int64_t>(p.rows) * p.H, (kThreads / 32) * (32 / L));
   cudaError_t e = cudaSuccess;
   KVQ_LAUNCH("int4_value_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
   return e;
 }
 
-template <bool kRes>
-cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
-  int nb = p.D / 16, L = 1;
+template <int kBlk, bool kRes>
+cudaError_t value_dispatch_blk(const Int4EncodeParams& p, cudaStream_t s) {
+  int nb = p.D / (16 * kBlk), L = 1;
   while (L < nb) L <<= 1;
   switch (L) {
-    case 1: return value_launch<1, kRes>(p, s);
-    case 2: return value_launch<2, kRes>(p, s);
-    case 4: return value_launch<4, kRes>(p, s);
-    case 8: return value_launch<8, kRes>(p, s);
-    case 16: return value_launch<16, kRes>(p, s);
-    case 32: return value_launch<32, kRes>(p, s);
+    case 1: return value_launch<1, kBlk, kRes>(p, s);
+    case 2: return value_launch<2, kBlk, kRes>(p, s);
+    case 4: return value_launch<4, kBlk, kRes>(p, s);
+    case 8: return value_launch<8, kBlk, kRes>(p, s);
+    case 16: return value_launch<16, kBlk, kRes>(p, s);
+    case 32: return value_launch<32, kBlk, kRes>(p, s);
   }
   return cudaErrorInvalidValue;
+}
+
+// Two blocks per lane when a lane's 32 channels stay inside one group.
+template <bool kRes>
+cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
+  if (p.D % 32 == 0 && p.G >= 32) return value_dispatch_blk<2, kRes>(p, s);
+  return value_dispatch_blk<1, kRes>(p, s);
 }
 
 template <bool kRes, int RS, int RPL>

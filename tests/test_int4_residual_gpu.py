@@ -45,7 +45,9 @@ def check_payload(pay, opay):
 
 @pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
 @pytest.mark.parametrize("T,H,D,G", [(256, 8, 128, 64), (4100, 2, 128, 64), (130, 3, 96, 64),
-                                     (64, 2, 32, 64), (200, 2, 128, 16), (77, 1, 512, 512)])
+                                     (64, 2, 32, 64), (200, 2, 128, 16), (77, 1, 512, 512),
+                                     (100, 3, 96, 32), (50, 2, 224, 64), (40, 1, 480, 128),
+                                     (33, 5, 80, 32), (9, 1, 256, 32)])
 def test_int4_pack_unpack_matches_oracle(kind, T, H, D, G):
     x = synth.normal_bf16((T, H, D), seed=50 + T, stream=1, outlier_frac=0.01, outlier_scale=20.0)
     pk, y = gpu_int4_pack(x.to(DEV), kind, G)
