@@ -144,8 +144,6 @@ __device__ __forceinline__ float group_min(uint32_t m, uint32_t any_sign) {
   const float v = __uint_as_float(m << 16);
   return v == 0.0f ? __uint_as_float(any_sign != 0u ? 0x80000000u : 0u) : v;
 }
-constexpr uint32_t kPosInf2 = 0x7F807F80u;  // bf16x2 +inf, +inf
-constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // bf16x2 -inf, -inf
 
 // The 8 bf16 values of one 16-byte chunk of a compact row (residual: bf16(cur-prev)).
 // Returns false for a residual row whose position is out of range (values zero).
@@ -184,14 +182,17 @@ __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row
   }
 }
 
-// KEY kind, register fallback for tiles too large for shared memory: a column task is
-// (group of G rows, head, 8-channel chunk).  RS = G / RPL lanes share a task; each
-// holds its RPL rows of the chunk in registers (all loads issued together), so every
-// row is read once.  The RS partial minima/maxima meet in a xor butterfly (in bf16
-// order keys, -0 below +0), then each lane codes its own rows.
-template <bool kResidual, int RS, int RPL>
+// KEY kind, in registers: a column task is (group of G rows, head, 8-channel chunk).
+// S = G / RPT lanes share a task, lane rs holding rows rs, rs + S, ... (RPT of them) of
+// the chunk, all loads issued together, so every row is read once.  The lanes' minima,
+// maxima (bf16x2 min/max) and sign ORs meet in a xor butterfly; a zero minimum takes
+// its sign from the group's OR (a zero minimum means no element is negative, so a set
+// sign bit is a -0).  Every lane then forms the 8 channels' parameters and codes its
+// rows.  Rows past a partial group repeat its last row and lanes past the last task
+// repeat that task: neither changes a group's extrema, and neither stores.
+template <bool kResidual, int S, int RPT>
 __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
-  constexpr int CW = 32 / RS;
+  constexpr int CW = 32 / S;  // column tasks per warp
   const int lane = threadIdx.x & 31;
   const int rs = lane / CW;
   const int cl = lane % CW;
@@ -204,73 +205,64 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
        wt += nwarps) {
     const int64_t task = wt * CW + cl;
     const bool valid = task < ntask;
-    const int64_t tk = valid ? task : 0;
+    const int64_t tk = valid ? task : ntask - 1;
     const int32_t chunk = static_cast<int32_t>(tk % nchunk);
     const int32_t h = static_cast<int32_t>((tk / nchunk) % p.H);
     const int32_t g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
     const int32_t r0 = g * p.G;
-    const int32_t r1 = valid ? min(p.rows, r0 + p.G) : r0;
+    const int32_t rlast = min(p.rows, r0 + p.G) - 1;
     const int32_t col = chunk * 8;
 
-    uint32_t v[RPL][4];
+    uint32_t v[RPT][4];
 #pragma unroll
-    for (int k = 0; k < RPL; ++k) {
-      const int32_t r = r0 + rs + k * RS;
-      if (r < r1) {
-        load_chunk8<kResidual>(p, r, h, col, v[k]);
-      } else {
-        v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0u;
-      }
-    }
-    uint32_t kmn[4], kmx[4];
+    for (int k = 0; k < RPT; ++k) load_chunk8<kResidual>(p, min(r0 + rs + k * S, rlast), h, col, v[k]);
+    uint32_t m[4], M[4], sg[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kmn[i] = 0xFFFFFFFFu;
-      kmx[i] = 0u;
-    }
+    for (int i = 0; i < 4; ++i) m[i] = M[i] = sg[i] = v[0][i];
 #pragma unroll
-    for (int k = 0; k < RPL; ++k) {
-      if (r0 + rs + k * RS >= r1) continue;
+    for (int k = 1; k < RPT; ++k) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t key = bf16x2_key(v[k][i]);
-        kmn[i] = min_u16x2(kmn[i], key);
-        kmx[i] = max_u16x2(kmx[i], key);
+        m[i] = hmin2(m[i], v[k][i]);
+        M[i] = hmax2(M[i], v[k][i]);
+        sg[i] |= v[k][i];
       }
     }
 #pragma unroll
     for (int o = CW; o < 32; o <<= 1) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        kmn[i] = min_u16x2(kmn[i], __shfl_xor_sync(0xFFFFFFFFu, kmn[i], o));
-        kmx[i] = max_u16x2(kmx[i], __shfl_xor_sync(0xFFFFFFFFu, kmx[i], o));
+        m[i] = hmin2(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], o));
+        M[i] = hmax2(M[i], __shfl_xor_sync(0xFFFFFFFFu, M[i], o));
+        sg[i] |= __shfl_xor_sync(0xFFFFFFFFu, sg[i], o);
       }
     }
-    if (!valid) continue;
     float mn[8], sc[8];
     uint64_t nmn[4], nsc[4], y[4];
     bool fast = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t a = bf16x2_unkey(kmn[i]), b = bf16x2_unkey(kmx[i]);
-      mn[2 * i] = bf16lo(a);
-      mn[2 * i + 1] = bf16hi(a);
-      sc[2 * i] = int4_scale(__fsub_rn(bf16lo(b), mn[2 * i]));
-      sc[2 * i + 1] = int4_scale(__fsub_rn(bf16hi(b), mn[2 * i + 1]));
+      mn[2 * i] = group_min(m[i], sg[i] & 0x8000u);
+      mn[2 * i + 1] = group_min(m[i] >> 16, sg[i] & 0x80000000u);
+      sc[2 * i] = int4_scale(__fsub_rn(bf16lo(M[i]), mn[2 * i]));
+      sc[2 * i + 1] = int4_scale(__fsub_rn(bf16hi(M[i]), mn[2 * i + 1]));
       nmn[i] = pack_f32x2(__float_as_uint(-mn[2 * i]), __float_as_uint(-mn[2 * i + 1]));
       nsc[i] = pack_f32x2(__float_as_uint(-sc[2 * i]), __float_as_uint(-sc[2 * i + 1]));
       y[i] = pack_f32x2(__float_as_uint(int4_recip(sc[2 * i])), __float_as_uint(int4_recip(sc[2 * i + 1])));
       fast = fast && int4_fast_scale(sc[2 * i]) && int4_fast_scale(sc[2 * i + 1]);
     }
+    uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(h) * (p.D / 2) + col / 2;
+    const int64_t cstride = static_cast<int64_t>(p.H) * (p.D / 2);
 #pragma unroll
-    for (int k = 0; k < RPL; ++k) {
-      const int32_t r = r0 + rs + k * RS;
-      if (r >= r1) continue;
-      if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
-      STX(reinterpret_cast<uint32_t*>(p.dst.codes + (static_cast<int64_t>(r) * p.H + h) * (p.D / 2) + col / 2),
-          fast ? int4_codes8(v[k], nmn, nsc, y) : int4_codes8_div(v[k], nmn, nsc));
+    for (int k = 0; k < RPT; ++k) {
+      const int32_t r = r0 + rs + k * S;
+      if (valid && r <= rlast) {
+        if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
+        STX(reinterpret_cast<uint32_t*>(cbase + r * cstride),
+            fast ? int4_codes8(v[k], nmn, nsc, y) : int4_codes8_div(v[k], nmn, nsc));
+      }
     }
-    if (rs == 0) {
+    if (valid && rs == 0) {
       uint32_t m16[4], s16[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -279,171 +271,11 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         s16[i] = static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i])) |
                  (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
       }
-      const int64_t m = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
-      store16B(p.dst.mn + m, m16);
-      store16B(p.dst.sc + m, s16);
+      const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
+      store16B(p.dst.mn + mi, m16);
+      store16B(p.dst.sc + mi, s16);
     }
   }
-}
-
-// KEY kind, tiled through shared memory: a block takes one tile (a group of up to G
-// rows x the D channels of one head) at a time, in kStages shared-memory buffers.
-// Thread (rq, ch) owns 16-byte chunk ch (channels 8ch .. 8ch + 7) of rows rq,
-// rq + RP, ... (RP = 256 / (D / 8) rows per pass) through every step:
-//  1. the tile's rows are copied into shared memory with 16-byte cp.async copies; with
-//     two stages the next tile's copies are in flight while this tile is coded.
-//     Residual mode gathers the rows at pos[] from cur and prev into two planes;
-//  2. each thread reduces its rows of its chunk (residual: forms bf16(cur - prev) in
-//     place first) to partial min / max / sign-OR words;
-//  3. one thread per channel pair combines the RP partials, computes the group's
-//     minimum, scale and reciprocal, keeps them in shared memory and writes the FP16
-//     metadata;
-//  4. each thread codes its rows of its chunk: 8 codes -> one 32-bit store.
-template <bool kResidual, int kStages>
-__global__ void __launch_bounds__(kThreads) int4_key_tile_kernel(const Int4EncodeParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int kPlanes = kResidual ? 2 : 1;
-  const int D = p.D;
-  const int nchunk = D / 8;  // 16-byte chunks per row
-  const int npair = D / 2;   // 32-bit words per row
-  const int RP = kThreads / nchunk;
-  const int tid = threadIdx.x;
-  const bool worker = tid < RP * nchunk;
-  const int ch = tid % nchunk;
-  const int rq = tid / nchunk;
-  const int tile_words = p.G * npair;
-  uint32_t* const buf = reinterpret_cast<uint32_t*>(smem);                             // [kStages][kPlanes][G][D/2]
-  uint4* const part = reinterpret_cast<uint4*>(buf + kStages * kPlanes * tile_words);  // [3][RP][D/8]
-  float2* const prm = reinterpret_cast<float2*>(part + 3 * RP * nchunk);               // [3][D/2]
-  const uint32_t ntiles = static_cast<uint32_t>((p.rows + p.G - 1) / p.G) * static_cast<uint32_t>(p.H);
-
-  // copies of tile `tile` into stage `st` (nothing past the last tile)
-  auto issue = [&](uint32_t tile, int st) {
-    if (!worker || tile >= ntiles) return;
-    uint32_t g, h;
-    p.div_h.divmod(tile, g, h);
-    const int32_t r0 = static_cast<int32_t>(g) * p.G;
-    const int32_t nr = min(p.G, p.rows - r0);
-    uint32_t* const cur = buf + st * kPlanes * tile_words + ch * 4;
-    for (int row = rq; row < nr; row += RP) {
-      uint32_t* const dst = cur + row * npair;
-      int64_t src = r0 + row;
-      if constexpr (kResidual) {
-        if (p.pos != nullptr) src = LDX(p.pos + r0 + row);
-        if (src < 0 || src >= p.src_rows) {  // a bad position codes zeros (and is flagged)
-          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(dst + tile_words) = make_uint4(0u, 0u, 0u, 0u);
-          continue;
-        }
-        cp_async16(dst + tile_words,
-                   p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + ch * 8);
-      }
-      cp_async16(dst, p.x + src * p.row_pitch + static_cast<int64_t>(h) * p.head_pitch + ch * 8);
-    }
-  };
-
-  uint32_t tile = blockIdx.x;
-  issue(tile, 0);
-  cp_async_commit();
-  if constexpr (kStages == 2) {
-    issue(tile + gridDim.x, 1);
-    cp_async_commit();
-  }
-  for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
-    const int st = kStages == 2 ? (it & 1) : 0;
-    if constexpr (kStages == 2) {
-      cp_async_wait<1>();  // this tile's group is complete; the next may be in flight
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    uint32_t g, h;
-    p.div_h.divmod(tile, g, h);
-    const int32_t r0 = static_cast<int32_t>(g) * p.G;
-    const int32_t nr = min(p.G, p.rows - r0);
-    uint32_t* const tw = buf + st * kPlanes * tile_words + ch * 4;  // this thread's column
-    // 2. partial minimum / maximum / sign-OR of this thread's rows of its chunk
-    if (worker) {
-      uint32_t mn[4] = {kPosInf2, kPosInf2, kPosInf2, kPosInf2};
-      uint32_t mx[4] = {kNegInf2, kNegInf2, kNegInf2, kNegInf2};
-      uint32_t sg[4] = {0u, 0u, 0u, 0u};
-      for (int row = rq; row < nr; row += RP) {
-        uint4 v = *reinterpret_cast<const uint4*>(tw + row * npair);
-        if constexpr (kResidual) {
-          const uint4 q = *reinterpret_cast<const uint4*>(tw + tile_words + row * npair);
-          v.x = pack_bf16x2(__fsub_rn(bf16lo(v.x), bf16lo(q.x)), __fsub_rn(bf16hi(v.x), bf16hi(q.x)));
-          v.y = pack_bf16x2(__fsub_rn(bf16lo(v.y), bf16lo(q.y)), __fsub_rn(bf16hi(v.y), bf16hi(q.y)));
-          v.z = pack_bf16x2(__fsub_rn(bf16lo(v.z), bf16lo(q.z)), __fsub_rn(bf16hi(v.z), bf16hi(q.z)));
-          v.w = pack_bf16x2(__fsub_rn(bf16lo(v.w), bf16lo(q.w)), __fsub_rn(bf16hi(v.w), bf16hi(q.w)));
-          *reinterpret_cast<uint4*>(tw + row * npair) = v;  // read back by this thread in step 4
-        }
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          mn[i] = hmin2(mn[i], w[i]);
-          mx[i] = hmax2(mx[i], w[i]);
-          sg[i] |= w[i];
-        }
-      }
-      part[(0 * RP + rq) * nchunk + ch] = make_uint4(mn[0], mn[1], mn[2], mn[3]);
-      part[(1 * RP + rq) * nchunk + ch] = make_uint4(mx[0], mx[1], mx[2], mx[3]);
-      part[(2 * RP + rq) * nchunk + ch] = make_uint4(sg[0], sg[1], sg[2], sg[3]);
-    }
-    __syncthreads();
-    // 3. per channel pair (32-bit word w = tid): the group's minimum, scale and
-    //    reciprocal, kept in shared memory (minimum and scale negated) at
-    //    [param][w % 4][w / 4] (so step 4 reads consecutive words), and the FP16 metadata
-    if (tid < npair) {
-      const uint32_t* pw = reinterpret_cast<const uint32_t*>(part);  // [3][RP][D/2] words
-      uint32_t m = kPosInf2, M = kNegInf2, sgn = 0u;
-      for (int k = 0; k < RP; ++k) {
-        m = hmin2(m, pw[(0 * RP + k) * npair + tid]);
-        M = hmax2(M, pw[(1 * RP + k) * npair + tid]);
-        sgn |= pw[(2 * RP + k) * npair + tid];
-      }
-      const float mnl = group_min(m, sgn & 0x8000u), mnh = group_min(m >> 16, sgn & 0x80000000u);
-      const float scl = int4_scale(__fsub_rn(bf16lo(M), mnl));
-      const float sch = int4_scale(__fsub_rn(bf16hi(M), mnh));
-      const int slot = (tid % 4) * nchunk + tid / 4;
-      prm[slot] = make_float2(-mnl, -mnh);
-      prm[4 * nchunk + slot] = make_float2(-scl, -sch);
-      prm[8 * nchunk + slot] = make_float2(int4_recip(scl), int4_recip(sch));
-      const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * D + 2 * tid;
-      STX(reinterpret_cast<uint32_t*>(p.dst.mn + mi),
-          static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16));
-      STX(reinterpret_cast<uint32_t*>(p.dst.sc + mi),
-          static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16));
-    }
-    __syncthreads();
-    // 4. codes of this thread's rows of its chunk
-    if (worker) {
-      const uint64_t* const pq = reinterpret_cast<const uint64_t*>(prm);
-      uint64_t nmn[4], nsc[4], y[4];
-      bool fast = true;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        nmn[i] = pq[i * nchunk + ch];
-        nsc[i] = pq[(4 + i) * nchunk + ch];
-        y[i] = pq[(8 + i) * nchunk + ch];
-        uint32_t sl, sh;
-        unpack_f32x2(nsc[i], sl, sh);
-        fast = fast && int4_fast_scale(-__uint_as_float(sl)) && int4_fast_scale(-__uint_as_float(sh));
-      }
-      uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(h) * npair + ch * 4;
-      const int64_t cstride = static_cast<int64_t>(p.H) * npair;
-      for (int row = rq; row < nr; row += RP) {
-        if (ch == 0 && h == 0) check_pos<kResidual>(p, r0 + row);
-        const uint4 v = *reinterpret_cast<const uint4*>(tw + row * npair);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        STX(reinterpret_cast<uint32_t*>(cbase + (r0 + row) * cstride),
-            fast ? int4_codes8(w, nmn, nsc, y) : int4_codes8_div(w, nmn, nsc));
-      }
-    }
-    __syncthreads();  // stage st, the partials and the parameters are free again
-    issue(tile + static_cast<uint32_t>(kStages) * gridDim.x, st);
-    cp_async_commit();
-  }
-  cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
 }
 
 // Signed-integer order keys of binary32 values: the integer order is the float order
@@ -603,57 +435,25 @@ cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   return value_dispatch_blk<1, kRes>(p, s);
 }
 
-template <bool kRes, int RS, int RPL>
+template <bool kRes, int S, int RPT>
 cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s) {
-  auto k = int4_key_kernel<kRes, RS, RPL>;
-  const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
+  auto k = int4_key_kernel<kRes, S, RPT>;
+  const int64_t warps = (ntask + 32 / S - 1) / (32 / S);
   const int grid = grid_cap(k, warps, kThreads / 32);
   cudaError_t e = cudaSuccess;
   KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
   return e;
 }
 
-// Shared memory of the tile kernel: kStages x planes tiles of G x D bf16, the
-// [3][RP][D/8] partial chunks and the [3][D/2] float2 group parameters.
-size_t key_tile_smem(int G, int D, int stages, int planes) {
-  const size_t nchunk = static_cast<size_t>(D / 8);
-  return static_cast<size_t>(stages) * planes * G * D * 2 + 3 * (kThreads / nchunk) * nchunk * 16 +
-         3 * static_cast<size_t>(D / 2) * 8;
-}
-
-constexpr size_t kTileSmemCap = 110 * 1024;  // two blocks per SM at least
-
-template <bool kRes, int kStages>
-cudaError_t key_tile_launch(const Int4EncodeParams& p, cudaStream_t s) {
-  auto k = int4_key_tile_kernel<kRes, kStages>;
-  const size_t smem = key_tile_smem(p.G, p.D, kStages, kRes ? 2 : 1);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem);
-  if (occ < 1) occ = 1;
-  const int64_t tiles = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
-  const int grid = static_cast<int>(tiles < cap ? (tiles < 1 ? 1 : tiles) : cap);
-  cudaError_t e = cudaSuccess;
-  KVQ_LAUNCH("int4_key_tile_kernel", s, k<<<grid, kThreads, smem, s>>>(p); e = cudaGetLastError());
-  return e;
-}
-
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
-  const int planes = kRes ? 2 : 1;
-  if (key_tile_smem(p.G, p.D, 2, planes) <= kTileSmemCap) return key_tile_launch<kRes, 2>(p, s);
-  if (key_tile_smem(p.G, p.D, 1, planes) <= kTileSmemCap) return key_tile_launch<kRes, 1>(p, s);
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
-  switch (p.G) {  // RS = G / RPL lanes per column task
-    case 16: return key_launch<kRes, 2, 8>(p, ntask, s);
-    case 32: return key_launch<kRes, 4, 8>(p, ntask, s);
-    case 64: return key_launch<kRes, 8, 8>(p, ntask, s);
-    case 128: return key_launch<kRes, 16, 8>(p, ntask, s);
-    case 256: return key_launch<kRes, 32, 8>(p, ntask, s);
+  switch (p.G) {  // S = G / 16 lanes per column task, 16 rows each
+    case 16: return key_launch<kRes, 1, 16>(p, ntask, s);
+    case 32: return key_launch<kRes, 2, 16>(p, ntask, s);
+    case 64: return key_launch<kRes, 4, 16>(p, ntask, s);
+    case 128: return key_launch<kRes, 8, 16>(p, ntask, s);
+    case 256: return key_launch<kRes, 16, 16>(p, ntask, s);
     case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
   }
   return cudaErrorInvalidValue;
