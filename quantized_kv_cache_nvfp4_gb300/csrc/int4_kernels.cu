@@ -184,15 +184,31 @@ __device__ __forceinline__ void check_pos(const Int4EncodeParams& p, int32_t row
 
 // KEY kind, in registers: a column task is (group of G rows, head, 8-channel chunk).
 // S = G / RPT lanes share a task, lane rs holding rows rs, rs + S, ... (RPT of them) of
-// the chunk, all loads issued together, so every row is read once.  The lanes' minima,
-// maxima (bf16x2 min/max) and sign ORs meet in a xor butterfly; a zero minimum takes
-// its sign from the group's OR (a zero minimum means no element is negative, so a set
-// sign bit is a -0).  Every lane then forms the 8 channels' parameters and codes its
-// rows.  Rows past a partial group repeat its last row and lanes past the last task
-// repeat that task: neither changes a group's extrema, and neither stores.
+// the chunk, so every row is read once.  The lanes' minima, maxima (bf16x2 min/max)
+// and sign ORs meet in a xor butterfly; a zero minimum takes its sign from the group's
+// OR (a zero minimum means no element is negative, so a set sign bit is a -0).  Every
+// lane then forms the 8 channels' parameters and codes its rows.  Rows past a partial
+// group repeat its last row and lanes past the last task repeat that task: neither
+// changes a group's extrema, and neither stores.
+//
+// The rows arrive through a per-warp shared-memory slot of RPT x 32 16-byte cells per
+// plane (lane l's row k at cell k * 32 + l): each lane copies its own cells with
+// cp.async and reads back only those, so the lane's own wait_group orders them and no
+// barrier is needed.  The next task's copies are issued once this task's cells have
+// been read into registers (the extrema depend on every read, and a warp issues in
+// order), so they travel while this task is coded.  Residual mode copies cur and prev
+// and forms bf16(cur - prev) on reading; a bad position fills zeros.
+template <bool kResidual>
+__host__ __device__ constexpr int key_threads() { return kResidual ? 128 : 256; }
+template <bool kResidual, int RPT>
+__host__ __device__ constexpr size_t key_smem() { return static_cast<size_t>(key_threads<kResidual>() / 32) * (kResidual ? 2 : 1) * RPT * 32 * 16; }
+
 template <bool kResidual, int S, int RPT>
-__global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodeParams p) {
+__global__ void __launch_bounds__(key_threads<kResidual>()) int4_key_kernel(const Int4EncodeParams p) {
+  constexpr int kWarps = key_threads<kResidual>() / 32;
   constexpr int CW = 32 / S;  // column tasks per warp
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint4* const slot = reinterpret_cast<uint4*>(smem) + (threadIdx.x / 32) * ((kResidual ? 2 : 1) * RPT * 32);
   const int lane = threadIdx.x & 31;
   const int rs = lane / CW;
   const int cl = lane % CW;
@@ -200,22 +216,68 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
   const int32_t ngroups = (p.rows + p.G - 1) / p.G;
   const int64_t ntask = static_cast<int64_t>(ngroups) * p.H * nchunk;
   const int64_t nwtask = (ntask + CW - 1) / CW;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
-  for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
-       wt += nwarps) {
-    const int64_t task = wt * CW + cl;
-    const bool valid = task < ntask;
-    const int64_t tk = valid ? task : ntask - 1;
-    const int32_t chunk = static_cast<int32_t>(tk % nchunk);
-    const int32_t h = static_cast<int32_t>((tk / nchunk) % p.H);
-    const int32_t g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
-    const int32_t r0 = g * p.G;
-    const int32_t rlast = min(p.rows, r0 + p.G) - 1;
-    const int32_t col = chunk * 8;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
 
+  struct Task {
+    int32_t chunk, h, g, r0, rlast;
+    bool valid;
+  };
+  auto task_of = [&](int64_t wt) {
+    Task t;
+    const int64_t task = wt * CW + cl;
+    t.valid = task < ntask;
+    const int64_t tk = t.valid ? task : ntask - 1;
+    t.chunk = static_cast<int32_t>(tk % nchunk);
+    t.h = static_cast<int32_t>((tk / nchunk) % p.H);
+    t.g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
+    t.r0 = t.g * p.G;
+    t.rlast = min(p.rows, t.r0 + p.G) - 1;
+    return t;
+  };
+  // copies of this lane's rows of warp task wt into the slot (nothing past the end)
+  auto issue = [&](int64_t wt) {
+    if (wt >= nwtask) return;  // uniform across the warp
+    const Task t = task_of(wt);
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      uint4* const cell = slot + k * 32 + lane;
+      int64_t src = min(t.r0 + rs + k * S, t.rlast);
+      if constexpr (kResidual) {
+        if (p.pos != nullptr) src = LDX(p.pos + src);
+        if (src < 0 || src >= p.src_rows) {
+          *cell = make_uint4(0u, 0u, 0u, 0u);
+          cell[RPT * 32] = make_uint4(0u, 0u, 0u, 0u);
+          continue;
+        }
+        cp_async16(cell + RPT * 32,
+                   p.prev + src * p.prev_row_pitch + static_cast<int64_t>(t.h) * p.prev_head_pitch + t.chunk * 8);
+      }
+      cp_async16(cell, p.x + src * p.row_pitch + static_cast<int64_t>(t.h) * p.head_pitch + t.chunk * 8);
+    }
+  };
+
+  int64_t wt = blockIdx.x * static_cast<int64_t>(kWarps) + threadIdx.x / 32;
+  issue(wt);
+  cp_async_commit();
+  for (; wt < nwtask; wt += nwarps) {
+    cp_async_wait<0>();
+    const Task t = task_of(wt);
     uint32_t v[RPT][4];
 #pragma unroll
-    for (int k = 0; k < RPT; ++k) load_chunk8<kResidual>(p, min(r0 + rs + k * S, rlast), h, col, v[k]);
+    for (int k = 0; k < RPT; ++k) {
+      uint4 a = slot[k * 32 + lane];
+      if constexpr (kResidual) {
+        const uint4 q = slot[(RPT + k) * 32 + lane];
+        a.x = pack_bf16x2(__fsub_rn(bf16lo(a.x), bf16lo(q.x)), __fsub_rn(bf16hi(a.x), bf16hi(q.x)));
+        a.y = pack_bf16x2(__fsub_rn(bf16lo(a.y), bf16lo(q.y)), __fsub_rn(bf16hi(a.y), bf16hi(q.y)));
+        a.z = pack_bf16x2(__fsub_rn(bf16lo(a.z), bf16lo(q.z)), __fsub_rn(bf16hi(a.z), bf16hi(q.z)));
+        a.w = pack_bf16x2(__fsub_rn(bf16lo(a.w), bf16lo(q.w)), __fsub_rn(bf16hi(a.w), bf16hi(q.w)));
+      }
+      v[k][0] = a.x;
+      v[k][1] = a.y;
+      v[k][2] = a.z;
+      v[k][3] = a.w;
+    }
     uint32_t m[4], M[4], sg[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) m[i] = M[i] = sg[i] = v[0][i];
@@ -228,6 +290,8 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         sg[i] |= v[k][i];
       }
     }
+    issue(wt + nwarps);  // every cell of this task has been read (the extrema use them all)
+    cp_async_commit();
 #pragma unroll
     for (int o = CW; o < 32; o <<= 1) {
 #pragma unroll
@@ -237,45 +301,69 @@ __global__ void __launch_bounds__(kThreads) int4_key_kernel(const Int4EncodePara
         sg[i] |= __shfl_xor_sync(0xFFFFFFFFu, sg[i], o);
       }
     }
-    float mn[8], sc[8];
-    uint64_t nmn[4], nsc[4], y[4];
+    // parameters: lane rs forms those of words rs, rs + S, ... (every lane of a task
+    // holds the same extrema), then each word's come from the lane that formed them
+    constexpr int WPL = S >= 4 ? 1 : 4 / S;  // words whose parameters this lane forms
+    uint64_t pn[WPL], ps[WPL], py[WPL];
+    uint32_t pm16[WPL], ps16[WPL];
     bool fast = true;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mn[2 * i] = group_min(m[i], sg[i] & 0x8000u);
-      mn[2 * i + 1] = group_min(m[i] >> 16, sg[i] & 0x80000000u);
-      sc[2 * i] = int4_scale(__fsub_rn(bf16lo(M[i]), mn[2 * i]));
-      sc[2 * i + 1] = int4_scale(__fsub_rn(bf16hi(M[i]), mn[2 * i + 1]));
-      nmn[i] = pack_f32x2(__float_as_uint(-mn[2 * i]), __float_as_uint(-mn[2 * i + 1]));
-      nsc[i] = pack_f32x2(__float_as_uint(-sc[2 * i]), __float_as_uint(-sc[2 * i + 1]));
-      y[i] = pack_f32x2(__float_as_uint(int4_recip(sc[2 * i])), __float_as_uint(int4_recip(sc[2 * i + 1])));
-      fast = fast && int4_fast_scale(sc[2 * i]) && int4_fast_scale(sc[2 * i + 1]);
+    for (int j = 0; j < WPL; ++j) {
+      const int i = S >= 4 ? rs % 4 : rs + j * S;
+      uint32_t mi = m[0], Mi = M[0], si = sg[0];
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {  // select word i without dynamic register indexing
+        if (i == q) {
+          mi = m[q];
+          Mi = M[q];
+          si = sg[q];
+        }
+      }
+      const float mnl = group_min(mi, si & 0x8000u), mnh = group_min(mi >> 16, si & 0x80000000u);
+      const float scl = int4_scale(__fsub_rn(bf16lo(Mi), mnl)), sch = int4_scale(__fsub_rn(bf16hi(Mi), mnh));
+      pn[j] = pack_f32x2(__float_as_uint(-mnl), __float_as_uint(-mnh));
+      ps[j] = pack_f32x2(__float_as_uint(-scl), __float_as_uint(-sch));
+      py[j] = pack_f32x2(__float_as_uint(int4_recip(scl)), __float_as_uint(int4_recip(sch)));
+      pm16[j] = static_cast<uint32_t>(f32_to_f16_bits(mnl)) | (static_cast<uint32_t>(f32_to_f16_bits(mnh)) << 16);
+      ps16[j] = static_cast<uint32_t>(f32_to_f16_bits(scl)) | (static_cast<uint32_t>(f32_to_f16_bits(sch)) << 16);
+      fast = fast && int4_fast_scale(scl) && int4_fast_scale(sch);
     }
-    uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(h) * (p.D / 2) + col / 2;
+    int fast_all = fast ? 1 : 0;  // AND over the lanes that formed parameters (every lane shuffles)
+#pragma unroll
+    for (int o = CW; o < CW * (S < 4 ? S : 4); o <<= 1) fast_all &= __shfl_xor_sync(0xFFFFFFFFu, fast_all, o);
+    fast = fast_all != 0;
+    uint64_t nmn[4], nsc[4], y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int src = (S >= 4 ? i : i % S) * CW + cl;
+      const int j = S >= 4 ? 0 : i / S;
+      nmn[i] = __shfl_sync(0xFFFFFFFFu, pn[j], src);
+      nsc[i] = __shfl_sync(0xFFFFFFFFu, ps[j], src);
+      y[i] = __shfl_sync(0xFFFFFFFFu, py[j], src);
+    }
+    const int32_t col = t.chunk * 8;
+    uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(t.h) * (p.D / 2) + col / 2;
     const int64_t cstride = static_cast<int64_t>(p.H) * (p.D / 2);
 #pragma unroll
     for (int k = 0; k < RPT; ++k) {
-      const int32_t r = r0 + rs + k * S;
-      if (valid && r <= rlast) {
-        if (chunk == 0 && h == 0) check_pos<kResidual>(p, r);
+      const int32_t r = t.r0 + rs + k * S;
+      if (t.valid && r <= t.rlast) {
+        if (t.chunk == 0 && t.h == 0) check_pos<kResidual>(p, r);
         STX(reinterpret_cast<uint32_t*>(cbase + r * cstride),
             fast ? int4_codes8(v[k], nmn, nsc, y) : int4_codes8_div(v[k], nmn, nsc));
       }
     }
-    if (valid && rs == 0) {
-      uint32_t m16[4], s16[4];
+    if (t.valid && rs < 4) {  // the FP16 metadata of the words this lane formed
+      const int64_t mi = (static_cast<int64_t>(t.g) * p.H + t.h) * p.D + col;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        m16[i] = static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i])) |
-                 (static_cast<uint32_t>(f32_to_f16_bits(mn[2 * i + 1])) << 16);
-        s16[i] = static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i])) |
-                 (static_cast<uint32_t>(f32_to_f16_bits(sc[2 * i + 1])) << 16);
+      for (int j = 0; j < WPL; ++j) {
+        const int i = S >= 4 ? rs : rs + j * S;
+        STX(reinterpret_cast<uint32_t*>(p.dst.mn + mi + 2 * i), pm16[j]);
+        STX(reinterpret_cast<uint32_t*>(p.dst.sc + mi + 2 * i), ps16[j]);
       }
-      const int64_t mi = (static_cast<int64_t>(g) * p.H + h) * p.D + col;
-      store16B(p.dst.mn + mi, m16);
-      store16B(p.dst.sc + mi, s16);
     }
   }
+  cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
 }
 
 // Signed-integer order keys of binary32 values: the integer order is the float order
@@ -393,13 +481,30 @@ __global__ void __launch_bounds__(kThreads, kBlk == 2 ? 3 : 4) int4_value_kernel
   }
 }
 
-template <typename K>
-int grid_cap(K kernel, int64_t work_items, int items_per_cta) {
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
-  if (occ < 1) occ = 1;
+// Resident blocks per SM of a kernel instance, with its dynamic shared memory opted in
+// first; computed once per device (0: the opt-in failed).
+template <auto Kernel>
+int occupancy(int threads, size_t smem) {
+  constexpr int kDevices = 64;
+  static int cache[kDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kDevices) dev = 0;
+  if (cache[dev] == 0) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      return 0;
+    int o = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, Kernel, threads, smem);
+    cache[dev] = o < 1 ? 1 : o;
+  }
+  return cache[dev];
+}
+
+// Blocks for `work_items` items at `items_per_cta` each, at most one wave.
+int grid_for(int occ, int64_t work_items, int items_per_cta) {
   int64_t need = (work_items + items_per_cta - 1) / items_per_cta;
-  int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
   if (need < 1) need = 1;
   return static_cast<int>(need < cap ? need : cap);
 }
@@ -407,7 +512,8 @@ int grid_cap(K kernel, int64_t work_items, int items_per_cta) {
 template <int L, int kBlk, bool kRes>
 cudaError_t value_launch(const Int4EncodeParams& p, cudaStream_t s) {
   auto k = int4_value_kernel<L, kBlk, kRes>;
-  int grid = grid_cap(k, static_cast<int64_t>(p.rows) * p.H, (kThreads / 32) * (32 / L));
+  const int grid = grid_for(occupancy<int4_value_kernel<L, kBlk, kRes>>(kThreads, 0),
+                            static_cast<int64_t>(p.rows) * p.H, (kThreads / 32) * (32 / L));
   cudaError_t e = cudaSuccess;
   KVQ_LAUNCH("int4_value_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
   return e;
@@ -438,22 +544,25 @@ cudaError_t value_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
 template <bool kRes, int S, int RPT>
 cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s) {
   auto k = int4_key_kernel<kRes, S, RPT>;
-  const int64_t warps = (ntask + 32 / S - 1) / (32 / S);
-  const int grid = grid_cap(k, warps, kThreads / 32);
+  constexpr int threads = key_threads<kRes>();
+  constexpr size_t smem = key_smem<kRes, RPT>();
+  const int occ = occupancy<int4_key_kernel<kRes, S, RPT>>(threads, smem);
+  if (occ == 0) return cudaErrorInvalidValue;
+  const int grid = grid_for(occ, (ntask + 32 / S - 1) / (32 / S), threads / 32);
   cudaError_t e = cudaSuccess;
-  KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, kThreads, 0, s>>>(p); e = cudaGetLastError());
+  KVQ_LAUNCH("int4_key_kernel", s, k<<<grid, threads, smem, s>>>(p); e = cudaGetLastError());
   return e;
 }
 
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
-  switch (p.G) {  // S = G / 16 lanes per column task, 16 rows each
-    case 16: return key_launch<kRes, 1, 16>(p, ntask, s);
-    case 32: return key_launch<kRes, 2, 16>(p, ntask, s);
-    case 64: return key_launch<kRes, 4, 16>(p, ntask, s);
-    case 128: return key_launch<kRes, 8, 16>(p, ntask, s);
-    case 256: return key_launch<kRes, 16, 16>(p, ntask, s);
+  switch (p.G) {  // S = G / RPT lanes per column task, RPT rows each (residual: 8, plain: 16)
+    case 16: return kRes ? key_launch<kRes, 2, 8>(p, ntask, s) : key_launch<kRes, 1, 16>(p, ntask, s);
+    case 32: return kRes ? key_launch<kRes, 4, 8>(p, ntask, s) : key_launch<kRes, 2, 16>(p, ntask, s);
+    case 64: return kRes ? key_launch<kRes, 8, 8>(p, ntask, s) : key_launch<kRes, 4, 16>(p, ntask, s);
+    case 128: return kRes ? key_launch<kRes, 16, 8>(p, ntask, s) : key_launch<kRes, 8, 16>(p, ntask, s);
+    case 256: return kRes ? key_launch<kRes, 32, 8>(p, ntask, s) : key_launch<kRes, 16, 16>(p, ntask, s);
     case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
   }
   return cudaErrorInvalidValue;
