@@ -22,8 +22,9 @@
 //    register pairs are interleaved by a mask-and-shift (or byte-permute) transpose.
 //  * K and V decode exactly to f16: e2m1 x e4m3 has at most 2 x 4 significant bits,
 //    and e4m3 fits f16.  K's FP32 row scale multiplies the score; V's multiplies P
-//    relative to a running maximum R of the tile row scales (P' = p * rs / R <= 1, so
-//    f16 holds it), and O is rescaled when R grows, like the softmax running maximum.
+//    relative to a reference R of the tile row scales.  R and the softmax reference m
+//    move only when a tile exceeds them by more than 2^6 and 2^8 (O is rescaled then),
+//    so P' = exp2(s - m) * rs / R stays below 2^14 and f16 holds it.
 //  * Q enters f16 exactly: each query row is scaled by a power of two that puts its
 //    largest element in [2^14, 2^15), undone in the score multiplier.
 //  * The warps of a CTA merge through shared memory; several splits of a sequence
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     }
   };
 
-  float m[2] = {kNegInf, kNegInf}, l[2] = {0.0f, 0.0f}, R = 0.0f;
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.0f, 0.0f}, R = 0.0f, rR = 0.0f;
   float o[kNT][4];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
@@ -364,18 +365,21 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       }
     }
     // scores (log2 domain): row scale of K, query scale; tokens past the end masked
+    // (only the split's last tile can hold any)
     const float* krs = reinterpret_cast<const float*>(sb + T::kOffKR);
     const float* vrs = reinterpret_cast<const float*>(sb + T::kOffVR);
     float rv[2][2];
     float mt[2] = {kNegInf, kNegInf};
+    const bool partial = t0 + 16 > t_end;  // uniform across the warp
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = 8 * j + 2 * c + (e & 1);
-        const float v = sc[j][e] * krs[tok] * qmul[e >> 1];
-        sc[j][e] = (t0 + tok < t_end) ? v : kNegInf;
-        mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
+        float v = sc[j][e] * krs[tok] * qmul[e >> 1];
+        if (partial && t0 + tok >= t_end) v = kNegInf;
+        sc[j][e] = v;
+        mt[e >> 1] = fmaxf(mt[e >> 1], v);
       }
       rv[j][0] = vrs[8 * j + 2 * c];
       rv[j][1] = vrs[8 * j + 2 * c + 1];
@@ -387,12 +391,14 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xFFFFFFFFu, mt[1], off));
       rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
     }
-    // running maxima: softmax m per row, V row-scale reference R
-    const float mn0 = fmaxf(m[0], mt[0]), mn1 = fmaxf(m[1], mt[1]);
-    const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
-    const float a0 = ex2(m[0] - mn0), a1 = ex2(m[1] - mn1);  // 0 while m is -inf
-    const float rr = R / Rn;
-    if (__any_sync(0xFFFFFFFFu, a0 != 1.0f || a1 != 1.0f || rr != 1.0f)) {
+    // references: the softmax reference m per row and the V row-scale reference R move
+    // only when a tile exceeds them by more than 2^8 and 2^6, so P' = exp2(s - m) *
+    // rs_v / R stays below 2^14 (f16 holds it) and O is rescaled on few tiles
+    if (__any_sync(0xFFFFFFFFu, mt[0] > m[0] + 8.0f || mt[1] > m[1] + 8.0f || rmax > R * 64.0f)) {
+      const float mn0 = fmaxf(m[0], mt[0]), mn1 = fmaxf(m[1], mt[1]);
+      const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
+      const float a0 = ex2(m[0] - mn0), a1 = ex2(m[1] - mn1);  // 0 while m is -inf
+      const float rr = R / Rn;
       const float f0 = a0 * rr, f1 = a1 * rr;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
@@ -401,19 +407,19 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
         o[nt][2] *= f1;
         o[nt][3] *= f1;
       }
+      l[0] *= a0;
+      l[1] *= a1;
+      m[0] = mn0;
+      m[1] = mn1;
+      R = Rn;
+      rR = rcp_approx(Rn);
     }
-    l[0] *= a0;
-    l[1] *= a1;
-    m[0] = mn0;
-    m[1] = mn1;
-    R = Rn;
     // P' = exp2(s - m) * rs_v / R as the A operand of P V
-    const float rR = rcp_approx(Rn);
     uint32_t pa[4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float p0 = ex2(sc[j][0] - mn0), p1 = ex2(sc[j][1] - mn0);
-      const float p2 = ex2(sc[j][2] - mn1), p3 = ex2(sc[j][3] - mn1);
+      const float p0 = ex2(sc[j][0] - m[0]), p1 = ex2(sc[j][1] - m[0]);
+      const float p2 = ex2(sc[j][2] - m[1]), p3 = ex2(sc[j][3] - m[1]);
       l[0] += p0 + p1;
       l[1] += p2 + p3;
       const float r0 = rv[j][0] * rR, r1 = rv[j][1] * rR;
@@ -448,7 +454,17 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
         lds_words<kW>(sb + T::kOffVC + (ta0 + 1) * T::kSV + g * (D / 16), v1);
         lds_words<kW>(sb + T::kOffVC + ta1 * T::kSV + g * (D / 16), v2);
         lds_words<kW>(sb + T::kOffVC + (ta1 + 1) * T::kSV + g * (D / 16), v3);
+        // block scales of this lane's dims g * D/8 .. + D/8 - 1 for its four tokens: one
+        // 16-dim block (D <= 128) or two (D = 256), as f16x2 pairs (tokens ta, ta + 1)
+        constexpr int kVB = D / 8 > 16 ? D / 128 : 1;
         const uint8_t* vbs = sb + T::kOffVB;
+        uint32_t bs01[kVB], bs23[kVB];
+#pragma unroll
+        for (int q = 0; q < kVB; ++q) {
+          const int blk = (g * (D / 8)) / 16 + q;
+          bs01[q] = e4m3x2_to_f16x2(vbs[ta0 * T::kBV + blk] | (vbs[(ta0 + 1) * T::kBV + blk] << 8));
+          bs23[q] = e4m3x2_to_f16x2(vbs[ta1 * T::kBV + blk] | (vbs[(ta1 + 1) * T::kBV + blk] << 8));
+        }
 #pragma unroll
         for (int i = 0; i < kW; ++i) {
           // nibble transpose: X byte b = (dim 2(4i+b) of token a | the same dim of token
@@ -465,11 +481,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
             const int nt = 8 * i + 2 * bb;  // and nt + 1: one 16-block for both
-            const int blk = (g * (D / 8) + nt) / 16;
-            const uint32_t bs01 = e4m3x2_to_f16x2(vbs[ta0 * T::kBV + blk] | (vbs[(ta0 + 1) * T::kBV + blk] << 8));
-            const uint32_t bs23 = e4m3x2_to_f16x2(vbs[ta1 * T::kBV + blk] | (vbs[(ta1 + 1) * T::kBV + blk] << 8));
-            mma_f16_16816(o[nt], pa, hmul2(hx01[bb], bs01), hmul2(hx23[bb], bs23));
-            mma_f16_16816(o[nt + 1], pa, hmul2(hy01[bb], bs01), hmul2(hy23[bb], bs23));
+            const int q = kVB == 1 ? 0 : nt / 16;  // g * D/8 is a multiple of 16 when D = 256
+            mma_f16_16816(o[nt], pa, hmul2(hx01[bb], bs01[q]), hmul2(hx23[bb], bs23[q]));
+            mma_f16_16816(o[nt + 1], pa, hmul2(hy01[bb], bs01[q]), hmul2(hy23[bb], bs23[q]));
           }
         }
       }
