@@ -238,12 +238,13 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
  *   out  bf16, indexed the same way through its own pitches.
  *   head_dim 64, 128 or 256; num_q_heads a multiple of num_heads, at most 16 query
  *   heads per KV head.  seq_lens[s] <= min(max_seq_len, max_blocks * block_size).
+ *   scale  positive and finite (KVQ_ERR_INVALID_ARG otherwise).
  *   workspace  device memory of kvq_decode_attention_workspace(...) bytes, 16-byte
  *              aligned (may be NULL when that is 0); caller-owned, reused by the next
  *              call on the same stream.
  * Accuracy: K, V and Q enter the f16 MMA exactly (Q through a power-of-two
  * prescale); products and sums are fp32; P is rounded once to f16 (relative 2^-11,
- * against a running maximum of V's row scales) and the output once to bf16, so
+ * relative to a reference of V's row scales) and the output once to bf16, so
  * |out - exact| <= 2^-9 |exact| + 2^-11 max|v| plus fp32 rounding, where exact is
  * the attention of the decoded rows.
  * An empty sequence writes zeros.  A bad length (KVQ_DEV_BAD_SEQLEN) or a block

@@ -364,26 +364,31 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
         }
       }
     }
-    // scores (log2 domain): row scale of K, query scale; tokens past the end masked
-    // (only the split's last tile can hold any)
-    const float* krs = reinterpret_cast<const float*>(sb + T::kOffKR);
-    const float* vrs = reinterpret_cast<const float*>(sb + T::kOffVR);
+    // scores times K's row scale; the query factor (scale, log2 e, Q's power of two,
+    // positive) enters with the reference in one FMA below, and the row maxima are
+    // scaled by it once.  Tokens past the end are masked (only a split's last tile can
+    // hold any).
+    const float2* krs = reinterpret_cast<const float2*>(sb + T::kOffKR);
+    const float2* vrs = reinterpret_cast<const float2*>(sb + T::kOffVR);
     float rv[2][2];
     float mt[2] = {kNegInf, kNegInf};
     const bool partial = t0 + 16 > t_end;  // uniform across the warp
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
+      const float2 kr = krs[4 * j + c], vr = vrs[4 * j + c];  // tokens 8j + 2c, + 1
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = 8 * j + 2 * c + (e & 1);
-        float v = sc[j][e] * krs[tok] * qmul[e >> 1];
+        float v = sc[j][e] * ((e & 1) ? kr.y : kr.x);
         if (partial && t0 + tok >= t_end) v = kNegInf;
         sc[j][e] = v;
         mt[e >> 1] = fmaxf(mt[e >> 1], v);
       }
-      rv[j][0] = vrs[8 * j + 2 * c];
-      rv[j][1] = vrs[8 * j + 2 * c + 1];
+      rv[j][0] = vr.x;
+      rv[j][1] = vr.y;
     }
+    mt[0] *= qmul[0];
+    mt[1] *= qmul[1];
     float rmax = fmaxf(fmaxf(rv[0][0], rv[0][1]), fmaxf(rv[1][0], rv[1][1]));
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
@@ -418,8 +423,8 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     uint32_t pa[4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float p0 = ex2(sc[j][0] - m[0]), p1 = ex2(sc[j][1] - m[0]);
-      const float p2 = ex2(sc[j][2] - m[1]), p3 = ex2(sc[j][3] - m[1]);
+      const float p0 = ex2(__fmaf_rn(sc[j][0], qmul[0], -m[0])), p1 = ex2(__fmaf_rn(sc[j][1], qmul[0], -m[0]));
+      const float p2 = ex2(__fmaf_rn(sc[j][2], qmul[1], -m[1])), p3 = ex2(__fmaf_rn(sc[j][3], qmul[1], -m[1]));
       l[0] += p0 + p1;
       l[1] += p2 + p3;
       const float r0 = rv[j][0] * rR, r1 = rv[j][1] * rR;

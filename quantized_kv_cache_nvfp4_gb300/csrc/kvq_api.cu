@@ -709,6 +709,8 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
   if (num_q_heads <= 0 || num_q_heads % H != 0)
     return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_heads");
   if (num_q_heads / H > 16) return fail(KVQ_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+  if (!(scale > 0.0f && scale <= 3.4028235e38f))
+    return fail(KVQ_ERR_INVALID_ARG, "scale must be positive and finite (got %g)", static_cast<double>(scale));
   if (num_seqs > 65535 || H > 65535) return fail(KVQ_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
   if (num_seqs == 0) return KVQ_OK;
   if (!fits_u31(static_cast<int64_t>(num_seqs) * num_q_heads * D))

@@ -110,6 +110,10 @@ def test_decode_attention_host_checks(kvq_lib_path):
     assert call(3) == 1 and b"multiple of num_heads" in lib.kvq_last_error()
     assert call(34) == 2 and b"16 query heads" in lib.kvq_last_error()
     assert call(8) == 1 and b"NULL" in lib.kvq_last_error()  # q's pointer
+    for bad_scale in (0.0, -0.1, float("inf"), float("nan")):
+        assert lib.kvq_decode_attention(ctypes.byref(pool), None, 1, 4, None, 64, ctypes.byref(q), 8, bad_scale,
+                                        ctypes.byref(o), None, 0, None, None) == 1
+        assert b"scale" in lib.kvq_last_error()
     assert lib.kvq_decode_attention(None, None, 1, 4, None, 64, ctypes.byref(q), 8, 0.1, ctypes.byref(o), None,
                                     0, None, None) == 1
 

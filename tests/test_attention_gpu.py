@@ -3,8 +3,8 @@ compared with the oracle's fp64 attention of the same pool rows.
 
 Tolerance, from the kernel's arithmetic: K and V decode exactly, Q enters f16
 exactly (a power-of-two prescale), products and sums run in fp32; the softmax
-weights are rounded once to f16 (relative 2^-11) against a running row-scale
-maximum, and the output once to bf16 (relative 2^-9).  Numerator and denominator
+weights are rounded once to f16 (relative 2^-11) relative to a reference of V's
+row scales, and the output once to bf16 (relative 2^-9).  Numerator and denominator
 see different weight roundings, so the weights contribute at most 2^-11 * vmax
 (vmax = the largest |v| the row attends to).  The test allows twice each term:
 |o - o_ref| <= 2^-8 |o_ref| + 2^-10 vmax (+ 1e-30 for exact zeros)."""
