@@ -278,17 +278,29 @@ __global__ void __launch_bounds__(key_threads<kResidual>()) int4_key_kernel(cons
       v[k][2] = a.z;
       v[k][3] = a.w;
     }
+    // the lane's minima, maxima and sign ORs over its RPT rows, as pairwise trees
     uint32_t m[4], M[4], sg[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m[i] = M[i] = sg[i] = v[0][i];
+    for (int i = 0; i < 4; ++i) {
+      uint32_t tm[RPT / 2], tM[RPT / 2], ts[RPT / 2];
 #pragma unroll
-    for (int k = 1; k < RPT; ++k) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        m[i] = hmin2(m[i], v[k][i]);
-        M[i] = hmax2(M[i], v[k][i]);
-        sg[i] |= v[k][i];
+      for (int k = 0; k < RPT / 2; ++k) {
+        tm[k] = hmin2(v[2 * k][i], v[2 * k + 1][i]);
+        tM[k] = hmax2(v[2 * k][i], v[2 * k + 1][i]);
+        ts[k] = v[2 * k][i] | v[2 * k + 1][i];
       }
+#pragma unroll
+      for (int w = RPT / 4; w >= 1; w /= 2) {
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+          tm[k] = hmin2(tm[2 * k], tm[2 * k + 1]);
+          tM[k] = hmax2(tM[2 * k], tM[2 * k + 1]);
+          ts[k] = ts[2 * k] | ts[2 * k + 1];
+        }
+      }
+      m[i] = tm[0];
+      M[i] = tM[0];
+      sg[i] = ts[0];
     }
     issue(wt + nwarps);  // every cell of this task has been read (the extrema use them all)
     cp_async_commit();
@@ -421,13 +433,23 @@ __global__ void __launch_bounds__(kThreads, kBlk == 2 ? 3 : 4) int4_value_kernel
     }
     // the lane's minimum / maximum (bf16x2 min/max, sign-OR for a zero minimum), then
     // the group's over W lanes in order keys
-    uint32_t m = w[0], M = w[0], s = w[0];
+    uint32_t tm[NW / 2], tM[NW / 2], ts[NW / 2];  // pairwise trees over the lane's words
 #pragma unroll
-    for (int i = 1; i < NW; ++i) {
-      m = hmin2(m, w[i]);
-      M = hmax2(M, w[i]);
-      s |= w[i];
+    for (int k = 0; k < NW / 2; ++k) {
+      tm[k] = hmin2(w[2 * k], w[2 * k + 1]);
+      tM[k] = hmax2(w[2 * k], w[2 * k + 1]);
+      ts[k] = w[2 * k] | w[2 * k + 1];
     }
+#pragma unroll
+    for (int n = NW / 4; n >= 1; n /= 2) {
+#pragma unroll
+      for (int k = 0; k < n; ++k) {
+        tm[k] = hmin2(tm[2 * k], tm[2 * k + 1]);
+        tM[k] = hmax2(tM[2 * k], tM[2 * k + 1]);
+        ts[k] = ts[2 * k] | ts[2 * k + 1];
+      }
+    }
+    uint32_t m = tm[0], M = tM[0], s = ts[0];
     m = hmin2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the lane's extremes
     M = hmax2(M, __byte_perm(M, 0u, 0x1032));
     int32_t kmn = f32_key(group_min(m, s & 0x80008000u)), kmx = f32_key(bf16lo(M));

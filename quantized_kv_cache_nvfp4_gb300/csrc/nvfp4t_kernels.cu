@@ -24,6 +24,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr float kRowScaleDiv = 2688.0f;  // 6 * 448
 
+// Per-half maximum of magnitudes of two bf16x2 words (the sign bits are cleared by the
+// caller); a bf16 maximum is one of its inputs, so nothing rounds.
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ void tensor_scale(const float* slot, float& rs, float& rinv) {
   const float amax = LDX(slot);
   rs = __fdiv_rn(amax, kRowScaleDiv);
@@ -81,57 +89,120 @@ __global__ void __launch_bounds__(kThreads) tensor_value_encode_kernel(const Ten
   }
 }
 
-// 2b. KEY kind: one thread per (group of 16 token rows, head, channel pair); the pair's
-// two blocks are its two channels over the group's rows (fewer in a partial group).
+// 2b. KEY kind: one thread per (group of 16 token rows, head, 8-channel chunk); the
+// chunk's 8 blocks are its channels over the group's rows.  Each row is one 16-byte
+// copy and one 4-byte code store; a partial group repeats its last row for the block
+// maxima (no change to them) and stores only its own rows.  The rows arrive by
+// cp.async in the thread's own shared-memory cells (row k at cell k * kThreads +
+// thread, so a warp's reads are conflict-free); the next task's copies are issued
+// once this task's cells have been read (the maxima use every read), so they travel
+// while this task is coded.  The thread's own wait_group orders its cells.
+constexpr size_t kKeySmem = static_cast<size_t>(16) * kThreads * 16;
+
 __global__ void __launch_bounds__(kThreads) tensor_key_encode_kernel(const TensorNvfp4Params p) {
-  const uint32_t npair = static_cast<uint32_t>(p.D / 2);
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint4* const cells = reinterpret_cast<uint4*>(smem) + threadIdx.x;
+  const uint32_t nb = static_cast<uint32_t>(p.D / 16);  // chunk pairs per row
   const uint32_t ngroups = static_cast<uint32_t>((p.rows + 15) / 16);
-  const uint32_t ntask = ngroups * static_cast<uint32_t>(p.H) * npair;
+  const uint32_t ntask = ngroups * static_cast<uint32_t>(p.H) * 2u * nb;
+  const uint32_t stride = gridDim.x * kThreads;
+  struct Task {
+    uint32_t g, h, ch;
+    int r0, n;
+  };
+  auto task_of = [&](uint32_t i) {
+    Task t;
+    uint32_t gh, cp2;
+    p.div_nb.divmod(i >> 1, gh, cp2);  // task i = gh * D/8 + chunk
+    p.div_h.divmod(gh, t.g, t.h);
+    t.ch = 2u * cp2 + (i & 1u);
+    t.r0 = static_cast<int>(t.g) * 16;
+    t.n = min(16, p.rows - t.r0);
+    return t;
+  };
+  auto issue = [&](uint32_t i) {
+    if (i >= ntask) return;
+    const Task t = task_of(i);
+    const uint16_t* const src = p.x + static_cast<int64_t>(t.h) * p.head_pitch + 8 * t.ch;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      cp_async16(cells + k * kThreads, src + static_cast<int64_t>(t.r0 + min(k, t.n - 1)) * p.row_pitch);
+  };
   float rs, rinv;
   tensor_scale(p.rscale, rs, rinv);
-  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < ntask; i += gridDim.x * kThreads) {
-    uint32_t gh, pr, g, h;
-    p.div_np.divmod(i, gh, pr);
-    p.div_h.divmod(gh, g, h);
-    const int r0 = static_cast<int>(g) * 16;
-    const int n = min(16, p.rows - r0);
-    uint32_t w[16];
-    uint32_t m = 0u;
+  uint32_t i = blockIdx.x * kThreads + threadIdx.x;
+  issue(i);
+  cp_async_commit();
+  for (; i < ntask; i += stride) {
+    cp_async_wait<0>();
+    const Task t = task_of(i);
+    uint32_t w[16][4];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      w[k] = 0u;
-      if (k < n)
-        w[k] = LDX(reinterpret_cast<const uint32_t*>(p.x + static_cast<int64_t>(r0 + k) * p.row_pitch +
-                                                       static_cast<int64_t>(h) * p.head_pitch + 2 * pr));
-      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(w[k]));
+      const uint4 v = cells[k * kThreads];
+      w[k][0] = v.x;
+      w[k][1] = v.y;
+      w[k][2] = v.z;
+      w[k][3] = v.w;
     }
-    m &= 0x7FFF7FFFu;
-    const uint32_t bl = block_scale_code(bf16lo(m), rs, rinv);
-    const uint32_t bh = block_scale_code(bf16hi(m), rs, rinv);
-    const float sl = __fmul_rn(e4m3_to_f32(bl), rs), sh = __fmul_rn(e4m3_to_f32(bh), rs);
-    const float il = sl != 0.0f ? __frcp_rn(sl) : 0.0f, ih = sh != 0.0f ? __frcp_rn(sh) : 0.0f;
-    const bool direct = isinf(il) || isinf(ih);  // a tiny scale: divide instead
-    const uint64_t inv2 = pack_f32x2(__float_as_uint(il), __float_as_uint(ih));
-    uint8_t* const cp = p.codes + (static_cast<int64_t>(r0) * p.H + h) * npair + pr;
-    const int64_t cstride = static_cast<int64_t>(p.H) * npair;
+    // |max| of each channel over the 16 rows, as a pairwise tree (depth 4)
+    uint32_t m[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t t[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = absmax2(w[2 * k][j], w[2 * k + 1][j]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) t[k] = absmax2(t[2 * k], t[2 * k + 1]);
+      m[j] = absmax2(absmax2(t[0], t[1]), absmax2(t[2], t[3]));
+    }
+    issue(i + stride);  // every cell has been read (the maxima use them all)
+    cp_async_commit();
+    uint32_t bsc[8];
+    float sc[8], inv[8];
+    bool direct = false;  // a tiny scale: divide instead
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t mj = m[j] & 0x7FFF7FFFu;
+      bsc[2 * j] = block_scale_code(bf16lo(mj), rs, rinv);
+      bsc[2 * j + 1] = block_scale_code(bf16hi(mj), rs, rinv);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      sc[c] = __fmul_rn(e4m3_to_f32(bsc[c]), rs);
+      inv[c] = sc[c] != 0.0f ? __frcp_rn(sc[c]) : 0.0f;
+      direct = direct || isinf(inv[c]);
+    }
+    uint64_t inv2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) inv2[j] = pack_f32x2(__float_as_uint(inv[2 * j]), __float_as_uint(inv[2 * j + 1]));
+    uint8_t* const cp = p.codes + (static_cast<int64_t>(t.r0) * p.H + t.h) * (p.D / 2) + 4 * t.ch;
+    const int64_t cstride = static_cast<int64_t>(p.H) * (p.D / 2);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      if (k >= n) break;
-      float ql, qh;
-      if (!direct) {
-        uint32_t a, b;
-        unpack_f32x2(mul_f32x2(pack_f32x2(w[k] << 16, w[k] & 0xFFFF0000u), inv2), a, b);
-        ql = __uint_as_float(a);
-        qh = __uint_as_float(b);
-      } else {
-        ql = isinf(il) ? __fdiv_rn(bf16lo(w[k]), sl) : __fmul_rn(bf16lo(w[k]), il);
-        qh = isinf(ih) ? __fdiv_rn(bf16hi(w[k]), sh) : __fmul_rn(bf16hi(w[k]), ih);
+      if (k >= t.n) break;
+      uint32_t byte[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float ql, qh;
+        if (!direct) {
+          uint32_t a, b;
+          unpack_f32x2(mul_f32x2(pack_f32x2(w[k][j] << 16, w[k][j] & 0xFFFF0000u), inv2[j]), a, b);
+          ql = __uint_as_float(a);
+          qh = __uint_as_float(b);
+        } else {
+          ql = isinf(inv[2 * j]) ? __fdiv_rn(bf16lo(w[k][j]), sc[2 * j]) : __fmul_rn(bf16lo(w[k][j]), inv[2 * j]);
+          qh = isinf(inv[2 * j + 1]) ? __fdiv_rn(bf16hi(w[k][j]), sc[2 * j + 1])
+                                     : __fmul_rn(bf16hi(w[k][j]), inv[2 * j + 1]);
+        }
+        byte[j] = e2m1x2_from_f32(ql, qh);
       }
-      STX(cp + k * cstride, static_cast<uint8_t>(e2m1x2_from_f32(ql, qh)));
+      STX(reinterpret_cast<uint32_t*>(cp + k * cstride), bytes4(byte[0], byte[1], byte[2], byte[3]));
     }
-    STX(reinterpret_cast<uint16_t*>(p.bscale + (static_cast<int64_t>(g) * p.H + h) * p.D + 2 * pr),
-        static_cast<uint16_t>(bl | (bh << 8)));
+    store8B(p.bscale + (static_cast<int64_t>(t.g) * p.H + t.h) * p.D + 8 * t.ch,
+            bytes4(bsc[0], bsc[1], bsc[2], bsc[3]), bytes4(bsc[4], bsc[5], bsc[6], bsc[7]));
   }
+  cp_async_wait<0>();  // only empty groups remain; nothing is left in flight at exit
 }
 
 // 3. The scale slot: amax -> rs (the decode multiplier).
@@ -193,9 +264,9 @@ __global__ void __launch_bounds__(kThreads) tensor_key_decode_kernel(const Tenso
 }
 
 template <typename K>
-int grid_for(K kernel, uint32_t work) {
+int grid_for(K kernel, uint32_t work, size_t smem = 0) {
   int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
   if (occ < 1) occ = 1;
   const int64_t need = (static_cast<int64_t>(work) + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
@@ -213,9 +284,12 @@ cudaError_t launch_tensor_nvfp4_pack(const TensorNvfp4Params& p, cudaStream_t s)
   if (e != cudaSuccess) return e;
   if (p.kind == 0) {
     const uint32_t ntask = static_cast<uint32_t>((p.rows + 15) / 16) * static_cast<uint32_t>(p.H) *
-                           static_cast<uint32_t>(p.D / 2);
+                           static_cast<uint32_t>(p.D / 8);
+    e = cudaFuncSetAttribute(tensor_key_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kKeySmem));  // the shared-memory opt-in (per device)
+    if (e != cudaSuccess) return e;
     KVQ_LAUNCH("tensor_key_encode_kernel", s,
-               tensor_key_encode_kernel<<<grid_for(tensor_key_encode_kernel, ntask), kThreads, 0, s>>>(p);
+               tensor_key_encode_kernel<<<grid_for(tensor_key_encode_kernel, ntask, kKeySmem), kThreads, kKeySmem, s>>>(p);
                e = cudaGetLastError());
   } else {
     KVQ_LAUNCH("tensor_value_encode_kernel", s,
