@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) tensor_value_encode_kernel(const Ten
 // while this task is coded.  The thread's own wait_group orders its cells.
 constexpr size_t kKeySmem = static_cast<size_t>(16) * kThreads * 16;
 
-__global__ void __launch_bounds__(kThreads) tensor_key_encode_kernel(const TensorNvfp4Params p) {
+__global__ void __launch_bounds__(kThreads, 2) tensor_key_encode_kernel(const TensorNvfp4Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint4* const cells = reinterpret_cast<uint4*>(smem) + threadIdx.x;
   const uint32_t nb = static_cast<uint32_t>(p.D / 16);  // chunk pairs per row
@@ -178,26 +178,35 @@ __global__ void __launch_bounds__(kThreads) tensor_key_encode_kernel(const Tenso
     for (int j = 0; j < 4; ++j) inv2[j] = pack_f32x2(__float_as_uint(inv[2 * j]), __float_as_uint(inv[2 * j + 1]));
     uint8_t* const cp = p.codes + (static_cast<int64_t>(t.r0) * p.H + t.h) * (p.D / 2) + 4 * t.ch;
     const int64_t cstride = static_cast<int64_t>(p.H) * (p.D / 2);
+    if (!direct && t.n == 16) {  // a full group with ordinary scales: unrolled
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      if (k >= t.n) break;
-      uint32_t byte[4];
+      for (int k = 0; k < 16; ++k) {
+        uint32_t byte[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float ql, qh;
-        if (!direct) {
+        for (int j = 0; j < 4; ++j) {
           uint32_t a, b;
           unpack_f32x2(mul_f32x2(pack_f32x2(w[k][j] << 16, w[k][j] & 0xFFFF0000u), inv2[j]), a, b);
-          ql = __uint_as_float(a);
-          qh = __uint_as_float(b);
-        } else {
-          ql = isinf(inv[2 * j]) ? __fdiv_rn(bf16lo(w[k][j]), sc[2 * j]) : __fmul_rn(bf16lo(w[k][j]), inv[2 * j]);
-          qh = isinf(inv[2 * j + 1]) ? __fdiv_rn(bf16hi(w[k][j]), sc[2 * j + 1])
-                                     : __fmul_rn(bf16hi(w[k][j]), inv[2 * j + 1]);
+          byte[j] = e2m1x2_from_f32(__uint_as_float(a), __uint_as_float(b));
         }
-        byte[j] = e2m1x2_from_f32(ql, qh);
+        STX(reinterpret_cast<uint32_t*>(cp + k * cstride), bytes4(byte[0], byte[1], byte[2], byte[3]));
       }
-      STX(reinterpret_cast<uint32_t*>(cp + k * cstride), bytes4(byte[0], byte[1], byte[2], byte[3]));
+    } else {  // a partial group, or a scale whose reciprocal overflows (divide): compact,
+              // the rows read again from global memory (the cells hold the next task)
+      const uint16_t* const src = p.x + static_cast<int64_t>(t.h) * p.head_pitch + 8 * t.ch;
+#pragma unroll 1
+      for (int k = 0; k < t.n; ++k) {
+        uint32_t wk[4];
+        load16B(src + static_cast<int64_t>(t.r0 + k) * p.row_pitch, wk);
+        uint32_t byte[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float xl = bf16lo(wk[j]), xh = bf16hi(wk[j]);
+          const float ql = isinf(inv[2 * j]) ? __fdiv_rn(xl, sc[2 * j]) : __fmul_rn(xl, inv[2 * j]);
+          const float qh = isinf(inv[2 * j + 1]) ? __fdiv_rn(xh, sc[2 * j + 1]) : __fmul_rn(xh, inv[2 * j + 1]);
+          byte[j] = e2m1x2_from_f32(ql, qh);
+        }
+        STX(reinterpret_cast<uint32_t*>(cp + k * cstride), bytes4(byte[0], byte[1], byte[2], byte[3]));
+      }
     }
     store8B(p.bscale + (static_cast<int64_t>(t.g) * p.H + t.h) * p.D + 8 * t.ch,
             bytes4(bsc[0], bsc[1], bsc[2], bsc[3]), bytes4(bsc[4], bsc[5], bsc[6], bsc[7]));
