@@ -204,7 +204,7 @@ template <bool kResidual, int RPT>
 __host__ __device__ constexpr size_t key_smem() { return static_cast<size_t>(key_threads<kResidual>() / 32) * (kResidual ? 2 : 1) * RPT * 32 * 16; }
 
 template <bool kResidual, int S, int RPT>
-__global__ void __launch_bounds__(key_threads<kResidual>()) int4_key_kernel(const Int4EncodeParams p) {
+__global__ void __launch_bounds__(key_threads<kResidual>(), kResidual ? 4 : 2) int4_key_kernel(const Int4EncodeParams p) {
   constexpr int kWarps = key_threads<kResidual>() / 32;
   constexpr int CW = 32 / S;  // column tasks per warp
   extern __shared__ __align__(16) unsigned char smem[];
@@ -356,13 +356,21 @@ __global__ void __launch_bounds__(key_threads<kResidual>()) int4_key_kernel(cons
     const int32_t col = t.chunk * 8;
     uint8_t* const cbase = p.dst.codes + static_cast<int64_t>(t.h) * (p.D / 2) + col / 2;
     const int64_t cstride = static_cast<int64_t>(p.H) * (p.D / 2);
+    if (fast && t.valid && t.r0 + rs + (RPT - 1) * S <= t.rlast) {  // every row, ordinary scales: unrolled
 #pragma unroll
-    for (int k = 0; k < RPT; ++k) {
-      const int32_t r = t.r0 + rs + k * S;
-      if (t.valid && r <= t.rlast) {
+      for (int k = 0; k < RPT; ++k) {
+        const int32_t r = t.r0 + rs + k * S;
+        if (t.chunk == 0 && t.h == 0) check_pos<kResidual>(p, r);
+        STX(reinterpret_cast<uint32_t*>(cbase + r * cstride), int4_codes8(v[k], nmn, nsc, y));
+      }
+    } else if (t.valid) {  // a partial group or a scale below 2^-64: compact, rows read again
+#pragma unroll 1
+      for (int32_t r = t.r0 + rs; r <= t.rlast; r += S) {
+        uint32_t wk[4];
+        load_chunk8<kResidual>(p, r, t.h, col, wk);
         if (t.chunk == 0 && t.h == 0) check_pos<kResidual>(p, r);
         STX(reinterpret_cast<uint32_t*>(cbase + r * cstride),
-            fast ? int4_codes8(v[k], nmn, nsc, y) : int4_codes8_div(v[k], nmn, nsc));
+            fast ? int4_codes8(wk, nmn, nsc, y) : int4_codes8_div(wk, nmn, nsc));
       }
     }
     if (t.valid && rs < 4) {  // the FP16 metadata of the words this lane formed
@@ -466,20 +474,31 @@ __global__ void __launch_bounds__(kThreads, kBlk == 2 ? 3 : 4) int4_value_kernel
     const uint64_t nsc2[4] = {dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc), dup_f32x2(-sc)};
     const float yv = int4_recip(sc);
     const uint64_t y2[4] = {dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv), dup_f32x2(yv)};
-    const bool fast = int4_fast_scale(sc);
-    uint32_t cw[2 * kBlk];
+    uint8_t* const dst = p.dst.codes + static_cast<int64_t>(rw) * (p.D / 2) + (C / 2) * b;
+    if (int4_fast_scale(sc)) {
+      uint32_t cw[2 * kBlk];
 #pragma unroll
-    for (int k = 0; k < 2 * kBlk; ++k) {
-      const uint32_t wk[4] = {w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]};
-      cw[k] = fast ? int4_codes8(wk, nmn2, nsc2, y2) : int4_codes8_div(wk, nmn2, nsc2);
+      for (int k = 0; k < 2 * kBlk; ++k) {
+        const uint32_t wk[4] = {w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]};
+        cw[k] = int4_codes8(wk, nmn2, nsc2, y2);
+      }
+      if (store) {
+        if constexpr (kBlk == 2) {
+          store16B(dst, cw);
+        } else {
+          store8B(dst, cw[0], cw[1]);
+        }
+      }
+    } else if (store) {  // a scale below 2^-64: divide, compact, the chunks read again
+      const int32_t h = static_cast<int32_t>(rw - static_cast<uint32_t>(r) * static_cast<uint32_t>(p.H));
+#pragma unroll 1
+      for (int k = 0; k < 2 * kBlk; ++k) {
+        uint32_t wk[4];
+        load_chunk8<kResidual>(p, r, h, C * b + 8 * k, wk);
+        STX(reinterpret_cast<uint32_t*>(dst + 4 * k), int4_codes8_div(wk, nmn2, nsc2));
+      }
     }
     if (store) {
-      uint8_t* const dst = p.dst.codes + static_cast<int64_t>(rw) * (p.D / 2) + (C / 2) * b;
-      if constexpr (kBlk == 2) {
-        store16B(dst, cw);
-      } else {
-        store8B(dst, cw[0], cw[1]);
-      }
       if (lead) {
         const int64_t mi = static_cast<int64_t>(rw) * ngv + gidx;
         STX(p.dst.mn + mi, f32_to_f16_bits(mn));
@@ -579,13 +598,24 @@ cudaError_t key_launch(const Int4EncodeParams& p, int64_t ntask, cudaStream_t s)
 template <bool kRes>
 cudaError_t key_dispatch(const Int4EncodeParams& p, cudaStream_t s) {
   const int64_t ntask = static_cast<int64_t>((p.rows + p.G - 1) / p.G) * p.H * (p.D / 8);
-  switch (p.G) {  // S = G / RPT lanes per column task, RPT rows each (residual: 8, plain: 16)
-    case 16: return kRes ? key_launch<kRes, 2, 8>(p, ntask, s) : key_launch<kRes, 1, 16>(p, ntask, s);
-    case 32: return kRes ? key_launch<kRes, 4, 8>(p, ntask, s) : key_launch<kRes, 2, 16>(p, ntask, s);
-    case 64: return kRes ? key_launch<kRes, 8, 8>(p, ntask, s) : key_launch<kRes, 4, 16>(p, ntask, s);
-    case 128: return kRes ? key_launch<kRes, 16, 8>(p, ntask, s) : key_launch<kRes, 8, 16>(p, ntask, s);
-    case 256: return kRes ? key_launch<kRes, 32, 8>(p, ntask, s) : key_launch<kRes, 16, 16>(p, ntask, s);
-    case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
+  if constexpr (kRes) {
+    switch (p.G) {  // S = G / RPT lanes per column task, RPT rows each (8; 16 for G512)
+      case 16: return key_launch<kRes, 2, 8>(p, ntask, s);
+      case 32: return key_launch<kRes, 4, 8>(p, ntask, s);
+      case 64: return key_launch<kRes, 8, 8>(p, ntask, s);
+      case 128: return key_launch<kRes, 16, 8>(p, ntask, s);
+      case 256: return key_launch<kRes, 32, 8>(p, ntask, s);
+      case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
+    }
+  } else {
+    switch (p.G) {  // S = G / 16 lanes per column task, 16 rows each
+      case 16: return key_launch<kRes, 1, 16>(p, ntask, s);
+      case 32: return key_launch<kRes, 2, 16>(p, ntask, s);
+      case 64: return key_launch<kRes, 4, 16>(p, ntask, s);
+      case 128: return key_launch<kRes, 8, 16>(p, ntask, s);
+      case 256: return key_launch<kRes, 16, 16>(p, ntask, s);
+      case 512: return key_launch<kRes, 32, 16>(p, ntask, s);
+    }
   }
   return cudaErrorInvalidValue;
 }
