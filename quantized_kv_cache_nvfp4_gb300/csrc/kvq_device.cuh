@@ -342,13 +342,6 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return r;
 }
 
-// fp16x2 * fp16x2, each half rounded to nearest even (exact for E2M1 x E4M3).
-__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 __device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) {
   lo = f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
   hi = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
@@ -436,33 +429,6 @@ __device__ __forceinline__ void fp8_decode16(const uint32_t (&c)[4], float rs, u
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// Order keys of two packed finite bf16: a positive value keeps its bits with the top
-// bit set, a negative one is complemented, so the unsigned order of the 16-bit keys
-// is the order of the values with -0 (key 0x7FFF) below +0 (key 0x8000) -- the total
-// order of IEEE 754-2019 minimum/maximum.  bf16x2_unkey inverts it.
-__device__ __forceinline__ uint32_t bf16x2_key(uint32_t w) {
-  return w ^ (((w >> 15) & 0x00010001u) * 0x7FFFu + 0x80008000u);
-}
-__device__ __forceinline__ uint32_t bf16x2_unkey(uint32_t k) {
-  return k ^ (((~k >> 15) & 0x00010001u) * 0x7FFFu + 0x80008000u);
-}
-__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
