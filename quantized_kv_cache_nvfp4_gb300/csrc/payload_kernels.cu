@@ -317,13 +317,24 @@ cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t
 template <bool kInPlace>
 cudaError_t key_decode_dispatch(const UnpackParams& u, cudaStream_t s) {
   const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
-  switch (u.pay.G) {  // RS = G / RPL lanes per column task
-    case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
-    case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
-    case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
-    case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
-    case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
-    case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
+  if constexpr (kInPlace) {
+    switch (u.pay.G) {  // RS = G / RPL lanes per column task; 4 rows a lane (prev held too)
+      case 16: return key_decode_launch<kInPlace, 4, 4>(u, ntask, s);
+      case 32: return key_decode_launch<kInPlace, 8, 4>(u, ntask, s);
+      case 64: return key_decode_launch<kInPlace, 16, 4>(u, ntask, s);
+      case 128: return key_decode_launch<kInPlace, 32, 4>(u, ntask, s);
+      case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
+      case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
+    }
+  } else {
+    switch (u.pay.G) {  // RS = G / RPL lanes per column task
+      case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
+      case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
+      case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
+      case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
+      case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
+      case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
+    }
   }
   return cudaErrorInvalidValue;
 }
