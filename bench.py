@@ -291,6 +291,7 @@ def run_ours(args):
         rows_other = other_rows(kvq, device, peak=measured_peaks()[0])
         rows_other["latency_us_one_residual_loop"] = residual_loop_latency(kvq, device)
         rows_other["decode_attention"] = attention_rows(kvq, device, peak=measured_peaks()[0])
+        rows_other["decode_step_store"] = decode_step_latency(kvq, device)
 
     if rank != 0:
         if dist is not None:
@@ -571,9 +572,21 @@ def attention_rows(kvq, device, peak=6795.5, iters=20, S=32, T=8192, H=8, Hq=32,
         res[f"kvq_decode_attention {name}"] = {"ms": round(ms, 4), "bytes": nbytes,
                                                "GB/s": round(nbytes / ms / 1e6, 1),
                                                "frac": round(nbytes / ms / 1e6 / peak, 4)}
-        if name == "nvfp4":  # the unfused path on the same pool, for context
+        if name == "nvfp4":  # the paged restore of the same pool, then the unfused path
             ko = torch.empty((S, T, H, D), dtype=torch.bfloat16, device=device)
             vo = torch.empty_like(ko)
+            for _ in range(3):
+                kvq.kvq_restore(pool, table, lens, T, ko, vo)
+            a.record()
+            for _ in range(iters):
+                kvq.kvq_restore(pool, table, lens, T, ko, vo)
+            b.record()
+            torch.cuda.synchronize(device)
+            ms = a.elapsed_time(b) / iters
+            rb = restore_bytes(S * T, H, D, nblocks, S)
+            res[f"kvq_restore nvfp4 ({S} x {T} tokens)"] = {"ms": round(ms, 4), "bytes": rb,
+                                                           "GB/s": round(rb / ms / 1e6, 1),
+                                                           "frac": round(rb / ms / 1e6 / peak, 4)}
 
             def unfused():
                 kvq.kvq_restore(pool, table, lens, T, ko, vo)
@@ -594,6 +607,38 @@ def attention_rows(kvq, device, peak=6795.5, iters=20, S=32, T=8192, H=8, Hq=32,
         del pool
     return {"workload": f"decode attention: {S} sequences x {T} tokens, {H} KV heads, {Hq} query heads, "
                         f"D{D}, block size {bs}, shuffled block table", "kernels": res}
+
+
+def decode_step_latency(kvq, device, iters=200):
+    """The decode-step store: 256 requests append one token each (H8, D128), K a view
+    of a fused qkv tensor (row pitch 1152), V its own tensor, into a 65,536-slot pool;
+    the quant-scatter captured in a CUDA graph, microseconds per replay."""
+    from quantized_kv_cache_nvfp4_gb300 import synth
+
+    qkv, _, v, slots = synth.decode_step_case(seed=2)
+    qkv, v, slots = qkv.to(device), v.to(device), slots.to(device)
+    k = qkv[:, :1024].unflatten(1, (8, 128))
+    pool = kvq.Nvfp4Pool.empty(65536, 8, 128, BLOCK, device=device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            kvq.kvq_quant_scatter(k, v, slots, pool, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kvq.kvq_quant_scatter(k, v, slots, pool, stream=stream)
+    for _ in range(10):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize(device)
+    return {"workload": "256 tokens x 8 KV heads x D128 (K a view of qkv [256, 1152]) into a 65,536-slot pool, "
+                        "one graph replay", "us_per_replay": round(a.elapsed_time(b) / iters * 1000, 2),
+            "bytes": scatter_bytes(256, 8, 128)}
 
 
 def residual_loop_latency(kvq, device, iters=50):
