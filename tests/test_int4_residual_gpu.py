@@ -306,3 +306,70 @@ def test_int4_tiny_and_subnormal_groups(kind, exps):
     codes, mn, sc = O.int4_pack(bits_in, kind, 64)
     check_int4(pk, codes, mn, sc)
     np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
+
+
+def test_int4_pack_unpack_at_the_bench_size_sampled():
+    """[262144, 8, 128] G64 (the size bench.py times, in the same launch shapes), both
+    kinds: 24 sampled K groups (64 rows x 8 heads x 128 channels each) and 256 sampled
+    V rows against the oracle run on just those rows, codes, metadata and the unpack."""
+    T, H, D, G = 262144, 8, 128, 64
+    x = synth.normal_bf16((T, H, D), seed=21, stream=1, outlier_frac=0.01, outlier_scale=20.0, device=DEV)
+    rng = np.random.default_rng(21)
+    y = torch.empty_like(x)
+    for kind in (kvq.KIND_KEY, kvq.KIND_VALUE):
+        pk = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G)
+        kvq.kvq_pack(x, pk)
+        kvq.kvq_unpack(pk, y)
+        torch.cuda.synchronize()
+        if kind == kvq.KIND_KEY:
+            for g in rng.choice(T // G, 24, replace=False):
+                rows = slice(int(g) * G, (int(g) + 1) * G)
+                xb = bits(x[rows])
+                codes, mn, sc = O.int4_pack(xb, kind, G)
+                np.testing.assert_array_equal(u8(pk.codes[rows]), codes)
+                np.testing.assert_array_equal(f16bits(pk.meta0[int(g):int(g) + 1]), mn)
+                np.testing.assert_array_equal(f16bits(pk.meta1[int(g):int(g) + 1]), sc)
+                np.testing.assert_array_equal(bits(y[rows]), O.int4_unpack(codes, mn, sc, kind, G))
+        else:
+            idx = np.sort(rng.choice(T, 256, replace=False))
+            it = torch.from_numpy(idx).to(DEV)
+            xb = bits(x[it])
+            codes, mn, sc = O.int4_pack(xb, kind, G)
+            np.testing.assert_array_equal(u8(pk.codes[it]), codes)
+            np.testing.assert_array_equal(f16bits(pk.meta0[it]), mn)
+            np.testing.assert_array_equal(f16bits(pk.meta1[it]), sc)
+            np.testing.assert_array_equal(bits(y[it]), O.int4_unpack(codes, mn, sc, kind, G))
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_residual_encode_at_the_bench_size_sampled(kind):
+    """Residual encode over [262144, 8, 128] with 25% of rows kept (65,536 compact rows),
+    as bench.py times it: 16 sampled K groups of 64 compact rows (V: 256 compact rows)
+    against the oracle's residual encode of just those rows."""
+    T, H, D, G = 262144, 8, 128, 64
+    cur = synth.normal_bf16((T, H, D), seed=22, stream=1, device=DEV)
+    prev = synth.normal_bf16((T, H, D), seed=22, stream=2, device=DEV)
+    pos = synth.sorted_positions(T, T // 4, 22, stream=synth.STREAM_POS).to(DEV)
+    P = pos.numel()
+    pay = kvq.Packed.empty(kvq.FMT_INT4, kind, P, H, D, G)
+    kvq.kvq_encode_residual(cur, prev, pos, pay)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(22)
+    if kind == kvq.KIND_KEY:
+        picks = [slice(int(g) * G, (int(g) + 1) * G) for g in rng.choice(P // G, 16, replace=False)]
+    else:
+        picks = [torch.from_numpy(np.sort(rng.choice(P, 256, replace=False))).to(DEV)]
+    for sel in picks:
+        src = pos[sel].long()
+        n = src.numel()
+        opay, ost = O.residual_encode(bits(cur[src]), bits(prev[src]), np.arange(n, dtype=np.int32), kvq.FMT_INT4,
+                                      kind, G)
+        assert ost == 0
+        np.testing.assert_array_equal(u8(pay.codes[sel]), opay["codes"])
+        if kind == kvq.KIND_KEY:
+            g = sel.start // G
+            np.testing.assert_array_equal(f16bits(pay.meta0[g:g + 1]), opay["meta_a"])
+            np.testing.assert_array_equal(f16bits(pay.meta1[g:g + 1]), opay["meta_b"])
+        else:
+            np.testing.assert_array_equal(f16bits(pay.meta0[sel]), opay["meta_a"])
+            np.testing.assert_array_equal(f16bits(pay.meta1[sel]), opay["meta_b"])

@@ -92,3 +92,32 @@ def test_residual_payloads_are_rejected():
     pay = kvq.Packed.empty(T4, kvq.KIND_VALUE, 16, 1, 64)
     with pytest.raises(kvq.KvqError, match="UNSUPPORTED"):
         kvq.kvq_encode_residual(x, x, None, pay)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_full_size_sampled(kind):
+    """[131072, 8, 128] (the size the per-tensor encoders are timed at), sampled: the
+    tensor's largest magnitude is planted in row 0, so row 0's group (K: rows 0-15; V:
+    row 0) with 12 sampled K groups (V: 255 sampled rows) reproduces the tensor scale,
+    and the oracle runs on just those rows."""
+    T, H, D = 131072, 8, 128
+    x = synth.normal_bf16((T, H, D), seed=31, stream=1, outlier_frac=0.01, outlier_scale=20.0, device=DEV)
+    x[0, 3, 17] = -1000.0  # the tensor's amax (|N(0,1)| x 20 stays far below)
+    pk = kvq.Packed.empty(T4, kind, T, H, D)
+    kvq.kvq_pack(x, pk)
+    y = torch.empty_like(x)
+    kvq.kvq_unpack(pk, y)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(31)
+    if kind == kvq.KIND_KEY:
+        groups = [0] + [int(g) for g in rng.choice(np.arange(1, T // 16), 12, replace=False)]
+        rows = torch.cat([torch.arange(16 * g, 16 * g + 16) for g in groups]).to(DEV)
+        sel_b = torch.tensor(groups, device=DEV)
+    else:
+        rows = torch.from_numpy(np.concatenate([[0], np.sort(rng.choice(np.arange(1, T), 255, replace=False))])).to(DEV)
+        sel_b = rows
+    c, b, r = O.nvfp4t_pack(bits(x[rows]), kind)
+    np.testing.assert_array_equal(f32bits(pk.rscale), f32bits(r), err_msg="tensor scale")
+    np.testing.assert_array_equal(u8(pk.codes[rows]), c, err_msg="codes")
+    np.testing.assert_array_equal(u8(pk.meta0[sel_b]), b, err_msg="block scales")
+    np.testing.assert_array_equal(bits(y[rows]), O.nvfp4t_unpack(c, b, r, kind), err_msg="decoded")
