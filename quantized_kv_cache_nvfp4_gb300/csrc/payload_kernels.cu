@@ -162,24 +162,55 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
       const int32_t t0 = static_cast<int32_t>(run * u.run);
       const int32_t t1 = min(u.src_rows, t0 + u.run);
       int32_t cur = (u.pos != nullptr) ? lower_bound(u.pos, u.num_pos, t0) : 0;
-      for (uint32_t row = static_cast<uint32_t>(t0) * u.H + sub; row < static_cast<uint32_t>(t1) * u.H;
-           row += kRowsPerWarp) {
-        uint32_t t, h;
-        u.div_h.divmod(row, t, h);
-        int64_t p = t;
-        if (u.pos != nullptr) {
-          while (cur < u.num_pos && LDX(u.pos + cur) < static_cast<int32_t>(t)) ++cur;
-          // both arms signed: -1 must stay negative
-          p = (cur < u.num_pos && LDX(u.pos + cur) == static_cast<int32_t>(t)) ? static_cast<int64_t>(cur)
-                                                                              : static_cast<int64_t>(-1);
+      const uint32_t rend = static_cast<uint32_t>(t1) * u.H;
+      // two rows a step: both rows' payload and prev loads are issued before either
+      // row is combined and stored
+      for (uint32_t row = static_cast<uint32_t>(t0) * u.H + sub; row < rend; row += 2 * kRowsPerWarp) {
+        uint32_t t[2], h[2];
+        int64_t p[2];
+        bool ok[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t rk = row + k * kRowsPerWarp;
+          ok[k] = rk < rend;
+          u.div_h.divmod(ok[k] ? rk : row, t[k], h[k]);
+          p[k] = t[k];
+          if (u.pos != nullptr) {  // the rows ascend, so one forward scan serves both
+            while (cur < u.num_pos && LDX(u.pos + cur) < static_cast<int32_t>(t[k])) ++cur;
+            // both arms signed: -1 must stay negative
+            p[k] = (cur < u.num_pos && LDX(u.pos + cur) == static_cast<int32_t>(t[k])) ? static_cast<int64_t>(cur)
+                                                                                      : static_cast<int64_t>(-1);
+          }
         }
-        uint32_t w[BPL][8];
-        if (p >= 0) decode_blocks<kFmt, BPL>(u, p, static_cast<int32_t>(h), b0, w);
-        add_store<kV8, true, BPL>(u.prev + static_cast<int64_t>(t) * u.prev_row_pitch +
-                                      static_cast<int64_t>(h) * u.prev_head_pitch,
-                                  u.y + static_cast<int64_t>(t) * u.y_row_pitch +
-                                      static_cast<int64_t>(h) * u.y_head_pitch,
-                                  b0, w, p >= 0);
+        uint32_t w[2][BPL][8], q[2][BPL][8];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (!ok[k]) continue;
+          if (p[k] >= 0) decode_blocks<kFmt, BPL>(u, p[k], static_cast<int32_t>(h[k]), b0, w[k]);
+          const uint16_t* pv =
+              u.prev + static_cast<int64_t>(t[k]) * u.prev_row_pitch + static_cast<int64_t>(h[k]) * u.prev_head_pitch;
+#pragma unroll
+          for (int j = 0; j < BPL; ++j) load32B<kV8, true>(pv + 16 * (b0 + j), q[k][j]);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (!ok[k]) continue;
+          uint16_t* out = u.y + static_cast<int64_t>(t[k]) * u.y_row_pitch + static_cast<int64_t>(h[k]) * u.y_head_pitch;
+#pragma unroll
+          for (int j = 0; j < BPL; ++j) {
+            if (p[k] >= 0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                uint32_t lo, hi;
+                unpack_f32x2(add_f32x2(pack_f32x2(q[k][j][i] << 16, q[k][j][i] & 0xFFFF0000u),
+                                       pack_f32x2(w[k][j][i] << 16, w[k][j][i] & 0xFFFF0000u)),
+                             lo, hi);
+                q[k][j][i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+              }
+            }
+            store32B<kV8>(out + 16 * (b0 + j), q[k][j]);
+          }
+        }
       }
     }
     return;
