@@ -164,8 +164,7 @@ __device__ __forceinline__ bool load_chunk8(const Int4EncodeParams& p, int32_t r
     load16B(p.prev + src * p.prev_row_pitch + static_cast<int64_t>(h) * p.prev_head_pitch + col, q);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      w[i] = pack_bf16x2(__fsub_rn(bf16lo(w[i]), bf16lo(q[i])),
-                         __fsub_rn(bf16hi(w[i]), bf16hi(q[i])));
+      w[i] = bf16x2_sub(w[i], q[i]);
   }
   return true;
 }
@@ -268,10 +267,10 @@ __global__ void __launch_bounds__(key_threads<kResidual>(), kResidual ? 4 : 2) i
       uint4 a = slot[k * 32 + lane];
       if constexpr (kResidual) {
         const uint4 q = slot[(RPT + k) * 32 + lane];
-        a.x = pack_bf16x2(__fsub_rn(bf16lo(a.x), bf16lo(q.x)), __fsub_rn(bf16hi(a.x), bf16hi(q.x)));
-        a.y = pack_bf16x2(__fsub_rn(bf16lo(a.y), bf16lo(q.y)), __fsub_rn(bf16hi(a.y), bf16hi(q.y)));
-        a.z = pack_bf16x2(__fsub_rn(bf16lo(a.z), bf16lo(q.z)), __fsub_rn(bf16hi(a.z), bf16hi(q.z)));
-        a.w = pack_bf16x2(__fsub_rn(bf16lo(a.w), bf16lo(q.w)), __fsub_rn(bf16hi(a.w), bf16hi(q.w)));
+        a.x = bf16x2_sub(a.x, q.x);
+        a.y = bf16x2_sub(a.y, q.y);
+        a.z = bf16x2_sub(a.z, q.z);
+        a.w = bf16x2_sub(a.w, q.w);
       }
       v[k][0] = a.x;
       v[k][1] = a.y;

@@ -212,6 +212,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// bf16(a - b) and bf16(a + b) of packed bf16 pairs, each half rounded once to nearest
+// even.  For finite bf16 operands this equals the binary32 difference (sum) rounded to
+// bf16: the binary32 result is exact when the exponents differ by at most 16, and
+// otherwise the smaller operand lies below half a bf16 ulp of the larger, so both
+// roundings return the larger (checked for all 4.3e9 pairs of finite bf16 values).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
   uint16_t h;
   asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));

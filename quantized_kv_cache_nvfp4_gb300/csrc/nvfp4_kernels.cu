@@ -86,8 +86,7 @@ __device__ __forceinline__ void load_source(const EncodeParams& p, const RowLoc&
       load32B<kV8, true>(q + 16 * (b0 + j), pw);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        w[j][i] = pack_bf16x2(__fsub_rn(bf16lo(w[j][i]), bf16lo(pw[i])),
-                              __fsub_rn(bf16hi(w[j][i]), bf16hi(pw[i])));
+        w[j][i] = bf16x2_sub(w[j][i], pw[i]);
     }
   }
 }

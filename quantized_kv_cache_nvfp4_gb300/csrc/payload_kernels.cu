@@ -110,13 +110,7 @@ __device__ __forceinline__ void add_store(const uint16_t* prev, uint16_t* out, i
     load32B<kV8, kNC>(prev + 16 * (b0 + j), q);
     if (add) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t lo, hi;
-        unpack_f32x2(add_f32x2(pack_f32x2(q[i] << 16, q[i] & 0xFFFF0000u),
-                               pack_f32x2(w[j][i] << 16, w[j][i] & 0xFFFF0000u)),
-                     lo, hi);
-        q[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
-      }
+      for (int i = 0; i < 8; ++i) q[i] = bf16x2_add(q[i], w[j][i]);
     }
     store32B<kV8>(out + 16 * (b0 + j), q);
   }
@@ -200,13 +194,7 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
           for (int j = 0; j < BPL; ++j) {
             if (p[k] >= 0) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                uint32_t lo, hi;
-                unpack_f32x2(add_f32x2(pack_f32x2(q[k][j][i] << 16, q[k][j][i] & 0xFFFF0000u),
-                                       pack_f32x2(w[k][j][i] << 16, w[k][j][i] & 0xFFFF0000u)),
-                             lo, hi);
-                q[k][j][i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
-              }
+              for (int i = 0; i < 8; ++i) q[k][j][i] = bf16x2_add(q[k][j][i], w[k][j][i]);
             }
             store32B<kV8>(out + 16 * (b0 + j), q[k][j]);
           }
@@ -316,13 +304,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
       uint16_t* o = u.y + t[k] * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col;
       if constexpr (kInPlace) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t lo, hi;
-          unpack_f32x2(add_f32x2(pack_f32x2(q[k][i] << 16, q[k][i] & 0xFFFF0000u),
-                                 pack_f32x2(y[i] << 16, y[i] & 0xFFFF0000u)),
-                       lo, hi);
-          y[i] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
-        }
+        for (int i = 0; i < 4; ++i) y[i] = bf16x2_add(q[k][i], y[i]);
       }
       store16B(o, y);
     }

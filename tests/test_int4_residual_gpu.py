@@ -373,3 +373,31 @@ def test_int4_residual_encode_at_the_bench_size_sampled(kind):
         else:
             np.testing.assert_array_equal(f16bits(pay.meta0[sel]), opay["meta_a"])
             np.testing.assert_array_equal(f16bits(pay.meta1[sel]), opay["meta_b"])
+
+
+@pytest.mark.parametrize("fmt,kind", [(kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_INT4, kvq.KIND_VALUE),
+                                      (kvq.FMT_NVFP4, kvq.KIND_VALUE), (kvq.FMT_FP8, kvq.KIND_VALUE)])
+def test_residual_arithmetic_across_exponent_gaps(fmt, kind):
+    """cur and prev at magnitudes 2^-30 .. 2^30 apart (per token), so bf16(cur - prev)
+    and bf16(prev + y) cross the regime where the binary32 result stops being exact;
+    payload and reconstruction against the oracle, copy and in place."""
+    T, H, D = 640, 2, 128
+    gaps = torch.tensor([-30, -17, -16, -9, -8, 0, 8, 9, 16, 17, 30], dtype=torch.float32)
+    e = gaps[torch.arange(T) % gaps.numel()].view(T, 1, 1)
+    cur = (synth.normal_bf16((T, H, D), 71, 1).float() * torch.exp2(e / 2)).to(torch.bfloat16)
+    prev = (synth.normal_bf16((T, H, D), 71, 2).float() * torch.exp2(-e / 2)).to(torch.bfloat16)
+    pos = synth.sorted_positions(T, T // 2, 71)
+    pay = kvq.Packed.empty(fmt, kind, pos.numel(), H, D, 64)
+    kvq.kvq_encode_residual(cur.to(DEV), prev.to(DEV), pos.to(DEV), pay)
+    out = poison_bf16((T, H, D))
+    kvq.kvq_decode_residual(pay, pos.to(DEV), prev.to(DEV), out)
+    ip = prev.to(DEV).clone()
+    kvq.kvq_decode_residual(pay, pos.to(DEV), ip, ip)
+    torch.cuda.synchronize()
+    opay, ost = O.residual_encode(bits(cur), bits(prev), pos.numpy(), fmt, kind, 64)
+    assert ost == 0
+    check_payload(pay, opay)
+    ref, dst = O.residual_decode(opay, bits(prev))
+    assert dst == 0
+    np.testing.assert_array_equal(bits(out), ref)
+    np.testing.assert_array_equal(bits(ip), ref)
