@@ -221,14 +221,27 @@ __global__ void __launch_bounds__(key_threads<kResidual>(), kResidual ? 4 : 2) i
     int32_t chunk, h, g, r0, rlast;
     bool valid;
   };
+  // task -> (group, head, chunk): multiply-shift divisions while the task count is
+  // below 2^31 (always, short of tensors near the memory size), else 64-bit ones
+  const bool small = ntask < (int64_t{1} << 31);
+  const FastDiv div_c(static_cast<uint32_t>(nchunk));  // built once per thread
   auto task_of = [&](int64_t wt) {
     Task t;
     const int64_t task = wt * CW + cl;
     t.valid = task < ntask;
     const int64_t tk = t.valid ? task : ntask - 1;
-    t.chunk = static_cast<int32_t>(tk % nchunk);
-    t.h = static_cast<int32_t>((tk / nchunk) % p.H);
-    t.g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
+    if (small) {
+      uint32_t gh, c, g, h;
+      div_c.divmod(static_cast<uint32_t>(tk), gh, c);
+      p.div_h.divmod(gh, g, h);
+      t.chunk = static_cast<int32_t>(c);
+      t.h = static_cast<int32_t>(h);
+      t.g = static_cast<int32_t>(g);
+    } else {
+      t.chunk = static_cast<int32_t>(tk % nchunk);
+      t.h = static_cast<int32_t>((tk / nchunk) % p.H);
+      t.g = static_cast<int32_t>(tk / (static_cast<int64_t>(nchunk) * p.H));
+    }
     t.r0 = t.g * p.G;
     t.rlast = min(p.rows, t.r0 + p.G) - 1;
     return t;

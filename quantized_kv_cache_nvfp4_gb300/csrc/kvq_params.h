@@ -16,7 +16,7 @@ namespace kvq {
 struct FastDiv {
   uint32_t d = 1, m = 0, l = 0;
   FastDiv() = default;
-  explicit FastDiv(uint32_t div) : d(div) {
+  __host__ __device__ explicit FastDiv(uint32_t div) : d(div) {
     l = 0;
     while ((1ull << l) < div) ++l;
     uint64_t two_l = 1ull << l;

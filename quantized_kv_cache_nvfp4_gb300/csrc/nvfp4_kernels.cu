@@ -301,36 +301,36 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_decode_kernel(cons
           store32B<kV8>(rr[r].y + 16 * (b0 + j), out);
         }
       }
-      continue;
-    }
-    uint32_t cw[R][2 * BPL];
-    uint32_t bsb[R];
-    float rs[R];
+    } else {
+      uint32_t cw[R][2 * BPL];
+      uint32_t bsb[R];
+      float rs[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (rr[r].srow < 0) continue;
-      const DecodeTensor& T = *rr[r].ten;
-      const int64_t srow = rr[r].srow;
-      rs[r] = LDX(T.rscale + srow);
-      if constexpr (BPL == 2) {
-        uint32_t c4[4];
-        load16B(T.codes + srow * (8 * p.nb) + 8 * b0, c4);
+      for (int r = 0; r < R; ++r) {
+        if (rr[r].srow < 0) continue;
+        const DecodeTensor& T = *rr[r].ten;
+        const int64_t srow = rr[r].srow;
+        rs[r] = LDX(T.rscale + srow);
+        if constexpr (BPL == 2) {
+          uint32_t c4[4];
+          load16B(T.codes + srow * (8 * p.nb) + 8 * b0, c4);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cw[r][i] = c4[i];
-        bsb[r] = LDX(reinterpret_cast<const uint16_t*>(T.bscale + srow * p.nb + b0));
-      } else {
-        load8B(T.codes + srow * (8 * p.nb) + 8 * b0, cw[r][0], cw[r][1]);
-        bsb[r] = LDX(T.bscale + srow * p.nb + b0);
+          for (int i = 0; i < 4; ++i) cw[r][i] = c4[i];
+          bsb[r] = LDX(reinterpret_cast<const uint16_t*>(T.bscale + srow * p.nb + b0));
+        } else {
+          load8B(T.codes + srow * (8 * p.nb) + 8 * b0, cw[r][0], cw[r][1]);
+          bsb[r] = LDX(T.bscale + srow * p.nb + b0);
+        }
       }
-    }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (rr[r].srow < 0) continue;
-      uint32_t out[8];
+      for (int r = 0; r < R; ++r) {
+        if (rr[r].srow < 0) continue;
+        uint32_t out[8];
 #pragma unroll
-      for (int j = 0; j < BPL; ++j) {
-        nvfp4_decode16(cw[r][2 * j], cw[r][2 * j + 1], (bsb[r] >> (8 * j)) & 0xFFu, rs[r], out);
-        store32B<kV8>(rr[r].y + 16 * (b0 + j), out);
+        for (int j = 0; j < BPL; ++j) {
+          nvfp4_decode16(cw[r][2 * j], cw[r][2 * j + 1], (bsb[r] >> (8 * j)) & 0xFFu, rs[r], out);
+          store32B<kV8>(rr[r].y + 16 * (b0 + j), out);
+        }
       }
     }
   }

@@ -250,13 +250,27 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
   const int64_t ntask = static_cast<int64_t>(ngroups) * u.H * nchunk;
   const int64_t nwtask = (ntask + CW - 1) / CW;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  // task -> (group, head, chunk): multiply-shift divisions while the task count is
+  // below 2^31 (always, short of tensors near the memory size), else 64-bit ones
+  const bool small = ntask < (int64_t{1} << 31);
+  const FastDiv div_c(static_cast<uint32_t>(nchunk));  // built once per thread
   for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
        wt += nwarps) {
     const int64_t task = wt * CW + cl;
     if (task >= ntask) continue;  // no shuffles in this kernel
-    const int32_t chunk = static_cast<int32_t>(task % nchunk);
-    const int32_t h = static_cast<int32_t>((task / nchunk) % u.H);
-    const int32_t g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * u.H));
+    int32_t chunk, h, g;
+    if (small) {
+      uint32_t gh, c, gg, hh;
+      div_c.divmod(static_cast<uint32_t>(task), gh, c);
+      u.div_h.divmod(gh, gg, hh);
+      chunk = static_cast<int32_t>(c);
+      h = static_cast<int32_t>(hh);
+      g = static_cast<int32_t>(gg);
+    } else {
+      chunk = static_cast<int32_t>(task % nchunk);
+      h = static_cast<int32_t>((task / nchunk) % u.H);
+      g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * u.H));
+    }
     const int32_t r0 = g * P.G;
     const int32_t r1 = min(P.rows, r0 + P.G);
     const int32_t col = chunk * 8;
