@@ -67,12 +67,13 @@ __device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, 
   } else {
     const uint16_t* mnp = static_cast<const uint16_t*>(P.meta0);
     const uint16_t* scp = static_cast<const uint16_t*>(P.meta1);
+    const int gshift = __ffs(P.G) - 1;  // G is a power of two (16 .. 512)
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       const int b = b0 + j;
       float mn[16], sc[16];
       if (P.kind == 0) {  // KEY: per-channel metadata of group p / G
-        const int64_t m = ((p / P.G) * u.H + h) * u.D + 16 * b;
+        const int64_t m = ((p >> gshift) * u.H + h) * u.D + 16 * b;  // group p / G
         uint32_t a[8], c[8];
         load32B<false, true>(mnp + m, a);
         load32B<false, true>(scp + m, c);
@@ -84,8 +85,8 @@ __device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, 
           sc[2 * i + 1] = f16_bits_to_f32(static_cast<uint16_t>(c[i] >> 16));
         }
       } else {  // VALUE: one group covers the whole 16-channel block
-        const int ngv = (u.D + P.G - 1) / P.G;
-        const int64_t m = prow * ngv + (16 * b) / P.G;
+        const int ngv = (u.D + P.G - 1) >> gshift;
+        const int64_t m = prow * ngv + ((16 * b) >> gshift);
         const float mv = f16_bits_to_f32(LDX(mnp + m));
         const float sv = f16_bits_to_f32(LDX(scp + m));
 #pragma unroll
