@@ -733,14 +733,15 @@ def run_reference(args):
 
 
 CASES = ("attention_nvfp4", "attention_fp8", "attention_k8v4", "int4_pack_key", "int4_pack_value",
-         "int4_residual_key", "nvfp4t_pack_key", "nvfp4t_pack_value")
+         "int4_residual_key", "int4_decode_inplace_key", "nvfp4t_pack_key", "nvfp4t_pack_value")
 
 
 def run_case(args):
     """One kernel's workload alone (for profiler captures): `args.warmup` untimed calls,
     then `args.steps` timed ones; prints one JSON line with the mean time per call.
     attention_*: the decode-attention pool of 32 x 8192 tokens, 8 KV / 32 query heads,
-    D128; int4_* and nvfp4t_*: a [131072, 8, 128] bf16 tensor (residual: 25% of rows)."""
+    D128; int4_* and nvfp4t_*: a [131072, 8, 128] bf16 tensor (residual encode and the
+    in-place decode: 25% of rows)."""
     import math
 
     import quantized_kv_cache_nvfp4_gb300 as kvq
@@ -780,6 +781,12 @@ def run_case(args):
             pos = synth.sorted_positions(T, T // 4, 4).to(device)
             pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 4, H, D, G, device=device)
             fn = lambda: kvq.kvq_encode_residual(cur, prev, pos, pay)
+        elif name.startswith("int4_decode_inplace"):
+            pos = synth.sorted_positions(T, T // 4, 4).to(device)
+            pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 4, H, D, G, device=device)
+            kvq.kvq_encode_residual(cur, prev, pos, pay)
+            y = prev.clone()
+            fn = lambda: kvq.kvq_decode_residual(pay, pos, y, y)
         else:
             pk = kvq.Packed.empty(kvq.FMT_NVFP4_TENSOR, kind, T, H, D, device=device)
             fn = lambda: kvq.kvq_pack(cur, pk)

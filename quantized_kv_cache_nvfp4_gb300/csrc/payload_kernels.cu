@@ -117,6 +117,14 @@ __device__ __forceinline__ void add_store(const uint16_t* prev, uint16_t* out, i
   }
 }
 
+// A 32-bit read the compiler keeps where it is written (volatile), read-only path.
+__device__ __forceinline__ int32_t ld_i32_early(const int32_t* p) {
+  if (!KVQ_OK(p, 4, 4)) return -1;
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ int32_t lower_bound(const int32_t* pos, int32_t n, int32_t t) {
   int32_t lo = 0, hi = n;  // first index with pos[i] >= t
   while (lo < hi) {
@@ -255,11 +263,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
   // below 2^31 (always, short of tensors near the memory size), else 64-bit ones
   const bool small = ntask < (int64_t{1} << 31);
   const FastDiv div_c(static_cast<uint32_t>(nchunk));  // built once per thread
-  for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
-       wt += nwarps) {
-    const int64_t task = wt * CW + cl;
-    if (task >= ntask) continue;  // no shuffles in this kernel
-    int32_t chunk, h, g;
+  auto decompose = [&](int64_t task, int32_t& chunk, int32_t& h, int32_t& g) {
     if (small) {
       uint32_t gh, c, gg, hh;
       div_c.divmod(static_cast<uint32_t>(task), gh, c);
@@ -272,6 +276,35 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
       h = static_cast<int32_t>((task / nchunk) % u.H);
       g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * u.H));
     }
+  };
+  // in place with a position map: the positions of the next task's rows, read a task
+  // ahead (the prev reads of a row wait on its position otherwise)
+  int32_t pn[RPL];
+  auto prefetch = [&](int64_t wt) {
+    if constexpr (kInPlace) {
+      const int64_t task = wt * CW + cl;
+      if (u.pos == nullptr || task >= ntask) return;
+      int32_t chunk, h, g;
+      decompose(task, chunk, h, g);
+      const int32_t r0 = g * P.G, r1 = min(P.rows, r0 + P.G);
+#pragma unroll
+      for (int k = 0; k < RPL; ++k) {
+        const int32_t r = r0 + rs + k * RS;
+        pn[k] = r < r1 ? ld_i32_early(u.pos + r) : -1;
+      }
+    }
+  };
+  int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32;
+  prefetch(wt);
+  for (; wt < nwtask; wt += nwarps) {
+    int32_t pc[RPL];
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) pc[k] = pn[k];
+    prefetch(wt + nwarps);
+    const int64_t task = wt * CW + cl;
+    if (task >= ntask) continue;  // no shuffles in this kernel
+    int32_t chunk, h, g;
+    decompose(task, chunk, h, g);
     const int32_t r0 = g * P.G;
     const int32_t r1 = min(P.rows, r0 + P.G);
     const int32_t col = chunk * 8;
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
       t[k] = r;
       if constexpr (kInPlace) {
         if (u.pos != nullptr) {
-          t[k] = LDX(u.pos + r);
+          t[k] = pc[k];
           if (chunk == 0 && h == 0 && r > 0 && LDX(u.pos + r - 1) >= t[k]) set_status(u.status, 4u);
           if (t[k] < 0 || t[k] >= u.src_rows) {
             if (chunk == 0 && h == 0) set_status(u.status, 4u);
