@@ -105,27 +105,36 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(cons
   uint32_t row = (blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * kRowsPerWarp + sub;
   const bool lane_active = b0 < p.nb;
 
-  // the loads of row r: this lane's blocks (lanes past the row's end keep zeros) and,
-  // when scattering, the token's slot id; nothing past the last row
-  auto fetch = [&](uint32_t r, uint32_t (&w)[BPL][8], int64_t& slot) {
-    if (r < total) {
-      const RowLoc l = locate(r, p.rows_per_tensor, p.div_h);
-      if (lane_active) load_source<kMode, kV8, BPL>(p, l, b0, w);
-      if constexpr (kMode == kEncScatter) slot = LDX(p.slot_ids + l.tok);
-    }
-  };
+  uint32_t w[BPL][8];
+#pragma unroll
+  for (int j = 0; j < BPL; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[j][i] = 0u;
+  if (lane_active && row < total)
+    load_source<kMode, kV8, BPL>(p, locate(row, p.rows_per_tensor, p.div_h), b0, w);
 
-  // the codes of row `r` from its values w (and slot id); every lane of the row group
-  // takes part in the amax shuffles, valid or not
-  auto body = [&](uint32_t r, const uint32_t (&w)[BPL][8], int64_t slot) {
-    const bool valid = r < total;
-    const RowLoc loc = locate(valid ? r : 0u, p.rows_per_tensor, p.div_h);
+  // The loop bound is uniform across the warp (row - sub is), so every lane runs
+  // every shuffle of every iteration.
+  for (; row - sub < total; row += stride) {
+    const bool valid = row < total;
+    const RowLoc loc = locate(valid ? row : 0u, p.rows_per_tensor, p.div_h);
+
+    // issue the next row's loads before this row's arithmetic
+    uint32_t nw[BPL][8];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nw[j][i] = 0u;
+    const uint32_t nrow = row + stride;
+    if (lane_active && nrow < total)
+      load_source<kMode, kV8, BPL>(p, locate(nrow, p.rows_per_tensor, p.div_h), b0, nw);
 
     // destination row and skip decision
     int64_t drow = static_cast<int64_t>(loc.tok) * p.H + loc.h;
     bool skip = !valid;
     if constexpr (kMode == kEncScatter) {
       if (valid) {
+        const int64_t slot = LDX(p.slot_ids + loc.tok);
         if (slot < 0) {
           skip = true;
         } else if (slot >= p.num_slots) {
@@ -168,7 +177,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(cons
         for (int j = 0; j < BPL; ++j) store16B(cp + 16 * j, c8[j]);
         if (li == 0) STX(d.rscale + drow, rs);
       }
-      return;
+#pragma unroll
+      for (int j = 0; j < BPL; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[j][i] = nw[j][i];
+      continue;
     }
     const float rs = __fdiv_rn(amax, kE2M1Max * kE4M3Max);
     const float rinv = (rs != 0.0f) ? __frcp_rn(rs) : 0.0f;
@@ -196,26 +209,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_encode_kernel(cons
       }
       if (li == 0) STX(d.rscale + drow, rs);
     }
-  };
 
-  // Two register sets alternate: the next row's loads (and slot id) are issued before
-  // this row's arithmetic, with no copies between iterations.  The loop bound is
-  // uniform across the warp (row - sub is), so every lane runs every shuffle.
-  uint32_t wa[BPL][8], wb[BPL][8];
 #pragma unroll
-  for (int j = 0; j < BPL; ++j)
+    for (int j = 0; j < BPL; ++j)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wa[j][i] = wb[j][i] = 0u;
-  int64_t sa = 0, sb = 0;
-  fetch(row, wa, sa);
-  while (row - sub < total) {
-    fetch(row + stride, wb, sb);
-    body(row, wa, sa);
-    row += stride;
-    if (row - sub >= total) break;
-    fetch(row + stride, wa, sa);
-    body(row, wb, sb);
-    row += stride;
+      for (int i = 0; i < 8; ++i) w[j][i] = nw[j][i];
   }
 }
 
