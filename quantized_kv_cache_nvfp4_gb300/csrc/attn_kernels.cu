@@ -9,17 +9,25 @@
 // One query token per sequence; query head qh reads KV head qh / group:
 //   o[s][qh] = softmax_t(scale * q . k_t) . v_t   over tokens t < seq_lens[s].
 //
-// Mapping (mma.sync m16n8k16, f16 operands, f32 accumulators).  A CTA takes one
-// (split of a sequence's tokens, KV head, sequence); its 4 warps take 16-token tiles
-// in turn, each through its own cp.async ring of pool tiles in shared memory.
-//  * M = the group's query heads (padded to 16): a warp's S = Q K^T tile is 16 heads
-//    x 16 tokens, and its P feeds P V directly as the A operand.
-//  * Q K^T contracts over the head dimension in a permuted order: k-step kb of lane c
+// Mapping (mma.sync m16n8k16, f16 operands, f32 accumulators), token-major.  A CTA
+// takes one (split of a sequence's tokens, KV head, sequence); its 4 warps take
+// 16-token tiles in turn, each through its own cp.async ring of pool tiles in shared
+// memory.
+//  * M = the tile's 16 tokens, N = the group's query heads in n-tiles of 8 (one for
+//    groups up to 8, two up to 16): a warp computes S^T = K Q^T, 16 tokens x 8 heads
+//    per n-tile, with K as the A operand, so no MMA row is padding.
+//  * S^T contracts over the head dimension in a permuted order: k-step kb of lane c
 //    (c = lane % 4) covers dims c*D/4 + 4kb .. + 3, so a lane's K operand for one token
-//    is one contiguous run of code bytes; Q is permuted the same way.
-//  * P V writes column n of n-tile nt to dim n*D/8 + nt, so a lane's V operand for
-//    one token is again one contiguous run; the nibbles (or bytes) of the two tokens a
-//    register pairs are interleaved by a mask-and-shift (or byte-permute) transpose.
+//    is one contiguous run of code bytes; Q^T is permuted the same way and stays in
+//    registers when its fragments fit in 16 of them (D = 64, or D = 128 with one
+//    n-tile), else it is read from shared memory per k-step.
+//  * The probabilities leave the S^T accumulators in the C layout (a lane holds two
+//    heads of tokens g and g + 8); an 8x8 transpose in registers (movmatrix) turns
+//    them into the B operand of O^T = V^T P^T (two tokens of one head).
+//  * O^T: m-tile mt, rows g and g + 8 = dims g*D/8 + 2mt and + 1, so a lane's V operand
+//    for one token is again one contiguous run; the nibbles (or bytes) of the two
+//    tokens a register pairs are interleaved by a mask-and-shift (or byte-permute)
+//    transpose.
 //  * K and V decode exactly to f16: e2m1 x e4m3 has at most 2 x 4 significant bits,
 //    and e4m3 fits f16.  K's FP32 row scale multiplies the score; V's multiplies P
 //    relative to a reference R of the tile row scales.  R and the softmax reference m
@@ -180,11 +188,21 @@ __device__ __forceinline__ void lds_words(const unsigned char* p, uint32_t (&w)[
   }
 }
 
-template <int D, int kFK, int kFV>
+// Transpose of an 8x8 f16 matrix held as one m16n8 fragment quarter: lane (g, c) gives
+// row g, columns 2c and 2c + 1, and receives row g, columns 2c and 2c + 1 of the
+// transpose.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+template <int D, int kFK, int kFV, int kNH>
 __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnParams p) {
   using T = AttnTile<D, kFK, kFV>;
-  constexpr int kKS = D / 16;  // Q K^T k-steps
-  constexpr int kNT = D / 8;   // P V n-tiles
+  constexpr int kKS = D / 16;  // k-steps of S^T = K Q^T
+  constexpr int kMT = D / 16;  // m-tiles of O^T = V^T P^T
+  constexpr bool kQReg = kNH * kKS <= 8;  // Q^T fragments kept in registers
   extern __shared__ __align__(16) unsigned char smem[];
 
   const int lane = threadIdx.x & 31;
@@ -200,15 +218,14 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   const int ntile = t_end > t_begin ? (t_end - t_begin + 15) / 16 : 0;
   if (bad_len && threadIdx.x == 0 && split == 0 && h == 0) set_status(p.status, 8u);
 
-  // ---- Q fragments (rows g and g + 8 of the group, scaled by 2^k into f16) and the
-  // per-row score factors, built once by warp 0 into shared memory ----
-  uint4* const qfrag = reinterpret_cast<uint4*>(smem);                   // [D/16][32 lanes]
-  float* const qfac = reinterpret_cast<float*>(smem + (D / 16) * 32 * 16);  // [16 rows]
+  // ---- Q^T fragments (query head 8nh + g of the group, scaled by 2^k into f16) and
+  // the per-head score factors, built once by warp 0 into shared memory ----
+  uint2* const qfrag = reinterpret_cast<uint2*>(smem);                         // [nh][k-step][32 lanes]
+  float* const qfac = reinterpret_cast<float*>(smem + kNH * kKS * 32 * 8);  // [8 kNH heads]
   if (warp == 0) {
-    uint32_t qa[kKS][4];
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int row = g + 8 * hr;
+    for (int nh = 0; nh < kNH; ++nh) {
+      const int row = 8 * nh + g;
       uint32_t w[D / 8];  // this lane's D/4 dims as bf16 pairs
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) w[i] = 0u;
@@ -236,16 +253,33 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
       const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
       if (c == 0) qfac[row] = p.scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
 #pragma unroll
-      for (int kb = 0; kb < kKS; ++kb) {
-        qa[kb][hr] = f32x2_to_f16x2(bf16lo(w[2 * kb]) * up, bf16hi(w[2 * kb]) * up);              // dims 4kb, +1
-        qa[kb][2 + hr] = f32x2_to_f16x2(bf16lo(w[2 * kb + 1]) * up, bf16hi(w[2 * kb + 1]) * up);  // dims 4kb+2, +3
-      }
+      for (int kb = 0; kb < kKS; ++kb)
+        qfrag[(nh * kKS + kb) * 32 + lane] =
+            make_uint2(f32x2_to_f16x2(bf16lo(w[2 * kb]) * up, bf16hi(w[2 * kb]) * up),            // dims 4kb, +1
+                       f32x2_to_f16x2(bf16lo(w[2 * kb + 1]) * up, bf16hi(w[2 * kb + 1]) * up));  // dims 4kb+2, +3
     }
-#pragma unroll
-    for (int kb = 0; kb < kKS; ++kb) qfrag[kb * 32 + lane] = make_uint4(qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3]);
   }
   __syncthreads();
-  const float qmul[2] = {qfac[g], qfac[g + 8]};
+  float qmul[kNH][2];  // heads 8nh + 2c, + 1
+#pragma unroll
+  for (int nh = 0; nh < kNH; ++nh) {
+    qmul[nh][0] = qfac[8 * nh + 2 * c];
+    qmul[nh][1] = qfac[8 * nh + 2 * c + 1];
+  }
+  uint2 qreg[kQReg ? kNH : 1][kQReg ? kKS : 1];
+  if constexpr (kQReg) {
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int kb = 0; kb < kKS; ++kb) qreg[nh][kb] = qfrag[(nh * kKS + kb) * 32 + lane];
+  }
+  auto qb = [&](int nh, int kb) -> uint2 {
+    if constexpr (kQReg) {
+      return qreg[nh][kb];
+    } else {
+      return qfrag[(nh * kKS + kb) * 32 + lane];
+    }
+  };
 
   // ---- the warp's tiles through its cp.async ring ----
   unsigned char* const ring = smem + T::kQ + warp * T::kStages * T::kBytes;
@@ -294,10 +328,20 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     }
   };
 
-  float m[2] = {kNegInf, kNegInf}, l[2] = {0.0f, 0.0f}, R = 0.0f, rR = 0.0f;
-  float o[kNT][4];
+  // per head (8nh + 2c + e): softmax reference m and partial sum l of this lane's tokens
+  float m[kNH][2], l[kNH][2], R = 0.0f, rR = 0.0f;
+  // O^T accumulators: o[mt][nh] = dims g*D/8 + 2mt (e = 0, 1) and + 1 (e = 2, 3) of
+  // heads 8nh + 2c (e even) and + 1 (e odd), relative to R
+  float o[kMT][kNH][4];
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
+  for (int nh = 0; nh < kNH; ++nh) {
+    m[nh][0] = m[nh][1] = kNegInf;
+    l[nh][0] = l[nh][1] = 0.0f;
+  }
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) o[mt][nh][0] = o[mt][nh][1] = o[mt][nh][2] = o[mt][nh][3] = 0.0f;
 
 #pragma unroll
   for (int j = 0; j < T::kStages - 1; ++j) {
@@ -312,22 +356,25 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     const unsigned char* const sb = ring + (it % T::kStages) * T::kBytes;
     const int t0 = t_begin + (warp + it * kAttnWarps) * 16;
 
-    // S = Q K^T over the 16 tokens: n-tile j holds tokens 8j .. 8j + 7 (this lane
-    // supplies token 8j + g); each Q fragment is read once for both n-tiles
-    float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    // S^T = K Q^T: rows g and g + 8 are tokens g and 8 + g (this lane's K rows), each
+    // K fragment serves every head n-tile
+    float sc[kNH][4];
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) sc[nh][0] = sc[nh][1] = sc[nh][2] = sc[nh][3] = 0.0f;
     if constexpr (kFK == 3) {
       uint32_t kw[2][D / 16];  // this lane's D/4 code bytes of tokens g and 8 + g
       lds_words<D / 16>(sb + T::kOffKC + g * T::kSK + c * (D / 4), kw[0]);
       lds_words<D / 16>(sb + T::kOffKC + (8 + g) * T::kSK + c * (D / 4), kw[1]);
 #pragma unroll
       for (int kb = 0; kb < kKS; ++kb) {
-        const uint4 qv = qfrag[kb * 32 + lane];
-        const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint32_t k0[2], k1[2];
+        e4m3x4_to_f16x2(kw[0][kb], k0);  // dims 4kb, 4kb+1 | 4kb+2, 4kb+3
+        e4m3x4_to_f16x2(kw[1][kb], k1);
+        const uint32_t a[4] = {k0[0], k1[0], k0[1], k1[1]};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t b2[2];
-          e4m3x4_to_f16x2(kw[j][kb], b2);  // dims 4kb, 4kb+1 | 4kb+2, 4kb+3
-          mma_f16_16816(sc[j], qa, b2[0], b2[1]);
+        for (int nh = 0; nh < kNH; ++nh) {
+          const uint2 b = qb(nh, kb);
+          mma_f16_16816(sc[nh], a, b.x, b.y);
         }
       }
     } else {
@@ -356,85 +403,96 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
         }
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
-          const int kb = 2 * wi + hs;
-          const uint4 qv = qfrag[kb * 32 + lane];
-          const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+          const uint32_t a[4] = {hk[0][2 * hs], hk[1][2 * hs], hk[0][2 * hs + 1], hk[1][2 * hs + 1]};
 #pragma unroll
-          for (int j = 0; j < 2; ++j) mma_f16_16816(sc[j], qa, hk[j][2 * hs], hk[j][2 * hs + 1]);
+          for (int nh = 0; nh < kNH; ++nh) {
+            const uint2 b = qb(nh, 2 * wi + hs);
+            mma_f16_16816(sc[nh], a, b.x, b.y);
+          }
         }
       }
     }
     // scores times K's row scale; the query factor (scale, log2 e, Q's power of two,
-    // positive) enters with the reference in one FMA below, and the row maxima are
-    // scaled by it once.  Tokens past the end are masked (only a split's last tile can
-    // hold any).
-    const float2* krs = reinterpret_cast<const float2*>(sb + T::kOffKR);
-    const float2* vrs = reinterpret_cast<const float2*>(sb + T::kOffVR);
-    float rv[2][2];
-    float mt[2] = {kNegInf, kNegInf};
+    // positive) enters with the reference in one FMA below, and the maxima are scaled
+    // by it once.  Tokens past the end are masked (only a split's last tile can hold
+    // any).
+    const float* krs = reinterpret_cast<const float*>(sb + T::kOffKR);
+    const float* vrs = reinterpret_cast<const float*>(sb + T::kOffVR);
+    const float kr0 = krs[g], kr1 = krs[g + 8];
+    const float vr0 = vrs[g], vr1 = vrs[g + 8];
     const bool partial = t0 + 16 > t_end;  // uniform across the warp
+    const bool dead0 = partial && t0 + g >= t_end, dead1 = partial && t0 + g + 8 >= t_end;
+    float mt[kNH][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float2 kr = krs[4 * j + c], vr = vrs[4 * j + c];  // tokens 8j + 2c, + 1
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = 8 * j + 2 * c + (e & 1);
-        float v = sc[j][e] * ((e & 1) ? kr.y : kr.x);
-        if (partial && t0 + tok >= t_end) v = kNegInf;
-        sc[j][e] = v;
-        mt[e >> 1] = fmaxf(mt[e >> 1], v);
-      }
-      rv[j][0] = vr.x;
-      rv[j][1] = vr.y;
+    for (int nh = 0; nh < kNH; ++nh) {
+      sc[nh][0] = dead0 ? kNegInf : sc[nh][0] * kr0;
+      sc[nh][1] = dead0 ? kNegInf : sc[nh][1] * kr0;
+      sc[nh][2] = dead1 ? kNegInf : sc[nh][2] * kr1;
+      sc[nh][3] = dead1 ? kNegInf : sc[nh][3] * kr1;
+      mt[nh][0] = fmaxf(sc[nh][0], sc[nh][2]);
+      mt[nh][1] = fmaxf(sc[nh][1], sc[nh][3]);
     }
-    mt[0] *= qmul[0];
-    mt[1] *= qmul[1];
-    float rmax = fmaxf(fmaxf(rv[0][0], rv[0][1]), fmaxf(rv[1][0], rv[1][1]));
+    float rmax = fmaxf(vr0, vr1);
 #pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-      mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xFFFFFFFFu, mt[0], off));
-      mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xFFFFFFFFu, mt[1], off));
+    for (int off = 4; off <= 16; off <<= 1) {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh) {
+        mt[nh][0] = fmaxf(mt[nh][0], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][0], off));
+        mt[nh][1] = fmaxf(mt[nh][1], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][1], off));
+      }
       rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
     }
-    // references: the softmax reference m per row and the V row-scale reference R move
-    // only when a tile exceeds them by more than 2^8 and 2^6, so P' = exp2(s - m) *
-    // rs_v / R stays below 2^14 (f16 holds it) and O is rescaled on few tiles
-    if (__any_sync(0xFFFFFFFFu, mt[0] > m[0] + 8.0f || mt[1] > m[1] + 8.0f || rmax > R * 64.0f)) {
-      const float mn0 = fmaxf(m[0], mt[0]), mn1 = fmaxf(m[1], mt[1]);
-      const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
-      const float a0 = ex2(m[0] - mn0), a1 = ex2(m[1] - mn1);  // 0 while m is -inf
-      const float rr = R / Rn;
-      const float f0 = a0 * rr, f1 = a1 * rr;
+    bool move = rmax > R * 64.0f;
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        o[nt][0] *= f0;
-        o[nt][1] *= f0;
-        o[nt][2] *= f1;
-        o[nt][3] *= f1;
+    for (int nh = 0; nh < kNH; ++nh) {
+      mt[nh][0] *= qmul[nh][0];
+      mt[nh][1] *= qmul[nh][1];
+      move = move || mt[nh][0] > m[nh][0] + 8.0f || mt[nh][1] > m[nh][1] + 8.0f;
+    }
+    // references: the softmax reference m per head and the V row-scale reference R
+    // move only when a tile exceeds them by more than 2^8 and 2^6, so P' = exp2(s - m)
+    // * rs_v / R stays below 2^14 (f16 holds it) and O is rescaled on few tiles
+    if (__any_sync(0xFFFFFFFFu, move)) {
+      const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
+      const float rr = R / Rn;
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float mn = fmaxf(m[nh][e], mt[nh][e]);
+          const float a = ex2(m[nh][e] - mn);  // 0 while m is -inf
+          const float f = a * rr;
+#pragma unroll
+          for (int q = 0; q < kMT; ++q) {
+            o[q][nh][e] *= f;
+            o[q][nh][e + 2] *= f;
+          }
+          l[nh][e] *= a;
+          m[nh][e] = mn;
+        }
       }
-      l[0] *= a0;
-      l[1] *= a1;
-      m[0] = mn0;
-      m[1] = mn1;
       R = Rn;
       rR = rcp_approx(Rn);
     }
-    // P' = exp2(s - m) * rs_v / R as the A operand of P V
-    uint32_t pa[4];
+    // P'^T = exp2(s - m) * rs_v / R, transposed in registers into the B operand of
+    // O^T += V^T P'^T: pb[nh][0] holds tokens 2c, 2c + 1 of head 8nh + g, pb[nh][1]
+    // tokens 2c + 8, 2c + 9
+    const float r0 = vr0 * rR, r1 = vr1 * rR;
+    uint32_t pb[kNH][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float p0 = ex2(__fmaf_rn(sc[j][0], qmul[0], -m[0])), p1 = ex2(__fmaf_rn(sc[j][1], qmul[0], -m[0]));
-      const float p2 = ex2(__fmaf_rn(sc[j][2], qmul[1], -m[1])), p3 = ex2(__fmaf_rn(sc[j][3], qmul[1], -m[1]));
-      l[0] += p0 + p1;
-      l[1] += p2 + p3;
-      const float r0 = rv[j][0] * rR, r1 = rv[j][1] * rR;
-      pa[2 * j] = f32x2_to_f16x2(p0 * r0, p1 * r1);      // row g, tokens 8j + 2c, +1
-      pa[2 * j + 1] = f32x2_to_f16x2(p2 * r0, p3 * r1);  // row g + 8
+    for (int nh = 0; nh < kNH; ++nh) {
+      const float p0 = ex2(__fmaf_rn(sc[nh][0], qmul[nh][0], -m[nh][0]));  // token g
+      const float p1 = ex2(__fmaf_rn(sc[nh][1], qmul[nh][1], -m[nh][1]));
+      const float p2 = ex2(__fmaf_rn(sc[nh][2], qmul[nh][0], -m[nh][0]));  // token g + 8
+      const float p3 = ex2(__fmaf_rn(sc[nh][3], qmul[nh][1], -m[nh][1]));
+      l[nh][0] += p0 + p2;
+      l[nh][1] += p1 + p3;
+      pb[nh][0] = transpose8x8(f32x2_to_f16x2(p0 * r0, p1 * r0));
+      pb[nh][1] = transpose8x8(f32x2_to_f16x2(p2 * r1, p3 * r1));
     }
-    // O += P' V: n-tile nt, column n = dim n * D/8 + nt; this lane supplies V for
-    // tokens (2c, 2c + 1) and (2c + 8, 2c + 9) at dims g * D/8 + nt
+    // O^T += V^T P'^T: m-tile mt, rows g and g + 8 = dims g * D/8 + 2mt and + 1; this
+    // lane supplies V for tokens (2c, 2c + 1) and (2c + 8, 2c + 9) at those dims
     {
-      // the two token pairs of this lane
       const int ta0 = 2 * c, ta1 = 2 * c + 8;
       if constexpr (kFV == 3) {
         uint32_t v0[D / 32], v1[D / 32], v2[D / 32], v3[D / 32];  // D/8 bytes of each token
@@ -443,14 +501,15 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
         lds_words<D / 32>(sb + T::kOffVC + ta1 * T::kSV + g * (D / 8), v2);
         lds_words<D / 32>(sb + T::kOffVC + (ta1 + 1) * T::kSV + g * (D / 8), v3);
 #pragma unroll
-        for (int np = 0; np < kNT / 2; ++np) {  // n-tiles 2np, 2np + 1: bytes of one half word
-          const int wd = np / 2, bo2 = 2 * (np % 2);
+        for (int q = 0; q < kMT; ++q) {  // dims 2q, 2q + 1: bytes of one half word
+          const int wd = q / 2, bo2 = 2 * (q % 2);
           const uint32_t sel = bo2 | ((4 + bo2) << 4) | ((bo2 + 1) << 8) | ((5 + bo2) << 12);
           uint32_t h01[2], h23[2];
           e4m3x4_to_f16x2(__byte_perm(v0[wd], v1[wd], sel), h01);
           e4m3x4_to_f16x2(__byte_perm(v2[wd], v3[wd], sel), h23);
-          mma_f16_16816(o[2 * np], pa, h01[0], h23[0]);
-          mma_f16_16816(o[2 * np + 1], pa, h01[1], h23[1]);
+          const uint32_t a[4] = {h01[0], h01[1], h23[0], h23[1]};
+#pragma unroll
+          for (int nh = 0; nh < kNH; ++nh) mma_f16_16816(o[q][nh], a, pb[nh][0], pb[nh][1]);
         }
       } else {
         constexpr int kW = D / 64;  // code words per lane per token (D/16 bytes)
@@ -473,7 +532,7 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 #pragma unroll
         for (int i = 0; i < kW; ++i) {
           // nibble transpose: X byte b = (dim 2(4i+b) of token a | the same dim of token
-          // b << 4), Y: the odd dims; then byte b of X / Y is n-tile 8i + 2b / 8i + 2b + 1
+          // b << 4), Y: the odd dims; then byte b of X / Y is m-tile 4i + b, row g / g + 8
           const uint32_t x01 = (v0[i] & 0x0F0F0F0Fu) | ((v1[i] & 0x0F0F0F0Fu) << 4);
           const uint32_t y01 = ((v0[i] >> 4) & 0x0F0F0F0Fu) | (v1[i] & 0xF0F0F0F0u);
           const uint32_t x23 = (v2[i] & 0x0F0F0F0Fu) | ((v3[i] & 0x0F0F0F0Fu) << 4);
@@ -485,10 +544,12 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
           e2m1x8_to_f16x2(y23, hy23);
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
-            const int nt = 8 * i + 2 * bb;  // and nt + 1: one 16-block for both
-            const int q = kVB == 1 ? 0 : nt / 16;  // g * D/8 is a multiple of 16 when D = 256
-            mma_f16_16816(o[nt], pa, hmul2(hx01[bb], bs01[q]), hmul2(hx23[bb], bs23[q]));
-            mma_f16_16816(o[nt + 1], pa, hmul2(hy01[bb], bs01[q]), hmul2(hy23[bb], bs23[q]));
+            const int q = 4 * i + bb;             // m-tile: dims 2q, 2q + 1, one 16-block
+            const int vb = kVB == 1 ? 0 : q / 8;  // g * D/8 is a multiple of 16 when D = 256
+            const uint32_t a[4] = {hmul2(hx01[bb], bs01[vb]), hmul2(hy01[bb], bs01[vb]),
+                                   hmul2(hx23[bb], bs23[vb]), hmul2(hy23[bb], bs23[vb])};
+#pragma unroll
+            for (int nh = 0; nh < kNH; ++nh) mma_f16_16816(o[q][nh], a, pb[nh][0], pb[nh][1]);
           }
         }
       }
@@ -499,28 +560,38 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   }
   cp_async_wait<0>();
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, 2u);
-  l[0] += __shfl_xor_sync(0xFFFFFFFFu, l[0], 1);
-  l[0] += __shfl_xor_sync(0xFFFFFFFFu, l[0], 2);
-  l[1] += __shfl_xor_sync(0xFFFFFFFFu, l[1], 1);
-  l[1] += __shfl_xor_sync(0xFFFFFFFFu, l[1], 2);
+  // row sums over the 8 lanes (tokens) of each head
+#pragma unroll
+  for (int off = 4; off <= 16; off <<= 1)
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) {
+      l[nh][0] += __shfl_xor_sync(0xFFFFFFFFu, l[nh][0], off);
+      l[nh][1] += __shfl_xor_sync(0xFFFFFFFFu, l[nh][1], off);
+    }
   const bool cta_bad = __syncthreads_or(bad ? 1 : 0) != 0 || bad_len;  // the ring is free after this
 
-  // per warp: O (true scale: O * R) by natural dim, and m, l per row
-  float* const mo = reinterpret_cast<float*>(smem + T::kQ) + warp * 16 * (D + 2);
+  // per warp: O (true scale: O * R) by head and natural dim, and m, l per head
+  constexpr int kHeads = 8 * kNH;
+  float* const mo = reinterpret_cast<float*>(smem + T::kQ) + warp * kHeads * (D + 2);
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
+  for (int q = 0; q < kMT; ++q)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = g + 8 * (e >> 1);
-      const int n = 2 * c + (e & 1);
-      mo[row * (D + 2) + n * (D / 8) + nt] = o[nt][e] * R;
-    }
-  }
-  if (c == 0) {
-    mo[g * (D + 2) + D] = m[0];
-    mo[g * (D + 2) + D + 1] = l[0];
-    mo[(g + 8) * (D + 2) + D] = m[1];
-    mo[(g + 8) * (D + 2) + D + 1] = l[1];
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = 8 * nh + 2 * c + (e & 1);
+        const int d = g * (D / 8) + 2 * q + (e >> 1);
+        mo[head * (D + 2) + d] = o[q][nh][e] * R;
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int head = 8 * nh + 2 * c + e;
+        mo[head * (D + 2) + D] = m[nh][e];
+        mo[head * (D + 2) + D + 1] = l[nh][e];
+      }
   }
   __syncthreads();
   const float* const mall = reinterpret_cast<const float*>(smem + T::kQ);
@@ -528,14 +599,14 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     const int row = idx / D, d = idx % D;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[(w * 16 + row) * (D + 2) + D]);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[(w * kHeads + row) * (D + 2) + D]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float mw = mall[(w * 16 + row) * (D + 2) + D];
+      const float mw = mall[(w * kHeads + row) * (D + 2) + D];
       const float f = mw == kNegInf ? 0.0f : ex2(mw - M);
-      L += mall[(w * 16 + row) * (D + 2) + D + 1] * f;
-      O += mall[(w * 16 + row) * (D + 2) + d] * f;
+      L += mall[(w * kHeads + row) * (D + 2) + D + 1] * f;
+      O += mall[(w * kHeads + row) * (D + 2) + d] * f;
     }
     const int qh = h * p.group + row;
     if (p.nsplit == 1) {
@@ -581,10 +652,10 @@ __global__ void __launch_bounds__(D) decode_attn_merge_kernel(const AttnParams p
       static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu));
 }
 
-template <int D, int kFK, int kFV>
+template <int D, int kFK, int kFV, int kNH>
 cudaError_t attn_launch(const AttnParams& p, cudaStream_t s) {
   using T = AttnTile<D, kFK, kFV>;
-  auto k = decode_attn_kernel<D, kFK, kFV>;
+  auto k = decode_attn_kernel<D, kFK, kFV, kNH>;
   if (T::kSmem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
     if (e != cudaSuccess) return e;
@@ -598,13 +669,19 @@ cudaError_t attn_launch(const AttnParams& p, cudaStream_t s) {
   return e;
 }
 
-template <int D>
+template <int D, int kNH>
 cudaError_t attn_dispatch_fmt(const AttnParams& p, cudaStream_t s) {
   const bool k8 = p.fmt_k == 3, v8 = p.fmt_v == 3;
-  if (!k8 && !v8) return attn_launch<D, 1, 1>(p, s);
-  if (k8 && !v8) return attn_launch<D, 3, 1>(p, s);
-  if (!k8 && v8) return attn_launch<D, 1, 3>(p, s);
-  return attn_launch<D, 3, 3>(p, s);
+  if (!k8 && !v8) return attn_launch<D, 1, 1, kNH>(p, s);
+  if (k8 && !v8) return attn_launch<D, 3, 1, kNH>(p, s);
+  if (!k8 && v8) return attn_launch<D, 1, 3, kNH>(p, s);
+  return attn_launch<D, 3, 3, kNH>(p, s);
+}
+
+// Query heads per KV head: one n-tile of 8 heads, or two for 9 to 16.
+template <int D>
+cudaError_t attn_dispatch_group(const AttnParams& p, cudaStream_t s) {
+  return p.group <= 8 ? attn_dispatch_fmt<D, 1>(p, s) : attn_dispatch_fmt<D, 2>(p, s);
 }
 
 }  // namespace
@@ -654,9 +731,9 @@ int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len) {
 
 cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s) {
   switch (p.D) {
-    case 64: return attn_dispatch_fmt<64>(p, s);
-    case 128: return attn_dispatch_fmt<128>(p, s);
-    case 256: return attn_dispatch_fmt<256>(p, s);
+    case 64: return attn_dispatch_group<64>(p, s);
+    case 128: return attn_dispatch_group<128>(p, s);
+    case 256: return attn_dispatch_group<256>(p, s);
   }
   return cudaErrorInvalidValue;
 }
