@@ -101,6 +101,14 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// The same with results below 2^-126 flushed to zero: used for probabilities, whose
+// row sum is at least 1, so a flushed term is below the sum's own rounding.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -309,15 +317,24 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     unsigned char* const sb = ring + st * T::kBytes;
     const int tt = lane & 15;
     constexpr int kPK = T::kCK / 16, kPV = T::kCV / 16;
+    if constexpr (kPK == kPV) {  // the same piece of K and V: one row exchange for both
 #pragma unroll
-    for (int i = lane; i < 16 * kPK; i += 32) {
-      const int64_t rr = shfl64(row, i / kPK);
-      cp_async16(sb + T::kOffKC + (i / kPK) * T::kSK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
-    }
+      for (int i = lane; i < 16 * kPK; i += 32) {
+        const int64_t rr = shfl64(row, i / kPK);
+        cp_async16(sb + T::kOffKC + (i / kPK) * T::kSK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
+        cp_async16(sb + T::kOffVC + (i / kPV) * T::kSV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
+      }
+    } else {
 #pragma unroll
-    for (int i = lane; i < 16 * kPV; i += 32) {
-      const int64_t rr = shfl64(row, i / kPV);
-      cp_async16(sb + T::kOffVC + (i / kPV) * T::kSV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
+      for (int i = lane; i < 16 * kPK; i += 32) {
+        const int64_t rr = shfl64(row, i / kPK);
+        cp_async16(sb + T::kOffKC + (i / kPK) * T::kSK + (i % kPK) * 16, p.k.codes + rr * T::kCK + (i % kPK) * 16);
+      }
+#pragma unroll
+      for (int i = lane; i < 16 * kPV; i += 32) {
+        const int64_t rr = shfl64(row, i / kPV);
+        cp_async16(sb + T::kOffVC + (i / kPV) * T::kSV + (i % kPV) * 16, p.v.codes + rr * T::kCV + (i % kPV) * 16);
+      }
     }
     if (lane < 16) {
       if constexpr (T::kBK > 0) cp_async_n<T::kBK>(sb + T::kOffKB + tt * T::kBK, p.k.bscale + row * T::kBK);
@@ -329,13 +346,13 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
   };
 
   // per head (8nh + 2c + e): softmax reference m and partial sum l of this lane's tokens
-  float m[kNH][2], l[kNH][2], R = 0.0f, rR = 0.0f;
+  float m[kNH][2], m8[kNH][2], l[kNH][2], R = 0.0f, R64 = 0.0f, rR = 0.0f;  // m8 = m + 8, R64 = 64 R
   // O^T accumulators: o[mt][nh] = dims g*D/8 + 2mt (e = 0, 1) and + 1 (e = 2, 3) of
   // heads 8nh + 2c (e even) and + 1 (e odd), relative to R
   float o[kMT][kNH][4];
 #pragma unroll
   for (int nh = 0; nh < kNH; ++nh) {
-    m[nh][0] = m[nh][1] = kNegInf;
+    m[nh][0] = m[nh][1] = m8[nh][0] = m8[nh][1] = kNegInf;
     l[nh][0] = l[nh][1] = 0.0f;
   }
 #pragma unroll
@@ -386,10 +403,16 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint8_t* kbs = sb + T::kOffKB + (8 * j + g) * T::kBK + c * (D / 64);
+        if constexpr (kNB == 1) {
+          const uint32_t bsh = e4m3_to_f16x2(kbs[0]) & 0xFFFFu;
+          bsb[j][0] = bsh | (bsh << 16);
+        } else {  // pairs of scale bytes, one conversion each, halves spread by a permute
 #pragma unroll
-        for (int i = 0; i < kNB; ++i) {
-          const uint32_t bsh = e4m3_to_f16x2(kbs[i]) & 0xFFFFu;
-          bsb[j][i] = bsh | (bsh << 16);
+          for (int i = 0; i < kNB; i += 2) {
+            const uint32_t two = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kbs + i));
+            bsb[j][i] = __byte_perm(two, 0u, 0x1010);
+            bsb[j][i + 1] = __byte_perm(two, 0u, 0x3232);
+          }
         }
       }
 #pragma unroll
@@ -422,37 +445,35 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     const float vr0 = vrs[g], vr1 = vrs[g + 8];
     const bool partial = t0 + 16 > t_end;  // uniform across the warp
     const bool dead0 = partial && t0 + g >= t_end, dead1 = partial && t0 + g + 8 >= t_end;
+    // this lane's maxima (two tokens per head) first: the references move when any
+    // lane's exceed them, and only then are the tile's maxima reduced across lanes
     float mt[kNH][2];
+    bool move = false;
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh) {
       sc[nh][0] = dead0 ? kNegInf : sc[nh][0] * kr0;
       sc[nh][1] = dead0 ? kNegInf : sc[nh][1] * kr0;
       sc[nh][2] = dead1 ? kNegInf : sc[nh][2] * kr1;
       sc[nh][3] = dead1 ? kNegInf : sc[nh][3] * kr1;
-      mt[nh][0] = fmaxf(sc[nh][0], sc[nh][2]);
-      mt[nh][1] = fmaxf(sc[nh][1], sc[nh][3]);
+      mt[nh][0] = fmaxf(sc[nh][0], sc[nh][2]) * qmul[nh][0];
+      mt[nh][1] = fmaxf(sc[nh][1], sc[nh][3]) * qmul[nh][1];
+      move = move || mt[nh][0] > m8[nh][0] || mt[nh][1] > m8[nh][1];
     }
     float rmax = fmaxf(vr0, vr1);
-#pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
-#pragma unroll
-      for (int nh = 0; nh < kNH; ++nh) {
-        mt[nh][0] = fmaxf(mt[nh][0], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][0], off));
-        mt[nh][1] = fmaxf(mt[nh][1], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][1], off));
-      }
-      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
-    }
-    bool move = rmax > R * 64.0f;
-#pragma unroll
-    for (int nh = 0; nh < kNH; ++nh) {
-      mt[nh][0] *= qmul[nh][0];
-      mt[nh][1] *= qmul[nh][1];
-      move = move || mt[nh][0] > m[nh][0] + 8.0f || mt[nh][1] > m[nh][1] + 8.0f;
-    }
+    move = move || rmax > R64;
     // references: the softmax reference m per head and the V row-scale reference R
     // move only when a tile exceeds them by more than 2^8 and 2^6, so P' = exp2(s - m)
     // * rs_v / R stays below 2^14 (f16 holds it) and O is rescaled on few tiles
     if (__any_sync(0xFFFFFFFFu, move)) {
+#pragma unroll
+      for (int off = 4; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh) {
+          mt[nh][0] = fmaxf(mt[nh][0], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][0], off));
+          mt[nh][1] = fmaxf(mt[nh][1], __shfl_xor_sync(0xFFFFFFFFu, mt[nh][1], off));
+        }
+        rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
+      }
       const float Rn = fmaxf(fmaxf(R, rmax), 0x1p-126f);
       const float rr = R / Rn;
 #pragma unroll
@@ -469,9 +490,11 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
           }
           l[nh][e] *= a;
           m[nh][e] = mn;
+          m8[nh][e] = mn + 8.0f;
         }
       }
       R = Rn;
+      R64 = Rn * 64.0f;
       rR = rcp_approx(Rn);
     }
     // P'^T = exp2(s - m) * rs_v / R, transposed in registers into the B operand of
@@ -481,10 +504,10 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     uint32_t pb[kNH][2];
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh) {
-      const float p0 = ex2(__fmaf_rn(sc[nh][0], qmul[nh][0], -m[nh][0]));  // token g
-      const float p1 = ex2(__fmaf_rn(sc[nh][1], qmul[nh][1], -m[nh][1]));
-      const float p2 = ex2(__fmaf_rn(sc[nh][2], qmul[nh][0], -m[nh][0]));  // token g + 8
-      const float p3 = ex2(__fmaf_rn(sc[nh][3], qmul[nh][1], -m[nh][1]));
+      const float p0 = ex2_ftz(__fmaf_rn(sc[nh][0], qmul[nh][0], -m[nh][0]));  // token g
+      const float p1 = ex2_ftz(__fmaf_rn(sc[nh][1], qmul[nh][1], -m[nh][1]));
+      const float p2 = ex2_ftz(__fmaf_rn(sc[nh][2], qmul[nh][0], -m[nh][0]));  // token g + 8
+      const float p3 = ex2_ftz(__fmaf_rn(sc[nh][3], qmul[nh][1], -m[nh][1]));
       l[nh][0] += p0 + p2;
       l[nh][1] += p1 + p3;
       pb[nh][0] = transpose8x8(f32x2_to_f16x2(p0 * r0, p1 * r0));
