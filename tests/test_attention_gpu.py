@@ -75,7 +75,7 @@ def _check(out, ref, v, lens, group):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("group", [1, 4, 7, 16])
+@pytest.mark.parametrize("group", [1, 4, 7, 8, 9, 16])  # one head n-tile up to 8, two from 9
 def test_matches_oracle_nvfp4(D, group):
     lens = [1, 37, 200, 0, 16]
     pool, table, lt, q, v, Tmax = _case(5, 2, group, D, lens, seed=D + group)
@@ -90,16 +90,18 @@ def test_matches_oracle_nvfp4(D, group):
 
 @pytest.mark.parametrize("fmt_k,fmt_v", [(F8, F8), (F8, NV), (NV, F8)])
 @pytest.mark.parametrize("D", [64, 128, 256])
-def test_matches_oracle_fp8_and_split_formats(fmt_k, fmt_v, D):
+@pytest.mark.parametrize("group", [4, 12])
+def test_matches_oracle_fp8_and_split_formats(fmt_k, fmt_v, D, group):
     lens = [130, 5, 64]
-    pool, table, lt, q, v, Tmax = _case(3, 2, 4, D, lens, fmt_k, fmt_v, seed=3 * D + fmt_k + 2 * fmt_v)
+    pool, table, lt, q, v, Tmax = _case(3, 2, group, D, lens, fmt_k, fmt_v,
+                                        seed=3 * D + fmt_k + 2 * fmt_v + group)
     scale = 1.0 / math.sqrt(D)
     out, st = _run(pool, table, lt, q, Tmax, scale)
     assert st == 0
     pk, pv = _planes(pool)
     ref, ost = O.decode_attention(pk, pv, fmt_k, fmt_v, 16, table.numpy(), lt.numpy(), bits(q), scale)
     assert ost == 0
-    _check(out, ref, v, lens, 4)
+    _check(out, ref, v, lens, group)
 
 
 def test_long_sequences_merge_several_splits():
