@@ -170,8 +170,10 @@ struct AttnTile {
   static constexpr int kBytes = kOffVR + 64;
   static constexpr int kStages = kBytes > 4096 ? 3 : 4;
   static constexpr int kRing = kAttnWarps * kStages * kBytes;
-  static constexpr int kMerge = kAttnWarps * 16 * (D + 2) * 4;  // per warp: 16 rows x (O, m, l)
-  static constexpr int kQ = (D / 16) * 32 * 16 + 64;             // Q fragments [k-step][lane] + 16 row factors
+  // per warp: up to 16 query heads x (O, m, l); Q^T fragments [n-tile][k-step][lane]
+  // (8 B each, up to two n-tiles) + up to 16 head factors
+  static constexpr int kMerge = kAttnWarps * 16 * (D + 2) * 4;
+  static constexpr int kQ = (D / 16) * 32 * 16 + 64;
   static constexpr int kSmem = kQ + (kRing > kMerge ? kRing : kMerge);
 };
 
