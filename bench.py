@@ -13,7 +13,8 @@ Prints one JSON line.  ``value`` is codec GB/s (algorithmic bytes read + written
 both kernels / device time), summed over ranks for N > 1 (weak scaling: each rank
 runs its own copy of the workload, no collective on the data path).  The
 reference arm (``--impl reference``) times the scalar CPU definition of the codec
-on the host cores over a bounded sample of the same workload.
+on every host core at once (one thread per core) over a bounded sample of the same
+workload.
 """
 
 from __future__ import annotations
@@ -681,18 +682,53 @@ def oracle_gbs(tokens: int, seconds: float) -> float:
     return b / seconds / 1e9
 
 
+def host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_all_cores(O, sample, threads: int) -> float:
+    """Wall seconds of `threads` oracle steps run at once, one per host thread, each on
+    the same read-only sample into its own pools and outputs (the C oracle keeps no
+    global state and ctypes releases the interpreter lock during each call)."""
+    import threading
+
+    k, v, slots, table = sample
+    go = threading.Barrier(threads + 1)
+
+    def work():
+        go.wait()
+        oracle_step(O, k, v, slots, table)
+
+    ts = [threading.Thread(target=work) for _ in range(threads)]
+    for t in ts:
+        t.start()
+    go.wait()
+    t0 = time.perf_counter()
+    for t in ts:
+        t.join()
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(args):
     import oracle as O
 
     tokens = args.cpu_tokens
-    k, v, slots, table = oracle_sample(tokens)
+    sample = oracle_sample(tokens)
     t0 = time.perf_counter()
-    oracle_step(O, k, v, slots, table)
+    oracle_step(O, *sample)
     dt = time.perf_counter() - t0
+    n = host_cores()
+    dt_all = oracle_all_cores(O, sample, n)
     return {"value": round(oracle_gbs(tokens, dt), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seconds": round(dt, 2),
             "sample": f"first {tokens} tokens of the workload (x4 heads x D256, K and V) with their own "
-                      f"block-shuffled {tokens // BLOCK}-block pool: scatter + restore, single-threaded scalar C"}
+                      f"block-shuffled {tokens // BLOCK}-block pool: scatter + restore, single-threaded scalar C",
+            "all_cores": {"value": round(n * oracle_gbs(tokens, dt_all), 4), "unit": "GB/s", "cores": n,
+                          "seconds": round(dt_all, 2),
+                          "sample": f"the same sample on {n} host threads at once, one oracle step each"}}
 
 
 def run_reference(args):
@@ -707,17 +743,15 @@ def run_reference(args):
     oracle_step(O, k, v, slots, table)
     per_tok = (time.perf_counter() - t0) / 256
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
-    tokens = int(max(BLOCK, min(65536, budget / per_tok)) // BLOCK * BLOCK)
-    k, v, slots, table = oracle_sample(tokens)
+    n = host_cores()
+    tokens = int(max(BLOCK, min(32768, budget / per_tok)) // BLOCK * BLOCK)
+    sample = oracle_sample(tokens)
     for _ in range(args.warmup):
-        oracle_step(O, k, v, slots, table)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(O, k, v, slots, table)
-    dt = (time.perf_counter() - t0) / args.steps
-    val = oracle_gbs(tokens, dt)
-    sample = (f"first {tokens} tokens of the workload per step (x4 heads x D256, K and V) with their own "
-              f"block-shuffled pool: scatter + restore, single-threaded scalar C")
+        oracle_all_cores(O, sample, n)
+    dt = sum(oracle_all_cores(O, sample, n) for _ in range(args.steps)) / args.steps
+    val = n * oracle_gbs(tokens, dt)
+    sample = (f"first {tokens} tokens of the workload (x4 heads x D256, K and V) with their own "
+              f"block-shuffled pool, on {n} host threads at once: scatter + restore per thread, scalar C")
     out = {
         "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
@@ -725,7 +759,7 @@ def run_reference(args):
         "data": "synthetic (seeded N(0,1) bf16 with 0.5% x50 outliers)",
         "config": {"workload": WORKLOAD, "tokens": T_TOKENS, "kv_heads": HEADS, "head_dim": HEAD_DIM,
                    "block_size": BLOCK, "sample_tokens_per_step": tokens},
-        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
