@@ -56,8 +56,12 @@ _lib = None
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        _declare(_lib)
+        L = ctypes.CDLL(build())
+        _declare(L)
+        if L.orc_subnormals_kept() != 1:
+            raise RuntimeError("the host flushes subnormals (FTZ/DAZ): the oracle's binary32 "
+                               "definitions do not hold in this process")
+        _lib = L
     return _lib
 
 
@@ -69,6 +73,7 @@ _U32 = ctypes.c_uint32
 
 def _declare(L: ctypes.CDLL) -> None:
     sig = {
+        "orc_subnormals_kept": (_I, []),
         "orc_f32_to_bf16_n": (None, [_P, _I64, _P]),
         "orc_f32_to_f16_n": (None, [_P, _I64, _P]),
         "orc_e2m1_encode_n": (None, [_P, _I64, _P]),

@@ -173,6 +173,15 @@ uint8_t orc_e4m3_encode(float t) {
   return (uint8_t)((signbit(t) ? 0x80 : 0) | c);
 }
 
+int orc_subnormals_kept(void) {
+  /* volatile operands: the products are computed at run time, under the FPU modes
+   * this process runs with */
+  volatile float smallest_normal = 0x1p-126f, half = 0.5f, sub = 0x1p-140f, two = 2.0f;
+  const float r1 = smallest_normal * half; /* a subnormal result: 2^-127 */
+  const float r2 = sub * two;              /* a subnormal operand and result: 2^-139 */
+  return r1 == 0x1p-127f && r2 == 0x1p-139f && r2 != 0.0f;
+}
+
 void orc_f32_to_bf16_n(const float* x, int64_t n, uint16_t* y) {
   for (int64_t i = 0; i < n; i++) y[i] = orc_f32_to_bf16(x[i]);
 }

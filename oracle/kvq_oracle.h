@@ -38,6 +38,11 @@ extern "C" {
 enum { ORC_FMT_NVFP4 = 1, ORC_FMT_INT4 = 2, ORC_FMT_FP8 = 3, ORC_FMT_NVFP4_TENSOR = 4 };
 enum { ORC_KIND_KEY = 0, ORC_KIND_VALUE = 1 };
 
+/* 1 when this host's binary32 arithmetic keeps subnormal operands and results (no
+ * flush-to-zero, no denormals-are-zero), else 0.  The oracle's definitions assume it;
+ * the Python loader refuses to use the library when it returns 0. */
+int orc_subnormals_kept(void);
+
 /* ---- scalar format primitives ---- */
 float orc_bf16_to_f32(uint16_t b);
 uint16_t orc_f32_to_bf16(float f);

@@ -43,6 +43,13 @@ def e4m3_table():
 # ---------------------------------------------------------------------------
 # E2M1
 # ---------------------------------------------------------------------------
+def test_host_keeps_subnormals():
+    """The oracle's binary32 definitions assume subnormals are kept (no FTZ/DAZ): the
+    library's own run-time probe agrees with numpy's float32 arithmetic on this host."""
+    assert O.lib().orc_subnormals_kept() == 1
+    assert np.float32(2.0 ** -126) * np.float32(0.5) == np.float32(2.0 ** -127)
+
+
 def test_e2m1_values_are_the_fp4_grid():
     got = [O.e2m1_value(c) for c in range(16)]
     assert got[:8] == list(E2M1_MAGS)
