@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -194,6 +195,22 @@ def sources_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
+def nearest_rank(xs, q: float) -> float:
+    """The q-quantile of xs by the nearest-rank rule (the smallest value with at least
+    a fraction q of the values at or below it)."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, math.ceil(q * len(ys)) - 1))]
+
+
+def kernel_row(times_ms, nbytes: int, peak: float) -> dict:
+    """One kernel's line: mean, P50 and P90 of its per-step event times, and the
+    mean's bandwidth as GB/s and as a fraction of the peak."""
+    ms = sum(times_ms) / len(times_ms)
+    return {"ms": round(ms, 4), "p50_ms": round(nearest_rank(times_ms, 0.5), 4),
+            "p90_ms": round(nearest_rank(times_ms, 0.9), 4), "bytes": nbytes,
+            "GB/s": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 4)}
+
+
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source changed since the capture."""
@@ -277,8 +294,9 @@ def run_ours(args):
         sampler.mark(False)
     barrier(dist, device)
     total_ms = start.elapsed_time(end)
-    scat_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    rest_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    scat_t = [e[0].elapsed_time(e[1]) for e in ev]
+    rest_t = [e[1].elapsed_time(e[2]) for e in ev]
+    scat_ms, rest_ms = sum(scat_t) / K, sum(rest_t) / K
     total_ms = max_over_ranks(dist, total_ms, device)
     clocks = sampler.stop() if sampler else None
 
@@ -327,12 +345,8 @@ def run_ours(args):
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "rows_per_s": round(world * 4 * T * H / (ms_per_step * 1e-3), 1),
         "kernels": {
-            "kvq_quant_scatter": {"ms": round(scat_ms, 4), "bytes": sb,
-                                  "GB/s": round(sb / scat_ms / 1e6, 1),
-                                  "frac": round(sb / scat_ms / 1e6 / peak, 4)},
-            "kvq_restore": {"ms": round(rest_ms, 4), "bytes": rb,
-                            "GB/s": round(rb / rest_ms / 1e6, 1),
-                            "frac": round(rb / rest_ms / 1e6 / peak, 4)},
+            "kvq_quant_scatter": kernel_row(scat_t, sb, peak),
+            "kvq_restore": kernel_row(rest_t, rb, peak),
         },
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",

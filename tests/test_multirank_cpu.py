@@ -63,6 +63,20 @@ def test_weak_scaling_value_uses_all_ranks_and_the_slowest_time():
     assert abs(2 * step / (ms * 1e-3) / 1e9 - 2 * step / 2e6) < 1e-6
 
 
+def test_kernel_line_quantiles_by_nearest_rank():
+    """P50 / P90 of the per-step kernel times: nearest rank on the sorted times."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.nearest_rank([5.0, 1.0, 3.0, 2.0, 4.0], 0.5) == 3.0
+    assert bench.nearest_rank([5.0, 1.0, 3.0, 2.0, 4.0], 0.9) == 5.0
+    assert bench.nearest_rank([float(i) for i in range(1, 101)], 0.9) == 90.0
+    assert bench.nearest_rank([7.0], 0.9) == 7.0
+    row = bench.kernel_row([1.0, 1.2, 0.8, 1.0], 6_000_000_000, 6000.0)
+    assert row["ms"] == 1.0 and row["p50_ms"] == 1.0 and row["p90_ms"] == 1.2
+    assert row["GB/s"] == 6000.0 and row["frac"] == 1.0
+
+
 def test_reference_arm_prints_from_rank_zero_only():
     port = _free_port()
     env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE="2")
