@@ -311,6 +311,10 @@ def run_ours(args):
         rows_other["latency_us_one_residual_loop"] = residual_loop_latency(kvq, device)
         rows_other["decode_attention"] = attention_rows(kvq, device, peak=measured_peaks()[0])
         rows_other["decode_step_store"] = decode_step_latency(kvq, device)
+        try:  # an auxiliary latency row: a failure is reported in the line, not fatal
+            rows_other["one_layer_latency"] = one_layer_latency(kvq, device)
+        except Exception as e:  # noqa: BLE001
+            rows_other["one_layer_latency"] = {"error": f"{type(e).__name__}: {e}"}
 
     if rank != 0:
         if dist is not None:
@@ -654,6 +658,45 @@ def decode_step_latency(kvq, device, iters=200):
     return {"workload": "256 tokens x 8 KV heads x D128 (K a view of qkv [256, 1152]) into a 65,536-slot pool, "
                         "one graph replay", "us_per_replay": round(a.elapsed_time(b) / iters * 1000, 2),
             "bytes": scatter_bytes(256, 8, 128)}
+
+
+def one_layer_latency(kvq, device, iters=200):
+    """The one-layer parity case as a latency row: K, V [256, 8, 128] (N(0,1), 1% x20)
+    quant-scattered into a 256-slot pool (16 blocks, slots 0..255), then restored
+    through the identity block table; each call captured in a CUDA graph, microseconds
+    per replay."""
+    from quantized_kv_cache_nvfp4_gb300 import synth
+
+    k, v, slots = synth.one_layer_case(seed=0)
+    k, v, slots = k.to(device), v.to(device), slots.to(device)
+    pool = kvq.Nvfp4Pool.empty(256, 8, 128, BLOCK, device=device)
+    table = torch.arange(256 // BLOCK, dtype=torch.int32, device=device).view(1, 256 // BLOCK)
+    lens = torch.tensor([256], dtype=torch.int32, device=device)
+    ko = torch.empty((1, 256, 8, 128), dtype=torch.bfloat16, device=device)
+    vo = torch.empty_like(ko)
+    stream = torch.cuda.Stream(device)
+    calls = (("kvq_quant_scatter", lambda: kvq.kvq_quant_scatter(k, v, slots, pool, stream=stream)),
+             ("kvq_restore", lambda: kvq.kvq_restore(pool, table, lens, 256, ko, vo, stream=stream)))
+    out = {"workload": "K, V [256, 8, 128] into a 256-slot pool and back, one graph replay per call"}
+    for name, fn in calls:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        for _ in range(10):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        out[name + "_us"] = round(a.elapsed_time(b) / iters * 1000, 2)
+    return out
 
 
 def residual_loop_latency(kvq, device, iters=50):
