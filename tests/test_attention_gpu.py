@@ -104,16 +104,17 @@ def test_matches_oracle_fp8_and_split_formats(fmt_k, fmt_v, D, group):
     _check(out, ref, v, lens, group)
 
 
-def test_long_sequences_merge_several_splits():
+@pytest.mark.parametrize("group", [8, 16])  # one and two head n-tiles
+def test_long_sequences_merge_several_splits(group):
     """Two sequences on one KV head: many splits per sequence, merged in the workspace."""
     lens = [4096, 1500]
-    pool, table, lt, q, v, Tmax = _case(2, 1, 8, 128, lens, seed=11)
-    assert kvq.kvq_decode_attention_workspace(2, 1, 8, 128, Tmax) > 0
+    pool, table, lt, q, v, Tmax = _case(2, 1, group, 128, lens, seed=11)
+    assert kvq.kvq_decode_attention_workspace(2, 1, group, 128, Tmax) > 0
     out, st = _run(pool, table, lt, q, Tmax, 0.0883883)
     assert st == 0
     pk, pv = _planes(pool)
     ref, _ = O.decode_attention(pk, pv, NV, NV, 16, table.numpy(), lt.numpy(), bits(q), 0.0883883)
-    _check(out, ref, v, lens, 8)
+    _check(out, ref, v, lens, group)
 
 
 @pytest.mark.parametrize("q_scale", [1e-30, 3e4])
