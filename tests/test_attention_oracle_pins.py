@@ -93,8 +93,9 @@ def _case(fmt_k, fmt_v, H=2, Hq=4, D=64, bs=16, lens=(37, 16, 1), seed=0):
 
 
 @pytest.mark.parametrize("fmt_k,fmt_v", [(NVFP4, NVFP4), (FP8, FP8), (FP8, NVFP4)])
-def test_attention_equals_torch_sdpa_on_the_decoded_rows(fmt_k, fmt_v):
-    planes, table, lens, q, rk, rv, H, Hq, D, bs = _case(fmt_k, fmt_v)
+@pytest.mark.parametrize("H,Hq", [(2, 4), (1, 16), (2, 18)])  # GQA 2, 16 and 9
+def test_attention_equals_torch_sdpa_on_the_decoded_rows(fmt_k, fmt_v, H, Hq):
+    planes, table, lens, q, rk, rv, H, Hq, D, bs = _case(fmt_k, fmt_v, H=H, Hq=Hq, seed=H + Hq)
     scale = 0.125
     out, st = O.decode_attention(planes[0], planes[1], fmt_k, fmt_v, bs, table, lens, q, scale)
     assert st == 0
