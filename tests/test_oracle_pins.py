@@ -752,3 +752,184 @@ def test_fp8_paged_round_trip_and_residuals():
     a, _ = O.residual_encode(cur, prev, np.arange(40, dtype=np.int32), O.FMT_FP8, 0)
     b, _ = O.residual_encode(cur, prev, None, O.FMT_FP8, 0)
     np.testing.assert_array_equal(O.residual_decode(a, prev)[0], O.residual_decode(b, prev)[0])
+
+
+# ---------------------------------------------------------------------------
+# decode rounding order on inexact scales, and INT4 half-integer ties
+# ---------------------------------------------------------------------------
+def _e4m3_via_fp16_identity(codes):
+    """E4M3 bytes -> float32 values by the fp16 bit identity printed on the FreeToken
+    page (fp8 store notes), not by the oracle's table: fp16 bits (v + (v & 0x80)) << 7
+    hold the value / 256."""
+    v = np.asarray(codes).astype(np.uint32)
+    h = (((v + (v & 0x80)) << 7) & 0xFFFF).astype(np.uint16)
+    return h.view(np.float16).astype(np.float32) * np.float32(256.0)
+
+
+def _torch_bf16(x32):
+    """float32 -> bf16 bit patterns by torch's own cast (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_nvfp4_decode_is_exact_block_product_then_one_float32_product_by_rs():
+    """Reading R4 on rows whose row scales are not powers of two: the decoded value is
+    (e2m1 * bs), exact in float32, times rs rounded once in float32, then torch's bf16
+    cast.  Grouping the other way, e2m1 * (bs * rs), gives other bits on some elements
+    of these rows, so this pin fixes the order (FreeToken PR #408, codec-delta port
+    note: quantise against the stored block scale; decode multiplies both scales)."""
+    n, D = 2000, 128
+    xb = synth.bf16_bits(synth.normal_bf16((n, D), seed=41, stream=1, outlier_frac=0.01, outlier_scale=20.0))
+    codes, bscale, rscale = O.nvfp4_encode_rows(xb)
+    mant = np.frexp(rscale.astype(np.float64))[0]
+    assert (mant != 0.5).mean() > 0.95  # the row scales are inexact
+    nib = np.stack([codes & 15, codes >> 4], -1).reshape(n, D)
+    e2m1 = (np.where(nib & 8, -1.0, 1.0) * E2M1_MAGS[nib & 7]).astype(np.float32)
+    bs = np.repeat(_e4m3_via_fp16_identity(bscale), 16, axis=1)
+    prod = e2m1 * bs
+    assert np.array_equal(prod.astype(np.float64), e2m1.astype(np.float64) * bs.astype(np.float64))
+    want = _torch_bf16(prod * rscale[:, None])
+    np.testing.assert_array_equal(O.nvfp4_decode_rows(codes, bscale, rscale), want)
+    other_order = _torch_bf16(e2m1 * (bs * rscale[:, None]))
+    assert (other_order != want).sum() > 20  # the pin tells the two orders apart
+
+
+def test_fp8_decode_is_one_float32_product_then_bf16():
+    """Reading R8's decode on inexact row scales: bf16(e4m3 * rs) with the product
+    rounded in float32 (numpy) and the narrowing done by torch's cast."""
+    xb = synth.bf16_bits(synth.normal_bf16((2000, 128), seed=42, stream=1, outlier_frac=0.01, outlier_scale=20.0))
+    codes, rscale = O.fp8_encode_rows(xb)
+    assert (np.frexp(rscale.astype(np.float64))[0] != 0.5).mean() > 0.95
+    want = _torch_bf16(_e4m3_via_fp16_identity(codes) * rscale[:, None])
+    np.testing.assert_array_equal(O.fp8_decode_rows(codes, rscale), want)
+
+
+@pytest.mark.parametrize("kind,G", [(O.KIND_KEY, 64), (O.KIND_VALUE, 64), (O.KIND_VALUE, 16)])
+def test_int4_decode_is_float32_mul_then_add_then_bf16(kind, G):
+    """Reading R5's decode on random groups (metadata not on any grid): numpy float32
+    code * sc16, then + mn16, then torch's bf16 cast; the FP16 metadata is widened by
+    numpy's own fp16 conversion (vllm-rlt PR #166, Purpose: FP32 arithmetic with FP16
+    min/scale)."""
+    T, H, D = 256, 3, 128
+    xb = synth.bf16_bits(synth.normal_bf16((T, H, D), seed=43, stream=1, outlier_frac=0.01, outlier_scale=20.0))
+    codes, mn16, sc16 = O.int4_pack(xb, kind, G)
+    nib = np.stack([codes & 15, codes >> 4], -1).reshape(T, H, D).astype(np.float32)
+    mn = mn16.view(np.float16).astype(np.float32)
+    sc = sc16.view(np.float16).astype(np.float32)
+    if kind == O.KIND_KEY:
+        mn, sc = mn[np.arange(T) // G], sc[np.arange(T) // G]
+    else:
+        mn, sc = mn[..., np.arange(D) // G], sc[..., np.arange(D) // G]
+    want = _torch_bf16(nib * sc + mn)
+    np.testing.assert_array_equal(O.int4_unpack(codes, mn16, sc16, kind, G), want)
+
+
+def test_int4_decode_product_is_exact_so_a_fused_multiply_add_agrees():
+    """A code has 4 significant bits and an FP16 scale 11, so code * sc16 is exact in
+    float32 for every code and every finite FP16 scale; the decode's only rounding is
+    the add, and a fused multiply-add rounds the same exact sum.  (This is why no pin
+    can tell mul-then-add from an FMA here: the two are the same function.)"""
+    h = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    h = h[(h & 0x7C00) != 0x7C00]
+    sc = h.view(np.float16)
+    c = np.arange(16, dtype=np.float32)[:, None]
+    p32 = c * sc.astype(np.float32)[None, :]
+    p64 = c.astype(np.float64) * sc.astype(np.float64)[None, :]
+    assert np.array_equal(p32.astype(np.float64), p64)
+    # fused: the exact sum (exact in float64: at most 45 significant bits) rounded once
+    rng = np.random.default_rng(44)
+    mn = h[rng.integers(0, h.size, 200000)].view(np.float16)
+    scs = h[rng.integers(0, h.size, 200000)].view(np.float16)
+    cs = rng.integers(0, 16, 200000).astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        mul_add = cs * scs.astype(np.float32) + mn.astype(np.float32)
+        fused = (cs.astype(np.float64) * scs.astype(np.float64) + mn.astype(np.float64)).astype(np.float32)
+    ok = np.isfinite(fused)
+    np.testing.assert_array_equal(mul_add[ok].view(np.uint32), fused[ok].view(np.uint32))
+
+
+def _tie_groups(mn, mx, ties):
+    """One 64-element group: mn, mx, then the tie values, padded with mn."""
+    g = np.full(64, mn, np.float64)
+    g[1] = mx
+    g[2:2 + len(ties)] = ties
+    return g
+
+
+@pytest.mark.parametrize("kind", [O.KIND_KEY, O.KIND_VALUE])
+def test_int4_half_integer_quotients_round_to_the_even_code(kind):
+    """Reading R5's rounding: groups whose scale (mx - mn)/15 is exact and whose
+    quotients (x - mn)/sc are exact half-integers.  Each code must be the even
+    neighbour (0.5 -> 0, 1.5 -> 2, 2.5 -> 2, 3.5 -> 4, ...), which is torch.round's
+    half-to-even; rounding half away from zero would give the odd one."""
+    half = np.arange(15) + 0.5
+    cases = [
+        (0.0, 15.0, half),              # sc = 1
+        (-8.0, 7.0, half - 8.0),        # sc = 1, negative minimum
+        (0.0, 30.0, 2.0 * half),        # sc = 2
+        (0.0, 7.5, 0.5 * half),         # sc = 0.5
+        (-3.0, 0.75, -3.0 + 0.25 * half),  # sc = 0.25
+    ]
+    groups = np.stack([_tie_groups(*c) for c in cases])        # [5, 64]
+    if kind == O.KIND_KEY:
+        x = groups.T[:, None, :]                                # [64 rows, 1 head, 5 channels] -> pad D
+        x = np.concatenate([x, np.zeros((64, 1, 11))], axis=2)  # D = 16
+    else:
+        x = groups[:, None, :]                                  # [5 rows, 1 head, 64 channels]
+    xb = _bits(x)
+    assert np.array_equal(O.bf16_to_f32(xb).astype(np.float64), x)
+    codes, mn16, sc16 = O.int4_pack(xb, kind, 64)
+    nib = np.stack([codes & 15, codes >> 4], -1).reshape(x.shape)
+    for i, (mn, mx, ties) in enumerate(cases):
+        sc = (mx - mn) / 15.0
+        q = (ties - mn) / sc
+        assert np.array_equal(q, np.arange(15) + 0.5)           # exact half-integers
+        want = torch.round(torch.from_numpy(q)).numpy().astype(np.int64)
+        got = nib[2:17, 0, i] if kind == O.KIND_KEY else nib[i, 0, 2:17]
+        np.testing.assert_array_equal(got, want)
+        assert (got % 2 == 0).all()
+
+
+def _double_rounding_scales(a, n, seed):
+    """Row scales rs for which the exact product a * rs (exact in float64) rounds in
+    float32 onto a bf16 midpoint without being one: there rounding once in float32 and
+    then to bf16 can differ from rounding the exact product to bf16 directly."""
+    rng = np.random.default_rng(seed)
+    rs = rng.uniform(0.5, 1.0, 4_000_000).astype(np.float32) * np.float32(2.0 ** -10)
+    e = np.float64(a) * rs.astype(np.float64)
+    hi = e.astype(np.float32)
+    hit = ((hi.view(np.uint32) & 0xFFFF) == 0x8000) & (hi.astype(np.float64) != e)
+    assert hit.sum() >= n
+    return rs[hit][:n]
+
+
+def _bf16_direct(e64):
+    """The exact float64 value rounded straight to bf16 (8 significant bits, ties to
+    even), as bit patterns."""
+    m, ex = np.frexp(e64)
+    r = np.ldexp(np.rint(m * 256.0) / 256.0, ex).astype(np.float32)
+    return _torch_bf16(r)
+
+
+def test_decode_rounds_in_float32_first_on_double_rounding_cases():
+    """Rows built so that the decode product lands, after its float32 rounding, exactly
+    on a bf16 midpoint: the oracle's result is the float32 product narrowed by torch's
+    cast (reading R4 and R8: one float32 rounding, then bf16), and on some of these
+    elements that differs from rounding the exact product to bf16 in one step."""
+    # FP8: code 0x39 = 1.125; NVFP4: code 7 (6.0) with block scale 0x39 (1.125) = 6.75
+    rs8 = _double_rounding_scales(1.125, 48, 45)
+    codes8 = np.full((48, 16), 0x39, np.uint8)
+    got8 = O.fp8_decode_rows(codes8, rs8)
+    want8 = _torch_bf16(np.float32(1.125) * rs8[:, None] * np.ones((1, 16), np.float32))
+    np.testing.assert_array_equal(got8, want8)
+    direct8 = _bf16_direct(1.125 * rs8.astype(np.float64))
+    assert (direct8 != want8[:, 0]).sum() >= 8
+
+    rs4 = _double_rounding_scales(6.75, 48, 46)
+    codes4 = np.full((48, 8), 0x77, np.uint8)
+    bscale4 = np.full((48, 1), 0x39, np.uint8)
+    got4 = O.nvfp4_decode_rows(codes4, bscale4, rs4)
+    want4 = _torch_bf16(np.float32(6.75) * rs4[:, None] * np.ones((1, 16), np.float32))
+    np.testing.assert_array_equal(got4, want4)
+    direct4 = _bf16_direct(6.75 * rs4.astype(np.float64))
+    assert (direct4 != want4[:, 0]).sum() >= 8
