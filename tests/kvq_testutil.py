@@ -47,3 +47,23 @@ def assert_rows_equal(got_codes, got_bs, got_rs, want_codes, want_bs, want_rs, w
 def oracle_rows(x: torch.Tensor):
     """Oracle NVFP4 encode of every (token, head) row of a [T, H, D] bf16 tensor."""
     return O.nvfp4_encode_rows(bits(x.contiguous()))
+
+
+def oracle_on_all_cores(fn, *arrays, threads=None):
+    """Apply a row-wise oracle function to every row of `arrays` (split along axis 0)
+    on every host core.  Each thread runs the unchanged oracle on its own contiguous
+    chunk; the C oracle keeps no global state and ctypes releases the interpreter
+    lock, so the chunks run in parallel.  Returns what fn returns, with the chunks'
+    results concatenated along axis 0."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    n = arrays[0].shape[0]
+    threads = threads or os.cpu_count() or 1
+    edges = np.linspace(0, n, 4 * threads + 1).astype(np.int64)
+    spans = [(a, b) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda ab: fn(*[np.ascontiguousarray(x[ab[0]:ab[1]]) for x in arrays]), spans))
+    if isinstance(parts[0], tuple):
+        return tuple(np.concatenate([p[j] for p in parts]) for j in range(len(parts[0])))
+    return np.concatenate(parts)

@@ -401,3 +401,95 @@ def test_residual_arithmetic_across_exponent_gaps(fmt, kind):
     assert dst == 0
     np.testing.assert_array_equal(bits(out), ref)
     np.testing.assert_array_equal(bits(ip), ref)
+
+
+# ---------------------------------------------------------------------------
+# CUDA Graph capture of pack / unpack and the residual entry points
+# (FreeToken PR #408, Summary: the KV writes are safe under CUDA Graph capture)
+# ---------------------------------------------------------------------------
+def _poison_packed(pk):
+    for t in (pk.codes, pk.meta0, pk.meta1, pk.rscale):
+        if t is not None:
+            t.view(torch.uint8).fill_(POISON)
+
+
+def _same_packed(a, b):
+    for x, y in ((a.codes, b.codes), (a.meta0, b.meta0), (a.meta1, b.meta1), (a.rscale, b.rscale)):
+        if x is not None:
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+def test_int4_pack_unpack_under_graph_capture(kind):
+    """kvq_pack and kvq_unpack (INT4 G64, a partial last K group) captured in one graph
+    and replayed twice: bit-identical to the eager calls and to the oracle."""
+    T, H, D, G = 4100, 8, 128, 64
+    x = synth.normal_bf16((T, H, D), seed=60, stream=1, outlier_frac=0.01, outlier_scale=20.0)
+    xd = x.to(DEV)
+    pk, y = gpu_int4_pack(xd, kind, G)
+    pk2 = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G)
+    y2 = torch.empty_like(y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kvq.kvq_pack(xd, pk2)
+        kvq.kvq_unpack(pk2, y2)
+    for _ in range(2):
+        _poison_packed(pk2)
+        y2.view(torch.uint8).fill_(POISON)
+        g.replay()
+        torch.cuda.synchronize()
+        _same_packed(pk2, pk)
+        assert torch.equal(y2.view(torch.int16), y.view(torch.int16))
+    codes, mn, sc = O.int4_pack(bits(x), kind, G)
+    check_int4(pk2, codes, mn, sc)
+    np.testing.assert_array_equal(bits(y2), O.int4_unpack(codes, mn, sc, kind, G))
+
+
+@pytest.mark.parametrize("fmt,kind", [(kvq.FMT_INT4, kvq.KIND_KEY), (kvq.FMT_INT4, kvq.KIND_VALUE),
+                                      (kvq.FMT_NVFP4, kvq.KIND_KEY), (kvq.FMT_FP8, kvq.KIND_VALUE)])
+def test_residual_encode_decode_under_graph_capture(fmt, kind):
+    """kvq_encode_residual with 25% of rows kept, then kvq_decode_residual into a
+    separate output and in place, captured in one graph and replayed: payload, owned
+    position map and both reconstructions bit-identical to the eager calls and to the
+    oracle."""
+    T, H, D, P = 4096, 8, 128, 1024
+    prev = synth.normal_bf16((T, H, D), seed=61, stream=1)
+    cur = synth.normal_bf16((T, H, D), seed=61, stream=2)
+    pos = synth.sorted_positions(T, P, seed=61)
+    cd, pd, posd = cur.to(DEV), prev.to(DEV), pos.to(DEV)
+    st = status_word()
+
+    def run(pay, pos_out, out, ip):
+        kvq.kvq_encode_residual(cd, pd, posd, pay, pos_out, st)
+        kvq.kvq_decode_residual(pay, posd, pd, out, st)
+        kvq.kvq_decode_residual(pay, posd, ip, ip, st)
+
+    pay = kvq.Packed.empty(fmt, kind, P, H, D, 64)
+    pos_out = torch.empty(P, dtype=torch.int32, device=DEV)
+    out, ip = poison_bf16((T, H, D)), pd.clone()
+    run(pay, pos_out, out, ip)
+    pay2 = kvq.Packed.empty(fmt, kind, P, H, D, 64)
+    pos_out2 = torch.empty(P, dtype=torch.int32, device=DEV)
+    out2, ip2 = poison_bf16((T, H, D)), pd.clone()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(pay2, pos_out2, out2, ip2)
+    for _ in range(2):
+        _poison_packed(pay2)
+        pos_out2.fill_(-7)
+        out2.view(torch.uint8).fill_(POISON)
+        ip2.copy_(pd)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        _same_packed(pay2, pay)
+        assert torch.equal(pos_out2, pos_out)
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+        assert torch.equal(ip2.view(torch.int16), out.view(torch.int16))
+    opay, ost = O.residual_encode(bits(cur), bits(prev), pos.numpy(), fmt, kind, 64)
+    assert ost == 0
+    check_payload(pay2, opay)
+    np.testing.assert_array_equal(pos_out2.cpu().numpy(), pos.numpy())
+    np.testing.assert_array_equal(bits(out2), O.residual_decode(opay, bits(prev))[0])
