@@ -22,7 +22,8 @@
  *   Memory   every pointer argument that a kernel touches is DEVICE memory
  *            (cudaMalloc / the torch caching allocator) owned by the caller.  The
  *            library allocates nothing, frees nothing and never synchronises, so
- *            every call may be captured in a CUDA graph.  Host or unregistered
+ *            every entry point but kvq_decode_attention_noalloc (see there) may be
+ *            captured in a CUDA graph.  Host or unregistered
  *            pointers are rejected with KVQ_ERR_NOT_DEVICE_PTR before any launch
  *            (the FreeToken page records a host tensor handed to a kernel).
  *   bf16     K/V tensors are bf16 [rows][heads][dim] views with inner stride 1 and
@@ -257,14 +258,28 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
                                         size_t workspace_bytes, uint32_t* dev_status,
                                         kvq_stream_t stream);
 
-/* kvq_decode_attention without a workspace argument: it allocates nothing and uses
- * the library's built-in scratch (48 MiB of device memory in the library image)
- * for the split partials.  The split policy keeps the partials under 40.2 MB on a
- * 152-SM GPU for every supported shape; KVQ_ERR_UNSUPPORTED if they would not fit
- * (kvq_decode_attention_workspace(...) > 48 MiB).  The scratch is one per device:
- * calls of this entry point must not overlap (different streams, or graphs
- * replayed concurrently); kvq_decode_attention with a caller workspace has no
- * such limit.  Same arguments, results and errors otherwise. */
+/* kvq_decode_attention for callers that cannot allocate device memory.  Some callers
+ * have no way to hand the library a workspace: an engine whose memory planner has
+ * already given all free HBM to the KV pool, or a host runtime that passes in only
+ * the tensors it owns and offers no allocator hook.  A cudaMalloc can also
+ * synchronise the device, which a decode step cannot afford.  This entry point
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine): the
+ * split partials go to a scratch array that is part of the library image, 48 MiB of
+ * device memory that every GPU which loads the library holds until the process exits.
+ * The pages have no counterpart to this entry point; it exists for such callers.
+ *   Limit    the partials need kvq_decode_attention_workspace(...) bytes; a call
+ *            that needs more than 48 MiB returns KVQ_ERR_UNSUPPORTED.  The split
+ *            policy keeps every supported shape under 40.2 MB on a 152-SM GPU.
+ *   Set-up   the first call on a device looks up the scratch array's device address
+ *            (with that device current) and keeps it; make that first call before
+ *            any stream capture.  A failed lookup returns KVQ_ERR_CUDA.
+ *   Sharing  there is one scratch array per device, shared by every call of this
+ *            entry point on it, and it keeps the last call's contents (each call
+ *            writes every partial it later reads, so nothing needs clearing).  Calls
+ *            that overlap on the GPU race on it; kvq_decode_attention with a caller
+ *            workspace has no such limit.
+ * Arguments, argument checks, results and device status are those of
+ * kvq_decode_attention without the workspace pair. */
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_pool* pool, const int32_t* block_table,
                                                 int32_t num_seqs, int32_t max_blocks,
                                                 const int32_t* seq_lens, int32_t max_seq_len,

@@ -37,6 +37,9 @@
 //    largest element in [2^14, 2^15), undone in the score multiplier.
 //  * The warps of a CTA merge through shared memory; several splits of a sequence
 //    merge through the caller's workspace in a second small kernel.
+#include <atomic>
+#include <mutex>
+
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 
@@ -716,17 +719,45 @@ cudaError_t attn_dispatch_group(const AttnParams& p, cudaStream_t s) {
 constexpr int kAttnCtasPerSm = 4;
 constexpr int kAttnMaxWaves = 4;
 
-// Built-in split scratch for kvq_decode_attention_noalloc: part of the library image,
-// so no call allocates.  One per device; calls that use it must not overlap.  The
-// policy above keeps S*H*nsplit <= 4 waves = 16 * SMs CTAs, so the partials take at
-// most 16 * SMs * 16 query heads * (256 + 2) * 4 bytes: 40.2 MB on 152 SMs, inside
-// these 48 MiB.
+// Built-in split scratch for kvq_decode_attention_noalloc, for callers that cannot
+// allocate device memory: it is part of the library image, so every GPU that loads
+// the library holds these 48 MiB until the process exits, and no call allocates.
+// One array per device, shared by every call on it: calls that overlap on the GPU
+// race on it.  Each call writes every partial it later reads, so nothing in it needs
+// clearing between calls.  The policy above keeps S*H*nsplit <= 4 waves = 16 * SMs
+// CTAs, so the partials take at most 16 * SMs * 16 query heads * (256 + 2) * 4
+// bytes: 40.2 MB on 152 SMs.
 constexpr size_t kAttnScratchBytes = size_t{48} << 20;
 static __device__ __align__(256) float g_attn_scratch[kAttnScratchBytes / sizeof(float)];
 
+// Host code may not pass g_attn_scratch itself to a kernel: on the host that name is a
+// stand-in, not a device address.  The device address is looked up once per device,
+// with that device current, on the first call there, and kept.
+constexpr int kScratchDevices = 64;
+static std::atomic<void*> g_scratch_addr[kScratchDevices];
+static std::mutex g_scratch_mu;
+
 cudaError_t attn_builtin_scratch(void** ptr, size_t* bytes) {
   *bytes = kAttnScratchBytes;
-  return cudaGetSymbolAddress(ptr, g_attn_scratch);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+  void* addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    addr = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (addr == nullptr) {
+      e = cudaGetSymbolAddress(&addr, g_attn_scratch);
+      if (e != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();  // leave no error behind for the launch check
+        return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+      }
+      g_scratch_addr[dev].store(addr, std::memory_order_release);
+    }
+  }
+  *ptr = addr;
+  return cudaSuccess;
 }
 
 size_t attn_builtin_scratch_bytes() { return kAttnScratchBytes; }

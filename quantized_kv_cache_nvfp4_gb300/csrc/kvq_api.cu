@@ -688,12 +688,17 @@ KVQ_API size_t kvq_decode_attention_workspace(int32_t num_seqs, int32_t num_head
   return static_cast<size_t>(num_seqs) * num_q_heads * nsplit * (head_dim + 2) * sizeof(float);
 }
 
-KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* block_table,
-                                        int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
-                                        int32_t max_seq_len, const kvq_bf16_in* q, int32_t num_q_heads,
-                                        float scale, const kvq_bf16_out* out, void* workspace,
-                                        size_t workspace_bytes, uint32_t* dev_status,
-                                        kvq_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode attention behind both entry points: the same argument checks, then the split
+// partials go to the caller's workspace, or (builtin) to the library's own scratch.
+kvq_status decode_attention_impl(const kvq_pool* pool, const int32_t* block_table, int32_t num_seqs,
+                                 int32_t max_blocks, const int32_t* seq_lens, int32_t max_seq_len,
+                                 const kvq_bf16_in* q, int32_t num_q_heads, float scale,
+                                 const kvq_bf16_out* out, void* workspace, size_t workspace_bytes,
+                                 bool builtin, uint32_t* dev_status, kvq_stream_t stream) {
   if (pool == nullptr || q == nullptr || out == nullptr)
     return fail(KVQ_ERR_INVALID_ARG, "pool, q and out must not be NULL");
   if (check_pool_fmt(pool) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
@@ -728,7 +733,13 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
   AttnParams p{};
   attn_geometry(num_seqs, H, max_seq_len, &p.nsplit, &p.split_len);
   const size_t need = kvq_decode_attention_workspace(num_seqs, H, num_q_heads, D, max_seq_len);
-  if (need > 0) {
+  if (builtin && need > 0) {
+    if (need > attn_builtin_scratch_bytes())
+      return fail(KVQ_ERR_UNSUPPORTED, "split partials need %zu bytes, more than the built-in %zu", need,
+                  attn_builtin_scratch_bytes());
+    const cudaError_t e = attn_builtin_scratch(&workspace, &workspace_bytes);
+    if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "built-in scratch: %s", cudaGetErrorString(e));
+  } else if (need > 0) {
     if ((st = check_dev(workspace, "workspace")) != KVQ_OK) return st;
     if (!aligned(workspace, 16)) return fail(KVQ_ERR_MISALIGNED, "workspace must be 16-byte aligned");
     if (workspace_bytes < need)
@@ -777,28 +788,28 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* blo
   return launched(launch_decode_attention(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // namespace
+
+extern "C" {
+
+KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* block_table,
+                                        int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
+                                        int32_t max_seq_len, const kvq_bf16_in* q, int32_t num_q_heads,
+                                        float scale, const kvq_bf16_out* out, void* workspace,
+                                        size_t workspace_bytes, uint32_t* dev_status,
+                                        kvq_stream_t stream) {
+  return decode_attention_impl(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, q, num_q_heads,
+                               scale, out, workspace, workspace_bytes, false, dev_status, stream);
+}
+
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_pool* pool, const int32_t* block_table,
                                                 int32_t num_seqs, int32_t max_blocks,
                                                 const int32_t* seq_lens, int32_t max_seq_len,
                                                 const kvq_bf16_in* q, int32_t num_q_heads, float scale,
                                                 const kvq_bf16_out* out, uint32_t* dev_status,
                                                 kvq_stream_t stream) {
-  if (pool == nullptr) return fail(KVQ_ERR_INVALID_ARG, "pool is NULL");
-  if (num_seqs <= 0) return kvq_decode_attention(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len,
-                                                 q, num_q_heads, scale, out, nullptr, 0, dev_status, stream);
-  const size_t need = kvq_decode_attention_workspace(num_seqs, pool->num_heads, num_q_heads, pool->head_dim,
-                                                     max_seq_len);
-  if (need > attn_builtin_scratch_bytes())
-    return fail(KVQ_ERR_UNSUPPORTED, "split partials need %zu bytes, more than the built-in %zu", need,
-                attn_builtin_scratch_bytes());
-  void* scratch = nullptr;
-  size_t cap = 0;
-  if (need > 0) {
-    const cudaError_t e = attn_builtin_scratch(&scratch, &cap);
-    if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "built-in scratch: %s", cudaGetErrorString(e));
-  }
-  return kvq_decode_attention(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, q, num_q_heads,
-                              scale, out, scratch, cap, dev_status, stream);
+  return decode_attention_impl(pool, block_table, num_seqs, max_blocks, seq_lens, max_seq_len, q, num_q_heads,
+                               scale, out, nullptr, 0, true, dev_status, stream);
 }
 
 KVQ_API size_t kvq_storage_bytes(kvq_format fmt, kvq_kind kind, int32_t group_size, int64_t rows,

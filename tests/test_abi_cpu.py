@@ -118,6 +118,28 @@ def test_decode_attention_host_checks(kvq_lib_path):
                                     0, None, None) == 1
 
 
+def test_noalloc_entry_point_checks_arguments_like_the_workspace_one(kvq_lib_path):
+    """The no-allocation attention entry point runs the same argument checks, in the
+    same order, as the workspace one, before it looks at its own scratch limit: a
+    bad num_q_heads on a shape that would need split partials gets the same status
+    and reason from both."""
+    from quantized_kv_cache_nvfp4_gb300 import _abi
+
+    lib = _abi.load()
+    pool = _abi.Pool(_abi.Plane(), _abi.Plane(), 16384 * 16, 16, 8, 128, 1)
+    q = _abi.Bf16In(None, 32 * 128, 128)
+    o = _abi.Bf16Out(None, 32 * 128, 128)
+    for hq, want in ((4095, 1), (0, 1), (8 * 17, 2), (32, 1)):  # 32: the NULL q pointer
+        a = lib.kvq_decode_attention(ctypes.byref(pool), None, 32, 512, None, 8192, ctypes.byref(q), hq, 0.1,
+                                     ctypes.byref(o), None, 0, None, None)
+        ea = lib.kvq_last_error()
+        b = lib.kvq_decode_attention_noalloc(ctypes.byref(pool), None, 32, 512, None, 8192, ctypes.byref(q), hq,
+                                             0.1, ctypes.byref(o), None, None)
+        eb = lib.kvq_last_error()
+        assert a == b == want, (hq, a, b, ea, eb)
+        assert ea == eb
+
+
 def test_noalloc_scratch_covers_every_split_workspace(kvq_lib_path):
     """The built-in 48 MiB scratch of kvq_decode_attention_noalloc holds the split
     partials of every supported shape (the workspace query is host-only)."""

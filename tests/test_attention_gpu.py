@@ -198,26 +198,3 @@ def test_paged_32_sequences_of_8192_tokens_sampled():
     ref2 = torch.nn.functional.scaled_dot_product_attention(q.float()[:, :, None], kr, vr,
                                                             scale=1.0 / math.sqrt(D))[:, :, 0]
     assert (out.float() - ref2).abs().max().item() < 0.02
-
-
-@pytest.mark.parametrize("lens,max_len", [([300, 77], None), ([4096, 1500], None), ([40], 8192)])
-def test_noalloc_entry_point_matches_the_workspace_one(lens, max_len):
-    """kvq_decode_attention_noalloc (built-in scratch, no allocation) gives the same bits
-    as kvq_decode_attention with a caller workspace, eagerly and under graph capture."""
-    pool, table, lt, q, v, Tmax = _case(len(lens), 1, 8, 128, lens, seed=15)
-    ml = max_len or Tmax
-    td, ld, qd = table.to(DEV), lt.to(DEV), q.to(DEV)
-    a = poison_bf16(tuple(q.shape))
-    kvq.kvq_decode_attention(pool, td, ld, ml, qd, 0.1, a)
-    b = poison_bf16(tuple(q.shape))
-    st = status_word()
-    kvq.kvq_decode_attention_noalloc(pool, td, ld, ml, qd, 0.1, b, dev_status=st)
-    c = poison_bf16(tuple(q.shape))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        kvq.kvq_decode_attention_noalloc(pool, td, ld, ml, qd, 0.1, c)
-    g.replay()
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
