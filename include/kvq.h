@@ -40,8 +40,16 @@
  *            traps or asserts, so a bad id never poisons the CUDA context (the
  *            FreeToken page records a device-side assert that did).
  *   Floats   every result is bit-exact against the plain CPU definition of the
- *            codec (one IEEE binary32 operation at a time, round to nearest even,
- *            no FMA contraction, no flush to zero); see the design doc for the order.
+ *            codec: one IEEE binary32 operation at a time, round to nearest even,
+ *            no FMA contraction, no flush to zero, in this order.  NVFP4 encode:
+ *            rs = amax / 2688; per 16-block t = min((vb / 6) / rs, 448) (0 if rs is
+ *            0), bs = E4M3(t), s = bs * rs, q = x * (1 / s) (x / s when 1 / s
+ *            overflows, signed zeros when s is 0), code = E2M1(min(|q|, 6)) with
+ *            x's sign.  NVFP4 decode: bf16((e2m1 * bs) * rs).  FP8: rs = amax / 448,
+ *            q = x * (1 / rs), decode bf16(e4m3 * rs).  INT4: sc = (mx - mn) / 15,
+ *            code = clamp(rint((x - mn) / sc), 0, 15) from the FP32 mn and sc (codes
+ *            0 when sc is 0), then FP16 metadata; decode bf16(code * sc16 + mn16).
+ *            Residuals: r = bf16(cur - prev), out = bf16(prev + decoded r).
  *   Inputs   finite values only; INT4 also needs |x| < 65504 (FP16 metadata).
  */
 #ifndef KVQ_H

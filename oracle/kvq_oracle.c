@@ -20,7 +20,7 @@
  *    the stored (rounded) block scale, 76 B per row at head_dim 128, paged slots
  *    given as a device tensor of slot ids.
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open, one per step of the method:
  *  R1  row scale rs = amax / 2688 (2688 = 6 * 448), stored as the decode multiplier.
  *  R2  block scale target t = (vb / 6) / rs, clamped to 448, then E4M3 RNE.
  *  R3  s = bs * rs; s == 0 -> every code is a signed zero; inv = 1/s; if inv is

@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "kvq.h"
 #include "kvq_params.h"
@@ -242,6 +243,37 @@ int num_sms() {
     g_sms[dev] = n > 0 ? n : 148;
   }
   return g_sms[dev];
+}
+
+namespace {
+struct OccEntry {
+  const void* kernel;
+  int threads;
+  size_t smem;
+  int dev;
+  int occ;
+};
+constexpr int kOccEntries = 512;
+OccEntry g_occ[kOccEntries];
+int g_nocc = 0;
+std::mutex g_occ_mu;
+}  // namespace
+
+int cached_occupancy(const void* kernel, int threads, size_t smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  for (int i = 0; i < g_nocc; ++i)
+    if (g_occ[i].kernel == kernel && g_occ[i].threads == threads && g_occ[i].smem == smem && g_occ[i].dev == dev)
+      return g_occ[i].occ;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 0;
+  }
+  if (occ < 1) occ = 1;
+  if (g_nocc < kOccEntries) g_occ[g_nocc++] = OccEntry{kernel, threads, smem, dev, occ};
+  return occ;
 }
 
 }  // namespace kvq

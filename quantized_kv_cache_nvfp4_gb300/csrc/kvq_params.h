@@ -241,4 +241,9 @@ cudaError_t launch_payload_decode(const UnpackParams& p, int lanes, bool v8, cud
 
 int num_sms();
 
+// Resident blocks per SM of a kernel at a block size and dynamic shared memory, on the
+// current device; queried once per (kernel, block size, shared memory, device) and
+// kept, so eager calls do not repeat the occupancy query.  At least 1.
+int cached_occupancy(const void* kernel, int threads, size_t smem);
+
 }  // namespace kvq

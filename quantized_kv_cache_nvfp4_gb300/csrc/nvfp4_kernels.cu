@@ -338,9 +338,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) nvfp4_decode_kernel(cons
 // times the number of blocks that can be resident at once (SMs x occupancy).
 template <typename K>
 int grid_for(K kernel, uint32_t rows, int rows_per_cta, int factor) {
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
-  if (occ < 1) occ = 1;
+  const int occ = cached_occupancy(reinterpret_cast<const void*>(kernel), kThreads, 0);
   int64_t need = (static_cast<int64_t>(rows) + rows_per_cta - 1) / rows_per_cta;
   int64_t cap = static_cast<int64_t>(num_sms()) * occ * factor;
   if (need < 1) need = 1;

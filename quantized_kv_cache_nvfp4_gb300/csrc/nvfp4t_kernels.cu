@@ -274,9 +274,7 @@ __global__ void __launch_bounds__(kThreads) tensor_key_decode_kernel(const Tenso
 
 template <typename K>
 int grid_for(K kernel, uint32_t work, size_t smem = 0) {
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
-  if (occ < 1) occ = 1;
+  const int occ = cached_occupancy(reinterpret_cast<const void*>(kernel), kThreads, smem);
   const int64_t need = (static_cast<int64_t>(work) + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
   return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));

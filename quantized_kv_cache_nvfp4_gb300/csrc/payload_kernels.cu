@@ -362,9 +362,7 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
 template <bool kInPlace, int RS, int RPL>
 cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t s) {
   auto k = int4_key_decode_kernel<kInPlace, RS, RPL>;
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
-  if (occ < 1) occ = 1;
+  const int occ = cached_occupancy(reinterpret_cast<const void*>(k), kThreads, 0);
   const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
   int64_t need = (warps + kThreads / 32 - 1) / (kThreads / 32);
   const int64_t cap = static_cast<int64_t>(num_sms()) * occ * 2;
@@ -403,9 +401,7 @@ cudaError_t key_decode_dispatch(const UnpackParams& u, cudaStream_t s) {
 template <int L, int BPL, bool kV8, int kFmt, int kMode>
 cudaError_t pl_launch(const UnpackParams& u, cudaStream_t s) {
   auto k = payload_kernel<L, BPL, kV8, kFmt, kMode>;
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0);
-  if (occ < 1) occ = 1;
+  const int occ = cached_occupancy(reinterpret_cast<const void*>(k), kThreads, 0);
   int64_t need;
   if (kMode == 2)  // one warp per run of u.run tokens
     need = ((static_cast<int64_t>(u.src_rows) + u.run - 1) / u.run + kThreads / 32 - 1) / (kThreads / 32);
