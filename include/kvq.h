@@ -4,8 +4,8 @@
  * The library turns bf16 K/V rows into compact KV-cache formats and back, with
  * hand-written sm_103a CUDA kernels:
  *   - NVFP4 row codec: per (token, KV head) row of head_dim values, packed E2M1
- *     nibbles (low nibble = even element), one E4M3 block scale per 16 values and
- *     one FP32 row scale: head_dim/2 + head_dim/16 + 4 bytes (76 B at head_dim 128).
+ *     nibbles (low nibble = even element), an E4M3 scale for each block of 16 and
+ *     an FP32 scale for the row: head_dim/2 + head_dim/16 + 4 bytes (76 B at head_dim 128).
  *     Source: "feat(kvcache): add nvfp4 kv quantization (FreeToken PR #408)",
  *     Summary and the codec-delta port note.
  *   - INT4 affine codec with group size G (G64 by default), FP32 arithmetic and
@@ -14,8 +14,8 @@
  *     packing/unpacking and cross-loop residual reconstruction", Purpose.
  *   - Residual encode/decode against the reconstructed predecessor with a compact
  *     int32 position map (same page, Purpose).
- *   - FP8 E4M3 row codec: head_dim E4M3 codes plus one FP32 symmetric scale per
- *     (token, KV head) row, in a code buffer with the geometry of the bf16 one.
+ *   - FP8 E4M3 row codec: one E4M3 byte per element and a single FP32 scale for
+ *     each (token, KV head) row, in a code buffer with the geometry of the bf16 one.
  *     Source: FreeToken PR #408, the fp8 store notes.
  *
  * Conventions shared by every entry point
@@ -164,7 +164,7 @@ typedef struct {
 /* Fused quantise + scatter of K and V into a paged pool (the encode hot path), each
  * in its plane's format (NVFP4, or FP8 E4M3 with one FP32 scale per row).
  * Source: FreeToken PR #408, Summary ("CUDA Graph-safe KV writes") and the fp8 store
- * notes (slot ids arrive as a device tensor; one launch under graph capture).
+ * notes (the destination slots are read from a device tensor; one launch under graph capture).
  *   k, v       bf16 [num_tokens][num_heads][head_dim] views; either may be NULL
  *              (that tensor is not stored); not both.
  *   slot_ids   device int64 [num_tokens]; token t goes to slot slot_ids[t]; a
@@ -206,7 +206,7 @@ KVQ_API kvq_status kvq_unpack(const kvq_packed* in, const kvq_bf16_out* y, kvq_s
 
 /* Residual encode against the reconstructed predecessor.
  * Source: vllm-rlt PR #166, Purpose (encode_residual(current, previous, kind,
- * format); compact sparse rows carry an owned int32 position map).
+ * format); the kept rows are packed together, each call owning its int32 position list).
  *   cur, prev   bf16 [num_rows][heads][dim] (heads/dim from payload).
  *   pos         device int32 [num_pos], strictly increasing in [0, num_rows), or
  *               NULL for the dense case (then num_pos must equal num_rows).

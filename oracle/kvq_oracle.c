@@ -6,19 +6,23 @@
  *
  * Sources (page title, then the section of the page):
  *  - "vllm-rlt PR #166: INT4 KV packing/unpacking and cross-loop residual
- *    reconstruction", Purpose: INT4 affine FP32 quantisation with FP16 min/scale;
- *    NVFP4 with E2M1 nearest-even codes, E4M3 block scales and an FP32 scale;
- *    direct-division fallback when a tiny scale's reciprocal overflows; K grouped
- *    over token rows per (head, channel), V over channels per (token, head);
- *    residuals subtract the reconstructed predecessor in the input dtype; compact
- *    sparse rows carry an int32 position map and absent rows inherit the
- *    predecessor.  Review by 0z5a: INT4 G64 costs 4 + 32/64 bits per element;
- *    codes are computed in FP32 before the FP16 metadata is rounded.
+ *    reconstruction", Purpose: the INT4 affine codec works in FP32 and keeps its
+ *    minimum and scale as FP16; the NVFP4 codec rounds elements to the nearest
+ *    E2M1 value (ties even) under E4M3 scales of 16-value blocks and one FP32
+ *    scale; a scale so small that its reciprocal is infinite is divided by
+ *    directly; K groups run along token rows at a fixed (head, channel) and V
+ *    groups along channels at a fixed (token, head); a residual is the current
+ *    tensor minus the reconstruction of its predecessor, taken in bf16; sparse
+ *    residuals keep their rows packed together with an int32 map of positions,
+ *    and a row missing from the map keeps its predecessor.  Review by 0z5a: the
+ *    G64 format spends 4 + 32/64 bits on each element; the codes come from the
+ *    FP32 minimum and scale, which are rounded to FP16 only afterwards.
  *  - "feat(kvcache): add nvfp4 kv quantization (FreeToken PR #408)", Summary and the
- *    codec-delta port note: one FP32 row scale per (token, KV head), packed E2M1
- *    nibbles low nibble first, one E4M3 scale per 16 values, quantisation against
- *    the stored (rounded) block scale, 76 B per row at head_dim 128, paged slots
- *    given as a device tensor of slot ids.
+ *    codec-delta port note: each (token, KV head) row has its own FP32 scale; two
+ *    E2M1 codes share a byte, the even element in the low nibble; every 16 values
+ *    share an E4M3 scale, and elements are quantised against that scale after
+ *    its rounding; a head_dim-128 row takes 76 B; the paged store reads its
+ *    destination slots from a device tensor.
  *
  * Readings where the pages leave a step open, one per step of the method:
  *  R1  row scale rs = amax / 2688 (2688 = 6 * 448), stored as the decode multiplier.
@@ -266,9 +270,10 @@ void orc_nvfp4_decode_rows(const uint8_t* codes, const uint8_t* bscale, const fl
 
 /* ------------------------------------------------------------------------- */
 /* FP8 E4M3 row codec ("feat(kvcache): add nvfp4 kv quantization (FreeToken PR */
-/* #408)", fp8 store notes: a row becomes head_dim e4m3 codes plus one FP32    */
-/* symmetric scale).  Readings, as for NVFP4: rs = amax / 448 stored as the    */
-/* decode multiplier; q = x * (1 / rs), or x / rs when the reciprocal          */
+/* #408)", fp8 store notes: every element of a row is stored as one E4M3     */
+/* byte, and the row has one FP32 scale).  Readings, as for NVFP4:             */
+/* rs = amax / 448 stored as the decode multiplier; q = x * (1 / rs), or       */
+/* x / rs when the reciprocal                                                  */
 /* overflows; code = e4m3_rne(q) (saturating at 448, sign of x);               */
 /* decode y = bf16(e4m3 * rs).                                                 */
 /* ------------------------------------------------------------------------- */
@@ -412,10 +417,10 @@ uint32_t orc_fp8_restore(const uint8_t* codes, const float* rscale, int64_t num_
 }
 
 /* ------------------------------------------------------------------------- */
-/* NVFP4 with one FP32 scale per tensor ("vllm-rlt PR #166", Purpose: E4M3     */
-/* block scales and a scalar FP32 global encoding multiplier after vLLM's      */
-/* reference; G16 blocks along the kind's axis, K over token rows, V over      */
-/* channels; partial groups allowed).  The scale is the tensor's amax / 2688,  */
+/* NVFP4 with one FP32 scale per tensor ("vllm-rlt PR #166", Purpose: blocks   */
+/* of 16 with E4M3 scales, plus one FP32 number for the whole tensor, as in     */
+/* vLLM's reference; K blocks run along token rows, V blocks along channels;   */
+/* the last block may be short).  The scale is the tensor's amax / 2688,       */
 /* stored as the decode multiplier (R1 read per tensor); each block follows    */
 /* R2-R3 against it.                                                           */
 /* ------------------------------------------------------------------------- */

@@ -2,17 +2,18 @@
 //
 // Format ("vllm-rlt PR #166: INT4 KV packing/unpacking and cross-loop residual
 // reconstruction", Purpose, and the review by 0z5a): groups of G values share an
-// FP16 minimum and an FP16 scale; codes are computed in FP32 BEFORE the metadata is
-// rounded to FP16; K groups run over G token rows per (head, channel), V groups over
-// G channels per (token, head); the last group may be partial.  Per group, in order
+// FP16 minimum and an FP16 scale; the codes come from the FP32 minimum and scale, and
+// only then is the metadata rounded to FP16; K groups span G token rows at a fixed
+// (head, channel), V groups G channels at a fixed (token, head); the last group may
+// be short.  Per group, in order
 // (binary32, nearest even):
 //   mn = min x;  mx = max x;  sc = (mx - mn) / 15
 //   code = 0 if sc == 0, else clamp(rint((x - mn) / sc), 0, 15)   (rint: ties even)
 //   stored: fp16(mn), fp16(sc); two codes per byte, low nibble = even channel.
 // The minimum and maximum order -0 below +0 (IEEE 754-2019 minimum/maximum).
 // Residual encode feeds the same codec with r = bf16(cur - prev) of the kept rows
-// (same page, Purpose: residuals subtract the reconstructed predecessor in the
-// input dtype; K groups follow the compact row order).
+// (same page, Purpose: a residual is taken against the reconstruction of the
+// previous loop, in bf16; K groups follow the order of the packed rows).
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 

@@ -12,8 +12,8 @@
 //                 inv = 1 / s (0 when s == 0);  q = x * inv, or x / s when inv is inf
 //                 code = e2m1(q) (nearest even, saturating at 6, sign of x)
 //   decode: y = bf16((e2m1 * bs) * rs)  (the inner product is exact)
-// The tiny-scale direct division follows "vllm-rlt PR #166: INT4 KV packing ...",
-// Purpose ("a direct-division fallback when their reciprocal overflows").
+// Dividing by s itself when 1 / s is infinite is the tiny-scale rule of "vllm-rlt
+// PR #166: INT4 KV packing ...", Purpose.
 //
 // FP8 E4M3 rows ("feat(kvcache): ... (FreeToken PR #408)", fp8 store notes) take the
 // same kernels with kFmt = 3: rs = amax / 448; q = x * (1 / rs) (x / rs when the

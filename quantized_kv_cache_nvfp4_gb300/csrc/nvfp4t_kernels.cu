@@ -1,8 +1,8 @@
 // nvfp4t_kernels.cu -- NVFP4 with one FP32 scale per tensor: the logical layout of
 // "vllm-rlt PR #166: INT4 KV packing/unpacking and cross-loop residual reconstruction"
-// (Purpose: E4M3 block scales and a scalar FP32 global encoding multiplier; G16
-// blocks along the kind's axis, K over token rows per head/channel, V over channels
-// per token/head; partial groups allowed).
+// (Purpose): blocks of 16 values with E4M3 scales plus one FP32 number for the
+// whole tensor; K blocks run along 16 token rows at a fixed head and channel, V
+// blocks along 16 channels at a fixed token and head; the last block may be short.
 //
 // rs = amax of the whole tensor / 2688, kept as the decode multiplier; each block of
 // 16 takes the row codec's steps against it: block scale e4m3(min((vb/6)/rs, 448)),
