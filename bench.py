@@ -837,16 +837,21 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
-CASES = ("attention_nvfp4", "attention_fp8", "attention_k8v4", "int4_pack_key", "int4_pack_value",
-         "int4_residual_key", "int4_decode_inplace_key", "nvfp4t_pack_key", "nvfp4t_pack_value")
+CASES = ("attention_nvfp4", "attention_fp8", "attention_k8v4",
+         "int4_pack_key", "int4_pack_value", "int4_unpack_key", "int4_unpack_value",
+         "int4_residual_key", "int4_residual_value", "int4_decode_copy_key", "int4_decode_copy_value",
+         "int4_decode_inplace_key", "int4_decode_inplace_value",
+         "nvfp4_pack", "nvfp4_unpack", "nvfp4_residual", "nvfp4_decode_copy", "nvfp4_decode_inplace",
+         "fp8_pack", "fp8_unpack", "fp8_residual", "fp8_decode_copy", "fp8_decode_inplace",
+         "nvfp4t_pack_key", "nvfp4t_pack_value", "nvfp4t_unpack_key", "nvfp4t_unpack_value")
 
 
 def run_case(args):
     """One kernel's workload alone (for profiler captures): `args.warmup` untimed calls,
     then `args.steps` timed ones; prints one JSON line with the mean time per call.
     attention_*: the decode-attention pool of 32 x 8192 tokens, 8 KV / 32 query heads,
-    D128; int4_* and nvfp4t_*: a [131072, 8, 128] bf16 tensor (residual encode and the
-    in-place decode: 25% of rows)."""
+    D128; the codec cases, <format>_<operation>[_<decode mode>][_<kind>]: a
+    [131072, 8, 128] bf16 tensor (residual encode and decode: 25% of rows kept)."""
     import math
 
     import quantized_kv_cache_nvfp4_gb300 as kvq
@@ -876,25 +881,35 @@ def run_case(args):
                          device=device)
         fn = lambda: kvq.kvq_decode_attention(pool, table, lens, T, q, 1.0 / math.sqrt(D), out, workspace=ws)
     else:
+        # <format>_<operation>[_<decode mode>][_<kind>] on a [131072, 8, 128] bf16 tensor
         T, H, D, G = 131072, 8, 128, 64
         cur, prev = synth.layer_kv(T, H, D, seed=4, device=str(device))
+        parts = name.split("_")
+        fmt = {"int4": kvq.FMT_INT4, "nvfp4": kvq.FMT_NVFP4, "fp8": kvq.FMT_FP8,
+               "nvfp4t": kvq.FMT_NVFP4_TENSOR}[parts[0]]
+        op = parts[1]
         kind = kvq.KIND_KEY if name.endswith("key") else kvq.KIND_VALUE
-        if name.startswith("int4_pack"):
-            pk = kvq.Packed.empty(kvq.FMT_INT4, kind, T, H, D, G, device=device)
-            fn = lambda: kvq.kvq_pack(cur, pk)
-        elif name.startswith("int4_residual"):
+        if op in ("pack", "unpack"):
+            pk = kvq.Packed.empty(fmt, kind, T, H, D, G, device=device)
+            if op == "pack":
+                fn = lambda: kvq.kvq_pack(cur, pk)
+            else:
+                kvq.kvq_pack(cur, pk)
+                y = torch.empty_like(cur)
+                fn = lambda: kvq.kvq_unpack(pk, y)
+        else:  # residual encode, or decode into a separate output / in place; 25% of rows kept
             pos = synth.sorted_positions(T, T // 4, 4).to(device)
-            pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 4, H, D, G, device=device)
-            fn = lambda: kvq.kvq_encode_residual(cur, prev, pos, pay)
-        elif name.startswith("int4_decode_inplace"):
-            pos = synth.sorted_positions(T, T // 4, 4).to(device)
-            pay = kvq.Packed.empty(kvq.FMT_INT4, kind, T // 4, H, D, G, device=device)
-            kvq.kvq_encode_residual(cur, prev, pos, pay)
-            y = prev.clone()
-            fn = lambda: kvq.kvq_decode_residual(pay, pos, y, y)
-        else:
-            pk = kvq.Packed.empty(kvq.FMT_NVFP4_TENSOR, kind, T, H, D, device=device)
-            fn = lambda: kvq.kvq_pack(cur, pk)
+            pay = kvq.Packed.empty(fmt, kind, T // 4, H, D, G, device=device)
+            if op == "residual":
+                fn = lambda: kvq.kvq_encode_residual(cur, prev, pos, pay)
+            else:
+                kvq.kvq_encode_residual(cur, prev, pos, pay)
+                if parts[2] == "copy":
+                    out = torch.empty_like(prev)
+                    fn = lambda: kvq.kvq_decode_residual(pay, pos, prev, out)
+                else:
+                    y = prev.clone()
+                    fn = lambda: kvq.kvq_decode_residual(pay, pos, y, y)
     for _ in range(max(args.warmup, 1)):
         fn()
     torch.cuda.synchronize(device)
