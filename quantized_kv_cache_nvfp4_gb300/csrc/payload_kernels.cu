@@ -125,18 +125,6 @@ __device__ __forceinline__ int32_t ld_i32_early(const int32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ int32_t lower_bound(const int32_t* pos, int32_t n, int32_t t) {
-  int32_t lo = 0, hi = n;  // first index with pos[i] >= t
-  while (lo < hi) {
-    const int32_t mid = (lo + hi) >> 1;
-    if (LDX(pos + mid) < t)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  return lo;
-}
-
 template <int L, int BPL, bool kV8, int kFmt, int kMode>
 __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u) {
   constexpr int kRowsPerWarp = 32 / L;
@@ -156,15 +144,43 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
       }
     }
   }
-  if (b0 >= u.nb) return;  // no shuffles below: idle lanes may leave
-
   if constexpr (kMode == 2) {
-    // residual decode into a separate output: every row t of out, runs of u.run tokens
+    // residual decode into a separate output: every row t of out, in runs of u.run <= 32
+    // tokens per warp.  The kept tokens of a run come from one read of the position
+    // map: a 32-way search finds the first position at or after the run's first token,
+    // the 32 lanes read the positions from there, and their OR is the run's bit mask of
+    // kept tokens; a kept token's compact index is that first index plus the kept
+    // tokens before it.  Lanes without a block of their own join the search and the OR
+    // and do nothing else.
+    const bool active = b0 < u.nb;
     const uint32_t nruns = (static_cast<uint32_t>(u.src_rows) + u.run - 1) / u.run;
     for (uint32_t run = gwarp; run < nruns; run += nwarps) {
       const int32_t t0 = static_cast<int32_t>(run * u.run);
       const int32_t t1 = min(u.src_rows, t0 + u.run);
-      int32_t cur = (u.pos != nullptr) ? lower_bound(u.pos, u.num_pos, t0) : 0;
+      int32_t cur = 0;
+      uint32_t kept = 0u;
+      if (u.pos != nullptr) {
+        // first index a with pos[a] >= t0 (num_pos if none), kept within [lo, hi]; with
+        // a sorted map the probes below t0 form a prefix of the lanes
+        int32_t lo = 0, hi = u.num_pos;
+        while (hi - lo >= 32) {
+          const int32_t step = (hi - lo + 31) / 32;
+          const int32_t idx = lo + lane * step;
+          const bool below = idx < hi && LDX(u.pos + idx) < t0;
+          const int n = __popc(__ballot_sync(0xFFFFFFFFu, below));
+          if (n == 0) {
+            hi = lo;
+          } else {
+            hi = min(hi, lo + n * step);
+            lo = lo + (n - 1) * step + 1;
+          }
+        }
+        const bool below = lo + lane < hi && LDX(u.pos + lo + lane) < t0;
+        cur = lo + __popc(__ballot_sync(0xFFFFFFFFu, below));
+        const int32_t pv = cur + lane < u.num_pos ? LDX(u.pos + cur + lane) : t1;
+        kept = __reduce_or_sync(0xFFFFFFFFu, (pv >= t0 && pv < t1) ? (1u << (pv - t0)) : 0u);
+      }
+      if (!active) continue;
       const uint32_t rend = static_cast<uint32_t>(t1) * u.H;
       // two rows a step: both rows' payload and prev loads are issued before either
       // row is combined and stored
@@ -178,11 +194,11 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
           ok[k] = rk < rend;
           u.div_h.divmod(ok[k] ? rk : row, t[k], h[k]);
           p[k] = t[k];
-          if (u.pos != nullptr) {  // the rows ascend, so one forward scan serves both
-            while (cur < u.num_pos && LDX(u.pos + cur) < static_cast<int32_t>(t[k])) ++cur;
+          if (u.pos != nullptr) {
+            const uint32_t bit = t[k] - static_cast<uint32_t>(t0);
             // both arms signed: -1 must stay negative
-            p[k] = (cur < u.num_pos && LDX(u.pos + cur) == static_cast<int32_t>(t[k])) ? static_cast<int64_t>(cur)
-                                                                                      : static_cast<int64_t>(-1);
+            p[k] = ((kept >> bit) & 1u) ? static_cast<int64_t>(cur + __popc(kept & ((1u << bit) - 1u)))
+                                        : static_cast<int64_t>(-1);
           }
         }
         uint32_t w[2][BPL][8], q[2][BPL][8];
@@ -212,6 +228,7 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
     }
     return;
   }
+  if (b0 >= u.nb) return;  // no shuffles below: idle lanes may leave
 
   const uint32_t stride = nwarps * kRowsPerWarp;
   for (uint32_t row = gwarp * kRowsPerWarp + sub; row < u.total_rows; row += stride) {
@@ -377,11 +394,11 @@ template <bool kInPlace>
 cudaError_t key_decode_dispatch(const UnpackParams& u, cudaStream_t s) {
   const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
   if constexpr (kInPlace) {
-    switch (u.pay.G) {  // RS = G / RPL lanes per column task; 4 rows a lane (prev held too)
-      case 16: return key_decode_launch<kInPlace, 4, 4>(u, ntask, s);
-      case 32: return key_decode_launch<kInPlace, 8, 4>(u, ntask, s);
-      case 64: return key_decode_launch<kInPlace, 16, 4>(u, ntask, s);
-      case 128: return key_decode_launch<kInPlace, 32, 4>(u, ntask, s);
+    switch (u.pay.G) {  // RS = G / RPL lanes per column task; 8 rows a lane (prev held too)
+      case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
+      case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
+      case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
+      case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
       case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
       case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
     }
@@ -439,9 +456,9 @@ cudaError_t pl_dispatch_fm(const UnpackParams& u, cudaStream_t s) {
 
 cudaError_t launch_payload_decode(const UnpackParams& u_in, int /*lanes*/, bool v8, cudaStream_t s) {
   UnpackParams u = u_in;
-  // copy mode: runs of 4..64 tokens, about 32 runs per SM
+  // copy mode: runs of 4..32 tokens, about 32 runs per SM
   const int64_t per = (static_cast<int64_t>(u.src_rows) + num_sms() * 32 - 1) / (num_sms() * 32);
-  u.run = static_cast<int32_t>(per < 4 ? 4 : (per > 64 ? 64 : per));
+  u.run = static_cast<int32_t>(per < 4 ? 4 : (per > 32 ? 32 : per));
   if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode != 2)
     return u.mode == 0 ? key_decode_dispatch<false>(u, s) : key_decode_dispatch<true>(u, s);
   const int bpl = (u.nb % 2 == 0) ? 2 : 1;
