@@ -704,20 +704,9 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
 
 // Splits and tokens per split of a decode-attention call (tokens per split a multiple
 // of 64: whole 16-token tiles for each of the 4 warps).
-static void attn_geometry(int32_t S, int32_t H, int32_t max_seq_len, int* nsplit, int* split_len) {
-  *nsplit = attn_num_splits(S, H, max_seq_len);
-  const int64_t per = (static_cast<int64_t>(max_seq_len) + *nsplit - 1) / *nsplit;
-  *split_len = static_cast<int>(((per + 63) / 64) * 64);
-  if (*split_len <= 0) *split_len = 64;
-}
-
 KVQ_API size_t kvq_decode_attention_workspace(int32_t num_seqs, int32_t num_heads, int32_t num_q_heads,
                                               int32_t head_dim, int32_t max_seq_len) {
-  if (num_seqs <= 0 || num_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
-  int nsplit = 1, split_len = 64;
-  attn_geometry(num_seqs, num_heads, max_seq_len, &nsplit, &split_len);
-  if (nsplit <= 1) return 0;
-  return static_cast<size_t>(num_seqs) * num_q_heads * nsplit * (head_dim + 2) * sizeof(float);
+  return attn_workspace_bytes(num_seqs, num_heads, num_q_heads, head_dim, max_seq_len);
 }
 
 }  // extern "C"
@@ -763,7 +752,7 @@ kvq_status decode_attention_impl(const kvq_pool* pool, const int32_t* block_tabl
   if (dev_status != nullptr && (st = check_dev(dev_status, "dev_status")) != KVQ_OK) return st;
 
   AttnParams p{};
-  attn_geometry(num_seqs, H, max_seq_len, &p.nsplit, &p.split_len);
+  p.max_len = max_seq_len;
   const size_t need = kvq_decode_attention_workspace(num_seqs, H, num_q_heads, D, max_seq_len);
   if (builtin && need > 0) {
     if (need > attn_builtin_scratch_bytes())

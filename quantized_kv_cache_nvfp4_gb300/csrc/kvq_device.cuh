@@ -515,6 +515,59 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// mbarrier objects in shared memory (8 bytes, 8-byte aligned), addressed by their
+// 32-bit shared-window address.
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t arrivals) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(arrivals) : "memory");
+}
+// Makes this thread's initialisations visible to the other threads and to the bulk-copy
+// unit; a __syncthreads follows it.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+// One arrival that also raises the phase's expected transaction count by `bytes`.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// Tests whether the phase of the given parity has completed; while it has not, the
+// thread may be suspended for at most about a microsecond first.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(mbar), "r"(parity), "r"(1000u)
+      : "memory");
+  return done != 0u;
+}
+// Waits for the phase of the given parity to complete, giving up after a bounded number
+// of tries (about 0.1 s); returns whether the phase completed.
+constexpr int kMbarTries = 1 << 17;
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  for (int n = 0; n < kMbarTries; ++n)
+    if (mbar_try_wait(mbar, parity)) return true;
+  return false;
+}
+// Bulk copy (cp.async.bulk) of `bytes` bytes (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory; its completion counts `bytes` against the
+// current phase of the mbarrier at `mbar`.  The checked build stores zeros, and
+// completes the count itself, instead of copying from outside a registered range.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  if (!KVQ_OK(src, bytes, 16)) {
+    for (uint32_t o = 0; o < bytes; o += 16)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + o), "r"(0u) : "memory");
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+    return;
+  }
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");

@@ -224,14 +224,18 @@ struct AttnParams {
   FastDiv div_bs;
   int64_t num_blocks;
   int32_t S, H, Hq, D, group;  // group = Hq / H query heads per KV head
-  int32_t nsplit;
-  int32_t split_len;        // tokens per split, a multiple of 64
+  int32_t max_len;          // max_seq_len of the call (the split policy's input)
+  int32_t nsplit;           // set by the launch: token splits per sequence
+  int32_t split_len;        // set by the launch: tokens per split
   float scale;              // softmax scale applied to q . k
   uint32_t* status;
 };
 
-// Split count for a call: enough CTAs to fill the GPU, each split at least 256 tokens.
+// Split count of the head-major kernel: enough CTAs to fill the GPU, each split at
+// least 256 tokens.
 int attn_num_splits(int32_t S, int32_t H, int32_t max_seq_len);
+// Workspace bytes for the split partials of a call, whichever kernel serves it.
+size_t attn_workspace_bytes(int32_t S, int32_t H, int32_t Hq, int32_t D, int32_t max_seq_len);
 cudaError_t launch_decode_attention(const AttnParams& p, cudaStream_t s);
 // The library's built-in split scratch (device memory in the library image, for the
 // entry point that allocates nothing): its device address and size in bytes.
