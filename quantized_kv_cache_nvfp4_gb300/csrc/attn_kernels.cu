@@ -618,6 +618,9 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
     cp_async_commit();
   }
   cp_async_wait<0>();
+  // the merge kernel (when the sequence is split) may be scheduled from here on; it
+  // waits for this grid's writes before it reads them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, 2u);
   // row sums over the 8 lanes (tokens) of each head
 #pragma unroll
@@ -685,30 +688,68 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 }
 
 // Merge of the splits of each (sequence, query head): o = sum_k O_k 2^(M_k - M) /
-// sum_k L_k 2^(M_k - M).  A NaN L (bad sequence) leaves the output untouched.
+// sum_k L_k 2^(M_k - M), one warp per (sequence, query head).  Lane k holds split k's
+// M and L (32 splits at a time), the warp reduces them, and then each lane sums its
+// D/32 dims over the splits, the splits' loads independent of one another.  A NaN L
+// (bad sequence) leaves the output untouched.
+constexpr int kMergeWarps = 4;
+
 template <int D>
-__global__ void __launch_bounds__(D) decode_attn_merge_kernel(const AttnParams p) {
-  const int sq = blockIdx.x;  // s * Hq + qh
+__global__ void __launch_bounds__(32 * kMergeWarps) decode_attn_merge_kernel(const AttnParams p) {
+  constexpr int kDL = D / 32 > 0 ? D / 32 : 1;  // dims per lane (D >= 64: 2, 4 or 8)
+  // launched as a programmatic dependent of the attention kernel: wait for its results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int sq = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // s * Hq + qh
+  if (sq >= p.S * p.Hq) return;
   const int s = sq / p.Hq, qh = sq % p.Hq;
-  const int d = threadIdx.x;
   const float* const base = p.ws + static_cast<int64_t>(sq) * p.nsplit * (D + 2);
   float M = kNegInf;
   bool bad = false;
-  for (int k = 0; k < p.nsplit; ++k) {
-    M = fmaxf(M, LDX(base + k * (D + 2) + D));
-    bad = bad || isnan(LDX(base + k * (D + 2) + D + 1));
+  for (int k0 = 0; k0 < p.nsplit; k0 += 32) {
+    const int k = k0 + lane;
+    if (k < p.nsplit) {
+      M = fmaxf(M, LDX(base + k * (D + 2) + D));
+      bad = bad || isnan(LDX(base + k * (D + 2) + D + 1));
+    }
   }
-  if (bad) return;
-  float L = 0.0f, O = 0.0f;
-  for (int k = 0; k < p.nsplit; ++k) {
-    const float mk = LDX(base + k * (D + 2) + D);
-    const float f = mk == kNegInf ? 0.0f : ex2(mk - M);
-    L += LDX(base + k * (D + 2) + D + 1) * f;
-    O += LDX(base + k * (D + 2) + d) * f;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  if (__any_sync(0xFFFFFFFFu, bad)) return;
+  float L = 0.0f;
+  float o[kDL];
+#pragma unroll
+  for (int i = 0; i < kDL; ++i) o[i] = 0.0f;
+  for (int k0 = 0; k0 < p.nsplit; k0 += 32) {
+    float f = 0.0f;
+    const int kk = k0 + lane;
+    if (kk < p.nsplit) {
+      const float mk = LDX(base + kk * (D + 2) + D);
+      f = mk == kNegInf ? 0.0f : ex2(mk - M);
+      L += LDX(base + kk * (D + 2) + D + 1) * f;
+    }
+    const int nk = min(32, p.nsplit - k0);
+#pragma unroll 4
+    for (int k = 0; k < nk; ++k) {
+      const float fk = __shfl_sync(0xFFFFFFFFu, f, k);
+      const float* const ok = base + (k0 + k) * (D + 2) + kDL * lane;
+#pragma unroll
+      for (int i = 0; i < kDL; i += 2) {
+        const float2 v = LDX(reinterpret_cast<const float2*>(ok + i));  // (D + 2) * 4 bytes is a multiple of 8
+        o[i] += v.x * fk;
+        o[i + 1] += v.y * fk;
+      }
+    }
   }
-  const float y = L > 0.0f ? O / L : 0.0f;
-  STX(p.out + static_cast<int64_t>(s) * p.o_row_pitch + static_cast<int64_t>(qh) * p.o_head_pitch + d,
-      static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, off);
+  uint16_t* const out = p.out + static_cast<int64_t>(s) * p.o_row_pitch + static_cast<int64_t>(qh) * p.o_head_pitch;
+#pragma unroll
+  for (int i = 0; i < kDL; i += 2) {
+    const float y0 = L > 0.0f ? o[i] / L : 0.0f;
+    const float y1 = L > 0.0f ? o[i + 1] / L : 0.0f;
+    STX(reinterpret_cast<uint32_t*>(out + kDL * lane + i), pack_bf16x2(y0, y1));
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -896,6 +937,9 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 2 : 1) decode_attn_page
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * stg);
   }
+  // the merge kernel (when the sequence is split) may be scheduled from here on; it
+  // waits for this grid's writes before it reads them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // row sums over the 8 lanes (tokens) of each head
 #pragma unroll
   for (int off = 4; off <= 16; off <<= 1) {
@@ -998,6 +1042,23 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 2 : 1) decode_attn_page
   }
 }
 
+// The merge as a programmatic dependent launch: it may be scheduled while the attention
+// kernel drains and waits (griddepcontrol.wait) for that kernel's writes.
+template <int D>
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.S * p.Hq + kMergeWarps - 1) / kMergeWarps);
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_attn_merge_kernel<D>, p);
+}
+
 template <int D, int kFK, int kFV, int kNH>
 cudaError_t attn_launch(const AttnParams& p, cudaStream_t s) {
   using T = AttnTile<D, kFK, kFV>;
@@ -1010,8 +1071,7 @@ cudaError_t attn_launch(const AttnParams& p, cudaStream_t s) {
   const dim3 grid(p.nsplit, p.H, p.S);
   KVQ_LAUNCH("decode_attn_kernel", s, k<<<grid, kAttnThreads, T::kSmem, s>>>(p); e = cudaGetLastError());
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  KVQ_LAUNCH("decode_attn_merge_kernel", s,
-             decode_attn_merge_kernel<D><<<p.S * p.Hq, D, 0, s>>>(p); e = cudaGetLastError());
+  KVQ_LAUNCH("decode_attn_merge_kernel", s, e = launch_merge<D>(p, s));
   return e;
 }
 
@@ -1039,8 +1099,7 @@ cudaError_t page_launch(const AttnParams& p, cudaStream_t s) {
   const dim3 grid(p.nsplit, 1, p.S);
   KVQ_LAUNCH("decode_attn_page_kernel", s, k<<<grid, (W + 1) * 32, T::kSmem, s>>>(p); e = cudaGetLastError());
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  KVQ_LAUNCH("decode_attn_merge_kernel", s,
-             decode_attn_merge_kernel<D><<<p.S * p.Hq, D, 0, s>>>(p); e = cudaGetLastError());
+  KVQ_LAUNCH("decode_attn_merge_kernel", s, e = launch_merge<D>(p, s));
   return e;
 }
 
