@@ -838,6 +838,7 @@ def run_reference(args):
 
 
 CASES = ("attention_nvfp4", "attention_fp8", "attention_k8v4",
+         "scatter_nvfp4", "scatter_fp8", "restore_nvfp4", "restore_fp8",
          "int4_pack_key", "int4_pack_value", "int4_unpack_key", "int4_unpack_value",
          "int4_residual_key", "int4_residual_value", "int4_decode_copy_key", "int4_decode_copy_value",
          "int4_decode_inplace_key", "int4_decode_inplace_value",
@@ -850,7 +851,8 @@ def run_case(args):
     """One kernel's workload alone (for profiler captures): `args.warmup` untimed calls,
     then `args.steps` timed ones; prints one JSON line with the mean time per call.
     attention_*: the decode-attention pool of 32 x 8192 tokens, 8 KV / 32 query heads,
-    D128; the codec cases, <format>_<operation>[_<decode mode>][_<kind>]: a
+    D128; scatter_* / restore_*: K and V of the same 32 x 8192-token paged workload; the
+    codec cases, <format>_<operation>[_<decode mode>][_<kind>]: a
     [131072, 8, 128] bf16 tensor (residual encode and decode: 25% of rows kept)."""
     import math
 
@@ -860,7 +862,28 @@ def run_case(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     name = args.case
-    if name.startswith("attention"):
+    if name.startswith(("scatter", "restore")):
+        # the paged restore workload: 32 sequences x 8192 tokens, 8 KV heads, D128, a
+        # shuffled table of 16,384 blocks; K and V
+        S, T, H, D, bs = 32, 8192, 8, 128, BLOCK
+        fmt = kvq.FMT_NVFP4 if name.endswith("nvfp4") else kvq.FMT_FP8
+        nblocks = S * T // bs
+        table = synth.block_permutation(nblocks, 3).to(device).view(S, T // bs).contiguous()
+        t = torch.arange(T, device=device)
+        slots = (table[:, t // bs].long() * bs + t % bs).reshape(-1)
+        lens = torch.full((S,), T, dtype=torch.int32, device=device)
+        pool = kvq.KvPool.empty(nblocks * bs, H, D, bs, device=device, fmt=fmt)
+        k = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_K, device=str(device))
+        v = synth.normal_bf16((S * T, H, D), 3, synth.STREAM_V, device=str(device))
+        kvq.kvq_quant_scatter(k, v, slots, pool)
+        if name.startswith("scatter"):
+            fn = lambda: kvq.kvq_quant_scatter(k, v, slots, pool)
+        else:
+            del k, v
+            ko = torch.empty((S, T, H, D), dtype=torch.bfloat16, device=device)
+            vo = torch.empty_like(ko)
+            fn = lambda: kvq.kvq_restore(pool, table, lens, T, ko, vo)
+    elif name.startswith("attention"):
         S, T, H, Hq, D, bs = 32, 8192, 8, 32, 128, BLOCK
         fk, fv = {"attention_nvfp4": (kvq.FMT_NVFP4, None), "attention_fp8": (kvq.FMT_FP8, None),
                   "attention_k8v4": (kvq.FMT_FP8, kvq.FMT_NVFP4)}[name]
