@@ -117,6 +117,29 @@ def test_long_sequences_merge_several_splits(group):
     _check(out, ref, v, lens, group)
 
 
+@pytest.mark.parametrize("H,bs,fmts", [
+    (4, 16, (NV, NV)), (8, 16, (F8, NV)), (16, 16, (NV, NV)), (16, 32, (F8, F8)),  # page-major kernel
+    (4, 64, (NV, F8)), (1, 32, (NV, NV)),
+    (3, 16, (NV, NV)), (8, 8, (NV, NV)),  # head-major kernel: H = 3, block size 8
+])
+def test_kv_head_counts_and_block_sizes(H, bs, fmts):
+    """Both attention kernels against the oracle: the page-major kernel (block sizes that
+    are multiples of 16, H in {1, 2, 4, 8, 16}: one to eight 16-token chunks a stage,
+    warps of one head merging through shared memory) and the head-major one (other
+    shapes).  Lengths with partial chunks and pages, one empty sequence, and a sequence
+    long enough to be split."""
+    fk, fv = fmts
+    lens = [1, 77, 0, 600, 3000]
+    pool, table, lt, q, v, Tmax = _case(5, H, 4, 128, lens, fk, fv, bs=bs, seed=20 + H + bs)
+    scale = 1.0 / math.sqrt(128)
+    out, st = _run(pool, table, lt, q, Tmax, scale)
+    assert st == 0
+    pk, pv = _planes(pool)
+    ref, ost = O.decode_attention(pk, pv, fk, fv, bs, table.numpy(), lt.numpy(), bits(q), scale)
+    assert ost == 0
+    _check(out, ref, v, lens, 4)
+
+
 @pytest.mark.parametrize("q_scale", [1e-30, 3e4])
 def test_query_magnitudes_outside_f16(q_scale):
     """Queries far below and above the f16 range enter the MMA through the power-of-two
