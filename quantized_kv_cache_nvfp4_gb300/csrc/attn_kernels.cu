@@ -689,14 +689,16 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_kernel(const AttnPar
 
 // Merge of the splits of each (sequence, query head): o = sum_k O_k 2^(M_k - M) /
 // sum_k L_k 2^(M_k - M), one warp per (sequence, query head).  Lane k holds split k's
-// M and L (32 splits at a time), the warp reduces them, and then each lane sums its
-// D/32 dims over the splits, the splits' loads independent of one another.  A NaN L
-// (bad sequence) leaves the output untouched.
+// M and L (32 splits at a time), the warp reduces them, and each lane sums its D/32
+// dims over the splits.  The O rows of the first kPre splits are loaded together with
+// M and L, so a call with up to kPre splits waits for memory once.  A NaN L (bad
+// sequence) leaves the output untouched.
 constexpr int kMergeWarps = 4;
 
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) decode_attn_merge_kernel(const AttnParams p) {
   constexpr int kDL = D / 32 > 0 ? D / 32 : 1;  // dims per lane (D >= 64: 2, 4 or 8)
+  constexpr int kPre = 64 / kDL;               // splits whose O is loaded up front
   // launched as a programmatic dependent of the attention kernel: wait for its results
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
@@ -704,6 +706,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps) decode_attn_merge_kernel(con
   if (sq >= p.S * p.Hq) return;
   const int s = sq / p.Hq, qh = sq % p.Hq;
   const float* const base = p.ws + static_cast<int64_t>(sq) * p.nsplit * (D + 2);
+  const int npre = min(p.nsplit, kPre);
+  float2 pre[kPre][kDL / 2];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k)
+#pragma unroll
+    for (int i = 0; i < kDL / 2; ++i)
+      pre[k][i] = k < npre ? LDX(reinterpret_cast<const float2*>(base + k * (D + 2) + kDL * lane + 2 * i))
+                           : make_float2(0.0f, 0.0f);  // (D + 2) * 4 bytes is a multiple of 8
   float M = kNegInf;
   bool bad = false;
   for (int k0 = 0; k0 < p.nsplit; k0 += 32) {
@@ -728,14 +738,26 @@ __global__ void __launch_bounds__(32 * kMergeWarps) decode_attn_merge_kernel(con
       f = mk == kNegInf ? 0.0f : ex2(mk - M);
       L += LDX(base + kk * (D + 2) + D + 1) * f;
     }
+    if (k0 == 0) {
+#pragma unroll
+      for (int k = 0; k < kPre; ++k) {
+        const float fk = __shfl_sync(0xFFFFFFFFu, f, k);  // 0 past the last split
+#pragma unroll
+        for (int i = 0; i < kDL / 2; ++i) {
+          o[2 * i] += pre[k][i].x * fk;
+          o[2 * i + 1] += pre[k][i].y * fk;
+        }
+      }
+    }
+    const int kfirst = k0 == 0 ? kPre : 0;
     const int nk = min(32, p.nsplit - k0);
 #pragma unroll 4
-    for (int k = 0; k < nk; ++k) {
+    for (int k = kfirst; k < nk; ++k) {
       const float fk = __shfl_sync(0xFFFFFFFFu, f, k);
       const float* const ok = base + (k0 + k) * (D + 2) + kDL * lane;
 #pragma unroll
       for (int i = 0; i < kDL; i += 2) {
-        const float2 v = LDX(reinterpret_cast<const float2*>(ok + i));  // (D + 2) * 4 bytes is a multiple of 8
+        const float2 v = LDX(reinterpret_cast<const float2*>(ok + i));
         o[i] += v.x * fk;
         o[i + 1] += v.y * fk;
       }
