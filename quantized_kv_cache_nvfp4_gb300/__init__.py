@@ -51,10 +51,17 @@ def _check(status: int) -> None:
         raise KvqError(status, _lib().kvq_last_error().decode())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The launch stream: the given torch stream, else the current stream of the
+    current device (its raw handle, without building a Stream object)."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -65,9 +72,10 @@ def _view3(t: torch.Tensor, name: str):
     """(ptr, row_pitch, head_pitch) of a bf16 [rows, heads, dim] tensor, inner stride 1."""
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
-    if t.dim() != 3 or (t.size(2) > 1 and t.stride(2) != 1):
+    st = t.stride()
+    if len(st) != 3 or (st[2] != 1 and t.size(2) > 1):
         raise ValueError(f"{name} must be [rows, heads, dim] with inner stride 1")
-    return t.data_ptr(), t.stride(0), t.stride(1)
+    return t.data_ptr(), st[0], st[1]
 
 
 def _bf16_in(t: torch.Tensor, name: str):
@@ -143,15 +151,25 @@ class KvPool:
         return sum(t.numel() * t.element_size() for t in self._planes())
 
     def _struct(self) -> _abi.Pool:
+        """The C struct of the pool, built once and kept while its planes are the same
+        tensors (a plane replaced by another tensor rebuilds it)."""
+        planes = (self.k_codes, self.k_bscale, self.k_rscale, self.v_codes, self.v_bscale, self.v_rscale)
+        key = tuple(None if t is None else (id(t), t.data_ptr()) for t in planes) + (
+            self.block_size, self.fmt, self.v_fmt)
+        cached = self.__dict__.get("_c_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
         for t in self._planes():
             if not t.is_contiguous():
                 raise ValueError("pool planes must be contiguous")
         bs = lambda t: None if t is None else t.data_ptr()
-        return _abi.Pool(
+        st = _abi.Pool(
             _abi.Plane(self.k_codes.data_ptr(), bs(self.k_bscale), self.k_rscale.data_ptr()),
             _abi.Plane(self.v_codes.data_ptr(), bs(self.v_bscale), self.v_rscale.data_ptr()),
             self.num_slots, self.block_size, self.num_heads, self.head_dim, self.fmt,
             0 if self.v_fmt is None else self.v_fmt)
+        self.__dict__["_c_struct"] = (key, st)
+        return st
 
 
 Nvfp4Pool = KvPool  # the NVFP4 pool is the default format of KvPool
@@ -203,13 +221,22 @@ class Packed:
                    if t is not None)
 
     def _struct(self) -> _abi.Packed:
-        for t in (self.codes, self.meta0, self.meta1, self.rscale):
+        """The C struct, built once and kept while the buffers and sizes are the same."""
+        bufs = (self.codes, self.meta0, self.meta1, self.rscale)
+        key = tuple(None if t is None else (id(t), t.data_ptr()) for t in bufs) + (
+            self.fmt, self.kind, self.group_size, self.rows, self.heads, self.dim)
+        cached = self.__dict__.get("_c_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        for t in bufs:
             if t is not None and not t.is_contiguous():
                 raise ValueError("packed buffers must be contiguous")
-        return _abi.Packed(self.fmt, self.kind, self.group_size, self.rows, self.heads, self.dim,
-                           self.codes.data_ptr(), None if self.meta0 is None else self.meta0.data_ptr(),
-                           None if self.meta1 is None else self.meta1.data_ptr(),
-                           None if self.rscale is None else self.rscale.data_ptr())
+        st = _abi.Packed(self.fmt, self.kind, self.group_size, self.rows, self.heads, self.dim,
+                         self.codes.data_ptr(), None if self.meta0 is None else self.meta0.data_ptr(),
+                         None if self.meta1 is None else self.meta1.data_ptr(),
+                         None if self.rscale is None else self.rscale.data_ptr())
+        self.__dict__["_c_struct"] = (key, st)
+        return st
 
 
 # ---------------------------------------------------------------------------
