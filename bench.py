@@ -545,6 +545,13 @@ def other_rows(kvq, device, T=262144, H=8, D=128, G=64, P=None, iters=20, peak=6
           2 * P * H * 2 * D + 4 * P + pb)
     timed("kvq_decode_residual fp8 25% copy", lambda: kvq.kvq_decode_residual(pay, pos, prev, y),
           rows_b + pb + 4 * P + rows_b)
+    # NVFP4 with one FP32 scale per tensor: pack reads the tensor twice (the amax pass,
+    # then the block encode); blocks run over 16 token rows (K) or 16 channels (V)
+    for kind, kname in ((0, "key"), (1, "value")):
+        nt = kvq.Packed.empty(kvq.FMT_NVFP4_TENSOR, kind, T, H, D, device=device)
+        ntb = T * H * (D // 2) + (-(-T // 16) * H * D if kind == 0 else T * H * (D // 16)) + 4
+        timed(f"kvq_pack nvfp4_tensor {kname}", lambda: kvq.kvq_pack(cur, nt), 2 * rows_b + ntb)
+        timed(f"kvq_unpack nvfp4_tensor {kname}", lambda: kvq.kvq_unpack(nt, y), ntb + rows_b)
     return {"workload": f"[{T} tokens, {H} KV heads, D{D}] bf16, INT4 G{G}, residual rows kept {P}/{T}",
             "kernels": out}
 

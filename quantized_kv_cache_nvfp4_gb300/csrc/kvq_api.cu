@@ -222,6 +222,7 @@ PayloadRef payload_ref(const kvq_packed* pk) {
   r.meta0 = pk->meta0;
   r.meta1 = pk->meta1;
   r.rscale = pk->rscale;
+  r.rs_stride = 1;
   r.rows = pk->rows;
   return r;
 }
@@ -516,6 +517,27 @@ KVQ_API kvq_status kvq_unpack(const kvq_packed* in, const kvq_bf16_out* y, kvq_s
   if (in->rows == 0) return KVQ_OK;
   bool v8 = true;
   if ((st = check_view(y->ptr, y->row_pitch, y->head_pitch, "y", v8)) != KVQ_OK) return st;
+  if (in->fmt == KVQ_FMT_NVFP4_TENSOR && in->kind == KVQ_KIND_VALUE) {
+    // V blocks run along channels: the row codec's layout with one scale shared by
+    // every row, decoded by the row-codec decode kernel with a row-scale stride of 0
+    UnpackParams u{};
+    u.pay = payload_ref(in);
+    u.pay.fmt = KVQ_FMT_NVFP4;
+    u.pay.rs_stride = 0;
+    u.H = in->heads;
+    u.D = in->dim;
+    u.nb = in->dim / 16;
+    u.div_h = FastDiv(static_cast<uint32_t>(in->heads));
+    u.total_rows = static_cast<uint32_t>(in->rows) * static_cast<uint32_t>(in->heads);
+    u.y = static_cast<uint16_t*>(y->ptr);
+    u.y_row_pitch = y->row_pitch;
+    u.y_head_pitch = y->head_pitch;
+    u.mode = 0;
+    dbg_clear();
+    dbg_add(y->ptr, view_bytes(in->rows, y->row_pitch, in->heads, y->head_pitch, in->dim), "y");
+    dbg_packed(in);
+    return launched(launch_payload_decode(u, lanes_for(in->dim), v8, reinterpret_cast<cudaStream_t>(stream)));
+  }
   if (in->fmt == KVQ_FMT_NVFP4_TENSOR) {
     TensorNvfp4Params p{};
     p.codes = in->codes;

@@ -139,7 +139,8 @@ struct PayloadRef {
   const uint8_t* codes;
   const void* meta0;   // nvfp4: bscale; int4: min
   const void* meta1;   // int4: scale
-  const float* rscale; // nvfp4
+  const float* rscale; // nvfp4 / fp8: row scale of row r at rscale[r * rs_stride]
+  int32_t rs_stride;   // 1 (one scale per row), or 0 (one scale for the whole tensor)
   int32_t rows;
 };
 

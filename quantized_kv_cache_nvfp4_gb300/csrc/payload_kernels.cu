@@ -36,7 +36,7 @@ __device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, 
   const PayloadRef& P = u.pay;
   const int64_t prow = p * u.H + h;
   if constexpr (kFmt == 3) {  // FP8: 16 E4M3 bytes per block, one scale per row
-    const float rs = LDX(P.rscale + prow);
+    const float rs = LDX(P.rscale + prow * P.rs_stride);
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
       uint32_t c4[4];
@@ -61,7 +61,7 @@ __device__ __forceinline__ void decode_blocks(const UnpackParams& u, int64_t p, 
       bsb = LDX(reinterpret_cast<const uint16_t*>(bsp));
     else
       bsb = LDX(bsp);
-    const float rs = LDX(P.rscale + prow);
+    const float rs = LDX(P.rscale + prow * P.rs_stride);
 #pragma unroll
     for (int j = 0; j < BPL; ++j) nvfp4_decode16(cw[2 * j], cw[2 * j + 1], (bsb >> (8 * j)) & 0xFFu, rs, w[j]);
   } else {
