@@ -92,6 +92,7 @@ typedef enum { KVQ_KIND_KEY = 0, KVQ_KIND_VALUE = 1 } kvq_kind;
 #define KVQ_DEV_BAD_BLOCK 2u  /* block-table entry < 0 or past the pool (row skipped) */
 #define KVQ_DEV_BAD_POS 4u    /* position outside [0, rows) or not strictly increasing */
 #define KVQ_DEV_BAD_SEQLEN 8u /* seq_lens[s] outside [0, min(max_seq_len, blocks*block_size)] */
+#define KVQ_DEV_TIMEOUT 16u   /* decode attention: a bounded wait for a copy ran out (results unspecified) */
 
 /* A bf16 view: element (r, h, d) is ptr[r*row_pitch + h*head_pitch + d].
  * ptr must be 16-byte aligned and both pitches multiples of 8 elements. */

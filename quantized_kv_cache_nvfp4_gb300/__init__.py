@@ -19,7 +19,7 @@ from typing import Optional
 import torch
 
 from . import _abi
-from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, FMT_FP8, FMT_INT4,
+from ._abi import (DEV_BAD_BLOCK, DEV_BAD_POS, DEV_BAD_SEQLEN, DEV_BAD_SLOT, DEV_TIMEOUT, FMT_FP8, FMT_INT4,
                    FMT_NVFP4_TENSOR,
                    FMT_NVFP4, KIND_KEY, KIND_VALUE)
 
@@ -28,7 +28,7 @@ __all__ = [
     "kvq_unpack", "kvq_encode_residual", "kvq_decode_residual", "kvq_decode_attention",
     "kvq_decode_attention_workspace", "kvq_decode_attention_noalloc", "kvq_storage_bytes",
     "kvq_status_string", "kvq_last_error", "library_path", "FMT_NVFP4", "FMT_INT4", "FMT_FP8", "FMT_NVFP4_TENSOR", "KIND_KEY",
-    "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN",
+    "KIND_VALUE", "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_POS", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
 ]
 
 

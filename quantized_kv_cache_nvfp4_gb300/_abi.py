@@ -28,6 +28,7 @@ DEV_BAD_SLOT = 1
 DEV_BAD_BLOCK = 2
 DEV_BAD_POS = 4
 DEV_BAD_SEQLEN = 8
+DEV_TIMEOUT = 16
 
 
 class Bf16In(ctypes.Structure):

@@ -154,3 +154,20 @@ def test_noalloc_scratch_covers_every_split_workspace(kvq_lib_path):
                     for T in (1, 255, 256, 4096, 1 << 20):
                         worst = max(worst, lib.kvq_decode_attention_workspace(S, H, H * group, D, T))
     assert 0 < worst <= 48 << 20
+
+
+def test_binding_constants_match_the_header():
+    """Every status code, format, kind and device-status bit the header defines has
+    the same value under the same name in the binding (KVQ_ prefix dropped, status
+    codes by name), and the binding names none the header lacks."""
+    from quantized_kv_cache_nvfp4_gb300 import _abi
+
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    header = {m[0]: int(m[1]) for m in re.findall(r"\b(KVQ_(?:FMT|KIND|DEV)_\w+)\s*(?:=\s*|\s+)(\d+)u?\b", text)}
+    status = {m[0]: int(m[1]) for m in re.findall(r"\b(KVQ_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
+    assert len(header) >= 11 and len(status) == 6
+    for name, value in header.items():
+        assert getattr(_abi, name[len("KVQ_"):]) == value, name
+    bound = {n for n in dir(_abi) if re.fullmatch(r"(FMT|KIND|DEV)_[A-Z0-9_]+", n)}
+    assert bound == {n[len("KVQ_"):] for n in header}
+    assert _abi.STATUS_NAMES == {v: k for k, v in status.items()}
