@@ -327,10 +327,20 @@ __device__ __forceinline__ void attn_tile(const TileView& tv, const QB& qb, cons
   bool move = false;
 #pragma unroll
   for (int nh = 0; nh < kNH; ++nh) {
-    sc[nh][0] = dead0 ? kNegInf : sc[nh][0] * kr0;
-    sc[nh][1] = dead0 ? kNegInf : sc[nh][1] * kr0;
-    sc[nh][2] = dead1 ? kNegInf : sc[nh][2] * kr1;
-    sc[nh][3] = dead1 ? kNegInf : sc[nh][3] * kr1;
+    sc[nh][0] *= kr0;
+    sc[nh][1] *= kr0;
+    sc[nh][2] *= kr1;
+    sc[nh][3] *= kr1;
+  }
+  if (nvalid < 16) {  // uniform: the tile ends inside the sequence
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) {
+      if (dead0) sc[nh][0] = sc[nh][1] = kNegInf;
+      if (dead1) sc[nh][2] = sc[nh][3] = kNegInf;
+    }
+  }
+#pragma unroll
+  for (int nh = 0; nh < kNH; ++nh) {
     mt[nh][0] = fmaxf(sc[nh][0], sc[nh][2]) * qmul[nh][0];
     mt[nh][1] = fmaxf(sc[nh][1], sc[nh][3]) * qmul[nh][1];
     move = move || mt[nh][0] > st.m8[nh][0] || mt[nh][1] > st.m8[nh][1];
@@ -813,21 +823,21 @@ struct PageStage {
   static constexpr int kSmem = kOffBar + 2 * kStages * 8 + 16;  // full + empty barriers, the bad flag
 };
 
-template <int D, int kFK, int kFV, int W>
+template <int D, int kFK, int kFV, int W, int H>
 __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 2 : 1) decode_attn_page_kernel(const AttnParams p) {
   using T = PageStage<D, kFK, kFV, W>;
   constexpr int kKS = D / 16;
   constexpr int kMT = D / 16;
   static_assert(kKS <= 8, "Q^T fragments of one head n-tile in registers");
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char page_smem[];
+  unsigned char* const smem = page_smem;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2;
   const int c = lane & 3;
   const int split = blockIdx.x, s = blockIdx.z;
-  const int H = p.H;
-  const int P = W / H;  // 16-token chunks per stage
+  constexpr int P = W / H;  // 16-token chunks per stage (the KV head count H is fixed per instance)
 
   const int len = LDX(p.seq_lens + s);
   const bool bad_len = len < 0 || len > p.seq_cap;
@@ -1112,10 +1122,10 @@ cudaError_t attn_dispatch_group(const AttnParams& p, cudaStream_t s) {
   return p.group <= 8 ? attn_dispatch_fmt<D, 1>(p, s) : attn_dispatch_fmt<D, 2>(p, s);
 }
 
-template <int D, int kFK, int kFV, int W>
+template <int D, int kFK, int kFV, int W, int H>
 cudaError_t page_launch(const AttnParams& p, cudaStream_t s) {
   using T = PageStage<D, kFK, kFV, W>;
-  auto k = decode_attn_page_kernel<D, kFK, kFV, W>;
+  auto k = decode_attn_page_kernel<D, kFK, kFV, W, H>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, 1, p.S);
@@ -1125,18 +1135,26 @@ cudaError_t page_launch(const AttnParams& p, cudaStream_t s) {
   return e;
 }
 
-template <int D, int W>
+template <int D, int W, int H>
 cudaError_t page_dispatch_fmt(const AttnParams& p, cudaStream_t s) {
   const bool k8 = p.fmt_k == 3, v8 = p.fmt_v == 3;
-  if (!k8 && !v8) return page_launch<D, 1, 1, W>(p, s);
-  if (k8 && !v8) return page_launch<D, 3, 1, W>(p, s);
-  if (!k8 && v8) return page_launch<D, 1, 3, W>(p, s);
-  return page_launch<D, 3, 3, W>(p, s);
+  if (!k8 && !v8) return page_launch<D, 1, 1, W, H>(p, s);
+  if (k8 && !v8) return page_launch<D, 3, 1, W, H>(p, s);
+  if (!k8 && v8) return page_launch<D, 1, 3, W, H>(p, s);
+  return page_launch<D, 3, 3, W, H>(p, s);
 }
 
+// One instance per KV head count: the stage layout's strides are then constants.
 template <int D>
 cudaError_t page_dispatch(const AttnParams& p, cudaStream_t s) {
-  return p.H == 16 ? page_dispatch_fmt<D, 16>(p, s) : page_dispatch_fmt<D, 8>(p, s);
+  switch (p.H) {
+    case 1: return page_dispatch_fmt<D, 8, 1>(p, s);
+    case 2: return page_dispatch_fmt<D, 8, 2>(p, s);
+    case 4: return page_dispatch_fmt<D, 8, 4>(p, s);
+    case 8: return page_dispatch_fmt<D, 8, 8>(p, s);
+    case 16: return page_dispatch_fmt<D, 16, 16>(p, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
