@@ -219,25 +219,6 @@ __global__ void tensor_scale_finalize_kernel(float* slot) {
   STX(slot, __fdiv_rn(LDX(slot), kRowScaleDiv));
 }
 
-// Unpack, VALUE kind: one thread per 16-channel block.
-__global__ void __launch_bounds__(kThreads) tensor_value_decode_kernel(const TensorNvfp4Params p) {
-  const uint32_t nb = static_cast<uint32_t>(p.D / 16);
-  const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * nb;
-  const float rs = LDX(p.rscale);
-  for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nblk; i += gridDim.x * kThreads) {
-    uint32_t rh, b, r, h;
-    p.div_nb.divmod(i, rh, b);
-    p.div_h.divmod(rh, r, h);
-    uint32_t c0, c1;
-    load8B(p.codes + static_cast<int64_t>(rh) * (p.D / 2) + 8 * b, c0, c1);
-    uint32_t out[8];
-    nvfp4_decode16(c0, c1, LDX(p.bscale + static_cast<int64_t>(rh) * nb + b), rs, out);
-    uint16_t* dst = p.y + static_cast<int64_t>(r) * p.y_row_pitch + static_cast<int64_t>(h) * p.y_head_pitch + 16 * b;
-    store16B(dst, *reinterpret_cast<const uint32_t(*)[4]>(&out[0]));
-    store16B(dst + 8, *reinterpret_cast<const uint32_t(*)[4]>(&out[4]));
-  }
-}
-
 // Unpack, KEY kind: one thread per 16 channels of a row; each channel has its own
 // block scale (of the row's 16-row group).
 __global__ void __launch_bounds__(kThreads) tensor_key_decode_kernel(const TensorNvfp4Params p) {
@@ -309,18 +290,15 @@ cudaError_t launch_tensor_nvfp4_pack(const TensorNvfp4Params& p, cudaStream_t s)
   return e;
 }
 
+// KEY kind only: V blocks run along channels, the row codec's layout with one scale for
+// every row, and decode through the row-codec decode kernel.
 cudaError_t launch_tensor_nvfp4_unpack(const TensorNvfp4Params& p, cudaStream_t s) {
+  if (p.kind != 0) return cudaErrorInvalidValue;
   const uint32_t nblk = static_cast<uint32_t>(p.rows) * static_cast<uint32_t>(p.H) * static_cast<uint32_t>(p.D / 16);
   cudaError_t e = cudaSuccess;
-  if (p.kind == 0) {
-    KVQ_LAUNCH("tensor_key_decode_kernel", s,
-               tensor_key_decode_kernel<<<grid_for(tensor_key_decode_kernel, nblk), kThreads, 0, s>>>(p);
-               e = cudaGetLastError());
-  } else {
-    KVQ_LAUNCH("tensor_value_decode_kernel", s,
-               tensor_value_decode_kernel<<<grid_for(tensor_value_decode_kernel, nblk), kThreads, 0, s>>>(p);
-               e = cudaGetLastError());
-  }
+  KVQ_LAUNCH("tensor_key_decode_kernel", s,
+             tensor_key_decode_kernel<<<grid_for(tensor_key_decode_kernel, nblk), kThreads, 0, s>>>(p);
+             e = cudaGetLastError());
   return e;
 }
 
