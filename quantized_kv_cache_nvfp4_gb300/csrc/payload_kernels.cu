@@ -17,8 +17,9 @@
 //                     to 64, so that short tensors still spread over the GPU): one
 //                     binary search of the sorted position map at the start of a run,
 //                     then a cursor that only moves forward
-// INT4 K payloads (groups over token rows) decode column-wise instead: see
-// int4_key_decode_kernel.
+// INT4 K unpack (groups over token rows) decodes column-wise instead: see
+// int4_key_decode_kernel.  INT4 K residual decodes run row by row here, each row
+// reading its group's FP16 minimum and scale per channel.
 #include "kvq_device.cuh"
 #include "kvq_params.h"
 
@@ -115,14 +116,6 @@ __device__ __forceinline__ void add_store(const uint16_t* prev, uint16_t* out, i
     }
     store32B<kV8>(out + 16 * (b0 + j), q);
   }
-}
-
-// A 32-bit read the compiler keeps where it is written (volatile), read-only path.
-__device__ __forceinline__ int32_t ld_i32_early(const int32_t* p) {
-  if (!KVQ_OK(p, 4, 4)) return -1;
-  int32_t v;
-  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
 }
 
 template <int L, int BPL, bool kV8, int kFmt, int kMode>
@@ -258,13 +251,12 @@ __global__ void __launch_bounds__(kThreads) payload_kernel(const UnpackParams u)
   }
 }
 
-// INT4 K payloads, unpack (kInPlace = false) or residual decode in place: a column
-// task is (group of G compact rows, head, 8-channel chunk); its FP16 minimum and
-// scale are read once.  RS = G / RPL lanes share a task; each loads the codes of its
-// RPL rows together (4 bytes per row), then writes 16 bytes of bf16 per row (in
-// place: adds to the 16 bytes of prev it also loaded up front).  A warp holds 32/RS
-// consecutive chunks of a row, so every row access is one coalesced span.
-template <bool kInPlace, int RS, int RPL>
+// INT4 K payloads, unpack: a column task is (group of G rows, head, 8-channel chunk);
+// its FP16 minimum and scale are read once.  RS = G / RPL lanes share a task; each
+// loads the codes of its RPL rows together (4 bytes per row), then writes 16 bytes of
+// bf16 per row.  A warp holds 32/RS consecutive chunks of a row, so every row access is
+// one coalesced span.  (The residual decodes of INT4 K run the row-wise payload kernel.)
+template <int RS, int RPL>
 __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackParams u) {
   constexpr int CW = 32 / RS;
   const int lane = threadIdx.x & 31;
@@ -280,7 +272,11 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
   // below 2^31 (always, short of tensors near the memory size), else 64-bit ones
   const bool small = ntask < (int64_t{1} << 31);
   const FastDiv div_c(static_cast<uint32_t>(nchunk));  // built once per thread
-  auto decompose = [&](int64_t task, int32_t& chunk, int32_t& h, int32_t& g) {
+  for (int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32; wt < nwtask;
+       wt += nwarps) {
+    const int64_t task = wt * CW + cl;
+    if (task >= ntask) continue;  // no shuffles in this kernel
+    int32_t chunk, h, g;
     if (small) {
       uint32_t gh, c, gg, hh;
       div_c.divmod(static_cast<uint32_t>(task), gh, c);
@@ -293,35 +289,6 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
       h = static_cast<int32_t>((task / nchunk) % u.H);
       g = static_cast<int32_t>(task / (static_cast<int64_t>(nchunk) * u.H));
     }
-  };
-  // in place with a position map: the positions of the next task's rows, read a task
-  // ahead (the prev reads of a row wait on its position otherwise)
-  int32_t pn[RPL];
-  auto prefetch = [&](int64_t wt) {
-    if constexpr (kInPlace) {
-      const int64_t task = wt * CW + cl;
-      if (u.pos == nullptr || task >= ntask) return;
-      int32_t chunk, h, g;
-      decompose(task, chunk, h, g);
-      const int32_t r0 = g * P.G, r1 = min(P.rows, r0 + P.G);
-#pragma unroll
-      for (int k = 0; k < RPL; ++k) {
-        const int32_t r = r0 + rs + k * RS;
-        pn[k] = r < r1 ? ld_i32_early(u.pos + r) : -1;
-      }
-    }
-  };
-  int64_t wt = blockIdx.x * static_cast<int64_t>(kThreads / 32) + threadIdx.x / 32;
-  prefetch(wt);
-  for (; wt < nwtask; wt += nwarps) {
-    int32_t pc[RPL];
-#pragma unroll
-    for (int k = 0; k < RPL; ++k) pc[k] = pn[k];
-    prefetch(wt + nwarps);
-    const int64_t task = wt * CW + cl;
-    if (task >= ntask) continue;  // no shuffles in this kernel
-    int32_t chunk, h, g;
-    decompose(task, chunk, h, g);
     const int32_t r0 = g * P.G;
     const int32_t r1 = min(P.rows, r0 + P.G);
     const int32_t col = chunk * 8;
@@ -329,29 +296,12 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
     uint32_t a[4], c[4];
     load16B(static_cast<const uint16_t*>(P.meta0) + m, a);
     load16B(static_cast<const uint16_t*>(P.meta1) + m, c);
-    // all loads of this lane's rows first
+    // all code loads of this lane's rows first
     uint32_t cw[RPL];
-    int64_t t[RPL];
-    uint32_t q[RPL][4];
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
       const int32_t r = r0 + rs + k * RS;
-      t[k] = -1;
-      if (r >= r1) continue;
-      cw[k] = LDX(reinterpret_cast<const uint32_t*>(P.codes + (static_cast<int64_t>(r) * u.H + h) * (u.D / 2) + col / 2));
-      t[k] = r;
-      if constexpr (kInPlace) {
-        if (u.pos != nullptr) {
-          t[k] = pc[k];
-          if (chunk == 0 && h == 0 && r > 0 && LDX(u.pos + r - 1) >= t[k]) set_status(u.status, 4u);
-          if (t[k] < 0 || t[k] >= u.src_rows) {
-            if (chunk == 0 && h == 0) set_status(u.status, 4u);
-            t[k] = -1;
-            continue;
-          }
-        }
-        load16B_rw(u.y + t[k] * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col, q[k]);
-      }
+      if (r < r1) cw[k] = LDX(reinterpret_cast<const uint32_t*>(P.codes + (static_cast<int64_t>(r) * u.H + h) * (u.D / 2) + col / 2));
     }
     float mn[8], sc[8];
 #pragma unroll
@@ -363,22 +313,18 @@ __global__ void __launch_bounds__(kThreads) int4_key_decode_kernel(const UnpackP
     }
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
-      if (t[k] < 0) continue;
+      const int32_t r = r0 + rs + k * RS;
+      if (r >= r1) continue;
       uint32_t y[4];
       int4_decode8(cw[k], mn, sc, y);
-      uint16_t* o = u.y + t[k] * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col;
-      if constexpr (kInPlace) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = bf16x2_add(q[k][i], y[i]);
-      }
-      store16B(o, y);
+      store16B(u.y + static_cast<int64_t>(r) * u.y_row_pitch + static_cast<int64_t>(h) * u.y_head_pitch + col, y);
     }
   }
 }
 
-template <bool kInPlace, int RS, int RPL>
+template <int RS, int RPL>
 cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t s) {
-  auto k = int4_key_decode_kernel<kInPlace, RS, RPL>;
+  auto k = int4_key_decode_kernel<RS, RPL>;
   const int occ = cached_occupancy(reinterpret_cast<const void*>(k), kThreads, 0);
   const int64_t warps = (ntask + 32 / RS - 1) / (32 / RS);
   int64_t need = (warps + kThreads / 32 - 1) / (kThreads / 32);
@@ -390,27 +336,15 @@ cudaError_t key_decode_launch(const UnpackParams& u, int64_t ntask, cudaStream_t
   return e;
 }
 
-template <bool kInPlace>
 cudaError_t key_decode_dispatch(const UnpackParams& u, cudaStream_t s) {
   const int64_t ntask = static_cast<int64_t>((u.pay.rows + u.pay.G - 1) / u.pay.G) * u.H * (u.D / 8);
-  if constexpr (kInPlace) {
-    switch (u.pay.G) {  // RS = G / RPL lanes per column task; 8 rows a lane (prev held too)
-      case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
-      case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
-      case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
-      case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
-      case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
-      case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
-    }
-  } else {
-    switch (u.pay.G) {  // RS = G / RPL lanes per column task
-      case 16: return key_decode_launch<kInPlace, 2, 8>(u, ntask, s);
-      case 32: return key_decode_launch<kInPlace, 4, 8>(u, ntask, s);
-      case 64: return key_decode_launch<kInPlace, 8, 8>(u, ntask, s);
-      case 128: return key_decode_launch<kInPlace, 16, 8>(u, ntask, s);
-      case 256: return key_decode_launch<kInPlace, 32, 8>(u, ntask, s);
-      case 512: return key_decode_launch<kInPlace, 32, 16>(u, ntask, s);
-    }
+  switch (u.pay.G) {  // RS = G / RPL lanes per column task
+    case 16: return key_decode_launch<2, 8>(u, ntask, s);
+    case 32: return key_decode_launch<4, 8>(u, ntask, s);
+    case 64: return key_decode_launch<8, 8>(u, ntask, s);
+    case 128: return key_decode_launch<16, 8>(u, ntask, s);
+    case 256: return key_decode_launch<32, 8>(u, ntask, s);
+    case 512: return key_decode_launch<32, 16>(u, ntask, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -459,8 +393,9 @@ cudaError_t launch_payload_decode(const UnpackParams& u_in, int /*lanes*/, bool 
   // copy mode: runs of 4..32 tokens, about 32 runs per SM
   const int64_t per = (static_cast<int64_t>(u.src_rows) + num_sms() * 32 - 1) / (num_sms() * 32);
   u.run = static_cast<int32_t>(per < 4 ? 4 : (per > 32 ? 32 : per));
-  if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode != 2)
-    return u.mode == 0 ? key_decode_dispatch<false>(u, s) : key_decode_dispatch<true>(u, s);
+  // INT4 K unpack runs column-wise; the residual decodes run row by row like every other
+  // payload (in place, the row-wise kernel measured 3% faster than a column-wise one)
+  if (u.pay.fmt == 2 && u.pay.kind == 0 && u.mode == 0) return key_decode_dispatch(u, s);
   const int bpl = (u.nb % 2 == 0) ? 2 : 1;
   int lanes = 1;
   while (lanes < u.nb / bpl) lanes <<= 1;
