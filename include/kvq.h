@@ -259,6 +259,8 @@ KVQ_API kvq_status kvq_decode_residual(const kvq_packed* payload, const int32_t*
  * the attention of the decoded rows.
  * An empty sequence writes zeros.  A bad length (KVQ_DEV_BAD_SEQLEN) or a block
  * entry outside the pool (KVQ_DEV_BAD_BLOCK) leaves that sequence's output untouched.
+ * Every wait of the kernel on a copy into shared memory is bounded (about 0.1 s); one
+ * that runs out sets KVQ_DEV_TIMEOUT, and the call's results are then unspecified.
  * One or two kernel launches. */
 KVQ_API kvq_status kvq_decode_attention(const kvq_pool* pool, const int32_t* block_table,
                                         int32_t num_seqs, int32_t max_blocks, const int32_t* seq_lens,
