@@ -221,3 +221,21 @@ def test_paged_32_sequences_of_8192_tokens_sampled():
     ref2 = torch.nn.functional.scaled_dot_product_attention(q.float()[:, :, None], kr, vr,
                                                             scale=1.0 / math.sqrt(D))[:, :, 0]
     assert (out.float() - ref2).abs().max().item() < 0.02
+
+
+@pytest.mark.parametrize("bs,fmts", [(16, (NV, NV)), (16, (F8, NV)), (8, (NV, F8))])
+def test_many_short_sequences(bs, fmts):
+    """A decode batch of 300 short sequences (0 to 200 tokens, a tenth of them empty):
+    few or no splits, so most outputs are written by the attention kernel itself.
+    Block size 16 runs the page-major kernel, 8 the head-major one."""
+    rng = np.random.default_rng(31 + bs)
+    lens = [0 if rng.random() < 0.1 else int(rng.integers(1, 201)) for _ in range(300)]
+    fk, fv = fmts
+    pool, table, lt, q, v, Tmax = _case(300, 8, 4, 128, lens, fk, fv, bs=bs, seed=40 + bs)
+    scale = 1.0 / math.sqrt(128)
+    out, st = _run(pool, table, lt, q, Tmax, scale)
+    assert st == 0
+    pk, pv = _planes(pool)
+    ref, ost = O.decode_attention(pk, pv, fk, fv, bs, table.numpy(), lt.numpy(), bits(q), scale)
+    assert ost == 0
+    _check(out, ref, v, lens, 4)
