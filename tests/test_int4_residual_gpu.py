@@ -66,21 +66,21 @@ def test_int4_constant_and_exact_groups():
         np.testing.assert_array_equal(bits(y), O.int4_unpack(codes, mn, sc, kind, 64))
 
 
-def _chain(kind, fmt_res, T=4096, H=8, D=128, P=1024, loops=4, seed=4, inplace_check=True):
+def _chain(kind, fmt_res, T=4096, H=8, D=128, P=1024, loops=4, seed=4, inplace_check=True, G=64):
     """Base INT4 pack of loop 0, then loops 1.. residual-encoded against the
     reconstructed predecessor with P kept rows; every step checked against the oracle."""
     stream = synth.STREAM_K if kind == kvq.KIND_KEY else synth.STREAM_V
     L = synth.residual_loops(T, H, D, loops, seed, stream=stream)
-    pk, recon = gpu_int4_pack(L[0].to(DEV), kind)
-    codes, mn, sc = O.int4_pack(bits(L[0]), kind, 64)
+    pk, recon = gpu_int4_pack(L[0].to(DEV), kind, G)
+    codes, mn, sc = O.int4_pack(bits(L[0]), kind, G)
     check_int4(pk, codes, mn, sc)
-    recon_o = O.int4_unpack(codes, mn, sc, kind, 64)
+    recon_o = O.int4_unpack(codes, mn, sc, kind, G)
     np.testing.assert_array_equal(bits(recon), recon_o)
     st = status_word()
     for i in range(1, loops):
         pos = synth.sorted_positions(T, P, seed, stream=synth.STREAM_POS + i) if P is not None else None
         n = T if pos is None else P
-        pay = kvq.Packed.empty(fmt_res, kind, n, H, D, 64)
+        pay = kvq.Packed.empty(fmt_res, kind, n, H, D, G)
         pos_out = torch.full((max(n, 1),), -7, dtype=torch.int32, device=DEV)[:n]
         posd = pos.to(DEV) if pos is not None else None
         kvq.kvq_encode_residual(L[i].to(DEV), recon, posd, pay, pos_out if pos is not None else None, st)
@@ -91,7 +91,7 @@ def _chain(kind, fmt_res, T=4096, H=8, D=128, P=1024, loops=4, seed=4, inplace_c
             kvq.kvq_decode_residual(pay, posd, ip, ip, st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        opay, ost = O.residual_encode(bits(L[i]), recon_o, None if pos is None else pos.numpy(), fmt_res, kind, 64)
+        opay, ost = O.residual_encode(bits(L[i]), recon_o, None if pos is None else pos.numpy(), fmt_res, kind, G)
         assert ost == 0
         check_payload(pay, opay)
         if pos is not None:
@@ -125,6 +125,14 @@ def test_int4_base_nvfp4_residual_chain(kind):
 def test_int4_base_fp8_residual_chain(kind):
     """A mixed chain: INT4 base, FP8 E4M3 residual rows."""
     _chain(kind, kvq.FMT_FP8, T=600, H=3, D=96, P=150)
+
+
+@pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
+@pytest.mark.parametrize("G", [16, 32, 128, 256, 512])
+def test_int4_residual_chain_every_group_size(kind, G):
+    """The other group sizes the encode and decode kernels specialise, with ragged
+    compact groups: 1100 tokens, 300 kept a loop (every size leaves a partial group)."""
+    _chain(kind, kvq.FMT_INT4, T=1100, H=2, D=128, P=300, loops=3, G=G)
 
 
 def test_ragged_compact_groups_and_odd_sizes():
