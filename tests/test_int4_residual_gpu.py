@@ -135,6 +135,14 @@ def test_int4_residual_chain_every_group_size(kind, G):
     _chain(kind, kvq.FMT_INT4, T=1100, H=2, D=128, P=300, loops=3, G=G)
 
 
+@pytest.mark.parametrize("fmt", [kvq.FMT_NVFP4, kvq.FMT_FP8])
+@pytest.mark.parametrize("D", [64, 256, 512])
+def test_row_codec_residual_chain_head_dims(fmt, D):
+    """NVFP4 and FP8 residual rows at the head dims that change the decode kernels' lane
+    layout (4, 16 and 32 blocks of 16 a row), on an INT4 base."""
+    _chain(kvq.KIND_VALUE, fmt, T=400, H=2, D=D, P=100, loops=3)
+
+
 def test_ragged_compact_groups_and_odd_sizes():
     _chain(kvq.KIND_KEY, kvq.FMT_INT4, T=777, H=1, D=48, P=333, loops=3)
 
