@@ -179,6 +179,33 @@ def test_ragged_paged_round_trip_all_shapes(H, D):
         assert (bits(vo[s, int(lens[s]):]) == 0xA5A5).all()
 
 
+@pytest.mark.parametrize("bs", [1, 8, 32, 64, 256])
+def test_ragged_paged_round_trip_block_sizes(bs):
+    """The restore's block-table arithmetic at block sizes other than 16, with a
+    sequence that ends inside a block and one shorter than a block."""
+    S, Tmax, H, D = 3, 300, 4, 128
+    lens = torch.tensor([300, 129, 5], dtype=torch.int32)
+    k, v, table, nblocks = _paged_case(S, Tmax, H, D, lens, seed=60 + bs, bs=bs)
+    pool = kvq.Nvfp4Pool.empty(nblocks * bs, H, D, bs, fill=POISON)
+    for s in range(S):
+        n = int(lens[s])
+        t = torch.arange(n)
+        slots = (table[s, t // bs].long() * bs + t % bs).to(DEV)
+        scatter_and_check(k[s, :n].to(DEV), v[s, :n].to(DEV), slots, pool)
+    ko, vo = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
+    st = status_word()
+    kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko, vo, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for plane, got in (((pool.k_codes, pool.k_bscale, pool.k_rscale), ko),
+                       ((pool.v_codes, pool.v_bscale, pool.v_rscale), vo)):
+        opool = tuple(np.ascontiguousarray(a) for a in (u8(plane[0]), u8(plane[1]), plane[2].cpu().numpy()))
+        want, ost = O.nvfp4_restore(opool, bs, table.numpy(), lens.numpy(), Tmax,
+                                    out=np.full((S, Tmax, H, D), 0xA5A5, np.uint16))
+        assert ost == 0
+        np.testing.assert_array_equal(bits(got), want)
+
+
 def test_unaligned_to_32_bytes_takes_the_16_byte_path():
     """A view 16 bytes off a 32-byte boundary (pitch 8 mod 16) is still exact."""
     T, H, D = 50, 2, 64
