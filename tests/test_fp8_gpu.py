@@ -101,6 +101,37 @@ def test_fp8_ragged_paged_round_trip_all_shapes(H, D):
         np.testing.assert_array_equal(bits(out), want)
 
 
+@pytest.mark.parametrize("bs", [1, 8, 32, 64, 256])
+def test_fp8_ragged_paged_round_trip_block_sizes(bs):
+    """The FP8 restore reads each row's sequence length and block-table entry an
+    iteration ahead; block sizes other than 16, with sequences ending inside a block
+    and one shorter than a block."""
+    S, Tmax, H, D = 3, 300, 4, 128
+    lens = torch.tensor([300, 129, 5], dtype=torch.int32)
+    mb = -(-Tmax // bs)
+    nblocks = S * mb + 3
+    table = synth.block_permutation(nblocks, 70 + bs)[: S * mb].view(S, mb).contiguous()
+    k = synth.normal_bf16((S, Tmax, H, D), 70 + bs, synth.STREAM_K)
+    v = synth.normal_bf16((S, Tmax, H, D), 70 + bs, synth.STREAM_V)
+    pool = fp8_pool(nblocks * bs, H, D, bs)
+    for s in range(S):
+        n = int(lens[s])
+        t = torch.arange(n)
+        slots = (table[s, t // bs].long() * bs + t % bs).to(DEV)
+        scatter_and_check(k[s, :n].to(DEV), v[s, :n].to(DEV), slots, pool)
+    ko, vo = poison_bf16((S, Tmax, H, D)), poison_bf16((S, Tmax, H, D))
+    st = status_word()
+    kvq.kvq_restore(pool, table.to(DEV), lens.to(DEV), Tmax, ko, vo, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for P, out in (((pool.k_codes, pool.k_rscale), ko), ((pool.v_codes, pool.v_rscale), vo)):
+        opool = (np.ascontiguousarray(u8(P[0])), np.ascontiguousarray(P[1].cpu().numpy()))
+        want, ost = O.fp8_restore(opool, bs, table.numpy(), lens.numpy(), Tmax,
+                                  out=np.full((S, Tmax, H, D), 0xA5A5, np.uint16))
+        assert ost == 0
+        np.testing.assert_array_equal(bits(out), want)
+
+
 def test_fp8_strided_k_under_graph_capture():
     """One-token appends: K a view of a fused qkv (row pitch 1152), V its own tensor,
     captured in a CUDA graph and replayed."""
