@@ -120,7 +120,8 @@ def test_long_sequences_merge_several_splits(group):
 @pytest.mark.parametrize("H,bs,fmts", [
     (4, 16, (NV, NV)), (8, 16, (F8, NV)), (16, 16, (NV, NV)), (16, 32, (F8, F8)),  # page-major kernel
     (4, 64, (NV, F8)), (1, 32, (NV, NV)), (2, 16, (F8, NV)), (8, 16, (NV, NV)),
-    (3, 16, (NV, NV)), (8, 8, (NV, NV)),  # head-major kernel: H = 3, block size 8
+    (8, 256, (NV, NV)),
+    (3, 16, (NV, NV)), (8, 8, (NV, NV)), (2, 1, (F8, NV)),  # head-major kernel: H = 3, block sizes 8, 1
 ])
 def test_kv_head_counts_and_block_sizes(H, bs, fmts):
     """Both attention kernels against the oracle: the page-major kernel (block sizes that
