@@ -35,7 +35,8 @@ def check(x_cpu, pk, y, kind):
 
 
 @pytest.mark.parametrize("kind", [kvq.KIND_KEY, kvq.KIND_VALUE])
-@pytest.mark.parametrize("T,H,D", [(256, 8, 128), (20, 3, 64), (4100, 2, 96), (1, 1, 512), (17, 4, 256)])
+@pytest.mark.parametrize("T,H,D", [(256, 8, 128), (20, 3, 64), (4100, 2, 96), (1, 1, 512), (17, 4, 256),
+                                   (33, 2, 16), (50, 1, 32)])
 def test_matches_oracle(kind, T, H, D):
     x = synth.normal_bf16((T, H, D), seed=T + D, stream=1, outlier_frac=0.01, outlier_scale=20.0)
     pk, y = gpu_pack(x.to(DEV), kind)
